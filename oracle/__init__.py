@@ -1,0 +1,135 @@
+"""fp64 CPU oracle for the row-wise log-sum-exp.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA path never
+calls it, and the two share no code: the oracle is the plain definition
+``out[b] = log sum_n exp(x[b, n])`` written out in C (``lse_oracle.c``), single
+threaded, in double precision.
+
+Source: "Speeding up Log-Sum-Exp: Kernel Fusion at the Memory Wall, Integer
+Arithmetic at the Compute Wall" -- Sec. 2.1 (the max-subtract recipe that
+torch.logsumexp expands into its sub-kernels, Fig. 1) and Sec. 4 (accuracy is
+measured against an FP64 baseline).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lse_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liblse_oracle.so")
+
+DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE semantics: no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class OracleLib:
+    """ctypes view of one compiled oracle library (the real one, or a test's mutant)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        lib.oracle_lse.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+        lib.oracle_lse.restype = ctypes.c_int
+        lib.oracle_decode.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                      ctypes.c_void_p]
+        lib.oracle_decode.restype = ctypes.c_int
+        self._lib = lib
+        self.path = path
+
+    def lse(self, x: np.ndarray, dtype: str = "f32", B: int | None = None,
+            N: int | None = None, row_stride: int | None = None) -> np.ndarray:
+        return _lse(self._lib, x, dtype, B, N, row_stride)
+
+    def decode(self, x: np.ndarray, dtype: str) -> np.ndarray:
+        return _decode(self._lib, x, dtype)
+
+
+def _load() -> OracleLib:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = OracleLib(build())
+    return _lib
+
+
+def lse(x: np.ndarray, dtype: str = "f32", B: int | None = None, N: int | None = None,
+        row_stride: int | None = None) -> np.ndarray:
+    """out[b] = log sum_n exp(x[b, n]) in float64 (see ``_lse``)."""
+    return _load().lse(x, dtype, B, N, row_stride)
+
+
+def decode(x: np.ndarray, dtype: str) -> np.ndarray:
+    """The oracle's exact element decode (raw elements -> float64)."""
+    return _load().decode(x, dtype)
+
+
+def _raw(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Contiguous raw-element view of ``x``: float32 for f32, 16-bit elements otherwise."""
+    if dtype == "f32":
+        if x.dtype != np.float32:
+            raise TypeError("f32 oracle input must be a float32 array")
+    elif x.dtype not in (np.uint16, np.float16, np.int16):
+        raise TypeError(f"{dtype} oracle input must be 16-bit raw elements")
+    return np.ascontiguousarray(x)
+
+
+def _lse(lib, x: np.ndarray, dtype: str, B: int | None, N: int | None,
+         row_stride: int | None) -> np.ndarray:
+    """out[b] = log sum_n exp(x[b, n]) in float64.
+
+    ``x`` is a 2-D array ``[B, row_stride]`` (only the first ``N`` columns are
+    read), or a flat buffer with ``B``, ``N`` and ``row_stride`` given.  For
+    bf16/f16 pass the raw 16-bit patterns (uint16) or float16 values.
+    """
+    if dtype not in DTYPE_CODES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    arr = _raw(x, dtype)
+    if arr.ndim == 2:
+        B = arr.shape[0] if B is None else B
+        row_stride = arr.shape[1] if row_stride is None else row_stride
+        N = row_stride if N is None else N
+    elif B is None or N is None:
+        raise ValueError("flat input needs B and N")
+    row_stride = N if row_stride is None else row_stride
+    if B > 0 and N > 0 and arr.size < (B - 1) * row_stride + N:
+        raise ValueError("buffer smaller than (B-1)*row_stride + N elements")
+    out = np.empty(max(B, 0), dtype=np.float64)
+    rc = lib.oracle_lse(arr.ctypes.data if arr.size else None, DTYPE_CODES[dtype],
+                        B, N, row_stride, out.ctypes.data if out.size else None)
+    if rc != 0:
+        raise ValueError(f"oracle_lse rejected B={B} N={N} row_stride={row_stride}")
+    return out
+
+
+def _decode(lib, x: np.ndarray, dtype: str) -> np.ndarray:
+    arr = _raw(x, dtype).reshape(-1)
+    out = np.empty(arr.size, dtype=np.float64)
+    if arr.size:
+        rc = lib.oracle_decode(arr.ctypes.data, DTYPE_CODES[dtype], arr.size,
+                               out.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_decode failed")
+    return out

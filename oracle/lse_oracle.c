@@ -1,0 +1,158 @@
+/*
+ * lse_oracle.c -- fp64 CPU oracle for the row-wise log-sum-exp.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load this library.  It shares
+ * no source, header, table or helper with the CUDA path, and the CUDA path
+ * never calls it.
+ *
+ * What it computes (source: "Speeding up Log-Sum-Exp: Kernel Fusion at the
+ * Memory Wall, Integer Arithmetic at the Compute Wall", TL;DR and Sec. 2):
+ * for every row b of a [B, N] tensor,
+ *
+ *     out[b] = log( sum_{n<N} exp(x[b, n]) ).
+ *
+ * The fused method of Sec. 3.1 reaches this same value up to float rounding
+ * (Sec. 4.1: it "matches torch at float precision", accuracy measured against
+ * an FP64 baseline in Sec. 4).  So the oracle is the plain definition, written
+ * as the max-subtract recipe of Sec. 2.1 (Fig. 1) evaluated in double:
+ *
+ *     m = max_n x[b, n];   s = sum_n exp(x[b, n] - m)  (index order);
+ *     out[b] = m + log(s).
+ *
+ * Special values follow torch.logsumexp over the last dimension (the paper's
+ * Table 3 covers edge cases but its cells are not reproduced on the page):
+ *   any NaN in the row            -> NaN
+ *   else any +inf in the row      -> +inf
+ *   else every entry -inf, or N=0 -> -inf   (log of an empty / zero sum)
+ * Mixed finite and -inf entries: each -inf contributes exp(-inf) = 0.
+ *
+ * Inputs are decoded exactly to double: f32 by widening, bf16 as the top 16
+ * bits of an IEEE-754 binary32, f16 from the IEEE-754 binary16 fields.
+ * Single-threaded on purpose; no blocking, fusion or reordering.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+/* IEEE-754 binary32 element -> double (exact widening). */
+static double decode_f32(const unsigned char *p)
+{
+    float f;
+    memcpy(&f, p, sizeof f);
+    return (double)f;
+}
+
+/* bfloat16 element: the upper half of a binary32 with the lower half zero. */
+static double decode_bf16(const unsigned char *p)
+{
+    uint16_t h;
+    uint32_t bits;
+    float f;
+    memcpy(&h, p, sizeof h);
+    bits = (uint32_t)h << 16;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* IEEE-754 binary16 element: sign, 5-bit biased exponent (bias 15), 10-bit
+ * fraction.  Normal: (1024 + frac) * 2^(e - 25); subnormal: frac * 2^-24. */
+static double decode_f16(const unsigned char *p)
+{
+    uint16_t h;
+    unsigned sign, e, frac;
+    double mag;
+    memcpy(&h, p, sizeof h);
+    sign = (unsigned)(h >> 15) & 1u;
+    e = (unsigned)(h >> 10) & 0x1fu;
+    frac = (unsigned)h & 0x3ffu;
+    if (e == 0u)
+        mag = ldexp((double)frac, -24);
+    else if (e == 31u)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024u + frac), (int)e - 25);
+    return sign ? -mag : mag;
+}
+
+static double decode(int dtype, const unsigned char *row, int64_t n)
+{
+    switch (dtype) {
+    case ORACLE_F32:  return decode_f32(row + 4 * n);
+    case ORACLE_BF16: return decode_bf16(row + 2 * n);
+    default:          return decode_f16(row + 2 * n);
+    }
+}
+
+static int64_t elem_size(int dtype)
+{
+    return dtype == ORACLE_F32 ? 4 : 2;
+}
+
+/* One row: max-subtract in double (Sec. 2.1), special values as above. */
+static double lse_row(int dtype, const unsigned char *row, int64_t N)
+{
+    int any_nan = 0, any_pos_inf = 0;
+    double m = -INFINITY, s = 0.0;
+    int64_t n;
+
+    for (n = 0; n < N; ++n) {
+        double v = decode(dtype, row, n);
+        if (isnan(v))
+            any_nan = 1;
+        else if (v == INFINITY)
+            any_pos_inf = 1;
+        else if (v > m)
+            m = v;
+    }
+    if (any_nan)
+        return NAN;
+    if (any_pos_inf)
+        return INFINITY;
+    if (m == -INFINITY)
+        return -INFINITY;
+
+    for (n = 0; n < N; ++n)
+        s += exp(decode(dtype, row, n) - m);
+    return m + log(s);
+}
+
+/*
+ * oracle_lse: out[b] = log sum_n exp(x[b, n]) for b < B, in double.
+ *   x          host pointer to B rows; row b starts at element b*row_stride
+ *   dtype      0 = f32, 1 = bf16, 2 = f16 (raw element bits)
+ *   row_stride elements between row starts, >= N
+ *   out        host pointer to B doubles
+ * Returns 0, or -1 on an invalid argument (nothing written).
+ */
+int oracle_lse(const void *x, int dtype, int64_t B, int64_t N,
+               int64_t row_stride, double *out)
+{
+    const unsigned char *base = (const unsigned char *)x;
+    int64_t b, es;
+
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16)
+        return -1;
+    if (B < 0 || N < 0 || row_stride < N)
+        return -1;
+    if (B > 0 && (out == NULL || (N > 0 && x == NULL)))
+        return -1;
+    es = elem_size(dtype);
+    for (b = 0; b < B; ++b)
+        out[b] = lse_row(dtype, base + b * row_stride * es, N);
+    return 0;
+}
+
+/* Exact decode of n raw elements to double, for checking the decoders
+ * against independent conversions. */
+int oracle_decode(const void *x, int dtype, int64_t n, double *out)
+{
+    int64_t i;
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16 || n < 0)
+        return -1;
+    for (i = 0; i < n; ++i)
+        out[i] = decode(dtype, (const unsigned char *)x, i);
+    return 0;
+}

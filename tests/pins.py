@@ -1,0 +1,275 @@
+"""Pins for the fp64 oracle: checks against what the mathematics fixes.
+
+Each ``check_*`` takes an oracle object (``.lse(x, dtype, B, N, row_stride)``
+and ``.decode(x, dtype)``) and raises AssertionError on a mismatch.  The same
+checks run against the real oracle (all must pass) and against deliberately
+broken copies of it (at least one must fail), which shows the pins are strong
+enough to catch a dropped term, a wrong sign, a wrong index or stride, or a
+wrong decode.
+
+Nothing here retypes the oracle's max-subtract-then-sum loop: references are
+closed forms, exact invariants, library routines (numpy/torch dtype decodes,
+scipy.special.logsumexp) and brute force in 40-digit arithmetic (mpmath).
+
+Source of the definition: "Speeding up Log-Sum-Exp: Kernel Fusion at the
+Memory Wall, Integer Arithmetic at the Compute Wall", TL;DR and Sec. 2; the
+pairwise operation is associative and commutative (Sec. 3.1).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+try:
+    import mpmath
+except ImportError:  # pragma: no cover - mpmath ships with sympy here
+    mpmath = None
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _same(got: float, want: float, tol_abs: float, tol_rel: float) -> bool:
+    if math.isnan(want):
+        return math.isnan(got)
+    if math.isinf(want):
+        return got == want
+    return (not math.isnan(got)) and abs(got - want) <= tol_abs + tol_rel * abs(want)
+
+
+def _row_array(row, dtype):
+    vals = np.array([float(v) for v in row], dtype=np.float64)
+    if dtype == "f32":
+        return vals.astype(np.float32)[None, :]
+    if dtype == "f16":
+        return vals.astype(np.float16)[None, :]
+    if dtype == "bf16":
+        f = vals.astype(np.float32)
+        assert np.all((f.view(np.uint32) & 0xFFFF) == 0) or np.all(np.isnan(f)), \
+            "bf16 fixture values must be exact"
+        return (f.view(np.uint32) >> 16).astype(np.uint16)[None, :]
+    raise ValueError(dtype)
+
+
+def _mp_eval(expr: str) -> float:
+    if expr in ("inf", "-inf", "nan"):
+        return float(expr)
+    mpmath.mp.dps = 40
+    return float(mpmath.mpf(eval(expr, {"log": mpmath.log, "e": mpmath.e,
+                                        "__builtins__": {}})))
+
+
+def check_golden(orc) -> None:
+    """Closed-form fixtures under tests/golden/closed_forms.json."""
+    with open(os.path.join(GOLDEN, "closed_forms.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        row = c["row"] if "row" in c else [c["row_repeat"][0]] * c["row_repeat"][1]
+        x = _row_array(row, c["dtype"]) if row else np.zeros((1, 0), np.float32)
+        if not row and c["dtype"] != "f32":
+            x = np.zeros((1, 0), np.uint16)
+        got = float(orc.lse(x, c["dtype"])[0])
+        want = _mp_eval(c["expected"])
+        assert _same(got, want, 1e-13, 1e-15), (c["name"], got, want)
+
+
+def check_decode_all_patterns(orc) -> None:
+    """Every 16-bit pattern decodes as numpy (f16) / torch (bf16) decode it."""
+    import torch
+
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want16 = bits.view(np.float16).astype(np.float64)
+    got16 = orc.decode(bits, "f16")
+    nan = np.isnan(want16)
+    assert np.array_equal(np.isnan(got16), nan)
+    assert np.array_equal(got16[~nan], want16[~nan])
+
+    wantbf = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16) \
+        .to(torch.float64).numpy()
+    gotbf = orc.decode(bits, "bf16")
+    nan = np.isnan(wantbf)
+    assert np.array_equal(np.isnan(gotbf), nan)
+    assert np.array_equal(gotbf[~nan], wantbf[~nan])
+
+    f = np.array([0.0, -0.0, 1.0, -2.5, 1e-45, 3.4e38, np.inf, -np.inf, np.nan],
+                 dtype=np.float32)
+    got = orc.decode(f, "f32")
+    assert np.array_equal(np.isnan(got), np.isnan(f.astype(np.float64)))
+    assert np.array_equal(got[:-1], f[:-1].astype(np.float64))
+
+
+def check_single_element_rows(orc) -> None:
+    """N = 1: log(exp(x)) = x for every 16-bit pattern (one row per pattern)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dt in ("f16", "bf16"):
+        want = orc.decode(bits, dt)
+        got = orc.lse(bits.reshape(-1, 1), dt)
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan), dt
+        assert np.array_equal(got[~nan], want[~nan]), dt
+
+
+def check_constant_rows(orc) -> None:
+    """A constant row c of length N gives c + log N."""
+    for n in (1, 2, 3, 7, 64, 1000, 4097, 100003):
+        for c in (0.0, -3.5, 12.25, 1000.0, -1000.0, 88.5, -104.0):
+            x = np.full((1, n), c, dtype=np.float32)
+            got = float(orc.lse(x)[0])
+            want = c + math.log(n)
+            assert abs(got - want) <= 4e-16 * (1 + abs(want)) + 1e-15 * math.log(n), \
+                (n, c, got, want)
+
+
+def check_special_values(orc) -> None:
+    """NaN > +inf > all -inf; -inf entries add nothing; N = 0 gives -inf."""
+    inf, nan = np.inf, np.nan
+    rows = [
+        ([nan], "nan"), ([0.0, nan], "nan"), ([nan, 5.0], "nan"), ([inf, nan], "nan"),
+        ([-inf, nan, inf], "nan"), ([inf], "inf"), ([-inf, inf], "inf"),
+        ([1e30, inf, -1e30], "inf"), ([-inf], "-inf"), ([-inf] * 9, "-inf"),
+    ]
+    for r, want in rows:
+        got = float(orc.lse(np.array([r], dtype=np.float32))[0])
+        assert _same(got, float(want), 0, 0), (r, got, want)
+    for n in (2, 5, 33):
+        for k in range(n):
+            x = np.full((1, n), -inf, dtype=np.float32)
+            x[0, k] = 0.0
+            assert float(orc.lse(x)[0]) == 0.0, (n, k)
+            x[0, k] = nan
+            assert math.isnan(float(orc.lse(x)[0])), (n, k)
+            x[0, k] = inf
+            assert float(orc.lse(x)[0]) == inf, (n, k)
+    assert float(orc.lse(np.zeros((3, 0), np.float32))[2]) == -inf
+    for dt in ("f16", "bf16"):
+        pinf = np.uint16(0x7C00 if dt == "f16" else 0x7F80)
+        ninf = np.uint16(0xFC00 if dt == "f16" else 0xFF80)
+        qnan = np.uint16(0x7E00 if dt == "f16" else 0x7FC0)
+        one = np.uint16(0x3C00 if dt == "f16" else 0x3F80)
+        x = np.array([[one, pinf], [one, qnan], [ninf, ninf], [ninf, one]], np.uint16)
+        got = orc.lse(x, dt)
+        assert got[0] == inf and math.isnan(got[1]) and got[2] == -inf, (dt, got)
+        assert got[3] == 1.0, (dt, got)
+
+
+def check_two_element_closed_form(orc) -> None:
+    """lse(a, b) = max(a, b) + log1p(exp(-|a - b|)), in 40-digit arithmetic."""
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(7)
+    ab = np.concatenate([rng.normal(0, 5, (200, 2)), rng.normal(0, 400, (50, 2))])
+    ab = ab.astype(np.float32)
+    got = orc.lse(ab)
+    for (a, b), g in zip(ab.astype(np.float64), got):
+        want = float(max(a, b) + mpmath.log1p(mpmath.exp(-abs(mpmath.mpf(a) - b))))
+        assert abs(g - want) <= 4e-16 * (1 + abs(want)), (a, b, g, want)
+
+
+def check_brute_force(orc) -> None:
+    """Tiny rows: log(sum exp(x)) directly in 40-digit arithmetic (no max-subtract)."""
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(11)
+    for n in range(1, 17):
+        x = rng.uniform(-30, 30, (8, n)).astype(np.float32)
+        if n > 2:
+            x[0, n // 2] = -np.inf
+        got = orc.lse(x)
+        for row, g in zip(x.astype(np.float64), got):
+            want = float(mpmath.log(mpmath.fsum(mpmath.exp(mpmath.mpf(v)) for v in row
+                                                if v != -np.inf)))
+            assert abs(g - want) <= 1e-14 * max(1.0, abs(want)), (n, g, want)
+
+
+def check_against_scipy(orc) -> None:
+    """scipy.special.logsumexp on random rows, three scales and all dtypes."""
+    from scipy.special import logsumexp
+
+    rng = np.random.default_rng(3)
+    for scale in (1.0, 30.0, 3000.0):
+        x = (rng.normal(0, scale, (32, 999)) + rng.uniform(-50, 50, (32, 1))) \
+            .astype(np.float32)
+        got = orc.lse(x)
+        want = logsumexp(x.astype(np.float64), axis=1)
+        assert np.allclose(got, want, rtol=1e-14, atol=1e-13), scale
+        h = x.astype(np.float16)
+        assert np.allclose(orc.lse(h, "f16"), logsumexp(h.astype(np.float64), axis=1),
+                           rtol=1e-14, atol=1e-13)
+        bf = (x.view(np.uint32) >> 16).astype(np.uint16)
+        bfv = (bf.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert np.allclose(orc.lse(bf, "bf16"), logsumexp(bfv, axis=1),
+                           rtol=1e-14, atol=1e-13)
+
+
+def check_shift_invariance(orc) -> None:
+    """lse(x + c) = lse(x) + c, with x on a 2^-6 grid so x + c is exact in f32."""
+    rng = np.random.default_rng(5)
+    x = (np.round(rng.uniform(-16, 16, (16, 513)) * 64) / 64).astype(np.float32)
+    base = orc.lse(x)
+    for c in (1000.0, -1000.0, 1e4, -1e4):
+        xs = x + np.float32(c)
+        assert np.array_equal(xs.astype(np.float64), x.astype(np.float64) + c)
+        got = orc.lse(xs)
+        assert np.all(np.abs(got - (base + c)) <= 4e-16 * np.abs(base + c) + 1e-13), c
+
+
+def check_permutation_invariance(orc) -> None:
+    """The pairwise operation is commutative: any order of a row gives one value."""
+    rng = np.random.default_rng(9)
+    x = rng.normal(0, 10, (8, 777)).astype(np.float32)
+    x[:, ::50] = -np.inf
+    base = orc.lse(x)
+    for _ in range(3):
+        p = rng.permutation(x.shape[1])
+        assert np.allclose(orc.lse(np.ascontiguousarray(x[:, p])), base,
+                           rtol=1e-14, atol=0)
+    assert np.allclose(orc.lse(np.ascontiguousarray(x[:, ::-1])), base, rtol=1e-14, atol=0)
+
+
+def check_split_associativity(orc) -> None:
+    """lse(x) = lse2(lse(x[:k]), lse(x[k:])) for every split point k (Sec. 3.1)."""
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(13)
+    x = rng.normal(0, 6, (1, 97)).astype(np.float32)
+    x[0, 40] = 20.0
+    whole = float(orc.lse(x)[0])
+    for k in range(0, 98):
+        a = float(orc.lse(np.ascontiguousarray(x[:, :k]))[0])
+        b = float(orc.lse(np.ascontiguousarray(x[:, k:]))[0])
+        if a == -np.inf:
+            comb = b
+        elif b == -np.inf:
+            comb = a
+        else:
+            comb = float(max(a, b) + mpmath.log1p(mpmath.exp(-abs(mpmath.mpf(a) - b))))
+        assert abs(comb - whole) <= 1e-14 * abs(whole) + 1e-14, (k, comb, whole)
+
+
+def check_bounds(orc) -> None:
+    """max x <= lse(x) <= max x + log N."""
+    rng = np.random.default_rng(17)
+    for n in (1, 2, 10, 1000):
+        x = rng.normal(0, 20, (50, n)).astype(np.float32)
+        got = orc.lse(x)
+        m = x.max(axis=1).astype(np.float64)
+        assert np.all(got >= m) and np.all(got <= m + math.log(n) + 1e-12), n
+
+
+def check_row_stride(orc) -> None:
+    """Only the first N columns of each padded row are read."""
+    rng = np.random.default_rng(19)
+    x = rng.normal(0, 3, (9, 100)).astype(np.float32)
+    padded = np.full((9, 131), np.nan, dtype=np.float32)
+    padded[:, :100] = x
+    assert np.array_equal(orc.lse(padded, "f32", 9, 100, 131), orc.lse(x))
+    flat = padded.reshape(-1)[: 8 * 131 + 100]
+    assert np.array_equal(orc.lse(flat, "f32", 9, 100, 131), orc.lse(x))
+
+
+ALL_CHECKS = [
+    check_golden, check_decode_all_patterns, check_single_element_rows,
+    check_constant_rows, check_special_values, check_two_element_closed_form,
+    check_brute_force, check_against_scipy, check_shift_invariance,
+    check_permutation_invariance, check_split_associativity, check_bounds,
+    check_row_stride,
+]

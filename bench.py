@@ -1,0 +1,409 @@
+"""Benchmark of the row-wise log-sum-exp on GB300: prints ONE JSON line.
+
+A step is one lse_forward call (every kernel of the path) over one batch of
+the workload, inputs already in HBM.  ``value`` is the algorithmic HBM bytes
+of all ranks' steps (B*N*elem read + B*4 written) divided by the max-over-ranks
+time, in GB/s.  The default workload is the paper's profiled shape
+(B, N) = (512, 128256) in f32 ("Speeding up Log-Sum-Exp ...", Sec. 2.1, Fig. 1;
+Tables 6 and 7 use the same shape).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from log_sum_exp_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "row-wise LSE achieved HBM GB/s (% of GB300 peak) and us/call, 1 GPU"
+DEFAULT_WORKLOAD = "vocab_512x128256_f32"
+L2_BYTES = 129 * 10**6
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
+                  "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu"]
+
+
+# ---------------------------------------------------------------------------
+# Host-side helpers (also exercised by the CPU tests).
+# ---------------------------------------------------------------------------
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(workload: wl.Workload, rank: int) -> int:
+    """Each rank draws its own batch of the same workload (weak scaling)."""
+    return workload.seed + 7919 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None) -> None:
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "log_sum_exp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
+
+
+def ncu_traffic(workload_key: str, kernel_path: str) -> float | None:
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    or None when there is none for this workload or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = kernel_source_hash()
+    for e in entries:
+        if e.get("workload") == workload_key and e.get("source_hash") == src \
+                and e.get("path") == kernel_path:
+            return float(e["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle, as it stands, on a bounded sample.
+# ---------------------------------------------------------------------------
+def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float) -> dict:
+    import oracle
+
+    bytes_per_row = w.N * w.elem_bytes + 4
+    t0 = time.perf_counter()
+    oracle.lse(x[:1], w.dtype)  # load / build outside the timing
+    rows_done, elapsed, reps = 0, 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.lse(x, w.dtype)
+        rows_done += x.shape[0]
+        reps += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s:
+            break
+    gbs = rows_done * bytes_per_row / elapsed / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} pass(es) over {x.shape[0]} rows x {w.N} {w.dtype} of the "
+                      f"workload ({elapsed:.1f} s single-threaded)",
+            "seconds": elapsed, "rows": rows_done}
+
+
+def oracle_sample_rows(w: wl.Workload, target_s: float) -> int:
+    """Rows of the workload that take roughly target_s of oracle time (~5 ns/elem)."""
+    per_row = w.N * 5e-9
+    return int(max(1, min(w.B, target_s / max(per_row, 1e-9))))
+
+
+# ---------------------------------------------------------------------------
+# The reference arm: the oracle as the comparison program.
+# ---------------------------------------------------------------------------
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+    rows = oracle_sample_rows(w, 4.0)
+    x = wl.generate(args.workload, B=rows)
+    import oracle
+
+    oracle.lse(x[:1], w.dtype)
+    for _ in range(args.warmup):
+        oracle.lse(x[: max(1, rows // 8)], w.dtype)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.lse(x, w.dtype)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    bytes_per_step = rows * (w.N * w.elem_bytes + 4)
+    gbs = bytes_per_step * len(times) / total / 1e9
+    sample = (f"each step: {rows} of the workload's {w.B} rows ({w.N} {w.dtype} each), "
+              f"fp64 oracle single-threaded")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "N": w.N, "input_dtype": w.dtype,
+                   "rows_per_step": rows, "recipe": w.recipe},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# The native arm.
+# ---------------------------------------------------------------------------
+def to_torch(x: np.ndarray, dtype: str):
+    import torch
+
+    if dtype == "f32":
+        return torch.from_numpy(x)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    return torch.from_numpy(x.view(np.int16)).view(tdt)
+
+
+def run_native(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local_rank = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from log_sum_exp_gb300 import build as lse_build
+    lse_build.build()
+    import log_sum_exp_gb300 as L
+
+    w = wl.WORKLOADS[args.workload]
+    x_host = wl.generate(args.workload, seed=rank_seed(w, rank))
+    xt_host = to_torch(x_host, w.dtype)
+    in_bytes = w.B * w.N * w.elem_bytes
+    # Rotate over enough copies that consecutive steps never find their rows in L2.
+    copies = max(1, -(-3 * L2_BYTES // max(in_bytes, 1)))
+    copies = min(copies, 64)
+    xs = [xt_host.to(dev) for _ in range(copies)]
+    outs = [torch.empty(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    dt = w.dtype
+    ptrs = [(t.data_ptr(), o.data_ptr()) for t, o in zip(xs, outs)]
+    plan = L.lse_plan_query(xs[0])
+    bytes_per_step = in_bytes + w.write_bytes
+
+    def step(i, evb=0, eve=0):
+        xp, op = ptrs[i % copies]
+        L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, None, evb, eve)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in kb + ke:
+        e.record(stream)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        time.sleep(0.25)  # a clock sample before the timed region
+        start.record(stream)
+        for i in range(K):
+            step(i, kb[i].cuda_event, ke[i].cuda_event)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        time.sleep(0.25)
+    barrier(dev)
+    ms_total = start.elapsed_time(end)
+    kernel_ms = [b.elapsed_time(e) for b, e in zip(kb, ke)]
+    ms_total = reduce_max(ms_total, dev)
+    ms_per_step = ms_total / K
+    value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+    # Graph-replayed µs/call (launch overhead removed), same step.
+    graph_us = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            L.lse_forward(xs[0], out=outs[0])
+        stream.wait_stream(s2)
+        reps = 100
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                L.lse_forward(xs[i % copies], out=outs[i % copies])
+        g.replay()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(10):
+            g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = 1e3 * t0.elapsed_time(t1) / (10 * reps)
+
+    # End to end through the host entry point: H2D of x, compute, D2H of out.
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    x_pinned = xt_host.pin_memory()
+    L.lse_forward_host(x_pinned)  # warm-up
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        res = L.lse_forward_host(x_pinned)
+    e2e_s = reduce_max(time.perf_counter() - t0, dev)
+    e2e_value = world * bytes_per_step * e2e_steps / e2e_s / 1e9
+    assert res.shape == (w.B,)
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    kmean_ms = sum(kernel_ms) / len(kernel_ms)
+    achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
+    main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
+                   "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel"}[plan["path"]]
+    traffic = ncu_traffic(args.workload, plan["path"])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": bytes_per_step,
+                "kernel_us_mean": 1e3 * kmean_ms,
+                "kernel_us_median": 1e3 * statistics.median(kernel_ms)}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = oracle_sample_rows(w, args.cpu_seconds / 4)
+        cpu = time_oracle(x_host[:rows], w, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "N": w.N, "input_dtype": w.dtype,
+                   "row_stride": w.N, "recipe": w.recipe, "plan": plan,
+                   "bytes_per_step": bytes_per_step,
+                   "l2": f"inputs larger than L2: {copies} rotating copies of "
+                         f"{in_bytes / 1e6:.1f} MB (L2 {L2_BYTES / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}, rows independent, no collective"},
+        "us_per_call": 1e3 * ms_per_step,
+        "pct_of_peak": 100.0 * value / peak,
+        "us_per_call_graph": graph_us,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": w.write_bytes, "steps": e2e_steps,
+                "call": "lse_forward_host (pinned host input)"},
+        "gpu_launches": K * plan["launches"],
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=list(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--graph", action="store_true", help="also time CUDA-graph replay")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

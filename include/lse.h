@@ -1,0 +1,153 @@
+/*
+ * lse.h -- C ABI of liblse, a GB300 (sm_103a) row-wise log-sum-exp.
+ *
+ *     out[b] = log( sum_{n<N} exp(x[b, n]) ),   b < B
+ *
+ * Source: "Speeding up Log-Sum-Exp: Kernel Fusion at the Memory Wall, Integer
+ * Arithmetic at the Compute Wall".  The operation is the LSE primitive of the
+ * TL;DR and Sec. 2; it is a drop-in replacement for torch.logsumexp over the
+ * last dimension (Abstract).  Sec. 3.1 defines the method: one pass over HBM,
+ * each input element read once, one scalar written per row, partial results
+ * combined with the associative, commutative pairwise LSE operation.
+ *
+ * Conventions shared by every entry point
+ *   x           device pointer (host pointer for lse_forward_host) to B rows;
+ *               row b starts at element b * row_stride.  Elements are f32,
+ *               bf16 or f16 (lse_dtype).  Read-only; not retained.
+ *   row_stride  distance between row starts, in ELEMENTS, >= N.  Any
+ *               alignment of x and row_stride is accepted; 16-byte aligned
+ *               rows take the vectorised path.
+ *   out         device pointer (host pointer for lse_forward_host) to B
+ *               floats, 4-byte aligned.  Written once per row; not retained.
+ *   stream      CUDA stream for all work (0 = legacy default stream).  The
+ *               device entry points are asynchronous and stream-ordered.
+ *   Special values (torch.logsumexp semantics): a row holding a NaN gives NaN;
+ *   otherwise a row holding +inf gives +inf; a row of only -inf, or N == 0,
+ *   gives -inf; -inf entries next to finite ones contribute nothing.
+ *   B == 0 is a no-op returning LSE_OK.  The library never aborts, never
+ *   falls back to the CPU, and never synchronises a device call except
+ *   lse_forward_host.
+ *
+ * Errors: every call returns an lse_status.  LSE_ERR_INVALID_ARG for B < 0,
+ * N < 0, row_stride < N, a NULL x (N > 0) or out (B > 0), a misaligned out, or
+ * sizes whose byte extent overflows int64; LSE_ERR_UNSUPPORTED_DTYPE for an
+ * unknown dtype; LSE_ERR_ALLOC when stream-ordered scratch cannot be
+ * allocated; LSE_ERR_CUDA when a CUDA call fails (lse_last_cuda_error gives
+ * the cudaError_t).  On any error nothing is guaranteed about out.
+ */
+#ifndef LSE_H
+#define LSE_H
+
+#include <stdint.h>
+
+/* Exported from liblse.so (built with hidden visibility by default). */
+#if defined(__GNUC__)
+#define LSE_API __attribute__((visibility("default")))
+#else
+#define LSE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA handle types, identical to cudaStream_t / cudaEvent_t. */
+typedef struct CUstream_st *lse_stream_t;
+typedef struct CUevent_st *lse_event_t;
+
+typedef enum {
+    LSE_F32 = 0,
+    LSE_BF16 = 1,
+    LSE_F16 = 2
+} lse_dtype;
+
+typedef enum {
+    LSE_OK = 0,
+    LSE_ERR_INVALID_ARG = 1,
+    LSE_ERR_UNSUPPORTED_DTYPE = 2,
+    LSE_ERR_ALLOC = 3,
+    LSE_ERR_CUDA = 4
+} lse_status;
+
+/* Kernel mappings.  AUTO lets the library choose from (dtype, B, N, layout). */
+typedef enum {
+    LSE_PATH_AUTO = 0,
+    LSE_PATH_EMPTY = 1,   /* N == 0: one fill kernel writes -inf           */
+    LSE_PATH_SUBWARP = 2, /* short rows: a group of 1..32 lanes per row     */
+    LSE_PATH_CTA = 3,     /* one CTA (1..8 warps) per row, online (m, s)    */
+    LSE_PATH_SPLIT = 4    /* `splits` CTAs per row write (m, s) partials;
+                             a second small kernel merges them in order   */
+} lse_path;
+
+/*
+ * A launch plan.  lse_plan_query fills one with the library's choice;
+ * lse_forward_plan runs a caller-edited one (fields left 0 are chosen by the
+ * library; a forced value outside its valid range gives LSE_ERR_INVALID_ARG).
+ */
+typedef struct {
+    int32_t path;           /* lse_path                                              */
+    int32_t vector_bytes;   /* 16: 128-bit loads; 1: element loads (unaligned rows);
+                               0 in a request: let the library choose              */
+    int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32         */
+    int32_t slots_per_lane; /* SUBWARP: vectors (or elements) per lane (output)      */
+    int32_t threads;        /* CTA / SPLIT: threads per CTA, 32 or 256              */
+    int32_t launches;       /* kernels launched per call (output)                    */
+    int64_t splits;         /* SPLIT: CTAs per row (>= 2); 1 otherwise               */
+    int64_t segment_slots;  /* CTA / SPLIT: vectors (or elements) per CTA (output)   */
+    int64_t grid;           /* CTAs launched by the main kernel (output)             */
+    int64_t scratch_bytes;  /* device scratch the plan allocates (output)           */
+} lse_plan;
+
+/*
+ * lse_forward -- out[b] = log sum_n exp(x[b, n]) on the GPU, one pass over x.
+ * Device pointers; asynchronous on `stream`.  The split-row mapping takes
+ * B * splits * 8 bytes of scratch with cudaMallocAsync / cudaFreeAsync on
+ * `stream` (stream-ordered, so concurrent calls on different streams do not
+ * share it).
+ */
+LSE_API lse_status lse_forward(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                       int64_t row_stride, float *out, lse_stream_t stream);
+
+/*
+ * lse_plan_query -- the plan lse_forward would use for these arguments on the
+ * current device (x is only inspected for its alignment; it may be NULL, which
+ * counts as 16-byte aligned).  Launches nothing.
+ */
+LSE_API lse_status lse_plan_query(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                          int64_t row_stride, lse_plan *plan);
+
+/*
+ * lse_forward_plan -- lse_forward with a caller-chosen plan (NULL = automatic).
+ * If ev_begin / ev_end are non-NULL they are recorded on `stream` immediately
+ * before and after the main (row-reading) kernel, so the caller can time that
+ * kernel alone.  On return *plan (if non-NULL) holds the plan that ran.
+ */
+LSE_API lse_status lse_forward_plan(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                            int64_t row_stride, float *out, lse_stream_t stream,
+                            lse_plan *plan, lse_event_t ev_begin, lse_event_t ev_end);
+
+/*
+ * lse_forward_host -- the same result from HOST buffers: copies x to the
+ * device, runs lse_forward, copies out back and synchronises `stream` before
+ * returning.  Device buffers are stream-ordered allocations freed before
+ * return.  Page-locked host memory gives full-speed copies; pageable memory
+ * works but is staged by the driver.
+ */
+LSE_API lse_status lse_forward_host(const void *x_host, lse_dtype dtype, int64_t B, int64_t N,
+                            int64_t row_stride, float *out_host, lse_stream_t stream);
+
+/* Short English description of a status code (static storage). */
+LSE_API const char *lse_status_string(lse_status status);
+
+/*
+ * The cudaError_t behind the calling thread's most recent LSE_ERR_CUDA or
+ * LSE_ERR_ALLOC (0 if none).  Returns LSE_OK, or LSE_ERR_INVALID_ARG if
+ * cuda_err is NULL.
+ */
+LSE_API lse_status lse_last_cuda_error(int *cuda_err);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSE_H */

@@ -1,1 +1,25 @@
-"""GB300-native row-wise log-sum-exp: out[b] = log sum_n exp(x[b, n])."""
+"""GB300-native row-wise log-sum-exp: out[b] = log sum_n exp(x[b, n]).
+
+The compute path is liblse (hand-written sm_103a CUDA kernels behind the C ABI
+in include/lse.h); this package only builds it and marshals arguments to it.
+Source of the method: "Speeding up Log-Sum-Exp: Kernel Fusion at the Memory
+Wall, Integer Arithmetic at the Compute Wall" (Sec. 3.1, FuseLSE).
+"""
+from ._binding import (  # noqa: F401
+    ABI_FUNCTIONS,
+    DTYPES,
+    PATHS,
+    LseError,
+    LsePlan,
+    library_path,
+    load,
+    lse_forward,
+    lse_forward_host,
+    lse_forward_host_ptr,
+    lse_forward_plan,
+    lse_forward_plan_ptr,
+    lse_forward_ptr,
+    lse_plan_query,
+    lse_plan_query_ptr,
+    status_string,
+)

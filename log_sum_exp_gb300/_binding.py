@@ -1,0 +1,264 @@
+"""ctypes binding of liblse (include/lse.h).  Argument marshalling only.
+
+Every function here passes pointers, sizes and the CUDA stream to the C ABI;
+all arithmetic runs in liblse's kernels.  There is no CPU fallback: if the
+library is missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+LSE_OK = 0
+STATUS_NAMES = {0: "LSE_OK", 1: "LSE_ERR_INVALID_ARG", 2: "LSE_ERR_UNSUPPORTED_DTYPE",
+                3: "LSE_ERR_ALLOC", 4: "LSE_ERR_CUDA"}
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+# Exported names, in header order.
+ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
+                 "lse_status_string", "lse_last_cuda_error"]
+
+
+class LsePlan(ctypes.Structure):
+    """Mirror of ``lse_plan``."""
+    _fields_ = [
+        ("path", ctypes.c_int32),
+        ("vector_bytes", ctypes.c_int32),
+        ("lanes_per_row", ctypes.c_int32),
+        ("slots_per_lane", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("launches", ctypes.c_int32),
+        ("splits", ctypes.c_int64),
+        ("segment_slots", ctypes.c_int64),
+        ("grid", ctypes.c_int64),
+        ("scratch_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["path"] = PATH_NAMES.get(self.path, self.path)
+        return d
+
+
+class LseError(RuntimeError):
+    def __init__(self, status: int, where: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{where}: {STATUS_NAMES.get(status, status)}"
+        if cuda_error:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load liblse.so; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"liblse.so is not built ({path}); run "
+                              "log_sum_exp_gb300.build.build() first")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.lse_forward.argtypes = [vp, i32, i64, i64, i64, vp, vp]
+        lib.lse_forward.restype = i32
+        lib.lse_plan_query.argtypes = [vp, i32, i64, i64, i64, ctypes.POINTER(LsePlan)]
+        lib.lse_plan_query.restype = i32
+        lib.lse_forward_plan.argtypes = [vp, i32, i64, i64, i64, vp, vp,
+                                         ctypes.POINTER(LsePlan), vp, vp]
+        lib.lse_forward_plan.restype = i32
+        lib.lse_forward_host.argtypes = [vp, i32, i64, i64, i64, vp, vp]
+        lib.lse_forward_host.restype = i32
+        lib.lse_status_string.argtypes = [i32]
+        lib.lse_status_string.restype = ctypes.c_char_p
+        lib.lse_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.lse_last_cuda_error.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != LSE_OK:
+        err = ctypes.c_int(0)
+        load().lse_last_cuda_error(ctypes.byref(err))
+        raise LseError(status, where, err.value)
+
+
+def status_string(status: int) -> str:
+    return load().lse_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------
+# Raw-pointer calls (same names and argument order as the C ABI).
+# ---------------------------------------------------------------------------
+def lse_forward_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, out_ptr: int,
+                    stream: int = 0) -> None:
+    _check(load().lse_forward(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
+                              stream or None), "lse_forward")
+
+
+def lse_forward_plan_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, out_ptr: int,
+                         stream: int = 0, plan: LsePlan | None = None, ev_begin: int = 0,
+                         ev_end: int = 0) -> LsePlan:
+    p = plan if plan is not None else LsePlan()
+    _check(load().lse_forward_plan(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
+                                   stream or None, ctypes.byref(p), ev_begin or None,
+                                   ev_end or None), "lse_forward_plan")
+    return p
+
+
+def lse_plan_query_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int) -> LsePlan:
+    p = LsePlan()
+    _check(load().lse_plan_query(x_ptr or None, DTYPES[dtype], B, N, row_stride, ctypes.byref(p)),
+           "lse_plan_query")
+    return p
+
+
+def lse_forward_host_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, out_ptr: int,
+                         stream: int = 0) -> None:
+    _check(load().lse_forward_host(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
+                                   stream or None), "lse_forward_host")
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor conveniences: torch supplies device memory and the stream only.
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_name(t) -> str:
+    torch = _torch()
+    names = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    if t.dtype not in names:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32, bfloat16 or float16")
+    return names[t.dtype]
+
+
+def _rows(x):
+    """(B, N, row_stride) of a 1-D or 2-D tensor whose last dimension has unit stride."""
+    if x.dim() == 1:
+        if x.numel() > 1 and x.stride(0) != 1:
+            raise ValueError("the reduced dimension must have unit stride")
+        return 1, x.shape[0], x.shape[0]
+    if x.dim() != 2:
+        raise ValueError("expected a [B, N] tensor (reduce over the last dimension)")
+    B, N = x.shape
+    if N > 1 and x.stride(1) != 1:
+        raise ValueError("the reduced (last) dimension must have unit stride")
+    row_stride = x.stride(0) if B > 1 else N
+    if row_stride < N:
+        raise ValueError("rows overlap (row stride < N)")
+    return B, N, row_stride
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def lse_forward(x, out=None, stream=None):
+    """out[b] = log sum_n exp(x[b, n]) for a CUDA tensor x of shape [B, N] (or [N]).
+
+    Returns a float32 tensor of shape [B] (a 0-d tensor for 1-D input).
+    """
+    out, _ = lse_forward_plan(x, out=out, stream=stream)
+    return out
+
+
+def lse_forward_plan(x, plan: LsePlan | dict | None = None, out=None, stream=None,
+                     ev_begin=None, ev_end=None):
+    """``lse_forward`` with an optional forced plan and timing events.
+
+    ``plan`` may be an LsePlan or a dict of its fields (``path`` may be a name).
+    ``ev_begin``/``ev_end`` are torch.cuda.Event objects recorded around the
+    main kernel.  Returns (out, plan_that_ran).
+    """
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (use lse_forward_host for host memory)")
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    if out is None:
+        out = torch.empty(B, dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or out.numel() != B or not out.is_contiguous() \
+            or out.device != x.device:
+        raise ValueError("out must be a contiguous float32 tensor of B elements on x's device")
+    p = _as_plan(plan)
+    with torch.cuda.device(x.device):
+        evb = _event_handle(ev_begin)
+        eve = _event_handle(ev_end)
+        p = lse_forward_plan_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
+                                 _stream_handle(stream, x.device), p, evb, eve)
+    if x.dim() == 1:
+        return out.reshape(()), p
+    return out, p
+
+
+def _event_handle(ev) -> int:
+    if ev is None:
+        return 0
+    if isinstance(ev, int):
+        return ev
+    if ev.cuda_event == 0:  # torch creates the event lazily on first record
+        ev.record()
+    return ev.cuda_event
+
+
+def _as_plan(plan) -> LsePlan | None:
+    if plan is None or isinstance(plan, LsePlan):
+        return plan
+    p = LsePlan()
+    for k, v in plan.items():
+        if k == "path" and isinstance(v, str):
+            v = PATHS[v]
+        setattr(p, k, v)
+    return p
+
+
+def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,
+                   row_stride: int | None = None) -> dict:
+    """The plan lse_forward would use, for a tensor or for (dtype, B, N, row_stride)."""
+    if x is not None:
+        dtype = _dtype_name(x)
+        B, N, row_stride = _rows(x)
+        ptr = x.data_ptr()
+    else:
+        ptr = 0
+        row_stride = N if row_stride is None else row_stride
+    return lse_plan_query_ptr(ptr, dtype, B, N, row_stride).as_dict()
+
+
+def lse_forward_host(x, stream=None):
+    """lse over a HOST tensor/array: copy in, compute, copy out, synchronise.
+
+    ``x`` is a CPU torch tensor (pin it for full-speed copies) of shape [B, N].
+    Returns a CPU float32 tensor of shape [B].
+    """
+    torch = _torch()
+    if x.is_cuda:
+        raise ValueError("lse_forward_host takes host memory")
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    out = torch.empty(B, dtype=torch.float32, pin_memory=x.is_pinned())
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lse_forward_host_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
+                         _stream_handle(stream, dev))
+    return out

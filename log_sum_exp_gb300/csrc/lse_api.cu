@@ -1,0 +1,412 @@
+// lse_api.cu -- the C ABI of liblse: argument checks, the choice of kernel
+// mapping, stream-ordered scratch, and the two type-independent kernels (the
+// N == 0 fill and the split-row merge).  See include/lse.h for the contract.
+//
+// Source of the operation: "Speeding up Log-Sum-Exp: Kernel Fusion at the
+// Memory Wall, Integer Arithmetic at the Compute Wall", Sec. 3.1 (one fused
+// pass; partial results combined with the pairwise LSE operation).
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/lse.h"
+#include "lse_device.cuh"
+#include "lse_internal.h"
+
+namespace lse {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+lse_status cuda_fail(cudaError_t e, lse_status st = LSE_ERR_CUDA) {
+    g_last_cuda_error = static_cast<int>(e);
+    return st;
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kSubwarpMaxSlots = 4;    // slots per lane in the subwarp kernel
+constexpr int kSegmentBatchVec = 8;    // slots per thread per batch (16-byte loads)
+constexpr int kSegmentBatchScalar = 16;
+constexpr int kMergeRowsPerCta = 8;    // one warp per row
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int seg_occ[3][2][2] = {};  // [dtype][vec][threads == 256]
+};
+
+std::mutex g_info_mutex;
+DeviceInfo g_info[kMaxDevices];
+
+int segment_occupancy(int dt, bool vec, int threads) {
+    switch (dt) {
+    case LSE_F32: return segment_occupancy_f32(vec, threads);
+    case LSE_BF16: return segment_occupancy_bf16(vec, threads);
+    default: return segment_occupancy_f16(vec, threads);
+    }
+}
+
+lse_status device_info(int* dev_out, const DeviceInfo** info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return LSE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    DeviceInfo& d = g_info[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        for (int dt = 0; dt < 3; ++dt)
+            for (int v = 0; v < 2; ++v)
+                for (int t = 0; t < 2; ++t) {
+                    const int occ = segment_occupancy(dt, v != 0, t ? 256 : 32);
+                    d.seg_occ[dt][v][t] = occ > 0 ? occ : 1;
+                }
+        d.ready = true;
+    }
+    *dev_out = dev;
+    *info = &d;
+    return LSE_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int elem_bytes(lse_dtype dt) { return dt == LSE_F32 ? 4 : 2; }
+
+bool valid_dtype(int dt) { return dt == LSE_F32 || dt == LSE_BF16 || dt == LSE_F16; }
+
+lse_status check_args(const void* x, int dt, int64_t B, int64_t N, int64_t row_stride,
+                      const void* out) {
+    if (!valid_dtype(dt)) return LSE_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || N < 0 || row_stride < N) return LSE_ERR_INVALID_ARG;
+    if (B > 0 && out == nullptr) return LSE_ERR_INVALID_ARG;
+    if (B > 0 && N > 0 && x == nullptr) return LSE_ERR_INVALID_ARG;
+    if (out != nullptr && (reinterpret_cast<uintptr_t>(out) & 3u) != 0) return LSE_ERR_INVALID_ARG;
+    // Byte extent of x and of out must fit in int64.
+    int64_t extent = 0;
+    if (B > 0 && __builtin_mul_overflow(B - 1, row_stride, &extent)) return LSE_ERR_INVALID_ARG;
+    if (__builtin_add_overflow(extent, N, &extent)) return LSE_ERR_INVALID_ARG;
+    if (__builtin_mul_overflow(extent, static_cast<int64_t>(elem_bytes(static_cast<lse_dtype>(dt))),
+                               &extent))
+        return LSE_ERR_INVALID_ARG;
+    if (B > INT64_MAX / 4) return LSE_ERR_INVALID_ARG;
+    return LSE_OK;
+}
+
+int pow2_ceil(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Fill in (or check) a plan.  `req` may be null (automatic).
+lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t row_stride,
+                     const DeviceInfo& info, const lse_plan* req, lse_plan* plan) {
+    lse_plan p;
+    std::memset(&p, 0, sizeof p);
+    const int eb = elem_bytes(dt);
+    const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16u == 0) &&
+                         ((row_stride * eb) % 16 == 0);
+    bool vec = aligned;
+    if (req && req->vector_bytes != 0) {
+        if (req->vector_bytes == 16) {
+            if (!aligned) return LSE_ERR_INVALID_ARG;
+            vec = true;
+        } else if (req->vector_bytes == 1) {
+            vec = false;
+        } else {
+            return LSE_ERR_INVALID_ARG;
+        }
+    }
+    p.vector_bytes = vec ? 16 : 1;
+    const int64_t epv = vec ? 16 / eb : 1;
+    const int64_t nv = N / epv;               // full slots per row
+    const int64_t nvt = ceil_div(N, epv);     // slots including the tail vector
+    int path = req ? req->path : LSE_PATH_AUTO;
+
+    if (N == 0) {
+        if (path != LSE_PATH_AUTO && path != LSE_PATH_EMPTY) return LSE_ERR_INVALID_ARG;
+        p.path = LSE_PATH_EMPTY;
+        p.splits = 1;
+        p.grid = ceil_div(B, 256);
+        p.launches = B > 0 ? 1 : 0;
+        *plan = p;
+        return LSE_OK;
+    }
+    if (path == LSE_PATH_EMPTY || path < 0 || path > LSE_PATH_SPLIT) return LSE_ERR_INVALID_ARG;
+
+    const int64_t sub_capacity = 32 * kSubwarpMaxSlots;  // slots per row
+    if (path == LSE_PATH_AUTO) path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
+
+    if (path == LSE_PATH_SUBWARP) {
+        if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
+        int G = req && req->lanes_per_row ? req->lanes_per_row
+                                          : static_cast<int>(pow2_ceil(nvt < 32 ? nvt : 32));
+        if (G < 1 || G > 32 || (G & (G - 1)) != 0) return LSE_ERR_INVALID_ARG;
+        int64_t V = ceil_div(nvt, G);
+        if (V > kSubwarpMaxSlots) return LSE_ERR_INVALID_ARG;
+        V = V <= 1 ? 1 : (V <= 2 ? 2 : 4);
+        const int64_t R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
+        const int64_t rows_per_warp_iter = (32 / G) * R;
+        const int64_t warps = ceil_div(B, rows_per_warp_iter);
+        int64_t grid = ceil_div(warps, kSubwarpThreads / 32);
+        if (grid > INT_MAX) grid = INT_MAX;  // grid-stride loop covers the rest
+        p.path = LSE_PATH_SUBWARP;
+        p.lanes_per_row = G;
+        p.threads = kSubwarpThreads;
+        p.splits = 1;
+        p.grid = grid;
+        p.slots_per_lane = static_cast<int32_t>(V);
+        p.launches = B > 0 ? 1 : 0;
+        *plan = p;
+        return LSE_OK;
+    }
+
+    // CTA / SPLIT: the segment kernel.
+    const int64_t batch_slots_256 = 256 * (vec ? kSegmentBatchVec : kSegmentBatchScalar);
+    int T = req && req->threads ? req->threads : 0;
+    if (T == 0) T = (nv >= batch_slots_256 || B < 8LL * info.sms) ? 256 : 32;
+    if (T != 32 && T != 256) return LSE_ERR_INVALID_ARG;
+    const int64_t batch = static_cast<int64_t>(T) * (vec ? kSegmentBatchVec : kSegmentBatchScalar);
+    const int64_t slots = vec ? nv : N;  // slots the segments cover (tail handled separately)
+    int64_t P = 1;
+    if (path == LSE_PATH_SPLIT) {
+        if (req && req->splits) {
+            P = req->splits;
+            if (P < 2 || P > (slots > 0 ? slots : 1)) return LSE_ERR_INVALID_ARG;
+        } else {
+            const int64_t resident = static_cast<int64_t>(info.sms) *
+                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
+            P = ceil_div(4 * resident, B);
+            const int64_t max_p = slots / batch;
+            if (P > max_p) P = max_p;
+            if (P < 2) P = 2;
+            if (P > slots) P = slots;
+            if (P < 2) return LSE_ERR_INVALID_ARG;
+        }
+    } else {
+        if (req && req->splits > 1) return LSE_ERR_INVALID_ARG;
+        if (!req || req->path == LSE_PATH_AUTO) {
+            // Few rows: split them so the grid covers the GPU several times over.
+            const int64_t resident = static_cast<int64_t>(info.sms) *
+                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
+            if (B < 4 * resident) {
+                int64_t want = ceil_div(4 * resident, B);
+                const int64_t max_p = slots / (2 * batch);
+                if (want > max_p) want = max_p;
+                if (want >= 2) P = want;
+            }
+        }
+    }
+    const int64_t seg_slots = ceil_div(slots, P);
+    P = ceil_div(slots, seg_slots);  // no empty trailing segments
+    if (P < 1) P = 1;
+    if (B > INT_MAX / P) return LSE_ERR_INVALID_ARG;  // grid.x = B * P must fit
+    p.path = P > 1 ? LSE_PATH_SPLIT : LSE_PATH_CTA;
+    p.threads = T;
+    p.splits = P;
+    p.grid = B * P;
+    p.scratch_bytes = P > 1 ? B * P * static_cast<int64_t>(sizeof(float2)) : 0;
+    p.launches = B > 0 ? (P > 1 ? 2 : 1) : 0;
+    p.segment_slots = seg_slots;
+    *plan = p;
+    return LSE_OK;
+}
+
+cudaError_t launch_subwarp(lse_dtype dt, const LaunchArgs& a, bool vec, int G, int V, int64_t grid) {
+    switch (dt) {
+    case LSE_F32: return launch_subwarp_f32(a, vec, G, V, grid);
+    case LSE_BF16: return launch_subwarp_bf16(a, vec, G, V, grid);
+    default: return launch_subwarp_f16(a, vec, G, V, grid);
+    }
+}
+
+cudaError_t launch_segment(lse_dtype dt, const LaunchArgs& a, bool vec, int T, int64_t P,
+                           int64_t seg_slots, float2* partial) {
+    switch (dt) {
+    case LSE_F32: return launch_segment_f32(a, vec, T, P, seg_slots, partial);
+    case LSE_BF16: return launch_segment_bf16(a, vec, T, P, seg_slots, partial);
+    default: return launch_segment_f16(a, vec, T, P, seg_slots, partial);
+    }
+}
+
+__global__ void fill_neg_inf_kernel(float* __restrict__ out, int64_t B) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t b = i; b < B; b += stride) out[b] = __int_as_float(kNegInfF32);
+}
+
+// One warp per row: lane l folds partials l, l+32, ... in order, then a fixed
+// butterfly merges the lanes.  Waits (griddepcontrol.wait) until the segment
+// kernel that produced the partials has completed and its writes are visible.
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta)
+merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __restrict__ out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= B) return;  // uniform per warp
+    Acc a = acc_identity();
+    const float2* pr = partial + row * P;
+    for (int64_t p = lane; p < P; p += 32) {
+        const float2 v = pr[p];
+        a = acc_merge(a, Acc{v.x, v.y});
+    }
+    a = warp_merge<32>(a);
+    if (lane == 0) out[row] = acc_finalize(a);
+}
+
+}  // namespace
+
+cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream) {
+    int64_t grid = ceil_div(B, 256);
+    if (grid > 65536) grid = 65536;
+    fill_neg_inf_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(out, B);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
+                         cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(B, kMergeRowsPerCta)));
+    cfg.blockDim = dim3(32 * kMergeRowsPerCta);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, partial, B, P, out);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace lse
+
+using namespace lse;
+
+extern "C" {
+
+const char* lse_status_string(lse_status status) {
+    switch (status) {
+    case LSE_OK: return "ok";
+    case LSE_ERR_INVALID_ARG: return "invalid argument";
+    case LSE_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case LSE_ERR_ALLOC: return "device scratch allocation failed";
+    case LSE_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+lse_status lse_last_cuda_error(int* cuda_err) {
+    if (cuda_err == nullptr) return LSE_ERR_INVALID_ARG;
+    *cuda_err = g_last_cuda_error;
+    return LSE_OK;
+}
+
+lse_status lse_plan_query(const void* x, lse_dtype dtype, int64_t B, int64_t N,
+                          int64_t row_stride, lse_plan* plan) {
+    if (plan == nullptr) return LSE_ERR_INVALID_ARG;
+    // Only the shape is checked here: stand-in non-null pointers for x and out.
+    const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    lse_status st = check_args(x ? x : stand_in, dtype, B, N, row_stride, stand_in);
+    if (st != LSE_OK) return st;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    if ((st = device_info(&dev, &info)) != LSE_OK) return st;
+    return make_plan(x, dtype, B, N, row_stride, *info, nullptr, plan);
+}
+
+lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N,
+                            int64_t row_stride, float* out, lse_stream_t stream_,
+                            lse_plan* plan, lse_event_t ev_begin, lse_event_t ev_end) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    lse_status st = check_args(x, dtype, B, N, row_stride, out);
+    if (st != LSE_OK) return st;
+    if (B == 0) return LSE_OK;  // no work, no device access
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    if ((st = device_info(&dev, &info)) != LSE_OK) return st;
+    lse_plan p;
+    if ((st = make_plan(x, dtype, B, N, row_stride, *info, plan, &p)) != LSE_OK) return st;
+    if (plan) *plan = p;
+
+    const LaunchArgs a{x, B, N, row_stride, out, stream};
+    cudaError_t e = cudaSuccess;
+    float2* scratch = nullptr;
+    if (p.scratch_bytes > 0) {
+        e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), static_cast<size_t>(p.scratch_bytes),
+                            stream);
+        if (e != cudaSuccess) return cuda_fail(e, LSE_ERR_ALLOC);
+    }
+    if (ev_begin && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev_begin), stream)) != cudaSuccess)
+        goto fail;
+    switch (p.path) {
+    case LSE_PATH_EMPTY:
+        e = launch_fill_neg_inf(out, B, stream);
+        break;
+    case LSE_PATH_SUBWARP:
+        e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
+        break;
+    default:
+        e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,
+                           scratch);
+        break;
+    }
+    if (e != cudaSuccess) goto fail;
+    if (ev_end && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev_end), stream)) != cudaSuccess)
+        goto fail;
+    if (p.path == LSE_PATH_SPLIT) {
+        e = launch_merge(scratch, B, p.splits, out, stream);
+        if (e != cudaSuccess) goto fail;
+    }
+    if (scratch && (e = cudaFreeAsync(scratch, stream)) != cudaSuccess) return cuda_fail(e);
+    return LSE_OK;
+
+fail:
+    if (scratch) cudaFreeAsync(scratch, stream);
+    return cuda_fail(e);
+}
+
+lse_status lse_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,
+                       float* out, lse_stream_t stream) {
+    return lse_forward_plan(x, dtype, B, N, row_stride, out, stream, nullptr, nullptr, nullptr);
+}
+
+lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int64_t N,
+                            int64_t row_stride, float* out_host, lse_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    lse_status st = check_args(x_host, dtype, B, N, row_stride, out_host);
+    if (st != LSE_OK) return st;
+    if (B == 0) return LSE_OK;
+    const size_t x_bytes = N > 0 ? static_cast<size_t>(((B - 1) * row_stride + N) * elem_bytes(dtype)) : 0;
+    const size_t out_bytes = static_cast<size_t>(B) * sizeof(float);
+    void* d_x = nullptr;
+    float* d_out = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (x_bytes && (e = cudaMallocAsync(&d_x, x_bytes, stream)) != cudaSuccess)
+        return cuda_fail(e, LSE_ERR_ALLOC);
+    if ((e = cudaMallocAsync(reinterpret_cast<void**>(&d_out), out_bytes, stream)) != cudaSuccess) {
+        if (d_x) cudaFreeAsync(d_x, stream);
+        return cuda_fail(e, LSE_ERR_ALLOC);
+    }
+    if (x_bytes) e = cudaMemcpyAsync(d_x, x_host, x_bytes, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) {
+        st = lse_forward(d_x, dtype, B, N, row_stride, d_out, stream_);
+        if (st == LSE_OK)
+            e = cudaMemcpyAsync(out_host, d_out, out_bytes, cudaMemcpyDeviceToHost, stream);
+    }
+    if (d_x) cudaFreeAsync(d_x, stream);
+    cudaFreeAsync(d_out, stream);
+    const cudaError_t es = cudaStreamSynchronize(stream);
+    if (st != LSE_OK) return st;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (es != cudaSuccess) return cuda_fail(es);
+    return LSE_OK;
+}
+
+}  // extern "C"

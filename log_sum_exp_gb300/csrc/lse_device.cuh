@@ -1,0 +1,247 @@
+// lse_device.cuh -- device building blocks of the row-wise log-sum-exp.
+//
+// The method ("Speeding up Log-Sum-Exp: Kernel Fusion at the Memory Wall,
+// Integer Arithmetic at the Compute Wall", Sec. 3.1) folds a row into a
+// register accumulator with the pairwise LSE operation and evaluates exp/log on
+// the special function unit.  Sec. 2.2 names the streaming form used here: a
+// running maximum m plus an exp-sum s rescaled whenever m grows.
+//
+// Accumulator (m, s): m is the largest element seen (NaN-free: max ignores
+// NaN), and s = sum 2^((x - mu) * log2 e) over the elements seen, where the
+// shift mu = m if m is finite and 0 otherwise.  With that choice
+//   * -inf elements add ex2(-inf) = 0, an all -inf row keeps (m, s) = (-inf, 0);
+//   * a +inf element adds ex2(+inf) = +inf, so s = +inf whenever m = +inf;
+//   * a NaN element makes s NaN, and NaN survives every rescale and merge;
+//   * no inf - inf or 0 * inf can occur, so s is NaN exactly when the row holds
+//     a NaN.
+// The pairwise operation on two accumulators (the merge below) is the paper's
+// associative, commutative LSE operation written in this (m, s) form.
+//
+// Exponentials use base 2 (ex2.approx.ftz.f32, one SFU op) on the argument
+// (x - mu) * log2 e; the final log uses lg2.approx.ftz.f32 times ln 2.  These
+// are PTX instructions, not CUDA math-library routines.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace lse {
+
+enum : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+template <int DT> struct DType;
+template <> struct DType<kF32>  { static constexpr int bytes = 4; };
+template <> struct DType<kBF16> { static constexpr int bytes = 2; };
+template <> struct DType<kF16>  { static constexpr int bytes = 2; };
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
+
+// Bit patterns of -inf: one f32, or two packed 16-bit elements.
+constexpr uint32_t kNegInfF32 = 0xff800000u;
+constexpr uint32_t kNegInfBF16x2 = 0xff80ff80u;
+constexpr uint32_t kNegInfF16x2 = 0xfc00fc00u;
+
+template <int DT> __device__ __forceinline__ constexpr uint32_t neg_inf_word() {
+    return DT == kF32 ? kNegInfF32 : (DT == kBF16 ? kNegInfBF16x2 : kNegInfF16x2);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Three-input maximum (sm_100+ PTX); a NaN operand is ignored like in max.f32.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed maxima of two 16-bit lanes; NaN lanes are ignored.
+__device__ __forceinline__ uint32_t hmax2_bf16(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmax2_f16(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 16-byte streaming load through the read-only path, no L1 allocation, with a
+// 256-byte L2 prefetch hint (rows are read exactly once).
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Exact conversion of one element at element index i of a row.
+template <int DT> __device__ __forceinline__ float load_elem(const void* row, int64_t i);
+template <> __device__ __forceinline__ float load_elem<kF32>(const void* row, int64_t i) {
+    return __ldg(reinterpret_cast<const float*>(row) + i);
+}
+template <> __device__ __forceinline__ float load_elem<kBF16>(const void* row, int64_t i) {
+    const uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+    return __uint_as_float(h << 16);
+}
+template <> __device__ __forceinline__ float load_elem<kF16>(const void* row, int64_t i) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+    return __half2float(__ushort_as_half(h));
+}
+
+// Low / high element of a 32-bit word holding one f32 or two 16-bit elements.
+template <int DT> __device__ __forceinline__ float word_lo(uint32_t w);
+template <int DT> __device__ __forceinline__ float word_hi(uint32_t w);
+template <> __device__ __forceinline__ float word_lo<kBF16>(uint32_t w) { return __uint_as_float(w << 16); }
+template <> __device__ __forceinline__ float word_hi<kBF16>(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+template <> __device__ __forceinline__ float word_lo<kF16>(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+template <> __device__ __forceinline__ float word_hi<kF16>(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// The shift mu for a maximum m (see the header comment).
+__device__ __forceinline__ float shift_of(float m) {
+    return fabsf(m) < __int_as_float(0x7f800000) ? m : 0.0f;
+}
+
+struct Acc {
+    float m;  // running maximum (never NaN)
+    float s;  // sum of 2^((x - shift_of(m)) log2 e)
+};
+
+__device__ __forceinline__ Acc acc_identity() { return Acc{__int_as_float(kNegInfF32), 0.0f}; }
+
+// Pairwise LSE on two accumulators.
+__device__ __forceinline__ Acc acc_merge(Acc a, Acc b) {
+    const float m = fmaxf(a.m, b.m);
+    const float mu = shift_of(m);
+    const float s = a.s * ex2((a.m - mu) * kLog2e) + b.s * ex2((b.m - mu) * kLog2e);
+    return Acc{m, s};
+}
+
+// log(sum exp) of a finished accumulator, with the special-value rules.
+__device__ __forceinline__ float acc_finalize(Acc a) {
+    if (a.s != a.s) return a.s;                       // NaN in the row
+    if (a.m == __int_as_float(0x7f800000)) return a.m;  // +inf
+    if (a.m == __int_as_float(kNegInfF32)) return a.m;  // all -inf, or empty
+    return a.m + kLn2 * lg2(a.s);
+}
+
+// Butterfly merge across `width` lanes (power of two <= 32); every lane of the
+// group ends with the group's accumulator.  The merge order is fixed, so the
+// result is deterministic.
+template <int WIDTH>
+__device__ __forceinline__ Acc warp_merge(Acc a) {
+#pragma unroll
+    for (int off = WIDTH / 2; off > 0; off >>= 1) {
+        Acc b;
+        b.m = __shfl_xor_sync(0xffffffffu, a.m, off);
+        b.s = __shfl_xor_sync(0xffffffffu, a.s, off);
+        a = acc_merge(a, b);
+    }
+    return a;
+}
+
+// Raise the running maximum to cm (a chunk maximum), rescaling s once.
+__device__ __forceinline__ void acc_raise(Acc& a, float& mu, float cm) {
+    if (cm > a.m) {
+        const float mu_new = shift_of(cm);
+        a.s *= ex2((a.m - mu_new) * kLog2e);
+        a.m = cm;
+        mu = mu_new;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Chunks of raw 32-bit words (one f32 or two packed 16-bit elements each).
+// ---------------------------------------------------------------------------
+
+// Maximum over W raw words.
+template <int DT, int W>
+__device__ __forceinline__ float words_max(const uint32_t (&w)[W]) {
+    if constexpr (DT == kF32) {
+        float m = __uint_as_float(w[0]);
+        int i = 1;
+#pragma unroll
+        for (; i + 1 < W; i += 2) m = fmax3(m, __uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+#pragma unroll
+        for (; i < W; ++i) m = fmaxf(m, __uint_as_float(w[i]));
+        return m;
+    } else {
+        // Packed pairwise tree on the 16-bit lanes, then the two halves.
+        uint32_t t[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) t[i] = w[i];
+#pragma unroll
+        for (int stride = 1; stride < W; stride *= 2) {
+#pragma unroll
+            for (int i = 0; i + stride < W; i += 2 * stride)
+                t[i] = DT == kBF16 ? hmax2_bf16(t[i], t[i + stride]) : hmax2_f16(t[i], t[i + stride]);
+        }
+        return fmaxf(word_lo<DT>(t[0]), word_hi<DT>(t[0]));
+    }
+}
+
+// sum of 2^((x - mu) log2 e) over W raw words (pairwise add tree).
+template <int DT, int W>
+__device__ __forceinline__ float words_expsum(const uint32_t (&w)[W], float mu) {
+    constexpr int E = DT == kF32 ? W : 2 * W;
+    float e[E];
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        if constexpr (DT == kF32) {
+            e[i] = ex2((__uint_as_float(w[i]) - mu) * kLog2e);
+        } else {
+            e[2 * i] = ex2((word_lo<DT>(w[i]) - mu) * kLog2e);
+            e[2 * i + 1] = ex2((word_hi<DT>(w[i]) - mu) * kLog2e);
+        }
+    }
+#pragma unroll
+    for (int stride = 1; stride < E; stride *= 2) {
+#pragma unroll
+        for (int i = 0; i + stride < E; i += 2 * stride) e[i] += e[i + stride];
+    }
+    return e[0];
+}
+
+// Fold a chunk of W raw words into an accumulator.
+template <int DT, int W>
+__device__ __forceinline__ void acc_add_words(Acc& a, float& mu, const uint32_t (&w)[W]) {
+    acc_raise(a, mu, words_max<DT, W>(w));
+    a.s += words_expsum<DT, W>(w, mu);
+}
+
+// Fold a chunk of K converted floats into an accumulator.
+template <int K>
+__device__ __forceinline__ void acc_add_floats(Acc& a, float& mu, const float (&v)[K]) {
+    float cm = v[0];
+#pragma unroll
+    for (int i = 1; i < K; ++i) cm = fmaxf(cm, v[i]);
+    acc_raise(a, mu, cm);
+    float e[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) e[i] = ex2((v[i] - mu) * kLog2e);
+#pragma unroll
+    for (int stride = 1; stride < K; stride *= 2) {
+#pragma unroll
+        for (int i = 0; i + stride < K; i += 2 * stride) e[i] += e[i + stride];
+    }
+    a.s += e[0];
+}
+
+}  // namespace lse

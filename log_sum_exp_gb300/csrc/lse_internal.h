@@ -1,0 +1,39 @@
+// lse_internal.h -- declarations shared by the host dispatcher and the
+// per-element-type kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lse {
+
+constexpr int kSubwarpThreads = 256;
+
+struct LaunchArgs {
+    const void* x;
+    int64_t B;
+    int64_t N;
+    int64_t row_stride;  // elements
+    float* out;
+    cudaStream_t stream;
+};
+
+// Per element type (f32 / bf16 / f16): launchers and occupancy queries.
+#define LSE_DECLARE_TYPE_ENTRY_POINTS(SUFFIX)                                                  \
+    cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
+                                        int64_t grid);                                         \
+    cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
+                                        int64_t seg_slots, float2* partial);                   \
+    int segment_occupancy_##SUFFIX(bool vec, int threads);                                     \
+    int subwarp_occupancy_##SUFFIX(bool vec);
+
+LSE_DECLARE_TYPE_ENTRY_POINTS(f32)
+LSE_DECLARE_TYPE_ENTRY_POINTS(bf16)
+LSE_DECLARE_TYPE_ENTRY_POINTS(f16)
+
+// Type-independent kernels (lse_api.cu).
+cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream);
+cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
+                         cudaStream_t stream);
+
+}  // namespace lse

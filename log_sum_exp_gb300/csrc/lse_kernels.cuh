@@ -1,0 +1,332 @@
+// lse_kernels.cuh -- the row-wise log-sum-exp kernels (sm_103a).
+//
+// One pass over x: every element is loaded once with coalesced 128-bit loads
+// (scalar loads when rows are not 16-byte aligned), folded into a register
+// accumulator, and each row writes one float ("Speeding up Log-Sum-Exp ...",
+// Sec. 3.1).  Three mappings:
+//   subwarp  rows of at most 32*4 vectors: G lanes per row hold the whole row
+//            in registers; max first, then the exp-sum (two passes over
+//            registers, one over HBM); lanes combine by xor shuffles.
+//   segment  one CTA per (row, segment): online (m, s) accumulation over
+//            batches of 8 vectors per thread, then warp shuffles and shared
+//            memory.  With one segment per row it writes out[row]; with P > 1
+//            segments it writes an (m, s) partial that lse_merge_kernel
+//            combines (the split-row mapping for long rows or few rows).
+// This header is included by one translation unit per element type.
+#pragma once
+
+#include "lse_device.cuh"
+#include "lse_internal.h"
+
+namespace lse {
+
+// Raw 32-bit words of up to 4 tail elements (fewer than one vector) starting at
+// element `start`, padded with -inf; 16-bit elements are packed in pairs.
+template <int DT>
+__device__ __forceinline__ void load_tail_words(const void* row, int64_t start, int count,
+                                                uint32_t (&w)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = neg_inf_word<DT>();
+    if constexpr (DT == kF32) {
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + start;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < count) w[i] = __ldg(p + i);
+    } else {
+        const unsigned short* p = reinterpret_cast<const unsigned short*>(row) + start;
+        const uint32_t ninf_half = neg_inf_word<DT>() & 0xffffu;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t h = i < count ? static_cast<uint32_t>(__ldg(p + i)) : ninf_half;
+            if (i & 1)
+                w[i >> 1] = (w[i >> 1] & 0xffffu) | (h << 16);
+            else
+                w[i >> 1] = (w[i >> 1] & 0xffff0000u) | h;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// subwarp: G lanes per row, V slots per lane, R row-groups per warp iteration.
+// VEC: a slot is one 16-byte vector (the lane holding vector index N/EPV also
+// loads the < EPV tail elements); !VEC: a slot is one element.
+// ---------------------------------------------------------------------------
+template <int DT, int G, int V, bool VEC>
+__global__ void __launch_bounds__(kSubwarpThreads)
+lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
+                   float* __restrict__ out) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = VEC ? 16 / EB : 1;  // elements per slot
+    constexpr int RPW = 32 / G;             // rows per warp per row-group
+    constexpr int R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (G - 1);
+    const int grp = lane / G;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nv = N / EPV;                        // full slots per row
+    const int tail = static_cast<int>(N - nv * EPV);   // VEC only: 0 .. EPV-1
+    const char* xb = reinterpret_cast<const char*>(x);
+
+    for (int64_t row0 = warp * (RPW * R); row0 < B; row0 += nwarps * (RPW * R)) {
+        if constexpr (VEC) {
+            uint32_t w[R][4 * V];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = row0 + r * RPW + grp;
+                const char* rp = xb + row * row_stride * EB;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const int64_t k = sub + j * G;
+                    uint32_t q[4];
+                    if (row < B && k < nv) {
+                        const uint4 u = ldg_stream16(rp + k * 16);
+                        q[0] = u.x; q[1] = u.y; q[2] = u.z; q[3] = u.w;
+                    } else if (row < B && k == nv && tail > 0) {
+                        load_tail_words<DT>(rp, nv * EPV, tail, q);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) q[i] = neg_inf_word<DT>();
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = row0 + r * RPW + grp;
+                float m = words_max<DT, 4 * V>(w[r]);
+#pragma unroll
+                for (int off = G / 2; off > 0; off >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                float s = words_expsum<DT, 4 * V>(w[r], shift_of(m));
+#pragma unroll
+                for (int off = G / 2; off > 0; off >>= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (sub == 0 && row < B) out[row] = acc_finalize(Acc{m, s});
+            }
+        } else {
+            float v[R][V];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = row0 + r * RPW + grp;
+                const char* rp = xb + row * row_stride * EB;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const int64_t k = sub + j * G;
+                    v[r][j] = (row < B && k < N) ? load_elem<DT>(rp, k)
+                                                 : __int_as_float(kNegInfF32);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = row0 + r * RPW + grp;
+                float m = v[r][0];
+#pragma unroll
+                for (int j = 1; j < V; ++j) m = fmaxf(m, v[r][j]);
+#pragma unroll
+                for (int off = G / 2; off > 0; off >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                const float mu = shift_of(m);
+                float s = 0.0f;
+#pragma unroll
+                for (int j = 0; j < V; ++j) s += ex2((v[r][j] - mu) * kLog2e);
+#pragma unroll
+                for (int off = G / 2; off > 0; off >>= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (sub == 0 && row < B) out[row] = acc_finalize(Acc{m, s});
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// segment: blockIdx.x = row * P + seg.  Segment seg covers slots
+// [seg * seg_slots, min(nv, (seg + 1) * seg_slots)) of its row; the last
+// segment also takes the < EPV tail elements (VEC only).
+// ---------------------------------------------------------------------------
+template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
+
+template <int DT, int T, bool VEC>
+__global__ void __launch_bounds__(T, SegmentOccupancy<T>::min_blocks)
+lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, int64_t P,
+                   int64_t seg_slots, float* __restrict__ out, float2* __restrict__ partial) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = VEC ? 16 / EB : 1;
+    constexpr int U = VEC ? 8 : 16;  // slots per thread per batch
+    constexpr int NW = T / 32;
+
+    if (P > 1) asm volatile("griddepcontrol.launch_dependents;");
+
+    const int64_t unit = blockIdx.x;
+    const int64_t row = unit / P;
+    const int64_t seg = unit - row * P;
+    const int64_t nv = N / EPV;
+    const int64_t s_begin = seg * seg_slots;
+    const int64_t s_end = s_begin + seg_slots < nv ? s_begin + seg_slots : nv;
+    const char* rp = reinterpret_cast<const char*>(x) + row * row_stride * EB;
+
+    Acc acc = acc_identity();
+    float mu = 0.0f;
+    int64_t k = s_begin + threadIdx.x;
+
+    if constexpr (VEC) {
+        for (; k + (U - 1) * T < s_end; k += U * T) {
+            uint32_t w[4 * U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const uint4 u = ldg_stream16(rp + (k + j * T) * 16);
+                w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+            }
+            acc_add_words<DT, 4 * U>(acc, mu, w);
+        }
+        if (k < s_end) {
+            uint32_t w[4 * U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t kk = k + j * T;
+                if (kk < s_end) {
+                    const uint4 u = ldg_stream16(rp + kk * 16);
+                    w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
+                }
+            }
+            acc_add_words<DT, 4 * U>(acc, mu, w);
+        }
+        const int tail = static_cast<int>(N - nv * EPV);
+        if (tail > 0 && seg == P - 1 && threadIdx.x == 0) {
+            uint32_t w[4];
+            load_tail_words<DT>(rp, nv * EPV, tail, w);
+            acc_add_words<DT, 4>(acc, mu, w);
+        }
+    } else {
+        for (; k + (U - 1) * T < s_end; k += U * T) {
+            float v[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) v[j] = load_elem<DT>(rp, k + j * T);
+            acc_add_floats<U>(acc, mu, v);
+        }
+        if (k < s_end) {
+            float v[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t kk = k + j * T;
+                v[j] = kk < s_end ? load_elem<DT>(rp, kk) : __int_as_float(kNegInfF32);
+            }
+            acc_add_floats<U>(acc, mu, v);
+        }
+    }
+
+    acc = warp_merge<32>(acc);
+    if constexpr (NW > 1) {
+        __shared__ float2 part[NW];
+        const int wid = threadIdx.x >> 5;
+        const int lane = threadIdx.x & 31;
+        if (lane == 0) part[wid] = make_float2(acc.m, acc.s);
+        __syncthreads();
+        if (wid == 0) {
+            acc = lane < NW ? Acc{part[lane].x, part[lane].y} : acc_identity();
+            acc = warp_merge<NW>(acc);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (P == 1)
+            out[row] = acc_finalize(acc);
+        else
+            partial[unit] = make_float2(acc.m, acc.s);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers for one element type.
+// ---------------------------------------------------------------------------
+template <int DT, int G, int V, bool VEC>
+cudaError_t launch_subwarp_gv(const LaunchArgs& a, int64_t grid) {
+    lse_subwarp_kernel<DT, G, V, VEC><<<static_cast<unsigned>(grid), kSubwarpThreads, 0, a.stream>>>(
+        a.x, a.B, a.N, a.row_stride, a.out);
+    return cudaGetLastError();
+}
+
+template <int DT, int G, bool VEC>
+cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
+    switch (V) {
+    case 1: return launch_subwarp_gv<DT, G, 1, VEC>(a, grid);
+    case 2: return launch_subwarp_gv<DT, G, 2, VEC>(a, grid);
+    case 4: return launch_subwarp_gv<DT, G, 4, VEC>(a, grid);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_subwarp_dt(const LaunchArgs& a, int G, int V, int64_t grid) {
+    switch (G) {
+    case 1: return launch_subwarp_g<DT, 1, VEC>(a, V, grid);
+    case 2: return launch_subwarp_g<DT, 2, VEC>(a, V, grid);
+    case 4: return launch_subwarp_g<DT, 4, VEC>(a, V, grid);
+    case 8: return launch_subwarp_g<DT, 8, VEC>(a, V, grid);
+    case 16: return launch_subwarp_g<DT, 16, VEC>(a, V, grid);
+    case 32: return launch_subwarp_g<DT, 32, VEC>(a, V, grid);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int DT, int T, bool VEC>
+cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial) {
+    const int64_t grid = a.B * P;
+    lse_segment_kernel<DT, T, VEC><<<static_cast<unsigned>(grid), T, 0, a.stream>>>(
+        a.x, a.N, a.row_stride, P, seg_slots, a.out, partial);
+    return cudaGetLastError();
+}
+
+template <int DT, int T, bool VEC>
+int segment_occupancy_t() {
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC>, T, 0) !=
+        cudaSuccess)
+        return 0;
+    return blocks;
+}
+
+template <int DT, int G, int V, bool VEC>
+int subwarp_occupancy_gv() {
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_subwarp_kernel<DT, G, V, VEC>,
+                                                      kSubwarpThreads, 0) != cudaSuccess)
+        return 0;
+    return blocks;
+}
+
+}  // namespace lse
+
+// Instantiates the per-type entry points declared in lse_internal.h.
+#define LSE_DEFINE_TYPE_ENTRY_POINTS(DT, SUFFIX)                                               \
+    namespace lse {                                                                            \
+    cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
+                                        int64_t grid) {                                        \
+        return vec ? launch_subwarp_dt<DT, true>(a, G, V, grid)                                \
+                   : launch_subwarp_dt<DT, false>(a, G, V, grid);                              \
+    }                                                                                          \
+    cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
+                                        int64_t seg_slots, float2* partial) {                  \
+        if (threads == 32)                                                                     \
+            return vec ? launch_segment_t<DT, 32, true>(a, P, seg_slots, partial)              \
+                       : launch_segment_t<DT, 32, false>(a, P, seg_slots, partial);            \
+        if (threads == 256)                                                                    \
+            return vec ? launch_segment_t<DT, 256, true>(a, P, seg_slots, partial)             \
+                       : launch_segment_t<DT, 256, false>(a, P, seg_slots, partial);           \
+        return cudaErrorInvalidValue;                                                          \
+    }                                                                                          \
+    int segment_occupancy_##SUFFIX(bool vec, int threads) {                                    \
+        if (threads == 32) return vec ? segment_occupancy_t<DT, 32, true>()                    \
+                                      : segment_occupancy_t<DT, 32, false>();                  \
+        if (threads == 256) return vec ? segment_occupancy_t<DT, 256, true>()                  \
+                                       : segment_occupancy_t<DT, 256, false>();                \
+        return 0;                                                                              \
+    }                                                                                          \
+    int subwarp_occupancy_##SUFFIX(bool vec) {                                                 \
+        return vec ? subwarp_occupancy_gv<DT, 8, 1, true>()                                    \
+                   : subwarp_occupancy_gv<DT, 8, 1, false>();                                  \
+    }                                                                                          \
+    }

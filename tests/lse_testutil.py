@@ -1,0 +1,83 @@
+"""Helpers shared by the GPU tests: tolerance check and device layouts."""
+from __future__ import annotations
+
+import numpy as np
+
+# Parity bar for finite outputs: |gpu - oracle| <= ATOL + RTOL * |oracle|;
+# NaN and +-inf must match exactly.
+ATOL = 1e-5
+RTOL = 1e-6
+
+
+def compare(got: np.ndarray, want: np.ndarray, atol: float = ATOL, rtol: float = RTOL) -> dict:
+    """Compare float32 GPU results with float64 oracle values; return a summary."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    nan_w, nan_g = np.isnan(want), np.isnan(got)
+    bad_nan = np.flatnonzero(nan_w != nan_g)
+    inf_w = np.isinf(want)
+    bad_inf = np.flatnonzero(inf_w & ~nan_g & (got != want))
+    fin = ~nan_w & ~inf_w
+    err = np.abs(got[fin] - want[fin])
+    lim = atol + rtol * np.abs(want[fin])
+    bad_fin = np.flatnonzero(fin)[~(err <= lim)]
+    summary = {
+        "n": int(got.size),
+        "finite": int(fin.sum()),
+        "max_abs_err": float(err.max()) if err.size else 0.0,
+        "max_err_over_tol": float((err / lim).max()) if err.size else 0.0,
+    }
+    if bad_nan.size or bad_inf.size or bad_fin.size:
+        idx = np.concatenate([bad_nan, bad_inf, bad_fin])[:8]
+        detail = [(int(i), float(got[i]), float(want[i])) for i in idx]
+        raise AssertionError(f"{bad_nan.size} NaN mismatches, {bad_inf.size} inf mismatches, "
+                             f"{bad_fin.size} out of tolerance; first: {detail}; {summary}")
+    return summary
+
+
+def torch_view(x: np.ndarray, dtype: str):
+    """A torch CPU tensor with the raw bits of ``x`` in the matching dtype."""
+    import torch
+
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    if dtype == "f16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.float16)
+    raise ValueError(dtype)
+
+
+NAN_BITS = {"f32": None, "bf16": 0x7FC0, "f16": 0x7E00}
+
+
+def canary_array(shape, dtype: str) -> np.ndarray:
+    """A host array of NaNs (raw bits for 16-bit types)."""
+    if dtype == "f32":
+        return np.full(shape, np.nan, dtype=np.float32)
+    return np.full(shape, NAN_BITS[dtype], dtype=np.uint16)
+
+
+def device_rows(x: np.ndarray, dtype: str, row_stride: int | None = None, offset: int = 0,
+                device: str = "cuda"):
+    """Place [B, N] rows on the device inside a NaN-filled buffer.
+
+    Rows start ``offset`` elements into the buffer, ``row_stride`` apart; every
+    element outside the rows (padding, before, after) is NaN, so a kernel that
+    reads outside [0, N) of a row returns NaN for it.  Returns (buffer, view).
+    """
+    import torch
+
+    B, N = x.shape
+    row_stride = N if row_stride is None else row_stride
+    total = offset + B * row_stride + 64
+    host = canary_array(total, dtype)
+    if B:
+        body = host[offset:offset + B * row_stride].reshape(B, row_stride)
+        body[:, :N] = x
+    buf = torch_view(host, dtype).to(device)
+    if B == 0:
+        return buf, buf[offset:offset].reshape(0, N)
+    view = buf[offset:offset + B * row_stride].reshape(B, row_stride)[:, :N]
+    return buf, view

@@ -1,0 +1,283 @@
+"""GPU parity: liblse (through its C ABI) against the fp64 oracle.
+
+Every finite output must satisfy |gpu - oracle| <= 1e-5 + 1e-6 |oracle|; NaN
+and +-inf must match exactly.  Inputs come from the seeded generators and are
+handed unchanged to both sides.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from log_sum_exp_gb300 import workloads as wl
+from lse_testutil import compare, device_rows, torch_view
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import log_sum_exp_gb300 as L  # noqa: E402
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run(x_view, plan=None, canary=16):
+    """Run lse_forward_plan into a NaN-canaried output buffer; return (out, plan)."""
+    B = x_view.shape[0]
+    out_buf = torch.full((B + canary,), float("nan"), dtype=torch.float32, device=x_view.device)
+    out, p = L.lse_forward_plan(x_view, plan=plan, out=out_buf[:B])
+    torch.cuda.synchronize()
+    tail = out_buf[B:].cpu().numpy()
+    assert np.all(np.isnan(tail)), "write past out[B-1]"
+    return out.cpu().numpy(), p
+
+
+# ---------------------------------------------------------------------------
+# The five workloads at full size, automatic plan.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("key", wl.ORDER)
+def test_workload_full_size(key):
+    _need_gpu()
+    w = wl.WORKLOADS[key]
+    x = wl.generate(key)
+    want = oracle.lse(x, w.dtype)
+    xd = torch_view(x, w.dtype).cuda()
+    got, p = run(xd)
+    s = compare(got, want)
+    print(key, p.as_dict(), s)
+    del xd
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Edge shapes x dtypes x layouts x every mapping.
+# ---------------------------------------------------------------------------
+LENGTHS = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255,
+           256, 257, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097,
+           8191, 12345, 65537, 131073]
+
+
+def plans_for(N, dtype, vec):
+    eb = 4 if dtype == "f32" else 2
+    epv = 16 // eb if vec else 1
+    nvt = -(-N // epv)
+    slots = N // epv if vec else N
+    plans = [None]
+    vb = 16 if vec else 1
+    if nvt <= 128:
+        G = 1
+        while G <= 32:
+            if -(-nvt // G) <= 4:
+                plans.append({"path": "subwarp", "lanes_per_row": G, "vector_bytes": vb})
+            G *= 2
+    if slots >= 1:
+        plans.append({"path": "cta", "threads": 32, "vector_bytes": vb})
+        plans.append({"path": "cta", "threads": 256, "vector_bytes": vb})
+    for P, T in ((2, 256), (3, 32), (7, 256), (64, 32)):
+        if slots >= P:
+            plans.append({"path": "split", "splits": P, "threads": T, "vector_bytes": vb})
+    return plans
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", LENGTHS)
+def test_edge_shapes(dtype, N):
+    _need_gpu()
+    B = 5
+    x = wl.random_rows(B, N, dtype, seed=N, scale=6.0, shift=-2.0)
+    # A special value in some rows at the first / last / middle position.
+    if N >= 3:
+        xi = x.view(np.uint16) if dtype != "f32" else x
+        ninf = {"f32": -np.inf, "bf16": 0xFF80, "f16": 0xFC00}[dtype]
+        pinf = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+        nan = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+        xi[1, N - 1] = nan
+        xi[2, 0] = pinf
+        xi[3, :] = ninf
+        xi[4, N // 2] = ninf
+    want = oracle.lse(x, dtype)
+    eb = 4 if dtype == "f32" else 2
+    layouts = [(N, 0), (N + 8, 0), (N + 1, 0), (N, 1)]
+    for row_stride, offset in layouts:
+        buf, xv = device_rows(x, dtype, row_stride=row_stride, offset=offset)
+        vec = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
+        for plan in plans_for(N, dtype, vec):
+            got, p = run(xv, plan)
+            try:
+                compare(got, want)
+            except AssertionError as e:
+                raise AssertionError(f"layout stride={row_stride} offset={offset} "
+                                     f"plan={plan} ran={p.as_dict()}: {e}") from None
+
+
+def test_scalar_path_forced_on_aligned_rows():
+    _need_gpu()
+    for dtype in ("f32", "bf16", "f16"):
+        x = wl.random_rows(9, 3001, dtype, seed=3)
+        want = oracle.lse(x, dtype)
+        _, xv = device_rows(x, dtype)
+        for plan in ({"vector_bytes": 1}, {"path": "split", "splits": 4, "vector_bytes": 1}):
+            got, p = run(xv, plan)
+            assert p.vector_bytes == 1
+            compare(got, want)
+
+
+# ---------------------------------------------------------------------------
+# Degenerate sizes and special values.
+# ---------------------------------------------------------------------------
+def test_empty_rows_give_neg_inf():
+    _need_gpu()
+    for dtype in ("f32", "bf16", "f16"):
+        x = np.zeros((7, 0), dtype=np.float32 if dtype == "f32" else np.uint16)
+        _, xv = device_rows(x, dtype)
+        got, p = run(xv)
+        assert p.as_dict()["path"] == "empty"
+        assert np.all(got == -np.inf)
+
+
+def test_zero_rows_is_noop():
+    _need_gpu()
+    x = torch.empty((0, 100), device="cuda")
+    out = L.lse_forward(x)
+    assert out.shape == (0,)
+
+
+def test_single_element_rows_exact():
+    """N = 1: the result is the element itself (every bf16 / f16 bit pattern)."""
+    _need_gpu()
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(-1, 1)
+    for dtype in ("bf16", "f16"):
+        want = oracle.lse(bits, dtype)
+        got, _ = run(torch_view(bits, dtype).cuda())
+        compare(got, want, atol=0.0, rtol=0.0)
+
+
+def test_extreme_magnitudes():
+    _need_gpu()
+    big = np.float32(3.0e38)
+    rows = [
+        [big, big], [-big, big], [big, -np.inf], [-big, -big],
+        [1e-40, -1e-40], [0.0, -0.0], [-1e30, -1e30 + 1e24], [88.7, 88.7, 88.7],
+        [-103.0, -103.0], [np.inf, -np.inf], [np.nan, -np.inf], [-np.inf, np.nan],
+    ]
+    n = max(len(r) for r in rows)
+    x = np.full((len(rows), n), -np.inf, dtype=np.float32)
+    for i, r in enumerate(rows):
+        x[i, :len(r)] = r
+    want = oracle.lse(x)
+    for plan in (None, {"path": "cta", "threads": 32}, {"path": "cta", "threads": 256}):
+        got, _ = run(torch.from_numpy(x).cuda(), plan)
+        compare(got, want)
+
+
+def test_special_value_in_every_split_segment():
+    """NaN / +inf / only -inf inside one segment of a split row."""
+    _need_gpu()
+    N, P = 40000, 8
+    base = wl.random_rows(1, N, "f32", seed=21)[0]
+    cases = []
+    for seg in range(P):
+        pos = seg * (N // P) + 17
+        for val in (np.nan, np.inf):
+            r = base.copy()
+            r[pos] = val
+            cases.append(r)
+    r = np.full(N, -np.inf, np.float32)
+    r[N - 1] = 3.0
+    cases.append(r)
+    x = np.stack(cases)
+    want = oracle.lse(x)
+    got, p = run(torch.from_numpy(x).cuda(), {"path": "split", "splits": P, "threads": 256})
+    assert p.splits == P
+    compare(got, want)
+
+
+def test_deterministic():
+    _need_gpu()
+    x = torch.from_numpy(wl.generate("vocab_512x128256_f32", B=64)).cuda()
+    a = L.lse_forward(x).cpu().numpy()
+    for _ in range(3):
+        assert np.array_equal(L.lse_forward(x).cpu().numpy(), a)
+
+
+def test_one_dimensional_input():
+    _need_gpu()
+    x = wl.random_rows(1, 777, "f32", seed=2)
+    got = L.lse_forward(torch.from_numpy(x[0]).cuda())
+    assert got.shape == ()
+    compare(np.array([got.item()]), oracle.lse(x))
+
+
+def test_plan_query_matches_forward():
+    _need_gpu()
+    for key in wl.ORDER:
+        w = wl.WORKLOADS[key]
+        q = L.lse_plan_query(dtype=w.dtype, B=w.B, N=w.N)
+        assert q["launches"] in (1, 2)
+        if key.startswith("short"):
+            assert q["path"] == "subwarp"
+        if key.startswith("particles"):
+            assert q["path"] == "split"
+
+
+def test_invalid_arguments_raise():
+    _need_gpu()
+    x = torch.zeros((4, 8), device="cuda")
+    out = torch.empty(4, device="cuda")
+    with pytest.raises(L.LseError) as e:
+        L.lse_forward_ptr(x.data_ptr(), "f32", 4, 8, 7, out.data_ptr())
+    assert e.value.status == 1
+    with pytest.raises(L.LseError):
+        L.lse_forward_ptr(x.data_ptr(), "f32", 4, 8, 8, out.data_ptr() + 2)
+    with pytest.raises(L.LseError):
+        L.lse_forward_plan(x, plan={"path": "subwarp", "lanes_per_row": 3})
+    with pytest.raises(L.LseError):
+        L.lse_forward_plan(x, plan={"path": "split", "splits": 100})
+    assert L.load().lse_forward(x.data_ptr(), 7, 4, 8, 8, out.data_ptr(), None) == 2
+    with pytest.raises(ValueError):
+        L.lse_forward(x.t())  # last dimension not unit-stride
+
+
+def test_host_entry_point_matches_device():
+    _need_gpu()
+    x = wl.generate("vocab_512x128256_f32", B=32)
+    want = oracle.lse(x)
+    xt = torch.from_numpy(x).pin_memory()
+    got = L.lse_forward_host(xt).numpy()
+    compare(got, want)
+    got2 = L.lse_forward_host(torch.from_numpy(x)).numpy()  # pageable
+    assert np.array_equal(got, got2)
+
+
+def test_cuda_graph_capture_and_replay():
+    _need_gpu()
+    for key, B in (("small_64x4096_f32", None), ("particles_16x16777216_f32", 2)):
+        w = wl.WORKLOADS[key]
+        N = w.N if B is None else 1 << 20
+        x = wl.generate(key, B=B, N=N)
+        xd = torch.from_numpy(x).cuda()
+        out = torch.empty(x.shape[0], device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            L.lse_forward(xd, out=out)  # warm-up outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            L.lse_forward(xd, out=out)
+        out.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        compare(out.cpu().numpy(), oracle.lse(x))
+
+
+def test_tolerance_bar_is_met_with_margin():
+    """The worst finite error on the long split rows stays below half the bar."""
+    _need_gpu()
+    x = wl.generate("particles_16x16777216_f32", B=4)
+    s = compare(run(torch.from_numpy(x).cuda())[0], oracle.lse(x))
+    assert s["max_err_over_tol"] < 0.5, s
+    assert math.isfinite(s["max_abs_err"])

@@ -101,9 +101,11 @@ typedef struct {
 /*
  * lse_forward -- out[b] = log sum_n exp(x[b, n]) on the GPU, one pass over x.
  * Device pointers; asynchronous on `stream`.  The split-row mapping takes
- * B * splits * 8 bytes of scratch with cudaMallocAsync / cudaFreeAsync on
- * `stream` (stream-ordered, so concurrent calls on different streams do not
- * share it).
+ * B * splits * 8 bytes of scratch, allocated and freed stream-ordered on
+ * `stream` (so concurrent calls on different streams never share it).
+ * Every kernel is launched with programmatic dependent launch: it may become
+ * resident while the previous kernel in `stream` finishes, and waits on the
+ * device for that kernel to complete before touching memory.
  */
 LSE_API lse_status lse_forward(const void *x, lse_dtype dtype, int64_t B, int64_t N,
                        int64_t row_stride, float *out, lse_stream_t stream);
@@ -135,6 +137,16 @@ LSE_API lse_status lse_forward_plan(const void *x, lse_dtype dtype, int64_t B, i
  */
 LSE_API lse_status lse_forward_host(const void *x_host, lse_dtype dtype, int64_t B, int64_t N,
                             int64_t row_stride, float *out_host, lse_stream_t stream);
+
+/*
+ * lse_trim_memory -- return the current device's cached stream-ordered memory
+ * to the system.  Split-row scratch and lse_forward_host's staging buffers come
+ * from a library-owned memory pool that keeps freed blocks mapped for reuse by
+ * later calls (while a stream is being captured into a CUDA graph, the
+ * device's default pool is used instead).  Call after synchronising every
+ * stream that used the library on this device.
+ */
+LSE_API lse_status lse_trim_memory(void);
 
 /* Short English description of a status code (static storage). */
 LSE_API const char *lse_status_string(lse_status status);

@@ -21,5 +21,6 @@ from ._binding import (  # noqa: F401
     lse_forward_ptr,
     lse_plan_query,
     lse_plan_query_ptr,
+    lse_trim_memory,
     status_string,
 )

@@ -21,7 +21,7 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
-                 "lse_status_string", "lse_last_cuda_error"]
+                 "lse_trim_memory", "lse_status_string", "lse_last_cuda_error"]
 
 
 class LsePlan(ctypes.Structure):
@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.lse_forward_plan.restype = i32
         lib.lse_forward_host.argtypes = [vp, i32, i64, i64, i64, vp, vp]
         lib.lse_forward_host.restype = i32
+        lib.lse_trim_memory.argtypes = []
+        lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
         lib.lse_status_string.restype = ctypes.c_char_p
         lib.lse_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -97,6 +99,11 @@ def _check(status: int, where: str) -> None:
         err = ctypes.c_int(0)
         load().lse_last_cuda_error(ctypes.byref(err))
         raise LseError(status, where, err.value)
+
+
+def lse_trim_memory() -> None:
+    """Release the library's cached device memory on the current device."""
+    _check(load().lse_trim_memory(), "lse_trim_memory")
 
 
 def status_string(status: int) -> str:

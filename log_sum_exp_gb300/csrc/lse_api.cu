@@ -36,6 +36,9 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int seg_occ[3][2][2] = {};  // [dtype][vec][threads == 256]
+    // Library-owned stream-ordered pool: freed blocks stay mapped for reuse by
+    // later calls (release threshold = max) until lse_trim_memory().
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_info_mutex;
@@ -65,6 +68,16 @@ lse_status device_info(int* dev_out, const DeviceInfo** info) {
                     const int occ = segment_occupancy(dt, v != 0, t ? 256 : 32);
                     d.seg_occ[dt][v][t] = occ > 0 ? occ : 1;
                 }
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        e = cudaMemPoolCreate(&d.pool, &props);
+        if (e != cudaSuccess) return cuda_fail(e);
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) return cuda_fail(e);
         d.ready = true;
     }
     *dev_out = dev;
@@ -75,6 +88,17 @@ lse_status device_info(int* dev_out, const DeviceInfo** info) {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int elem_bytes(lse_dtype dt) { return dt == LSE_F32 ? 4 : 2; }
+
+// Stream-ordered device allocation from the library pool.  While `stream` is
+// being captured into a CUDA graph the device's default pool is used instead,
+// so the allocation becomes a graph memory node.
+cudaError_t scratch_alloc(const DeviceInfo& info, void** p, size_t bytes, cudaStream_t stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) return cudaMallocAsync(p, bytes, stream);
+    return cudaMallocFromPoolAsync(p, bytes, info.pool, stream);
+}
 
 bool valid_dtype(int dt) { return dt == LSE_F32 || dt == LSE_BF16 || dt == LSE_F16; }
 
@@ -143,8 +167,11 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
 
     if (path == LSE_PATH_SUBWARP) {
         if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
-        int G = req && req->lanes_per_row ? req->lanes_per_row
-                                          : static_cast<int>(pow2_ceil(nvt < 32 ? nvt : 32));
+        // Fewest lanes per row that keep <= kSubwarpMaxSlots slots per lane:
+        // more independent 16-byte loads in flight per thread.
+        int G = req && req->lanes_per_row
+                    ? req->lanes_per_row
+                    : pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
         if (G < 1 || G > 32 || (G & (G - 1)) != 0) return LSE_ERR_INVALID_ARG;
         int64_t V = ceil_div(nvt, G);
         if (V > kSubwarpMaxSlots) return LSE_ERR_INVALID_ARG;
@@ -165,22 +192,25 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         return LSE_OK;
     }
 
-    // CTA / SPLIT: the segment kernel.
-    const int64_t batch_slots_256 = 256 * (vec ? kSegmentBatchVec : kSegmentBatchScalar);
-    int T = req && req->threads ? req->threads : 0;
-    if (T == 0) T = (nv >= batch_slots_256 || B < 8LL * info.sms) ? 256 : 32;
-    if (T != 32 && T != 256) return LSE_ERR_INVALID_ARG;
-    const int64_t batch = static_cast<int64_t>(T) * (vec ? kSegmentBatchVec : kSegmentBatchScalar);
+    // CTA / SPLIT: the segment kernel.  One-warp CTAs when there are rows
+    // enough to fill the GPU with them and each warp gets >= 4 batches;
+    // otherwise 8-warp CTAs.  Rows are split only when B * threads would not
+    // cover half the GPU's resident threads (a split adds a merge kernel).
+    const int U = vec ? kSegmentBatchVec : kSegmentBatchScalar;
     const int64_t slots = vec ? nv : N;  // slots the segments cover (tail handled separately)
+    int T = req && req->threads ? req->threads : 0;
+    if (T == 0) T = (B >= 16LL * info.sms && slots >= 4LL * 32 * U) ? 32 : 256;
+    if (T != 32 && T != 256) return LSE_ERR_INVALID_ARG;
+    const int64_t batch = static_cast<int64_t>(T) * U;
+    const int64_t resident_threads = static_cast<int64_t>(info.sms) * T *
+                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
     int64_t P = 1;
     if (path == LSE_PATH_SPLIT) {
         if (req && req->splits) {
             P = req->splits;
             if (P < 2 || P > (slots > 0 ? slots : 1)) return LSE_ERR_INVALID_ARG;
         } else {
-            const int64_t resident = static_cast<int64_t>(info.sms) *
-                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
-            P = ceil_div(4 * resident, B);
+            P = ceil_div(4 * resident_threads, B * T);
             const int64_t max_p = slots / batch;
             if (P > max_p) P = max_p;
             if (P < 2) P = 2;
@@ -189,16 +219,11 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         }
     } else {
         if (req && req->splits > 1) return LSE_ERR_INVALID_ARG;
-        if (!req || req->path == LSE_PATH_AUTO) {
-            // Few rows: split them so the grid covers the GPU several times over.
-            const int64_t resident = static_cast<int64_t>(info.sms) *
-                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
-            if (B < 4 * resident) {
-                int64_t want = ceil_div(4 * resident, B);
-                const int64_t max_p = slots / (2 * batch);
-                if (want > max_p) want = max_p;
-                if (want >= 2) P = want;
-            }
+        if ((!req || req->path == LSE_PATH_AUTO) && 2 * B * T < resident_threads) {
+            int64_t want = ceil_div(4 * resident_threads, B * T);
+            const int64_t max_p = slots / (2 * batch);
+            if (want > max_p) want = max_p;
+            if (want >= 2) P = want;
         }
     }
     const int64_t seg_slots = ceil_div(slots, P);
@@ -234,17 +259,20 @@ cudaError_t launch_segment(lse_dtype dt, const LaunchArgs& a, bool vec, int T, i
 }
 
 __global__ void fill_neg_inf_kernel(float* __restrict__ out, int64_t B) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t b = i; b < B; b += stride) out[b] = __int_as_float(kNegInfF32);
 }
 
 // One warp per row: lane l folds partials l, l+32, ... in order, then a fixed
-// butterfly merges the lanes.  Waits (griddepcontrol.wait) until the segment
-// kernel that produced the partials has completed and its writes are visible.
+// butterfly merges the lanes.  pdl_wait() returns once the segment kernel that
+// produced the partials has completed and its writes are visible.
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta)
 merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __restrict__ out) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
+    pdl_wait();
     const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= B) return;  // uniform per warp
@@ -263,26 +291,14 @@ merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __
 cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream) {
     int64_t grid = ceil_div(B, 256);
     if (grid > 65536) grid = 65536;
-    fill_neg_inf_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(out, B);
-    return cudaGetLastError();
+    return launch_pdl(fill_neg_inf_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), stream, out,
+                      B);
 }
 
 cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
                          cudaStream_t stream) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(B, kMergeRowsPerCta)));
-    cfg.blockDim = dim3(32 * kMergeRowsPerCta);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, partial, B, P, out);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(ceil_div(B, kMergeRowsPerCta))),
+                      dim3(32 * kMergeRowsPerCta), stream, partial, B, P, out);
 }
 
 }  // namespace lse
@@ -339,8 +355,8 @@ lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N
     cudaError_t e = cudaSuccess;
     float2* scratch = nullptr;
     if (p.scratch_bytes > 0) {
-        e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), static_cast<size_t>(p.scratch_bytes),
-                            stream);
+        e = scratch_alloc(*info, reinterpret_cast<void**>(&scratch),
+                          static_cast<size_t>(p.scratch_bytes), stream);
         if (e != cudaSuccess) return cuda_fail(e, LSE_ERR_ALLOC);
     }
     if (ev_begin && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev_begin), stream)) != cudaSuccess)
@@ -383,14 +399,19 @@ lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int6
     lse_status st = check_args(x_host, dtype, B, N, row_stride, out_host);
     if (st != LSE_OK) return st;
     if (B == 0) return LSE_OK;
-    const size_t x_bytes = N > 0 ? static_cast<size_t>(((B - 1) * row_stride + N) * elem_bytes(dtype)) : 0;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    if ((st = device_info(&dev, &info)) != LSE_OK) return st;
+    const size_t x_bytes =
+        N > 0 ? static_cast<size_t>(((B - 1) * row_stride + N) * elem_bytes(dtype)) : 0;
     const size_t out_bytes = static_cast<size_t>(B) * sizeof(float);
     void* d_x = nullptr;
     float* d_out = nullptr;
     cudaError_t e = cudaSuccess;
-    if (x_bytes && (e = cudaMallocAsync(&d_x, x_bytes, stream)) != cudaSuccess)
+    if (x_bytes && (e = scratch_alloc(*info, &d_x, x_bytes, stream)) != cudaSuccess)
         return cuda_fail(e, LSE_ERR_ALLOC);
-    if ((e = cudaMallocAsync(reinterpret_cast<void**>(&d_out), out_bytes, stream)) != cudaSuccess) {
+    if ((e = scratch_alloc(*info, reinterpret_cast<void**>(&d_out), out_bytes, stream)) !=
+        cudaSuccess) {
         if (d_x) cudaFreeAsync(d_x, stream);
         return cuda_fail(e, LSE_ERR_ALLOC);
     }
@@ -407,6 +428,15 @@ lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int6
     if (e != cudaSuccess) return cuda_fail(e);
     if (es != cudaSuccess) return cuda_fail(es);
     return LSE_OK;
+}
+
+lse_status lse_trim_memory(void) {
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    lse_status st = device_info(&dev, &info);
+    if (st != LSE_OK) return st;
+    const cudaError_t e = cudaMemPoolTrimTo(info->pool, 0);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
 }  // extern "C"

@@ -114,6 +114,14 @@ template <> __device__ __forceinline__ float word_hi<kF16>(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
+// Programmatic dependent launch.  Every kernel of the library lets the next
+// kernel in its stream launch early (its CTAs become resident and wait), and
+// waits for the previous kernel in its stream to complete, with its memory
+// visible, before the first global access.  Without a programmatic predecessor
+// the wait returns at once.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // The shift mu for a maximum m (see the header comment).
 __device__ __forceinline__ float shift_of(float m) {
     return fabsf(m) < __int_as_float(0x7f800000) ? m : 0.0f;

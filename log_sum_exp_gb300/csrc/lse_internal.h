@@ -3,6 +3,9 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 namespace lse {
@@ -17,6 +20,27 @@ struct LaunchArgs {
     float* out;
     cudaStream_t stream;
 };
+
+// Launch with programmatic stream serialization (see pdl_trigger / pdl_wait in
+// lse_device.cuh): the kernel may start while its predecessor in the stream is
+// finishing, and waits for it on the device before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 // Per element type (f32 / bf16 / f16): launchers and occupancy queries.
 #define LSE_DECLARE_TYPE_ENTRY_POINTS(SUFFIX)                                                  \

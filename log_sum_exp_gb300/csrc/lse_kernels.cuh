@@ -67,6 +67,8 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
     const int64_t nv = N / EPV;                        // full slots per row
     const int tail = static_cast<int>(N - nv * EPV);   // VEC only: 0 .. EPV-1
     const char* xb = reinterpret_cast<const char*>(x);
+    pdl_trigger();
+    pdl_wait();
 
     for (int64_t row0 = warp * (RPW * R); row0 < B; row0 += nwarps * (RPW * R)) {
         if constexpr (VEC) {
@@ -156,7 +158,8 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
     constexpr int U = VEC ? 8 : 16;  // slots per thread per batch
     constexpr int NW = T / 32;
 
-    if (P > 1) asm volatile("griddepcontrol.launch_dependents;");
+    pdl_trigger();
+    pdl_wait();
 
     const int64_t unit = blockIdx.x;
     const int64_t row = unit / P;
@@ -244,9 +247,8 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
 // ---------------------------------------------------------------------------
 template <int DT, int G, int V, bool VEC>
 cudaError_t launch_subwarp_gv(const LaunchArgs& a, int64_t grid) {
-    lse_subwarp_kernel<DT, G, V, VEC><<<static_cast<unsigned>(grid), kSubwarpThreads, 0, a.stream>>>(
-        a.x, a.B, a.N, a.row_stride, a.out);
-    return cudaGetLastError();
+    return launch_pdl(lse_subwarp_kernel<DT, G, V, VEC>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kSubwarpThreads), a.stream, a.x, a.B, a.N, a.row_stride, a.out);
 }
 
 template <int DT, int G, bool VEC>
@@ -275,9 +277,8 @@ cudaError_t launch_subwarp_dt(const LaunchArgs& a, int G, int V, int64_t grid) {
 template <int DT, int T, bool VEC>
 cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial) {
     const int64_t grid = a.B * P;
-    lse_segment_kernel<DT, T, VEC><<<static_cast<unsigned>(grid), T, 0, a.stream>>>(
-        a.x, a.N, a.row_stride, P, seg_slots, a.out, partial);
-    return cudaGetLastError();
+    return launch_pdl(lse_segment_kernel<DT, T, VEC>, dim3(static_cast<unsigned>(grid)), dim3(T),
+                      a.stream, a.x, a.N, a.row_stride, P, seg_slots, a.out, partial);
 }
 
 template <int DT, int T, bool VEC>

@@ -75,7 +75,7 @@ def device_rows(x: np.ndarray, dtype: str, row_stride: int | None = None, offset
     host = canary_array(total, dtype)
     if B:
         body = host[offset:offset + B * row_stride].reshape(B, row_stride)
-        body[:, :N] = x
+        body[:, :N] = x if dtype == "f32" else np.ascontiguousarray(x).view(np.uint16)
     buf = torch_view(host, dtype).to(device)
     if B == 0:
         return buf, buf[offset:offset].reshape(0, N)

@@ -158,6 +158,38 @@ LSE_API const char *lse_status_string(lse_status status);
  */
 LSE_API lse_status lse_last_cuda_error(int *cuda_err);
 
+/* Size of the fixed device scratch array of lse_forward_split_static:
+ * 1 MiB, i.e. 131072 (m, s) partials of 8 bytes. */
+#define LSE_STATIC_SCRATCH_BYTES (1 << 20)
+
+/*
+ * lse_forward_split_static -- the same result as lse_forward, through the
+ * split-row mapping, without allocating any device memory.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * while they run (a memory budget reserved up front, real-time loops where an
+ * allocator call and the synchronisation or page mapping it may trigger are not
+ * allowed, allocators owned by another runtime).  It calls no cudaMalloc,
+ * cudaFree, stream-ordered allocator or allocating library routine.
+ *
+ * The per-row partials live in a file-scope __device__ array of
+ * LSE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  The first call on a device (with that device current) looks
+ * up the array's device address with cudaGetSymbolAddress and caches it; make
+ * that first call before any stream capture.  All calls share the array, so
+ * calls whose kernels overlap on the GPU (different streams, or unordered host
+ * threads) race; calls on one stream are ordered and safe.  Nothing needs
+ * clearing between calls: each call writes every partial it reads.
+ *
+ * Same arguments and conventions as lse_forward.  Extra limits, reported as
+ * LSE_ERR_INVALID_ARG: B <= LSE_STATIC_SCRATCH_BYTES / 16 (65536 rows, two
+ * partials per row at least), and rows long enough to split (N >= 2 vectors of
+ * 16 bytes when rows are 16-byte aligned, N >= 2 otherwise).  The number of
+ * splits per row is chosen to fill the GPU and capped so B * splits partials
+ * fit the array.
+ */
+LSE_API lse_status lse_forward_split_static(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                                            int64_t row_stride, float *out, lse_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

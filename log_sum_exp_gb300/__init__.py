@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     lse_forward_plan,
     lse_forward_plan_ptr,
     lse_forward_ptr,
+    lse_forward_split_static_ptr,
     lse_plan_query,
     lse_plan_query_ptr,
     lse_trim_memory,

@@ -21,7 +21,8 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
-                 "lse_trim_memory", "lse_status_string", "lse_last_cuda_error"]
+                 "lse_trim_memory", "lse_status_string", "lse_last_cuda_error",
+                 "lse_forward_split_static"]
 
 
 class LsePlan(ctypes.Structure):
@@ -140,6 +141,22 @@ def lse_forward_host_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int
                          stream: int = 0) -> None:
     _check(load().lse_forward_host(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
                                    stream or None), "lse_forward_host")
+
+
+def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
+                                 out_ptr: int, stream: int = 0) -> None:
+    """The split-row mapping with no device allocation (fixed 1 MiB scratch).
+
+    For callers that may not allocate device memory during the call.  Calls
+    whose kernels overlap on the GPU share the scratch and must not run
+    concurrently; make the first call on a device before any stream capture.
+    """
+    fn = load().lse_forward_split_static
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    fn.argtypes = [vp, i32, i64, i64, i64, vp, vp]
+    fn.restype = i32
+    _check(fn(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None, stream or None),
+           "lse_forward_split_static")
 
 
 # ---------------------------------------------------------------------------

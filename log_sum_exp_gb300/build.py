@@ -12,7 +12,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD, "liblse.so")
 
-SOURCES = ["lse_api.cu", "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu"]
+SOURCES = ["lse_api.cu", "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
+           "lse_noalloc.cu"]
 HEADERS = ["lse_device.cuh", "lse_kernels.cuh", "lse_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

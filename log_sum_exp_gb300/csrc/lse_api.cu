@@ -288,6 +288,8 @@ merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream) {
     int64_t grid = ceil_div(B, 256);
     if (grid > 65536) grid = 65536;

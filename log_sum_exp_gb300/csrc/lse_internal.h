@@ -59,5 +59,7 @@ LSE_DECLARE_TYPE_ENTRY_POINTS(f16)
 cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream);
 cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
                          cudaStream_t stream);
+// Sets the calling thread's error reported by lse_last_cuda_error.
+void record_cuda_error(cudaError_t e);
 
 }  // namespace lse

@@ -285,7 +285,9 @@ def run_native(args) -> None:
     K = args.steps
     # Every EVENT_EVERY-th timed step brackets its main kernel with events (the
     # roofline's launch duration); the other steps run back to back untouched.
-    sampled = list(range(0, K, EVENT_EVERY))
+    # A one-kernel plan needs no per-step events: its launches are the whole
+    # timed region.  Multi-kernel plans sample the main kernel's duration.
+    sampled = list(range(0, K, EVENT_EVERY)) if plan["launches"] > 1 else []
     kb = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     ke = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     for e in list(kb.values()) + list(ke.values()):
@@ -353,7 +355,15 @@ def run_native(args) -> None:
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
-    kmean_ms = sum(kernel_ms) / len(kernel_ms)
+    if kernel_ms:
+        kmean_ms = sum(kernel_ms) / len(kernel_ms)
+        kmed_ms = statistics.median(kernel_ms)
+        timing = (f"CUDA events around the main kernel on every {EVENT_EVERY}th timed step "
+                  f"({len(kernel_ms)} launches); includes the launch latency they bracket")
+    else:
+        kmean_ms = kmed_ms = ms_per_step
+        timing = (f"one-kernel plan: CUDA events around the {K} back-to-back launches of the "
+                  f"timed region, divided by {K}")
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
     main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel"}[plan["path"]]
@@ -363,10 +373,8 @@ def run_native(args) -> None:
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": bytes_per_step,
                 "kernel_us_mean": 1e3 * kmean_ms,
-                "kernel_us_median": 1e3 * statistics.median(kernel_ms),
-                "kernel_timing": f"CUDA events around the main kernel on every "
-                                 f"{EVENT_EVERY}th timed step ({len(kernel_ms)} launches); "
-                                 f"includes the launch latency the events bracket"}
+                "kernel_us_median": 1e3 * kmed_ms,
+                "kernel_timing": timing}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rows = oracle_sample_rows(w, args.cpu_seconds / 4)

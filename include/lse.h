@@ -90,7 +90,7 @@ typedef struct {
                                0 in a request: let the library choose              */
     int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32         */
     int32_t slots_per_lane; /* SUBWARP: vectors (or elements) per lane (output)      */
-    int32_t threads;        /* CTA / SPLIT: threads per CTA, 32 or 256              */
+    int32_t threads;        /* CTA / SPLIT: threads per CTA, 32/64/128/256/512      */
     int32_t launches;       /* kernels launched per call (output)                    */
     int64_t splits;         /* SPLIT: CTAs per row (>= 2); 1 otherwise               */
     int64_t segment_slots;  /* CTA / SPLIT: vectors (or elements) per CTA (output)   */

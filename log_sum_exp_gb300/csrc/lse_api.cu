@@ -35,7 +35,7 @@ constexpr int kMergeRowsPerCta = 8;    // one warp per row
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int seg_occ[3][2][2] = {};  // [dtype][vec][threads == 256]
+    int seg_occ[3][2][5] = {};  // [dtype][vec][log2(threads / 32)]
     // Library-owned stream-ordered pool: freed blocks stay mapped for reuse by
     // later calls (release threshold = max) until lse_trim_memory().
     cudaMemPool_t pool = nullptr;
@@ -64,8 +64,8 @@ lse_status device_info(int* dev_out, const DeviceInfo** info) {
         if (e != cudaSuccess) return cuda_fail(e);
         for (int dt = 0; dt < 3; ++dt)
             for (int v = 0; v < 2; ++v)
-                for (int t = 0; t < 2; ++t) {
-                    const int occ = segment_occupancy(dt, v != 0, t ? 256 : 32);
+                for (int t = 0; t < 5; ++t) {
+                    const int occ = segment_occupancy(dt, v != 0, 32 << t);
                     d.seg_occ[dt][v][t] = occ > 0 ? occ : 1;
                 }
         cudaMemPoolProps props;
@@ -168,10 +168,9 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     if (path == LSE_PATH_SUBWARP) {
         if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
         // Fewest lanes per row that keep <= kSubwarpMaxSlots slots per lane:
-        // more independent 16-byte loads in flight per thread.
-        int G = req && req->lanes_per_row
-                    ? req->lanes_per_row
-                    : pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
+        // four independent 16-byte loads per thread (V * R = 4 in the kernel).
+        int G = req && req->lanes_per_row ? req->lanes_per_row
+                                          : pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
         if (G < 1 || G > 32 || (G & (G - 1)) != 0) return LSE_ERR_INVALID_ARG;
         int64_t V = ceil_div(nvt, G);
         if (V > kSubwarpMaxSlots) return LSE_ERR_INVALID_ARG;
@@ -192,25 +191,34 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         return LSE_OK;
     }
 
-    // CTA / SPLIT: the segment kernel.  One-warp CTAs when there are rows
-    // enough to fill the GPU with them and each warp gets >= 4 batches;
-    // otherwise 8-warp CTAs.  Rows are split only when B * threads would not
-    // cover half the GPU's resident threads (a split adds a merge kernel).
+    // CTA / SPLIT: the segment kernel.  Threads per CTA: the most (<= 512)
+    // that still give every thread >= 2 batches; at most 128 when rows are
+    // plentiful (B >= 16 per SM), at least 256 when there are fewer rows than
+    // SMs.  Rows are split only when B * threads would not cover half the
+    // GPU's resident threads (a split adds a merge kernel).
     const int U = vec ? kSegmentBatchVec : kSegmentBatchScalar;
     const int64_t slots = vec ? nv : N;  // slots the segments cover (tail handled separately)
     int T = req && req->threads ? req->threads : 0;
-    if (T == 0) T = (B >= 16LL * info.sms && slots >= 4LL * 32 * U) ? 32 : 256;
-    if (T != 32 && T != 256) return LSE_ERR_INVALID_ARG;
+    if (T == 0) {
+        T = 512;
+        while (T > 32 && slots < 2LL * U * T) T /= 2;
+        if (B >= 16LL * info.sms && T > 128) T = 128;
+        if (B < info.sms && T < 256) T = 256;
+    }
+    int t_index = -1;
+    for (int t = 0; t < 5; ++t)
+        if (T == (32 << t)) t_index = t;
+    if (t_index < 0) return LSE_ERR_INVALID_ARG;
     const int64_t batch = static_cast<int64_t>(T) * U;
     const int64_t resident_threads = static_cast<int64_t>(info.sms) * T *
-                                     info.seg_occ[dt][vec ? 1 : 0][T == 256 ? 1 : 0];
+                                     info.seg_occ[dt][vec ? 1 : 0][t_index];
     int64_t P = 1;
     if (path == LSE_PATH_SPLIT) {
         if (req && req->splits) {
             P = req->splits;
             if (P < 2 || P > (slots > 0 ? slots : 1)) return LSE_ERR_INVALID_ARG;
         } else {
-            P = ceil_div(4 * resident_threads, B * T);
+            P = ceil_div(8 * resident_threads, B * T);
             const int64_t max_p = slots / batch;
             if (P > max_p) P = max_p;
             if (P < 2) P = 2;
@@ -220,7 +228,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     } else {
         if (req && req->splits > 1) return LSE_ERR_INVALID_ARG;
         if ((!req || req->path == LSE_PATH_AUTO) && 2 * B * T < resident_threads) {
-            int64_t want = ceil_div(4 * resident_threads, B * T);
+            int64_t want = ceil_div(8 * resident_threads, B * T);
             const int64_t max_p = slots / (2 * batch);
             if (want > max_p) want = max_p;
             if (want >= 2) P = want;

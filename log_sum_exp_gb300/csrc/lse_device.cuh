@@ -205,26 +205,21 @@ __device__ __forceinline__ float words_max(const uint32_t (&w)[W]) {
     }
 }
 
-// sum of 2^((x - mu) log2 e) over W raw words (pairwise add tree).
+// sum of 2^((x - mu) log2 e) over W raw words, into four interleaved
+// accumulators (few live registers, short dependent add chains).
 template <int DT, int W>
 __device__ __forceinline__ float words_expsum(const uint32_t (&w)[W], float mu) {
-    constexpr int E = DT == kF32 ? W : 2 * W;
-    float e[E];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int i = 0; i < W; ++i) {
         if constexpr (DT == kF32) {
-            e[i] = ex2((__uint_as_float(w[i]) - mu) * kLog2e);
+            acc[i & 3] += ex2((__uint_as_float(w[i]) - mu) * kLog2e);
         } else {
-            e[2 * i] = ex2((word_lo<DT>(w[i]) - mu) * kLog2e);
-            e[2 * i + 1] = ex2((word_hi<DT>(w[i]) - mu) * kLog2e);
+            acc[(2 * i) & 3] += ex2((word_lo<DT>(w[i]) - mu) * kLog2e);
+            acc[(2 * i + 1) & 3] += ex2((word_hi<DT>(w[i]) - mu) * kLog2e);
         }
     }
-#pragma unroll
-    for (int stride = 1; stride < E; stride *= 2) {
-#pragma unroll
-        for (int i = 0; i + stride < E; i += 2 * stride) e[i] += e[i + stride];
-    }
-    return e[0];
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // Fold a chunk of W raw words into an accumulator.

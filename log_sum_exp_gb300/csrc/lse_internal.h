@@ -11,6 +11,9 @@
 namespace lse {
 
 constexpr int kSubwarpThreads = 256;
+// Five resident CTAs per SM (<= 48 registers, no spills): one-shot CTAs whose
+// 16-byte loads are all in flight at once; occupancy sets the bytes in flight.
+constexpr int kSubwarpMinBlocks = 5;
 
 struct LaunchArgs {
     const void* x;

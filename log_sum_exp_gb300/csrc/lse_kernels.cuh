@@ -52,7 +52,7 @@ __device__ __forceinline__ void load_tail_words(const void* row, int64_t start, 
 // loads the < EPV tail elements); !VEC: a slot is one element.
 // ---------------------------------------------------------------------------
 template <int DT, int G, int V, bool VEC>
-__global__ void __launch_bounds__(kSubwarpThreads)
+__global__ void __launch_bounds__(kSubwarpThreads, kSubwarpMinBlocks)
 lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                    float* __restrict__ out) {
     constexpr int EB = DType<DT>::bytes;
@@ -80,18 +80,25 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
                     const int64_t k = sub + j * G;
-                    uint32_t q[4];
-                    if (row < B && k < nv) {
-                        const uint4 u = ldg_stream16(rp + k * 16);
-                        q[0] = u.x; q[1] = u.y; q[2] = u.z; q[3] = u.w;
-                    } else if (row < B && k == nv && tail > 0) {
-                        load_tail_words<DT>(rp, nv * EPV, tail, q);
-                    } else {
+                    uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                         neg_inf_word<DT>());
+                    if (row < B && k < nv) u = ldg_stream16(rp + k * 16);
+                    w[r][4 * j] = u.x; w[r][4 * j + 1] = u.y; w[r][4 * j + 2] = u.z; w[r][4 * j + 3] = u.w;
+                }
+            }
+            if (tail > 0) {  // same for every lane: depends on N only
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) q[i] = neg_inf_word<DT>();
+                for (int r = 0; r < R; ++r) {
+                    const int64_t row = row0 + r * RPW + grp;
+#pragma unroll
+                    for (int j = 0; j < V; ++j) {
+                        if (row < B && sub + j * G == nv) {
+                            uint32_t q[4];
+                            load_tail_words<DT>(xb + row * row_stride * EB, nv * EPV, tail, q);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                        }
                     }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
                 }
             }
 #pragma unroll
@@ -311,20 +318,34 @@ int subwarp_occupancy_gv() {
     }                                                                                          \
     cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
                                         int64_t seg_slots, float2* partial) {                  \
-        if (threads == 32)                                                                     \
-            return vec ? launch_segment_t<DT, 32, true>(a, P, seg_slots, partial)              \
-                       : launch_segment_t<DT, 32, false>(a, P, seg_slots, partial);            \
-        if (threads == 256)                                                                    \
-            return vec ? launch_segment_t<DT, 256, true>(a, P, seg_slots, partial)             \
-                       : launch_segment_t<DT, 256, false>(a, P, seg_slots, partial);           \
-        return cudaErrorInvalidValue;                                                          \
+        switch (threads) {                                                                     \
+        case 32: return vec ? launch_segment_t<DT, 32, true>(a, P, seg_slots, partial)         \
+                            : launch_segment_t<DT, 32, false>(a, P, seg_slots, partial);       \
+        case 64: return vec ? launch_segment_t<DT, 64, true>(a, P, seg_slots, partial)         \
+                            : launch_segment_t<DT, 64, false>(a, P, seg_slots, partial);       \
+        case 128: return vec ? launch_segment_t<DT, 128, true>(a, P, seg_slots, partial)       \
+                             : launch_segment_t<DT, 128, false>(a, P, seg_slots, partial);     \
+        case 256: return vec ? launch_segment_t<DT, 256, true>(a, P, seg_slots, partial)       \
+                             : launch_segment_t<DT, 256, false>(a, P, seg_slots, partial);     \
+        case 512: return vec ? launch_segment_t<DT, 512, true>(a, P, seg_slots, partial)       \
+                             : launch_segment_t<DT, 512, false>(a, P, seg_slots, partial);     \
+        default: return cudaErrorInvalidValue;                                                 \
+        }                                                                                      \
     }                                                                                          \
     int segment_occupancy_##SUFFIX(bool vec, int threads) {                                    \
-        if (threads == 32) return vec ? segment_occupancy_t<DT, 32, true>()                    \
-                                      : segment_occupancy_t<DT, 32, false>();                  \
-        if (threads == 256) return vec ? segment_occupancy_t<DT, 256, true>()                  \
-                                       : segment_occupancy_t<DT, 256, false>();                \
-        return 0;                                                                              \
+        switch (threads) {                                                                     \
+        case 32: return vec ? segment_occupancy_t<DT, 32, true>()                              \
+                            : segment_occupancy_t<DT, 32, false>();                            \
+        case 64: return vec ? segment_occupancy_t<DT, 64, true>()                              \
+                            : segment_occupancy_t<DT, 64, false>();                            \
+        case 128: return vec ? segment_occupancy_t<DT, 128, true>()                            \
+                             : segment_occupancy_t<DT, 128, false>();                          \
+        case 256: return vec ? segment_occupancy_t<DT, 256, true>()                            \
+                             : segment_occupancy_t<DT, 256, false>();                          \
+        case 512: return vec ? segment_occupancy_t<DT, 512, true>()                            \
+                             : segment_occupancy_t<DT, 512, false>();                          \
+        default: return 0;                                                                     \
+        }                                                                                      \
     }                                                                                          \
     int subwarp_occupancy_##SUFFIX(bool vec) {                                                 \
         return vec ? subwarp_occupancy_gv<DT, 8, 1, true>()                                    \

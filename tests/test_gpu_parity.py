@@ -74,9 +74,9 @@ def plans_for(N, dtype, vec):
                 plans.append({"path": "subwarp", "lanes_per_row": G, "vector_bytes": vb})
             G *= 2
     if slots >= 1:
-        plans.append({"path": "cta", "threads": 32, "vector_bytes": vb})
-        plans.append({"path": "cta", "threads": 256, "vector_bytes": vb})
-    for P, T in ((2, 256), (3, 32), (7, 256), (64, 32)):
+        for T in (32, 64, 128, 256, 512):
+            plans.append({"path": "cta", "threads": T, "vector_bytes": vb})
+    for P, T in ((2, 256), (3, 32), (5, 512), (7, 128), (64, 64)):
         if slots >= P:
             plans.append({"path": "split", "splits": P, "threads": T, "vector_bytes": vb})
     return plans
@@ -168,7 +168,8 @@ def test_extreme_magnitudes():
     for i, r in enumerate(rows):
         x[i, :len(r)] = r
     want = oracle.lse(x)
-    for plan in (None, {"path": "cta", "threads": 32}, {"path": "cta", "threads": 256}):
+    for plan in (None, {"path": "cta", "threads": 32}, {"path": "cta", "threads": 256},
+                 {"path": "cta", "threads": 512}):
         got, _ = run(torch.from_numpy(x).cuda(), plan)
         compare(got, want)
 

@@ -396,7 +396,8 @@ def run_native(args) -> None:
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": in_bytes,
                 "d2h_bytes_per_step": w.write_bytes, "steps": e2e_steps,
-                "call": "lse_forward_host (pinned host input)"},
+                "call": "lse_forward_host on page-locked host x and out: the kernel "
+                        "streams x over NVLink-C2C in place (zero copy), writes out in place"},
         "gpu_launches": K * plan["launches"],
         "clocks": clocks.summary(),
     }

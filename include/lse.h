@@ -129,11 +129,12 @@ LSE_API lse_status lse_forward_plan(const void *x, lse_dtype dtype, int64_t B, i
                             lse_plan *plan, lse_event_t ev_begin, lse_event_t ev_end);
 
 /*
- * lse_forward_host -- the same result from HOST buffers: copies x to the
- * device, runs lse_forward, copies out back and synchronises `stream` before
- * returning.  Device buffers are stream-ordered allocations freed before
- * return.  Page-locked host memory gives full-speed copies; pageable memory
- * works but is staged by the driver.
+ * lse_forward_host -- the same result from HOST buffers, synchronising
+ * `stream` before returning.  A page-locked x (cudaHostAlloc'ed or registered)
+ * is read in place by the kernel over the host link (zero copy; the bytes
+ * still cross the link once), and a page-locked out is written in place.
+ * Pageable buffers are copied through stream-ordered device buffers from the
+ * library pool (cudaMemcpyAsync), freed before return.
  */
 LSE_API lse_status lse_forward_host(const void *x_host, lse_dtype dtype, int64_t B, int64_t N,
                             int64_t row_stride, float *out_host, lse_stream_t stream);

@@ -271,10 +271,11 @@ def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: in
 
 
 def lse_forward_host(x, stream=None):
-    """lse over a HOST tensor/array: copy in, compute, copy out, synchronise.
+    """lse over a HOST tensor: the result for x in host memory, synchronised.
 
-    ``x`` is a CPU torch tensor (pin it for full-speed copies) of shape [B, N].
-    Returns a CPU float32 tensor of shape [B].
+    ``x`` is a CPU torch tensor of shape [B, N].  A pinned ``x`` is streamed by
+    the kernel in place (zero copy); a pageable one is copied to the device
+    first.  Returns a CPU float32 tensor of shape [B] (pinned when x is).
     """
     torch = _torch()
     if x.is_cuda:

@@ -403,6 +403,17 @@ lse_status lse_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
     return lse_forward_plan(x, dtype, B, N, row_stride, out, stream, nullptr, nullptr, nullptr);
 }
 
+// Device address of a page-locked (registered or cudaHostAlloc'ed) host
+// buffer, or nullptr for pageable memory.
+static void* mapped_host_pointer(const void* p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return nullptr;
+    }
+    return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+
 lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int64_t N,
                             int64_t row_stride, float* out_host, lse_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -415,24 +426,38 @@ lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int6
     const size_t x_bytes =
         N > 0 ? static_cast<size_t>(((B - 1) * row_stride + N) * elem_bytes(dtype)) : 0;
     const size_t out_bytes = static_cast<size_t>(B) * sizeof(float);
-    void* d_x = nullptr;
-    float* d_out = nullptr;
+
+    // Page-locked buffers are used in place: the kernel streams x over the
+    // host link and writes out directly.  Pageable ones go through pooled
+    // device buffers with cudaMemcpyAsync.
+    const void* x_mapped = x_bytes ? mapped_host_pointer(x_host) : nullptr;
+    float* out_mapped = static_cast<float*>(mapped_host_pointer(out_host));
+    const void* d_x = x_mapped;
+    float* d_out = out_mapped;
+    void* x_staged = nullptr;
+    float* out_staged = nullptr;
     cudaError_t e = cudaSuccess;
-    if (x_bytes && (e = scratch_alloc(*info, &d_x, x_bytes, stream)) != cudaSuccess)
-        return cuda_fail(e, LSE_ERR_ALLOC);
-    if ((e = scratch_alloc(*info, reinterpret_cast<void**>(&d_out), out_bytes, stream)) !=
-        cudaSuccess) {
-        if (d_x) cudaFreeAsync(d_x, stream);
-        return cuda_fail(e, LSE_ERR_ALLOC);
+    if (x_bytes && !x_mapped) {
+        if ((e = scratch_alloc(*info, &x_staged, x_bytes, stream)) != cudaSuccess)
+            return cuda_fail(e, LSE_ERR_ALLOC);
+        d_x = x_staged;
     }
-    if (x_bytes) e = cudaMemcpyAsync(d_x, x_host, x_bytes, cudaMemcpyHostToDevice, stream);
+    if (!out_mapped) {
+        if ((e = scratch_alloc(*info, reinterpret_cast<void**>(&out_staged), out_bytes, stream)) !=
+            cudaSuccess) {
+            if (x_staged) cudaFreeAsync(x_staged, stream);
+            return cuda_fail(e, LSE_ERR_ALLOC);
+        }
+        d_out = out_staged;
+    }
+    if (x_staged) e = cudaMemcpyAsync(x_staged, x_host, x_bytes, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) {
         st = lse_forward(d_x, dtype, B, N, row_stride, d_out, stream_);
-        if (st == LSE_OK)
-            e = cudaMemcpyAsync(out_host, d_out, out_bytes, cudaMemcpyDeviceToHost, stream);
+        if (st == LSE_OK && out_staged)
+            e = cudaMemcpyAsync(out_host, out_staged, out_bytes, cudaMemcpyDeviceToHost, stream);
     }
-    if (d_x) cudaFreeAsync(d_x, stream);
-    cudaFreeAsync(d_out, stream);
+    if (x_staged) cudaFreeAsync(x_staged, stream);
+    if (out_staged) cudaFreeAsync(out_staged, stream);
     const cudaError_t es = cudaStreamSynchronize(stream);
     if (st != LSE_OK) return st;
     if (e != cudaSuccess) return cuda_fail(e);

@@ -242,15 +242,34 @@ def test_invalid_arguments_raise():
         L.lse_forward(x.t())  # last dimension not unit-stride
 
 
-def test_host_entry_point_matches_device():
+def test_host_entry_point_pinned_and_pageable():
+    """lse_forward_host: pinned buffers are used in place (zero copy), pageable
+    ones are staged through device memory; every combination gives the oracle."""
     _need_gpu()
     x = wl.generate("vocab_512x128256_f32", B=32)
+    x[3, 5] = np.nan
+    x[4, :] = -np.inf
     want = oracle.lse(x)
-    xt = torch.from_numpy(x).pin_memory()
-    got = L.lse_forward_host(xt).numpy()
-    compare(got, want)
-    got2 = L.lse_forward_host(torch.from_numpy(x)).numpy()  # pageable
-    assert np.array_equal(got, got2)
+    B, N = x.shape
+    for pin_x in (True, False):
+        for pin_out in (True, False):
+            xt = torch.from_numpy(x.copy())
+            if pin_x:
+                xt = xt.pin_memory()
+            out = torch.full((B,), 7.0, dtype=torch.float32)
+            if pin_out:
+                out = out.pin_memory()
+            L.lse_forward_host_ptr(xt.data_ptr(), "f32", B, N, N, out.data_ptr(),
+                                   torch.cuda.current_stream().cuda_stream)
+            compare(out.numpy(), want)
+    # Padded rows through the host entry.
+    padded = np.full((B, N + 3), np.nan, dtype=np.float32)
+    padded[:, :N] = x
+    pt = torch.from_numpy(padded).pin_memory()
+    out = torch.empty(B, dtype=torch.float32)
+    L.lse_forward_host_ptr(pt.data_ptr(), "f32", B, N, N + 3, out.data_ptr())
+    compare(out.numpy(), want)
+    compare(L.lse_forward_host(torch.from_numpy(x)).numpy(), want)
 
 
 def test_cuda_graph_capture_and_replay():

@@ -56,6 +56,14 @@ class OracleLib:
         lib.oracle_decode.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                       ctypes.c_void_p]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_token_logprob.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_token_logprob.restype = ctypes.c_int
+        lib.oracle_lse_backward.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_lse_backward.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -65,6 +73,14 @@ class OracleLib:
 
     def decode(self, x: np.ndarray, dtype: str) -> np.ndarray:
         return _decode(self._lib, x, dtype)
+
+    def token_logprob(self, x: np.ndarray, target: np.ndarray, dtype: str = "f32",
+                      row_stride: int | None = None, N: int | None = None):
+        return _token_logprob(self._lib, x, target, dtype, row_stride, N)
+
+    def backward(self, x: np.ndarray, lse: np.ndarray, grad: np.ndarray, dtype: str = "f32",
+                 row_stride: int | None = None, N: int | None = None) -> np.ndarray:
+        return _backward(self._lib, x, lse, grad, dtype, row_stride, N)
 
 
 def _load() -> OracleLib:
@@ -84,6 +100,64 @@ def lse(x: np.ndarray, dtype: str = "f32", B: int | None = None, N: int | None =
 def decode(x: np.ndarray, dtype: str) -> np.ndarray:
     """The oracle's exact element decode (raw elements -> float64)."""
     return _load().decode(x, dtype)
+
+
+def token_logprob(x: np.ndarray, target: np.ndarray, dtype: str = "f32",
+                  row_stride: int | None = None, N: int | None = None):
+    """(logprob, lse): logprob[b] = x[b, target[b]] - lse[b] in float64 (NaN for a
+    target outside [0, N)).  ``x`` is 2-D [B, row_stride]; the first N columns
+    are the row."""
+    return _load().token_logprob(x, target, dtype, row_stride, N)
+
+
+def backward(x: np.ndarray, lse: np.ndarray, grad: np.ndarray, dtype: str = "f32",
+             row_stride: int | None = None, N: int | None = None) -> np.ndarray:
+    """dx[b, n] = grad[b] * exp(x[b, n] - lse[b]) in float64, dense [B, N]."""
+    return _load().backward(x, lse, grad, dtype, row_stride, N)
+
+
+def _shape2d(arr: np.ndarray, row_stride, N):
+    if arr.ndim != 2:
+        raise ValueError("expected a 2-D [B, row_stride] array")
+    B = arr.shape[0]
+    row_stride = arr.shape[1] if row_stride is None else row_stride
+    N = row_stride if N is None else N
+    if row_stride != arr.shape[1] or N > row_stride:
+        raise ValueError("row_stride must equal the array's second dimension and N <= it")
+    return B, N, row_stride
+
+
+def _token_logprob(lib, x, target, dtype, row_stride, N):
+    arr = _raw(x, dtype)
+    B, N, row_stride = _shape2d(arr, row_stride, N)
+    t = np.ascontiguousarray(target, dtype=np.int64).reshape(-1)
+    if t.size != B:
+        raise ValueError("one target per row")
+    logprob = np.empty(B, np.float64)
+    lse_out = np.empty(B, np.float64)
+    rc = lib.oracle_token_logprob(arr.ctypes.data if arr.size else None, DTYPE_CODES[dtype], B, N,
+                                  row_stride, t.ctypes.data if B else None,
+                                  logprob.ctypes.data if B else None,
+                                  lse_out.ctypes.data if B else None)
+    if rc != 0:
+        raise ValueError("oracle_token_logprob rejected its arguments")
+    return logprob, lse_out
+
+
+def _backward(lib, x, lse, grad, dtype, row_stride, N):
+    arr = _raw(x, dtype)
+    B, N, row_stride = _shape2d(arr, row_stride, N)
+    lse = np.ascontiguousarray(lse, dtype=np.float64).reshape(-1)
+    grad = np.ascontiguousarray(grad, dtype=np.float64).reshape(-1)
+    if lse.size != B or grad.size != B:
+        raise ValueError("one lse and one grad per row")
+    dx = np.empty((B, N), np.float64)
+    if B and N:
+        rc = lib.oracle_lse_backward(arr.ctypes.data, DTYPE_CODES[dtype], B, N, row_stride,
+                                     lse.ctypes.data, grad.ctypes.data, dx.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_lse_backward rejected its arguments")
+    return dx
 
 
 def _raw(x: np.ndarray, dtype: str) -> np.ndarray:

@@ -30,6 +30,13 @@
  * Inputs are decoded exactly to double: f32 by widening, bf16 as the top 16
  * bits of an IEEE-754 binary32, f16 from the IEEE-754 binary16 fields.
  * Single-threaded on purpose; no blocking, fusion or reordering.
+ *
+ * Two consumers of the row value are defined here as well, each by its plain
+ * formula in double with IEEE special-value arithmetic:
+ *   token log-probability (the RLHF log-prob step of Sec. 5.1 / Fig. 6):
+ *       logprob[b] = x[b, target[b]] - lse[b]   (NaN if target[b] not in [0, N))
+ *   gradient of the row value (backward support, Table 3):
+ *       dx[b, n] = grad[b] * exp(x[b, n] - lse[b])
  */
 #include <math.h>
 #include <stdint.h>
@@ -154,5 +161,62 @@ int oracle_decode(const void *x, int dtype, int64_t n, double *out)
         return -1;
     for (i = 0; i < n; ++i)
         out[i] = decode(dtype, (const unsigned char *)x, i);
+    return 0;
+}
+
+/*
+ * oracle_token_logprob: logprob[b] = x[b, t] - log sum_n exp(x[b, n]) with
+ * t = target[b]; NaN when t is outside [0, N).  lse (may be NULL) receives
+ * the row values.  Returns 0, or -1 on an invalid argument.
+ */
+int oracle_token_logprob(const void *x, int dtype, int64_t B, int64_t N,
+                         int64_t row_stride, const int64_t *target,
+                         double *logprob, double *lse)
+{
+    const unsigned char *base = (const unsigned char *)x;
+    int64_t b, es;
+
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16)
+        return -1;
+    if (B < 0 || N < 0 || row_stride < N)
+        return -1;
+    if (B > 0 && (logprob == NULL || target == NULL || (N > 0 && x == NULL)))
+        return -1;
+    es = elem_size(dtype);
+    for (b = 0; b < B; ++b) {
+        const unsigned char *row = base + b * row_stride * es;
+        const double v = lse_row(dtype, row, N);
+        const int64_t t = target[b];
+        if (lse)
+            lse[b] = v;
+        logprob[b] = (t >= 0 && t < N) ? decode(dtype, row, t) - v : NAN;
+    }
+    return 0;
+}
+
+/*
+ * oracle_lse_backward: dx[b * N + n] = grad[b] * exp(x[b, n] - lse[b]) for a
+ * dense [B, N] double output.  lse and grad are given per row (lse normally
+ * from oracle_lse).  Returns 0, or -1 on an invalid argument.
+ */
+int oracle_lse_backward(const void *x, int dtype, int64_t B, int64_t N,
+                        int64_t row_stride, const double *lse, const double *grad,
+                        double *dx)
+{
+    const unsigned char *base = (const unsigned char *)x;
+    int64_t b, n, es;
+
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16)
+        return -1;
+    if (B < 0 || N < 0 || row_stride < N)
+        return -1;
+    if (B > 0 && N > 0 && (x == NULL || lse == NULL || grad == NULL || dx == NULL))
+        return -1;
+    es = elem_size(dtype);
+    for (b = 0; b < B; ++b) {
+        const unsigned char *row = base + b * row_stride * es;
+        for (n = 0; n < N; ++n)
+            dx[b * N + n] = grad[b] * exp(decode(dtype, row, n) - lse[b]);
+    }
     return 0;
 }

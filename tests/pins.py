@@ -266,10 +266,128 @@ def check_row_stride(orc) -> None:
     assert np.array_equal(orc.lse(flat, "f32", 9, 100, 131), orc.lse(x))
 
 
+# ---------------------------------------------------------------------------
+# Token log-probability: logprob[b] = x[b, t] - lse[b]
+# ---------------------------------------------------------------------------
+def check_logprob_closed_forms(orc) -> None:
+    """Constant row: -log N; one-hot: 0 at the hot column, -inf elsewhere;
+    targets outside [0, N): NaN; a NaN row: NaN."""
+    for n in (1, 3, 1000):
+        for c in (0.0, -7.25, 1000.0):
+            x = np.full((n, n), c, dtype=np.float32)
+            lp, lse = orc.token_logprob(x, np.arange(n))
+            assert np.all(np.abs(lp + math.log(n)) <= 1e-15 * (1 + abs(c))), (n, c)
+    x = np.full((4, 6), -np.inf, dtype=np.float32)
+    x[:, 2] = 0.0
+    lp, _ = orc.token_logprob(x, np.array([2, 0, 5, 2]))
+    assert lp[0] == 0.0 and lp[3] == 0.0 and lp[1] == -np.inf and lp[2] == -np.inf, lp
+    y = np.zeros((5, 4), dtype=np.float32)
+    lp, _ = orc.token_logprob(y, np.array([-1, 4, 1 << 40, -(1 << 40), 3]))
+    assert np.all(np.isnan(lp[:4])) and abs(lp[4] + math.log(4)) < 1e-15, lp
+    y[1, 0] = np.nan
+    lp, _ = orc.token_logprob(y[:2], np.array([1, 1]))
+    assert not math.isnan(lp[0]) and math.isnan(lp[1])
+
+
+def check_logprob_normalizes(orc) -> None:
+    """sum over every target t of exp(logprob_t) = 1 (40-digit sum)."""
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(23)
+    for n in (2, 17, 300):
+        row = rng.normal(0, 8, n).astype(np.float32)
+        lp, _ = orc.token_logprob(np.tile(row, (n, 1)), np.arange(n))
+        total = mpmath.fsum(mpmath.exp(mpmath.mpf(v)) for v in lp)
+        assert abs(float(total) - 1.0) <= 1e-13, (n, float(total))
+
+
+def check_logprob_against_scipy(orc) -> None:
+    from scipy.special import logsumexp
+
+    rng = np.random.default_rng(29)
+    x = (rng.normal(0, 5, (64, 777)) + rng.uniform(-30, 30, (64, 1))).astype(np.float32)
+    t = rng.integers(0, 777, 64)
+    lp, lse = orc.token_logprob(x, t)
+    want_lse = logsumexp(x.astype(np.float64), axis=1)
+    want = x[np.arange(64), t].astype(np.float64) - want_lse
+    assert np.allclose(lse, want_lse, rtol=1e-14, atol=1e-13)
+    assert np.allclose(lp, want, rtol=1e-12, atol=1e-12)
+
+
+def check_logprob_shift_invariance(orc) -> None:
+    rng = np.random.default_rng(31)
+    x = (np.round(rng.uniform(-16, 16, (8, 129)) * 64) / 64).astype(np.float32)
+    t = rng.integers(0, 129, 8)
+    base, _ = orc.token_logprob(x, t)
+    for c in (1000.0, -1000.0):
+        got, _ = orc.token_logprob(x + np.float32(c), t)
+        assert np.all(np.abs(got - base) <= 1e-12), c
+
+
+# ---------------------------------------------------------------------------
+# Backward: dx[b, n] = g[b] * exp(x[b, n] - lse[b])
+# ---------------------------------------------------------------------------
+def check_backward_sums_to_grad(orc) -> None:
+    """Each row of exp(x - lse) is a probability vector: sum_n dx[b, n] = g[b]."""
+    rng = np.random.default_rng(37)
+    x = rng.normal(0, 6, (16, 513)).astype(np.float32)
+    x[3, ::7] = -np.inf
+    g = rng.normal(0, 2, 16)
+    dx = orc.backward(x, orc.lse(x), g)
+    assert np.allclose(dx.sum(axis=1), g, rtol=1e-13, atol=1e-13)
+    assert np.all(dx[3, ::7] == 0.0)
+
+
+def check_backward_finite_difference(orc) -> None:
+    """d lse / d x[n] by central differences of the forward oracle (x on a 2^-10
+    grid, step 2^-10, both exact in f32) matches exp(x[n] - lse)."""
+    rng = np.random.default_rng(41)
+    x = (np.round(rng.uniform(-4, 4, (3, 9)) * 1024) / 1024).astype(np.float32)
+    h = 2.0 ** -10
+    dx = orc.backward(x, orc.lse(x), np.ones(3))
+    for b in range(3):
+        for n in range(9):
+            xp, xm = x[b:b + 1].copy(), x[b:b + 1].copy()
+            xp[0, n] += np.float32(h)
+            xm[0, n] -= np.float32(h)
+            fd = (orc.lse(xp)[0] - orc.lse(xm)[0]) / (2 * h)
+            assert abs(fd - dx[b, n]) <= 2e-7, (b, n, fd, dx[b, n])
+
+
+def check_backward_against_scipy(orc) -> None:
+    from scipy.special import softmax
+
+    rng = np.random.default_rng(43)
+    x = (rng.normal(0, 4, (32, 200)) + rng.uniform(-50, 50, (32, 1))).astype(np.float32)
+    g = rng.normal(0, 1, 32)
+    for dt in ("f32", "bf16", "f16"):
+        if dt == "f32":
+            xx, xv = x, x.astype(np.float64)
+        elif dt == "f16":
+            xx = x.astype(np.float16)
+            xv = xx.astype(np.float64)
+        else:
+            xx = (x.view(np.uint32) >> 16).astype(np.uint16)
+            xv = (xx.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        dx = orc.backward(xx, orc.lse(xx, dt), g, dt)
+        assert np.allclose(dx, g[:, None] * softmax(xv, axis=1), rtol=1e-12, atol=1e-15), dt
+
+
+def check_backward_special(orc) -> None:
+    """One-hot rows give g at the hot column; an all -inf row gives NaN
+    (exp(-inf - (-inf))), as the plain formula does in IEEE arithmetic."""
+    x = np.full((2, 5), -np.inf, dtype=np.float32)
+    x[0, 3] = 2.0
+    dx = orc.backward(x, orc.lse(x), np.array([1.5, 1.0]))
+    assert np.array_equal(dx[0], [0, 0, 0, 1.5, 0]) and np.all(np.isnan(dx[1]))
+
+
 ALL_CHECKS = [
     check_golden, check_decode_all_patterns, check_single_element_rows,
     check_constant_rows, check_special_values, check_two_element_closed_form,
     check_brute_force, check_against_scipy, check_shift_invariance,
     check_permutation_invariance, check_split_associativity, check_bounds,
-    check_row_stride,
+    check_row_stride, check_logprob_closed_forms, check_logprob_normalizes,
+    check_logprob_against_scipy, check_logprob_shift_invariance,
+    check_backward_sums_to_grad, check_backward_finite_difference,
+    check_backward_against_scipy, check_backward_special,
 ]

@@ -27,19 +27,28 @@ MUTANTS = [
     ("missing_nan_rule", "    if (any_nan)\n        return NAN;\n", ""),
     ("missing_pos_inf_rule", "    if (any_pos_inf)\n        return INFINITY;\n", ""),
     ("log2_not_ln", "return m + log(s);", "return m + log2(s);"),
-    ("stride_ignored", "base + b * row_stride * es", "base + b * N * es"),
+    ("stride_ignored", "lse_row(dtype, base + b * row_stride * es, N)",
+     "lse_row(dtype, base + b * N * es, N)"),
     ("f16_bias", "(int)e - 25", "(int)e - 24"),
     ("f16_subnormal", "ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
     ("bf16_shift", "(uint32_t)h << 16", "(uint32_t)h << 15"),
     ("bf16_as_f16", "case ORACLE_BF16: return decode_bf16", "case ORACLE_BF16: return decode_f16"),
     ("float_accumulator", "double m = -INFINITY, s = 0.0;", "double m = -INFINITY; float s = 0.0f;"),
+    ("logprob_sign", "decode(dtype, row, t) - v : NAN", "v - decode(dtype, row, t) : NAN"),
+    ("logprob_drops_target_0", "(t >= 0 && t < N)", "(t > 0 && t < N)"),
+    ("logprob_wrong_column", "decode(dtype, row, t) - v", "decode(dtype, row, t > 0 ? t - 1 : t) - v"),
+    ("logprob_first_row_lse", "const double v = lse_row(dtype, row, N);",
+     "const double v = lse_row(dtype, base, N);"),
+    ("backward_no_grad", "= grad[b] * exp(decode", "= exp(decode"),
+    ("backward_sign", "exp(decode(dtype, row, n) - lse[b])", "exp(lse[b] - decode(dtype, row, n))"),
+    ("backward_first_row_lse", "n) - lse[b])", "n) - lse[0])"),
 ]
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(name, old, new, tmp_path):
     src = open(SRC).read()
-    assert old in src, f"mutation site for {name} not found"
+    assert src.count(old) == 1, f"mutation site for {name} must occur exactly once"
     mutated = tmp_path / "mutant.c"
     mutated.write_text(src.replace(old, new, 1))
     so = tmp_path / "libmutant.so"

@@ -140,6 +140,34 @@ LSE_API lse_status lse_forward_host(const void *x_host, lse_dtype dtype, int64_t
                             int64_t row_stride, float *out_host, lse_stream_t stream);
 
 /*
+ * lse_token_logprob -- fused token log-probability, the consumer the paper
+ * benchmarks in RLHF (Sec. 5.1, Fig. 6: per-token log-probabilities over
+ * vocabularies of 32K-256K):
+ *
+ *     logprob[b] = x[b, target[b]] - log sum_n exp(x[b, n])
+ *
+ * in the same single pass over x as lse_forward (x[b, target[b]] is taken
+ * from registers on short rows and gathered once per row on long ones).
+ *   target   device pointer to B int64 column indices, 8-byte aligned; a
+ *            target outside [0, N) gives logprob NaN (it is never read).
+ *   logprob  device pointer to B floats, 4-byte aligned.
+ *   lse_out  device pointer to B floats for the row values, or NULL.
+ * Special values follow IEEE arithmetic on x[b, t] - lse[b] with lse[b] as in
+ * lse_forward (e.g. a row holding NaN gives NaN; an all -inf row gives NaN).
+ * Split rows take B * (splits * 8 + 4) bytes of stream-ordered scratch.
+ */
+LSE_API lse_status lse_token_logprob(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                                     int64_t row_stride, const int64_t *target, float *logprob,
+                                     float *lse_out, lse_stream_t stream);
+
+/* lse_token_logprob with a caller-chosen plan (NULL = automatic); on return
+ * *plan (if non-NULL) holds the plan that ran. */
+LSE_API lse_status lse_token_logprob_plan(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                                          int64_t row_stride, const int64_t *target,
+                                          float *logprob, float *lse_out, lse_stream_t stream,
+                                          lse_plan *plan);
+
+/*
  * lse_trim_memory -- return the current device's cached stream-ordered memory
  * to the system.  Split-row scratch and lse_forward_host's staging buffers come
  * from a library-owned memory pool that keeps freed blocks mapped for reuse by

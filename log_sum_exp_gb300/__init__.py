@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     lse_forward_split_static_ptr,
     lse_plan_query,
     lse_plan_query_ptr,
+    lse_token_logprob,
+    lse_token_logprob_ptr,
     lse_trim_memory,
     status_string,
 )

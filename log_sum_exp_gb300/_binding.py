@@ -21,8 +21,8 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
-                 "lse_trim_memory", "lse_status_string", "lse_last_cuda_error",
-                 "lse_forward_split_static"]
+                 "lse_token_logprob", "lse_token_logprob_plan", "lse_trim_memory",
+                 "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
 
 
 class LsePlan(ctypes.Structure):
@@ -85,6 +85,11 @@ def load() -> ctypes.CDLL:
         lib.lse_forward_plan.restype = i32
         lib.lse_forward_host.argtypes = [vp, i32, i64, i64, i64, vp, vp]
         lib.lse_forward_host.restype = i32
+        lib.lse_token_logprob.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, vp]
+        lib.lse_token_logprob.restype = i32
+        lib.lse_token_logprob_plan.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, vp,
+                                               ctypes.POINTER(LsePlan)]
+        lib.lse_token_logprob_plan.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
@@ -141,6 +146,16 @@ def lse_forward_host_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int
                          stream: int = 0) -> None:
     _check(load().lse_forward_host(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
                                    stream or None), "lse_forward_host")
+
+
+def lse_token_logprob_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
+                          target_ptr: int, logprob_ptr: int, lse_ptr: int = 0, stream: int = 0,
+                          plan: LsePlan | None = None) -> LsePlan:
+    p = plan if plan is not None else LsePlan()
+    _check(load().lse_token_logprob_plan(x_ptr or None, DTYPES[dtype], B, N, row_stride,
+                                         target_ptr or None, logprob_ptr or None, lse_ptr or None,
+                                         stream or None, ctypes.byref(p)), "lse_token_logprob")
+    return p
 
 
 def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
@@ -255,6 +270,32 @@ def _as_plan(plan) -> LsePlan | None:
             v = PATHS[v]
         setattr(p, k, v)
     return p
+
+
+def lse_token_logprob(x, target, lse_out=None, plan=None, stream=None, return_plan=False):
+    """logprob[b] = x[b, target[b]] - logsumexp(x[b, :]) for a CUDA [B, N] tensor.
+
+    ``target`` is a CUDA int64 tensor of B column indices (out-of-range -> NaN).
+    ``lse_out`` (optional float32 [B]) receives the row values.  Returns the
+    float32 [B] log-probabilities (and the plan that ran if ``return_plan``).
+    """
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    if target.dtype != torch.int64 or target.device != x.device or target.numel() != B \
+            or not target.is_contiguous():
+        raise ValueError("target must be a contiguous int64 tensor of B elements on x's device")
+    logprob = torch.empty(B, dtype=torch.float32, device=x.device)
+    if lse_out is not None and (lse_out.dtype != torch.float32 or lse_out.numel() != B
+                                or not lse_out.is_contiguous() or lse_out.device != x.device):
+        raise ValueError("lse_out must be a contiguous float32 tensor of B elements on x's device")
+    with torch.cuda.device(x.device):
+        p = lse_token_logprob_ptr(x.data_ptr(), dt, B, N, row_stride, target.data_ptr(),
+                                  logprob.data_ptr(), lse_out.data_ptr() if lse_out is not None else 0,
+                                  _stream_handle(stream, x.device), _as_plan(plan))
+    return (logprob, p) if return_plan else logprob
 
 
 def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,

@@ -128,7 +128,8 @@ int pow2_ceil(int64_t v) {
 
 // Fill in (or check) a plan.  `req` may be null (automatic).
 lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t row_stride,
-                     const DeviceInfo& info, const lse_plan* req, lse_plan* plan) {
+                     const DeviceInfo& info, const lse_plan* req, bool with_logprob,
+                     lse_plan* plan) {
     lse_plan p;
     std::memset(&p, 0, sizeof p);
     const int eb = elem_bytes(dt);
@@ -234,15 +235,20 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
             if (want >= 2) P = want;
         }
     }
-    const int64_t seg_slots = ceil_div(slots, P);
-    P = ceil_div(slots, seg_slots);  // no empty trailing segments
-    if (P < 1) P = 1;
+    // Rows shorter than one vector have no full slots: one segment whose CTA
+    // reads only the tail.
+    const int64_t seg_slots = slots > 0 ? ceil_div(slots, P) : 1;
+    P = slots > 0 ? ceil_div(slots, seg_slots) : 1;  // no empty trailing segments
     if (B > INT_MAX / P) return LSE_ERR_INVALID_ARG;  // grid.x = B * P must fit
     p.path = P > 1 ? LSE_PATH_SPLIT : LSE_PATH_CTA;
     p.threads = T;
     p.splits = P;
     p.grid = B * P;
-    p.scratch_bytes = P > 1 ? B * P * static_cast<int64_t>(sizeof(float2)) : 0;
+    // Split scratch: B*P (m, s) partials, then (token log-probability) the
+    // gathered x[b, target[b]] per row.
+    p.scratch_bytes = P > 1 ? B * P * static_cast<int64_t>(sizeof(float2)) +
+                                  (with_logprob ? B * static_cast<int64_t>(sizeof(float)) : 0)
+                            : 0;
     p.launches = B > 0 ? (P > 1 ? 2 : 1) : 0;
     p.segment_slots = seg_slots;
     *plan = p;
@@ -250,35 +256,47 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
 }
 
 cudaError_t launch_subwarp(lse_dtype dt, const LaunchArgs& a, bool vec, int G, int V, int64_t grid) {
+    const bool tl = a.tl.logprob != nullptr;
     switch (dt) {
-    case LSE_F32: return launch_subwarp_f32(a, vec, G, V, grid);
-    case LSE_BF16: return launch_subwarp_bf16(a, vec, G, V, grid);
-    default: return launch_subwarp_f16(a, vec, G, V, grid);
+    case LSE_F32: return tl ? launch_subwarp_lp_f32(a, vec, G, V, grid) : launch_subwarp_f32(a, vec, G, V, grid);
+    case LSE_BF16: return tl ? launch_subwarp_lp_bf16(a, vec, G, V, grid) : launch_subwarp_bf16(a, vec, G, V, grid);
+    default: return tl ? launch_subwarp_lp_f16(a, vec, G, V, grid) : launch_subwarp_f16(a, vec, G, V, grid);
     }
 }
 
 cudaError_t launch_segment(lse_dtype dt, const LaunchArgs& a, bool vec, int T, int64_t P,
-                           int64_t seg_slots, float2* partial) {
+                           int64_t seg_slots, float2* partial, float* xt_buf) {
+    const bool tl = a.tl.logprob != nullptr;
     switch (dt) {
-    case LSE_F32: return launch_segment_f32(a, vec, T, P, seg_slots, partial);
-    case LSE_BF16: return launch_segment_bf16(a, vec, T, P, seg_slots, partial);
-    default: return launch_segment_f16(a, vec, T, P, seg_slots, partial);
+    case LSE_F32:
+        return tl ? launch_segment_lp_f32(a, vec, T, P, seg_slots, partial, xt_buf)
+                  : launch_segment_f32(a, vec, T, P, seg_slots, partial, xt_buf);
+    case LSE_BF16:
+        return tl ? launch_segment_lp_bf16(a, vec, T, P, seg_slots, partial, xt_buf)
+                  : launch_segment_bf16(a, vec, T, P, seg_slots, partial, xt_buf);
+    default:
+        return tl ? launch_segment_lp_f16(a, vec, T, P, seg_slots, partial, xt_buf)
+                  : launch_segment_f16(a, vec, T, P, seg_slots, partial, xt_buf);
     }
 }
 
-__global__ void fill_neg_inf_kernel(float* __restrict__ out, int64_t B) {
+// N == 0: every row value is log(0) = -inf, and no target is in range.
+__global__ void fill_neg_inf_kernel(float* __restrict__ out, float* __restrict__ logprob,
+                                    int64_t B) {
     pdl_trigger();
     pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t b = i; b < B; b += stride) out[b] = __int_as_float(kNegInfF32);
+    for (int64_t b = i; b < B; b += stride)
+        store_row(out, logprob, b, __int_as_float(kNegInfF32), __int_as_float(0x7fc00000));
 }
 
 // One warp per row: lane l folds partials l, l+32, ... in order, then a fixed
 // butterfly merges the lanes.  pdl_wait() returns once the segment kernel that
 // produced the partials has completed and its writes are visible.
 __global__ void __launch_bounds__(32 * kMergeRowsPerCta)
-merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __restrict__ out) {
+merge_kernel(const float2* __restrict__ partial, const float* __restrict__ xt_buf, int64_t B,
+             int64_t P, float* __restrict__ out, float* __restrict__ logprob) {
     pdl_trigger();
     pdl_wait();
     const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -291,24 +309,24 @@ merge_kernel(const float2* __restrict__ partial, int64_t B, int64_t P, float* __
         a = acc_merge(a, Acc{v.x, v.y});
     }
     a = warp_merge<32>(a);
-    if (lane == 0) out[row] = acc_finalize(a);
+    if (lane == 0) store_row(out, logprob, row, acc_finalize(a), logprob ? xt_buf[row] : 0.0f);
 }
 
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
-cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream) {
+cudaError_t launch_fill_neg_inf(float* out, float* logprob, int64_t B, cudaStream_t stream) {
     int64_t grid = ceil_div(B, 256);
     if (grid > 65536) grid = 65536;
     return launch_pdl(fill_neg_inf_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), stream, out,
-                      B);
+                      logprob, B);
 }
 
-cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
-                         cudaStream_t stream) {
+cudaError_t launch_merge(const float2* partial, const float* xt_buf, int64_t B, int64_t P,
+                         float* out, float* logprob, cudaStream_t stream) {
     return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(ceil_div(B, kMergeRowsPerCta))),
-                      dim3(32 * kMergeRowsPerCta), stream, partial, B, P, out);
+                      dim3(32 * kMergeRowsPerCta), stream, partial, xt_buf, B, P, out, logprob);
 }
 
 }  // namespace lse
@@ -344,50 +362,61 @@ lse_status lse_plan_query(const void* x, lse_dtype dtype, int64_t B, int64_t N,
     int dev = 0;
     const DeviceInfo* info = nullptr;
     if ((st = device_info(&dev, &info)) != LSE_OK) return st;
-    return make_plan(x, dtype, B, N, row_stride, *info, nullptr, plan);
+    return make_plan(x, dtype, B, N, row_stride, *info, nullptr, false, plan);
 }
 
-lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N,
-                            int64_t row_stride, float* out, lse_stream_t stream_,
-                            lse_plan* plan, lse_event_t ev_begin, lse_event_t ev_end) {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    lse_status st = check_args(x, dtype, B, N, row_stride, out);
-    if (st != LSE_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// The forward pass behind lse_forward_plan and lse_token_logprob_plan.  `out`
+// may be null when `tl.logprob` is set; arguments are already checked.
+lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,
+                       float* out, TokenLogprob tl, cudaStream_t stream, lse_plan* plan,
+                       lse_event_t ev_begin, lse_event_t ev_end) {
     if (B == 0) return LSE_OK;  // no work, no device access
     int dev = 0;
     const DeviceInfo* info = nullptr;
-    if ((st = device_info(&dev, &info)) != LSE_OK) return st;
+    lse_status st = device_info(&dev, &info);
+    if (st != LSE_OK) return st;
     lse_plan p;
-    if ((st = make_plan(x, dtype, B, N, row_stride, *info, plan, &p)) != LSE_OK) return st;
+    if ((st = make_plan(x, dtype, B, N, row_stride, *info, plan, tl.logprob != nullptr, &p)) !=
+        LSE_OK)
+        return st;
     if (plan) *plan = p;
 
-    const LaunchArgs a{x, B, N, row_stride, out, stream};
+    LaunchArgs a{x, B, N, row_stride, out, stream};
+    a.tl = tl;
     cudaError_t e = cudaSuccess;
-    float2* scratch = nullptr;
+    char* scratch = nullptr;
     if (p.scratch_bytes > 0) {
         e = scratch_alloc(*info, reinterpret_cast<void**>(&scratch),
                           static_cast<size_t>(p.scratch_bytes), stream);
         if (e != cudaSuccess) return cuda_fail(e, LSE_ERR_ALLOC);
     }
+    float2* partial = reinterpret_cast<float2*>(scratch);
+    float* xt_buf = tl.logprob && scratch
+                        ? reinterpret_cast<float*>(scratch + B * p.splits * sizeof(float2))
+                        : nullptr;
     if (ev_begin && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev_begin), stream)) != cudaSuccess)
         goto fail;
     switch (p.path) {
     case LSE_PATH_EMPTY:
-        e = launch_fill_neg_inf(out, B, stream);
+        e = launch_fill_neg_inf(out, tl.logprob, B, stream);
         break;
     case LSE_PATH_SUBWARP:
         e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
         break;
     default:
         e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,
-                           scratch);
+                           partial, xt_buf);
         break;
     }
     if (e != cudaSuccess) goto fail;
     if (ev_end && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev_end), stream)) != cudaSuccess)
         goto fail;
     if (p.path == LSE_PATH_SPLIT) {
-        e = launch_merge(scratch, B, p.splits, out, stream);
+        e = launch_merge(partial, xt_buf, B, p.splits, out, tl.logprob, stream);
         if (e != cudaSuccess) goto fail;
     }
     if (scratch && (e = cudaFreeAsync(scratch, stream)) != cudaSuccess) return cuda_fail(e);
@@ -396,6 +425,43 @@ lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N
 fail:
     if (scratch) cudaFreeAsync(scratch, stream);
     return cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N,
+                            int64_t row_stride, float* out, lse_stream_t stream,
+                            lse_plan* plan, lse_event_t ev_begin, lse_event_t ev_end) {
+    const lse_status st = check_args(x, dtype, B, N, row_stride, out);
+    if (st != LSE_OK) return st;
+    return run_forward(x, dtype, B, N, row_stride, out, TokenLogprob{},
+                       reinterpret_cast<cudaStream_t>(stream), plan, ev_begin, ev_end);
+}
+
+lse_status lse_token_logprob_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N,
+                                  int64_t row_stride, const int64_t* target, float* logprob,
+                                  float* lse_out, lse_stream_t stream, lse_plan* plan) {
+    const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    lse_status st = check_args(x, dtype, B, N, row_stride, lse_out ? lse_out : stand_in);
+    if (st != LSE_OK) return st;
+    if (B > 0 && (target == nullptr || logprob == nullptr)) return LSE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(target) & 7u) != 0 ||
+        (reinterpret_cast<uintptr_t>(logprob) & 3u) != 0)
+        return LSE_ERR_INVALID_ARG;
+    TokenLogprob tl;
+    tl.target = target;
+    tl.logprob = logprob;
+    return run_forward(x, dtype, B, N, row_stride, lse_out, tl,
+                       reinterpret_cast<cudaStream_t>(stream), plan, nullptr, nullptr);
+}
+
+lse_status lse_token_logprob(const void* x, lse_dtype dtype, int64_t B, int64_t N,
+                             int64_t row_stride, const int64_t* target, float* logprob,
+                             float* lse_out, lse_stream_t stream) {
+    return lse_token_logprob_plan(x, dtype, B, N, row_stride, target, logprob, lse_out, stream,
+                                  nullptr);
 }
 
 lse_status lse_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,

@@ -150,6 +150,26 @@ __device__ __forceinline__ float acc_finalize(Acc a) {
     return a.m + kLn2 * lg2(a.s);
 }
 
+// Write a finished row: the row value, and the token log-probability when
+// requested (xt is x[row, target[row]], NaN for an invalid target).
+__device__ __forceinline__ void store_row(float* out, float* logprob, int64_t row, float lse,
+                                          float xt) {
+    if (out) out[row] = lse;
+    if (logprob) logprob[row] = xt - lse;
+}
+
+// Element i (0 .. elements-per-vector - 1) of a 16-byte vector held as 4 words.
+template <int DT>
+__device__ __forceinline__ float word_elem(const uint32_t* w4, int i) {
+    if constexpr (DT == kF32) {
+        return __uint_as_float(i == 0 ? w4[0] : i == 1 ? w4[1] : i == 2 ? w4[2] : w4[3]);
+    } else {
+        const int q = i >> 1;
+        const uint32_t w = q == 0 ? w4[0] : q == 1 ? w4[1] : q == 2 ? w4[2] : w4[3];
+        return (i & 1) ? word_hi<DT>(w) : word_lo<DT>(w);
+    }
+}
+
 // Butterfly merge across `width` lanes (power of two <= 32); every lane of the
 // group ends with the group's accumulator.  The merge order is fixed, so the
 // result is deterministic.

@@ -15,13 +15,21 @@ constexpr int kSubwarpThreads = 256;
 // 16-byte loads are all in flight at once; occupancy sets the bytes in flight.
 constexpr int kSubwarpMinBlocks = 5;
 
+// Optional fused consumer of the row value, the token log-probability
+// logprob[b] = x[b, target[b]] - lse[b] (NaN when target[b] is not in [0, N)).
+struct TokenLogprob {
+    const int64_t* target = nullptr;  // device, one per row; nullptr = not requested
+    float* logprob = nullptr;         // device, one per row
+};
+
 struct LaunchArgs {
     const void* x;
     int64_t B;
     int64_t N;
     int64_t row_stride;  // elements
-    float* out;
+    float* out;          // row values; may be nullptr when tl.logprob is set
     cudaStream_t stream;
+    TokenLogprob tl;
 };
 
 // Launch with programmatic stream serialization (see pdl_trigger / pdl_wait in
@@ -50,18 +58,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStre
     cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
                                         int64_t grid);                                         \
     cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
-                                        int64_t seg_slots, float2* partial);                   \
+                                        int64_t seg_slots, float2* partial, float* xt_buf);    \
     int segment_occupancy_##SUFFIX(bool vec, int threads);                                     \
     int subwarp_occupancy_##SUFFIX(bool vec);
 
 LSE_DECLARE_TYPE_ENTRY_POINTS(f32)
 LSE_DECLARE_TYPE_ENTRY_POINTS(bf16)
 LSE_DECLARE_TYPE_ENTRY_POINTS(f16)
+// The same kernels with the fused token log-probability epilogue.
+LSE_DECLARE_TYPE_ENTRY_POINTS(lp_f32)
+LSE_DECLARE_TYPE_ENTRY_POINTS(lp_bf16)
+LSE_DECLARE_TYPE_ENTRY_POINTS(lp_f16)
 
 // Type-independent kernels (lse_api.cu).
-cudaError_t launch_fill_neg_inf(float* out, int64_t B, cudaStream_t stream);
-cudaError_t launch_merge(const float2* partial, int64_t B, int64_t P, float* out,
-                         cudaStream_t stream);
+cudaError_t launch_fill_neg_inf(float* out, float* logprob, int64_t B, cudaStream_t stream);
+cudaError_t launch_merge(const float2* partial, const float* xt_buf, int64_t B, int64_t P,
+                         float* out, float* logprob, cudaStream_t stream);
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);
 

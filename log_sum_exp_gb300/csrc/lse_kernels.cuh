@@ -51,10 +51,11 @@ __device__ __forceinline__ void load_tail_words(const void* row, int64_t start, 
 // VEC: a slot is one 16-byte vector (the lane holding vector index N/EPV also
 // loads the < EPV tail elements); !VEC: a slot is one element.
 // ---------------------------------------------------------------------------
-template <int DT, int G, int V, bool VEC>
+template <int DT, int G, int V, bool VEC, bool TL>
 __global__ void __launch_bounds__(kSubwarpThreads, kSubwarpMinBlocks)
 lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
-                   float* __restrict__ out) {
+                   float* __restrict__ out, const int64_t* __restrict__ target,
+                   float* __restrict__ logprob) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;  // elements per slot
     constexpr int RPW = 32 / G;             // rows per warp per row-group
@@ -71,6 +72,16 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
     pdl_wait();
 
     for (int64_t row0 = warp * (RPW * R); row0 < B; row0 += nwarps * (RPW * R)) {
+        // Targets, loaded with the rows (token log-probability only); rows on
+        // this path hold at most 32 * 4 * 8 elements, so an in-range target
+        // fits in 32 bits and -1 marks an invalid one.
+        int t[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = row0 + r * RPW + grp;
+            const int64_t tt = (TL && row < B) ? __ldg(target + row) : -1;
+            t[r] = (tt >= 0 && tt < N) ? static_cast<int>(tt) : -1;
+        }
         if constexpr (VEC) {
             uint32_t w[R][4 * V];
 #pragma unroll
@@ -112,7 +123,23 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (sub == 0 && row < B) out[row] = acc_finalize(Acc{m, s});
+                // x[row, t] is already in the group's registers: the lane holding
+                // it contributes it, the others 0, and a shuffle-sum combines.
+                float xt = 0.0f;
+                if constexpr (TL) {
+                    const bool valid = t[r] >= 0;
+                    if (valid) {
+                        const int kv = t[r] / EPV;
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            if (sub + j * G == kv) xt = word_elem<DT>(&w[r][4 * j], t[r] - kv * EPV);
+                    }
+#pragma unroll
+                    for (int off = G / 2; off > 0; off >>= 1)
+                        xt += __shfl_xor_sync(0xffffffffu, xt, off);
+                    if (!valid) xt = __int_as_float(0x7fc00000);
+                }
+                if (sub == 0 && row < B) store_row(out, TL ? logprob : nullptr, row, acc_finalize(Acc{m, s}), xt);
             }
         } else {
             float v[R][V];
@@ -143,7 +170,18 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (sub == 0 && row < B) out[row] = acc_finalize(Acc{m, s});
+                float xt = 0.0f;
+                if constexpr (TL) {
+                    const bool valid = t[r] >= 0;
+#pragma unroll
+                    for (int j = 0; j < V; ++j)
+                        if (valid && sub + j * G == t[r]) xt = v[r][j];
+#pragma unroll
+                    for (int off = G / 2; off > 0; off >>= 1)
+                        xt += __shfl_xor_sync(0xffffffffu, xt, off);
+                    if (!valid) xt = __int_as_float(0x7fc00000);
+                }
+                if (sub == 0 && row < B) store_row(out, TL ? logprob : nullptr, row, acc_finalize(Acc{m, s}), xt);
             }
         }
     }
@@ -156,10 +194,12 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 // ---------------------------------------------------------------------------
 template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
 
-template <int DT, int T, bool VEC>
+template <int DT, int T, bool VEC, bool TL>
 __global__ void __launch_bounds__(T, SegmentOccupancy<T>::min_blocks)
 lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, int64_t P,
-                   int64_t seg_slots, float* __restrict__ out, float2* __restrict__ partial) {
+                   int64_t seg_slots, float* __restrict__ out, float2* __restrict__ partial,
+                   const int64_t* __restrict__ target, float* __restrict__ logprob,
+                   float* __restrict__ xt_buf) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 8 : 16;  // slots per thread per batch
@@ -180,6 +220,13 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
     float mu = 0.0f;
     int64_t k = s_begin + threadIdx.x;
 
+    // Token log-probability: thread 0 of the row's first segment gathers
+    // x[row, target[row]] once, issued behind its first batch of loads.
+    const bool gather = TL && seg == 0 && threadIdx.x == 0;
+    const int64_t t = gather ? __ldg(target + row) : -1;
+    bool xt_pending = gather;
+    float xt = __int_as_float(0x7fc00000);
+
     if constexpr (VEC) {
         for (; k + (U - 1) * T < s_end; k += U * T) {
             uint32_t w[4 * U];
@@ -187,6 +234,10 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             for (int j = 0; j < U; ++j) {
                 const uint4 u = ldg_stream16(rp + (k + j * T) * 16);
                 w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+            }
+            if (xt_pending) {
+                if (t >= 0 && t < N) xt = load_elem<DT>(rp, t);
+                xt_pending = false;
             }
             acc_add_words<DT, 4 * U>(acc, mu, w);
         }
@@ -229,6 +280,8 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
         }
     }
 
+    if (xt_pending && t >= 0 && t < N) xt = load_elem<DT>(rp, t);
+
     acc = warp_merge<32>(acc);
     if constexpr (NW > 1) {
         __shared__ float2 part[NW];
@@ -242,65 +295,70 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
         }
     }
     if (threadIdx.x == 0) {
-        if (P == 1)
-            out[row] = acc_finalize(acc);
-        else
+        if (P == 1) {
+            store_row(out, TL ? logprob : nullptr, row, acc_finalize(acc), xt);
+        } else {
             partial[unit] = make_float2(acc.m, acc.s);
+            if (gather) xt_buf[row] = xt;
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
 // Host-side launchers for one element type.
 // ---------------------------------------------------------------------------
-template <int DT, int G, int V, bool VEC>
+template <int DT, int G, int V, bool VEC, bool TL>
 cudaError_t launch_subwarp_gv(const LaunchArgs& a, int64_t grid) {
-    return launch_pdl(lse_subwarp_kernel<DT, G, V, VEC>, dim3(static_cast<unsigned>(grid)),
-                      dim3(kSubwarpThreads), a.stream, a.x, a.B, a.N, a.row_stride, a.out);
+    return launch_pdl(lse_subwarp_kernel<DT, G, V, VEC, TL>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kSubwarpThreads), a.stream, a.x, a.B, a.N, a.row_stride, a.out,
+                      a.tl.target, a.tl.logprob);
 }
 
-template <int DT, int G, bool VEC>
+template <int DT, int G, bool VEC, bool TL>
 cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     switch (V) {
-    case 1: return launch_subwarp_gv<DT, G, 1, VEC>(a, grid);
-    case 2: return launch_subwarp_gv<DT, G, 2, VEC>(a, grid);
-    case 4: return launch_subwarp_gv<DT, G, 4, VEC>(a, grid);
+    case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL>(a, grid);
+    case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL>(a, grid);
+    case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL>(a, grid);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool TL>
 cudaError_t launch_subwarp_dt(const LaunchArgs& a, int G, int V, int64_t grid) {
     switch (G) {
-    case 1: return launch_subwarp_g<DT, 1, VEC>(a, V, grid);
-    case 2: return launch_subwarp_g<DT, 2, VEC>(a, V, grid);
-    case 4: return launch_subwarp_g<DT, 4, VEC>(a, V, grid);
-    case 8: return launch_subwarp_g<DT, 8, VEC>(a, V, grid);
-    case 16: return launch_subwarp_g<DT, 16, VEC>(a, V, grid);
-    case 32: return launch_subwarp_g<DT, 32, VEC>(a, V, grid);
+    case 1: return launch_subwarp_g<DT, 1, VEC, TL>(a, V, grid);
+    case 2: return launch_subwarp_g<DT, 2, VEC, TL>(a, V, grid);
+    case 4: return launch_subwarp_g<DT, 4, VEC, TL>(a, V, grid);
+    case 8: return launch_subwarp_g<DT, 8, VEC, TL>(a, V, grid);
+    case 16: return launch_subwarp_g<DT, 16, VEC, TL>(a, V, grid);
+    case 32: return launch_subwarp_g<DT, 32, VEC, TL>(a, V, grid);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int DT, int T, bool VEC>
-cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial) {
+template <int DT, int T, bool VEC, bool TL>
+cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial,
+                             float* xt_buf) {
     const int64_t grid = a.B * P;
-    return launch_pdl(lse_segment_kernel<DT, T, VEC>, dim3(static_cast<unsigned>(grid)), dim3(T),
-                      a.stream, a.x, a.N, a.row_stride, P, seg_slots, a.out, partial);
+    return launch_pdl(lse_segment_kernel<DT, T, VEC, TL>, dim3(static_cast<unsigned>(grid)), dim3(T),
+                      a.stream, a.x, a.N, a.row_stride, P, seg_slots, a.out, partial,
+                      a.tl.target, a.tl.logprob, xt_buf);
 }
 
-template <int DT, int T, bool VEC>
+template <int DT, int T, bool VEC, bool TL>
 int segment_occupancy_t() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC>, T, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC, TL>, T, 0) !=
         cudaSuccess)
         return 0;
     return blocks;
 }
 
-template <int DT, int G, int V, bool VEC>
+template <int DT, int G, int V, bool VEC, bool TL>
 int subwarp_occupancy_gv() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_subwarp_kernel<DT, G, V, VEC>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_subwarp_kernel<DT, G, V, VEC, TL>,
                                                       kSubwarpThreads, 0) != cudaSuccess)
         return 0;
     return blocks;
@@ -308,47 +366,48 @@ int subwarp_occupancy_gv() {
 
 }  // namespace lse
 
-// Instantiates the per-type entry points declared in lse_internal.h.
-#define LSE_DEFINE_TYPE_ENTRY_POINTS(DT, SUFFIX)                                               \
+// Instantiates the per-type entry points declared in lse_internal.h; TL selects
+// the kernels with the fused token log-probability epilogue.
+#define LSE_DEFINE_TYPE_ENTRY_POINTS(DT, SUFFIX, TL)                                               \
     namespace lse {                                                                            \
     cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
                                         int64_t grid) {                                        \
-        return vec ? launch_subwarp_dt<DT, true>(a, G, V, grid)                                \
-                   : launch_subwarp_dt<DT, false>(a, G, V, grid);                              \
+        return vec ? launch_subwarp_dt<DT, true, TL>(a, G, V, grid)                                \
+                   : launch_subwarp_dt<DT, false, TL>(a, G, V, grid);                              \
     }                                                                                          \
     cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
-                                        int64_t seg_slots, float2* partial) {                  \
+                                        int64_t seg_slots, float2* partial, float* xt_buf) {   \
         switch (threads) {                                                                     \
-        case 32: return vec ? launch_segment_t<DT, 32, true>(a, P, seg_slots, partial)         \
-                            : launch_segment_t<DT, 32, false>(a, P, seg_slots, partial);       \
-        case 64: return vec ? launch_segment_t<DT, 64, true>(a, P, seg_slots, partial)         \
-                            : launch_segment_t<DT, 64, false>(a, P, seg_slots, partial);       \
-        case 128: return vec ? launch_segment_t<DT, 128, true>(a, P, seg_slots, partial)       \
-                             : launch_segment_t<DT, 128, false>(a, P, seg_slots, partial);     \
-        case 256: return vec ? launch_segment_t<DT, 256, true>(a, P, seg_slots, partial)       \
-                             : launch_segment_t<DT, 256, false>(a, P, seg_slots, partial);     \
-        case 512: return vec ? launch_segment_t<DT, 512, true>(a, P, seg_slots, partial)       \
-                             : launch_segment_t<DT, 512, false>(a, P, seg_slots, partial);     \
+        case 32: return vec ? launch_segment_t<DT, 32, true, TL>(a, P, seg_slots, partial, xt_buf)         \
+                            : launch_segment_t<DT, 32, false, TL>(a, P, seg_slots, partial, xt_buf);       \
+        case 64: return vec ? launch_segment_t<DT, 64, true, TL>(a, P, seg_slots, partial, xt_buf)         \
+                            : launch_segment_t<DT, 64, false, TL>(a, P, seg_slots, partial, xt_buf);       \
+        case 128: return vec ? launch_segment_t<DT, 128, true, TL>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 128, false, TL>(a, P, seg_slots, partial, xt_buf);     \
+        case 256: return vec ? launch_segment_t<DT, 256, true, TL>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 256, false, TL>(a, P, seg_slots, partial, xt_buf);     \
+        case 512: return vec ? launch_segment_t<DT, 512, true, TL>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 512, false, TL>(a, P, seg_slots, partial, xt_buf);     \
         default: return cudaErrorInvalidValue;                                                 \
         }                                                                                      \
     }                                                                                          \
     int segment_occupancy_##SUFFIX(bool vec, int threads) {                                    \
         switch (threads) {                                                                     \
-        case 32: return vec ? segment_occupancy_t<DT, 32, true>()                              \
-                            : segment_occupancy_t<DT, 32, false>();                            \
-        case 64: return vec ? segment_occupancy_t<DT, 64, true>()                              \
-                            : segment_occupancy_t<DT, 64, false>();                            \
-        case 128: return vec ? segment_occupancy_t<DT, 128, true>()                            \
-                             : segment_occupancy_t<DT, 128, false>();                          \
-        case 256: return vec ? segment_occupancy_t<DT, 256, true>()                            \
-                             : segment_occupancy_t<DT, 256, false>();                          \
-        case 512: return vec ? segment_occupancy_t<DT, 512, true>()                            \
-                             : segment_occupancy_t<DT, 512, false>();                          \
+        case 32: return vec ? segment_occupancy_t<DT, 32, true, TL>()                              \
+                            : segment_occupancy_t<DT, 32, false, TL>();                            \
+        case 64: return vec ? segment_occupancy_t<DT, 64, true, TL>()                              \
+                            : segment_occupancy_t<DT, 64, false, TL>();                            \
+        case 128: return vec ? segment_occupancy_t<DT, 128, true, TL>()                            \
+                             : segment_occupancy_t<DT, 128, false, TL>();                          \
+        case 256: return vec ? segment_occupancy_t<DT, 256, true, TL>()                            \
+                             : segment_occupancy_t<DT, 256, false, TL>();                          \
+        case 512: return vec ? segment_occupancy_t<DT, 512, true, TL>()                            \
+                             : segment_occupancy_t<DT, 512, false, TL>();                          \
         default: return 0;                                                                     \
         }                                                                                      \
     }                                                                                          \
     int subwarp_occupancy_##SUFFIX(bool vec) {                                                 \
-        return vec ? subwarp_occupancy_gv<DT, 8, 1, true>()                                    \
-                   : subwarp_occupancy_gv<DT, 8, 1, false>();                                  \
+        return vec ? subwarp_occupancy_gv<DT, 8, 1, true, TL>()                                    \
+                   : subwarp_occupancy_gv<DT, 8, 1, false, TL>();                                  \
     }                                                                                          \
     }

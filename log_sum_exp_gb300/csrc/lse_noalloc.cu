@@ -135,11 +135,11 @@ extern "C" lse_status lse_forward_split_static(const void* x, lse_dtype dtype, i
     const LaunchArgs a{x, B, N, row_stride, out, stream};
     cudaError_t e;
     switch (dtype) {
-    case LSE_F32: e = launch_segment_f32(a, vec, kThreads, P, seg_slots, s->ptr); break;
-    case LSE_BF16: e = launch_segment_bf16(a, vec, kThreads, P, seg_slots, s->ptr); break;
-    default: e = launch_segment_f16(a, vec, kThreads, P, seg_slots, s->ptr); break;
+    case LSE_F32: e = launch_segment_f32(a, vec, kThreads, P, seg_slots, s->ptr, nullptr); break;
+    case LSE_BF16: e = launch_segment_bf16(a, vec, kThreads, P, seg_slots, s->ptr, nullptr); break;
+    default: e = launch_segment_f16(a, vec, kThreads, P, seg_slots, s->ptr, nullptr); break;
     }
-    if (e == cudaSuccess) e = launch_merge(s->ptr, B, P, out, stream);
+    if (e == cudaSuccess) e = launch_merge(s->ptr, nullptr, B, P, out, nullptr, stream);
     if (e != cudaSuccess) return fail(e);
     return LSE_OK;
 }

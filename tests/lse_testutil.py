@@ -9,8 +9,13 @@ ATOL = 1e-5
 RTOL = 1e-6
 
 
-def compare(got: np.ndarray, want: np.ndarray, atol: float = ATOL, rtol: float = RTOL) -> dict:
-    """Compare float32 GPU results with float64 oracle values; return a summary."""
+def compare(got: np.ndarray, want: np.ndarray, atol: float = ATOL, rtol: float = RTOL,
+            scale: np.ndarray | None = None) -> dict:
+    """Compare float32 GPU results with float64 oracle values; return a summary.
+
+    Finite values must satisfy |got - want| <= atol + rtol * scale, where scale
+    defaults to |want|.
+    """
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
@@ -20,13 +25,14 @@ def compare(got: np.ndarray, want: np.ndarray, atol: float = ATOL, rtol: float =
     bad_inf = np.flatnonzero(inf_w & ~nan_g & (got != want))
     fin = ~nan_w & ~inf_w
     err = np.abs(got[fin] - want[fin])
-    lim = atol + rtol * np.abs(want[fin])
+    sc = np.abs(want) if scale is None else np.abs(np.asarray(scale, dtype=np.float64))
+    lim = atol + rtol * sc[fin]
     bad_fin = np.flatnonzero(fin)[~(err <= lim)]
     summary = {
         "n": int(got.size),
         "finite": int(fin.sum()),
         "max_abs_err": float(err.max()) if err.size else 0.0,
-        "max_err_over_tol": float((err / lim).max()) if err.size else 0.0,
+        "max_err_over_tol": float((err / lim).max()) if err.size and lim.min() > 0 else 0.0,
     }
     if bad_nan.size or bad_inf.size or bad_fin.size:
         idx = np.concatenate([bad_nan, bad_inf, bad_fin])[:8]
@@ -47,6 +53,14 @@ def torch_view(x: np.ndarray, dtype: str):
     if dtype == "f16":
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.float16)
     raise ValueError(dtype)
+
+
+def compare_logprob(got_lp: np.ndarray, want_lp: np.ndarray, want_lse: np.ndarray) -> dict:
+    """Token log-probabilities: the row value's error carries over, so the bar
+    is |d| <= ATOL + RTOL * (|logprob| + |lse|) (>= the bar on x[b, t] - lse)."""
+    scale = np.abs(np.nan_to_num(want_lp, posinf=0, neginf=0)) + \
+        np.abs(np.nan_to_num(want_lse, posinf=0, neginf=0))
+    return compare(got_lp, want_lp, ATOL, RTOL, scale)
 
 
 NAN_BITS = {"f32": None, "bf16": 0x7FC0, "f16": 0x7E00}

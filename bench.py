@@ -36,7 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 EVENT_EVERY = 16
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
-                  "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu"]
+                  "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
+                  "lse_backward.cu"]
 
 
 # ---------------------------------------------------------------------------

@@ -168,6 +168,25 @@ LSE_API lse_status lse_token_logprob_plan(const void *x, lse_dtype dtype, int64_
                                           lse_plan *plan);
 
 /*
+ * lse_backward -- gradient of the row value with respect to x:
+ *
+ *     dx[b, n] = grad[b] * exp(x[b, n] - lse[b])
+ *
+ * (d lse / d x is the row's softmax; the paper lists backward support among
+ * its kernel variants, Table 3).  One pass: x read once, dx written once.
+ *   lse      device pointer to B floats: the saved forward values.
+ *   grad     device pointer to B floats: the upstream gradient of each row value.
+ *   dx       device pointer, same element type as x, row b at b * dx_row_stride
+ *            (elements, >= N); computed in f32, rounded to nearest-even on store.
+ *            dx may be x itself (same row_stride); other overlaps are undefined.
+ * Special values follow IEEE arithmetic on that formula (an all -inf row, whose
+ * lse is -inf, gives NaN).  Asynchronous on `stream`; allocates nothing.
+ */
+LSE_API lse_status lse_backward(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                                int64_t row_stride, const float *lse, const float *grad,
+                                void *dx, int64_t dx_row_stride, lse_stream_t stream);
+
+/*
  * lse_trim_memory -- return the current device's cached stream-ordered memory
  * to the system.  Split-row scratch and lse_forward_host's staging buffers come
  * from a library-owned memory pool that keeps freed blocks mapped for reuse by

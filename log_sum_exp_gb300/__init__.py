@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     LsePlan,
     library_path,
     load,
+    lse_backward,
+    lse_backward_ptr,
     lse_forward,
     lse_forward_host,
     lse_forward_host_ptr,

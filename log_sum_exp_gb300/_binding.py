@@ -21,7 +21,7 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
-                 "lse_token_logprob", "lse_token_logprob_plan", "lse_trim_memory",
+                 "lse_token_logprob", "lse_token_logprob_plan", "lse_backward", "lse_trim_memory",
                  "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
 
 
@@ -90,6 +90,8 @@ def load() -> ctypes.CDLL:
         lib.lse_token_logprob_plan.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, vp,
                                                ctypes.POINTER(LsePlan)]
         lib.lse_token_logprob_plan.restype = i32
+        lib.lse_backward.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, i64, vp]
+        lib.lse_backward.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
@@ -156,6 +158,13 @@ def lse_token_logprob_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: in
                                          target_ptr or None, logprob_ptr or None, lse_ptr or None,
                                          stream or None, ctypes.byref(p)), "lse_token_logprob")
     return p
+
+
+def lse_backward_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, lse_ptr: int,
+                     grad_ptr: int, dx_ptr: int, dx_row_stride: int, stream: int = 0) -> None:
+    _check(load().lse_backward(x_ptr or None, DTYPES[dtype], B, N, row_stride, lse_ptr or None,
+                               grad_ptr or None, dx_ptr or None, dx_row_stride, stream or None),
+           "lse_backward")
 
 
 def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
@@ -296,6 +305,30 @@ def lse_token_logprob(x, target, lse_out=None, plan=None, stream=None, return_pl
                                   logprob.data_ptr(), lse_out.data_ptr() if lse_out is not None else 0,
                                   _stream_handle(stream, x.device), _as_plan(plan))
     return (logprob, p) if return_plan else logprob
+
+
+def lse_backward(x, lse, grad, dx=None, stream=None):
+    """dx[b, n] = grad[b] * exp(x[b, n] - lse[b]) for a CUDA [B, N] tensor x.
+
+    ``lse`` and ``grad`` are float32 CUDA tensors of B elements; ``dx`` (optional)
+    has x's dtype and shape.  Returns dx.
+    """
+    torch = _torch()
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    for name, t in (("lse", lse), ("grad", grad)):
+        if t.dtype != torch.float32 or t.numel() != B or not t.is_contiguous() \
+                or t.device != x.device:
+            raise ValueError(f"{name} must be a contiguous float32 tensor of B elements")
+    if dx is None:
+        dx = torch.empty((B, N), dtype=x.dtype, device=x.device)
+    if dx.shape != (B, N) or dx.dtype != x.dtype or (N > 1 and dx.stride(1) != 1):
+        raise ValueError("dx must match x's shape and dtype with unit last stride")
+    dx_stride = dx.stride(0) if B > 1 else N
+    with torch.cuda.device(x.device):
+        lse_backward_ptr(x.data_ptr(), dt, B, N, row_stride, lse.data_ptr(), grad.data_ptr(),
+                         dx.data_ptr(), dx_stride, _stream_handle(stream, x.device))
+    return dx
 
 
 def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,

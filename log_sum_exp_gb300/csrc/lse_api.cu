@@ -457,6 +457,60 @@ lse_status lse_token_logprob_plan(const void* x, lse_dtype dtype, int64_t B, int
                        reinterpret_cast<cudaStream_t>(stream), plan, nullptr, nullptr);
 }
 
+lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,
+                        const float* lse_in, const float* grad, void* dx, int64_t dx_row_stride,
+                        lse_stream_t stream) {
+    const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    lse_status st = check_args(x, dtype, B, N, row_stride, stand_in);
+    if (st != LSE_OK) return st;
+    if (dx_row_stride < N) return LSE_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    int64_t extent = 0;
+    if (B > 0 && __builtin_mul_overflow(B - 1, dx_row_stride, &extent)) return LSE_ERR_INVALID_ARG;
+    if (__builtin_add_overflow(extent, N, &extent) ||
+        __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &extent))
+        return LSE_ERR_INVALID_ARG;
+    if (B == 0 || N == 0) return LSE_OK;
+    if (lse_in == nullptr || grad == nullptr || dx == nullptr) return LSE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lse_in) & 3u) || (reinterpret_cast<uintptr_t>(grad) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dx) % static_cast<uintptr_t>(eb)))
+        return LSE_ERR_INVALID_ARG;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    if ((st = device_info(&dev, &info)) != LSE_OK) return st;
+
+    const bool vec = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (row_stride * eb) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(dx) % 16u == 0 && (dx_row_stride * eb) % 16 == 0;
+    const int64_t epv = vec ? 16 / eb : 1;
+    const int64_t nvt = ceil_div(N, epv);  // slots per row including the tail vector
+    const int U = backward_slots_per_thread();
+    const int threads = backward_threads();
+    int TX = pow2_ceil(ceil_div(nvt, U));
+    if (TX > threads) TX = threads;
+    const int TY = threads / TX;
+    const int64_t seg = nvt <= static_cast<int64_t>(TX) * U * 4 ? nvt : static_cast<int64_t>(TX) * U * 4;
+    const int64_t P = ceil_div(nvt, seg);
+    if (P > INT_MAX) return LSE_ERR_INVALID_ARG;
+    int64_t gy = ceil_div(B, TY);
+    if (gy > 65535) gy = 65535;  // grid-stride over the remaining rows
+
+    BackwardArgs a;
+    a.x = x;
+    a.B = B;
+    a.N = N;
+    a.row_stride = row_stride;
+    a.lse = lse_in;
+    a.grad = grad;
+    a.dx = dx;
+    a.dx_row_stride = dx_row_stride;
+    a.seg_slots = seg;
+    a.grid = dim3(static_cast<unsigned>(P), static_cast<unsigned>(gy));
+    a.block = dim3(static_cast<unsigned>(TX), static_cast<unsigned>(TY));
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = launch_backward(dtype, vec, a);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
 lse_status lse_token_logprob(const void* x, lse_dtype dtype, int64_t B, int64_t N,
                              int64_t row_stride, const int64_t* target, float* logprob,
                              float* lse_out, lse_stream_t stream) {

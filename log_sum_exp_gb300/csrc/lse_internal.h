@@ -74,6 +74,25 @@ LSE_DECLARE_TYPE_ENTRY_POINTS(lp_f16)
 cudaError_t launch_fill_neg_inf(float* out, float* logprob, int64_t B, cudaStream_t stream);
 cudaError_t launch_merge(const float2* partial, const float* xt_buf, int64_t B, int64_t P,
                          float* out, float* logprob, cudaStream_t stream);
+// Backward (lse_backward.cu).
+struct BackwardArgs {
+    const void* x;
+    int64_t B;
+    int64_t N;
+    int64_t row_stride;
+    const float* lse;
+    const float* grad;
+    void* dx;
+    int64_t dx_row_stride;
+    int64_t seg_slots;  // slots (16-byte vectors or elements) per blockIdx.x segment
+    dim3 grid;
+    dim3 block;
+    cudaStream_t stream;
+};
+cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a);
+int backward_slots_per_thread();
+int backward_threads();
+
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);
 

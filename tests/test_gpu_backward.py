@@ -1,0 +1,149 @@
+"""GPU parity of lse_backward against the fp64 oracle:
+dx[b, n] = grad[b] * exp(x[b, n] - lse[b]).
+
+The GPU receives the oracle's row values rounded to f32 (as a saved forward
+output would be), the oracle keeps them in fp64.  Per-element bar, from the
+f32 arithmetic of the kernel (ex2.approx ~2^-22, rounding of lse and of
+x - lse at 2^-24 of their magnitudes) and the output rounding of the dtype:
+    |d| <= |g| * 1e-37 + |ref| * (2^-21 + 2^-23 (|lse| + |x - lse|) + q)
+with q = 0 (f32), 2^-8 (bf16), 2^-11 (f16) plus 2^-24 absolute for f16
+subnormals.  NaN and +-inf must match exactly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from log_sum_exp_gb300 import workloads as wl
+from lse_testutil import canary_array, torch_view
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import log_sum_exp_gb300 as L  # noqa: E402
+
+Q = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _decode(x, dtype):
+    return oracle.decode(x, dtype).reshape(x.shape)
+
+
+def _check(got_raw, x, dtype, lse64, g, want):
+    got = _decode(got_raw, dtype)
+    xv = _decode(x, dtype)
+    nan_w, nan_g = np.isnan(want), np.isnan(got)
+    assert np.array_equal(nan_w, nan_g), f"NaN mismatch at {np.argwhere(nan_w != nan_g)[:5]}"
+    inf_w = np.isinf(want)
+    assert np.array_equal(got[inf_w], want[inf_w])
+    fin = ~nan_w & ~inf_w
+    lse_b = np.broadcast_to(np.abs(np.nan_to_num(lse64, posinf=0, neginf=0))[:, None], want.shape)
+    dist = np.abs(np.nan_to_num(xv - lse64[:, None], posinf=0, neginf=0))
+    rel = 2.0 ** -21 + 2.0 ** -23 * (lse_b + dist) + Q[dtype]
+    lim = np.abs(g)[:, None] * 1e-37 + np.abs(want) * rel + (2.0 ** -24 if dtype == "f16" else 0)
+    err = np.abs(got - want)
+    bad = fin & ~(err <= lim)
+    assert not bad.any(), (f"{bad.sum()} out of tolerance; first "
+                           f"{[(tuple(i), got[tuple(i)], want[tuple(i)]) for i in np.argwhere(bad)[:4]]}")
+    return float((err[fin] / np.maximum(lim[fin], 1e-300)).max()) if fin.any() else 0.0
+
+
+def _run(x, dtype, g, row_stride=None, offset=0, dx_row_stride=None, dx_offset=0, inplace=False):
+    """Call lse_backward on device copies inside NaN-canaried buffers."""
+    B, N = x.shape
+    lse64 = oracle.lse(x, dtype)
+    want = oracle.backward(x, lse64, g, dtype)
+    rs = N if row_stride is None else row_stride
+    ds = rs if inplace else (N if dx_row_stride is None else dx_row_stride)
+    xh = canary_array(offset + B * rs + 32, dtype)
+    xh[offset:offset + B * rs].reshape(B, rs)[:, :N] = x if dtype == "f32" else x.view(np.uint16)
+    xbuf = torch_view(xh, dtype).cuda()
+    if inplace:
+        dbuf, doff = xbuf, offset
+    else:
+        dbuf = torch_view(canary_array(dx_offset + B * ds + 32, dtype), dtype).cuda()
+        doff = dx_offset
+    eb = 4 if dtype == "f32" else 2
+    lse_d = torch.from_numpy(lse64.astype(np.float32)).cuda()
+    g_d = torch.from_numpy(g.astype(np.float32)).cuda()
+    L.lse_backward_ptr(xbuf.data_ptr() + offset * eb, dtype, B, N, rs, lse_d.data_ptr(),
+                       g_d.data_ptr(), dbuf.data_ptr() + doff * eb, ds)
+    torch.cuda.synchronize()
+    host = dbuf.cpu()
+    raw = host.numpy() if dtype == "f32" else host.view(torch.int16).numpy().view(np.uint16)
+    body = raw[doff:doff + B * ds].reshape(B, ds)
+    got = np.ascontiguousarray(body[:, :N])
+    # Canaries: nothing outside the [B, N] block of dx may change.
+    mask = np.ones(raw.shape, bool)
+    mask[doff:doff + B * ds] = False
+    pad = np.ones((B, ds), bool)
+    pad[:, :N] = False
+    outside = np.concatenate([raw[mask], body[pad]])
+    if dtype == "f32":
+        assert np.all(np.isnan(outside)), "write outside dx rows"
+    else:
+        assert np.all(outside == (0x7FC0 if dtype == "bf16" else 0x7E00)), "write outside dx rows"
+    return got, lse64, want
+
+
+@pytest.mark.parametrize("key,B,N", [
+    ("vocab_512x128256_f32", 32, None),
+    ("vocab_8192x32000_bf16", 256, None),
+    ("short_1048576x32_f32", 100000, None),
+    ("particles_16x16777216_f32", 2, 1 << 21),
+    ("small_64x4096_f32", None, None),
+])
+def test_workload_backward(key, B, N):
+    _need_gpu()
+    w = wl.WORKLOADS[key]
+    x = wl.generate(key, B=B, N=N)
+    g = np.random.default_rng(w.index).normal(0, 2, x.shape[0])
+    got, lse64, want = _run(x, w.dtype, g)
+    r = _check(got, x, w.dtype, lse64, g, want)
+    print(key, "max err / tol", r)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 33, 1000, 4097, 20001])
+def test_backward_edge_shapes(dtype, N):
+    _need_gpu()
+    B = 7
+    x = wl.random_rows(B, N, dtype, seed=200 + N, scale=4.0)
+    if N >= 3:
+        xi = x.view(np.uint16) if dtype != "f32" else x
+        ninf = {"f32": -np.inf, "bf16": 0xFF80, "f16": 0xFC00}[dtype]
+        nan = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+        xi[2, :] = ninf           # lse = -inf: NaN gradient
+        xi[3, N // 2] = nan       # NaN row
+        xi[4, ::2] = ninf         # zeros in the gradient
+    g = np.random.default_rng(N).normal(0, 3, B)
+    g[5] = 0.0
+    layouts = [dict(), dict(row_stride=N + 8, dx_row_stride=N + 8), dict(row_stride=N + 3),
+               dict(offset=1), dict(dx_offset=1), dict(inplace=True)]
+    for lay in layouts:
+        got, lse64, want = _run(x, dtype, g, **lay)
+        try:
+            _check(got, x, dtype, lse64, g, want)
+        except AssertionError as e:
+            raise AssertionError(f"layout {lay}: {e}") from None
+
+
+def test_backward_tensor_api_and_bad_args():
+    _need_gpu()
+    x = torch.randn(8, 100, device="cuda")
+    lse = L.lse_forward(x)
+    g = torch.ones(8, device="cuda")
+    dx = L.lse_backward(x, lse, g)
+    assert torch.allclose(dx.sum(dim=1), g, rtol=1e-5)
+    with pytest.raises(L.LseError):
+        L.lse_backward_ptr(x.data_ptr(), "f32", 8, 100, 100, lse.data_ptr(), g.data_ptr(),
+                           dx.data_ptr(), 99)
+    with pytest.raises(L.LseError):
+        L.lse_backward_ptr(x.data_ptr(), "f32", 8, 100, 100, 0, g.data_ptr(), dx.data_ptr(), 100)
+    with pytest.raises(L.LseError):
+        L.lse_backward_ptr(x.data_ptr(), "f32", 8, 100, 100, lse.data_ptr(), g.data_ptr(),
+                           dx.data_ptr() + 2, 100)

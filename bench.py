@@ -34,6 +34,8 @@ DEFAULT_WORKLOAD = "vocab_512x128256_f32"
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 EVENT_EVERY = 16
+OP_NAMES = {"forward": "row value", "logprob": "fused token log-probability",
+            "backward": "backward dx = g exp(x - lse)"}
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
                   "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
@@ -92,7 +94,7 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
-def ncu_traffic(workload_key: str, kernel_path: str) -> float | None:
+def ncu_traffic(workload_key: str, kernel_path: str, op: str = "forward") -> float | None:
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     or None when there is none for this workload or the kernels changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -104,7 +106,7 @@ def ncu_traffic(workload_key: str, kernel_path: str) -> float | None:
     src = kernel_source_hash()
     for e in entries:
         if e.get("workload") == workload_key and e.get("source_hash") == src \
-                and e.get("path") == kernel_path:
+                and e.get("path") == kernel_path and e.get("op", "forward") == op:
             return float(e["dram_bytes_per_launch"])
     return None
 
@@ -166,25 +168,36 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle, as it stands, on a bounded sample.
 # ---------------------------------------------------------------------------
-def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float) -> dict:
+def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float, op: str = "forward") -> dict:
     import oracle
 
-    bytes_per_row = w.N * w.elem_bytes + 4
-    t0 = time.perf_counter()
+    rows = x.shape[0]
+    if op == "logprob":
+        t = np.random.default_rng(w.seed + 1).integers(0, w.N, rows)
+        fn = lambda: oracle.token_logprob(x, t, w.dtype)  # noqa: E731
+        bytes_per_row = w.N * w.elem_bytes + 12
+    elif op == "backward":
+        lse = oracle.lse(x, w.dtype)
+        g = np.ones(rows)
+        fn = lambda: oracle.backward(x, lse, g, w.dtype)  # noqa: E731
+        bytes_per_row = 2 * w.N * w.elem_bytes + 8
+    else:
+        fn = lambda: oracle.lse(x, w.dtype)  # noqa: E731
+        bytes_per_row = w.N * w.elem_bytes + 4
     oracle.lse(x[:1], w.dtype)  # load / build outside the timing
     rows_done, elapsed, reps = 0, 0.0, 0
     t0 = time.perf_counter()
     while True:
-        oracle.lse(x, w.dtype)
-        rows_done += x.shape[0]
+        fn()
+        rows_done += rows
         reps += 1
         elapsed = time.perf_counter() - t0
         if elapsed >= budget_s:
             break
     gbs = rows_done * bytes_per_row / elapsed / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} pass(es) over {x.shape[0]} rows x {w.N} {w.dtype} of the "
-                      f"workload ({elapsed:.1f} s single-threaded)",
+            "sample": f"{reps} pass(es) of the oracle's {OP_NAMES[op]} over {rows} rows x "
+                      f"{w.N} {w.dtype} of the workload ({elapsed:.1f} s single-threaded)",
             "seconds": elapsed, "rows": rows_done}
 
 
@@ -273,12 +286,37 @@ def run_native(args) -> None:
     sh = stream.cuda_stream
     dt = w.dtype
     ptrs = [(t.data_ptr(), o.data_ptr()) for t, o in zip(xs, outs)]
-    plan = L.lse_plan_query(xs[0])
-    bytes_per_step = in_bytes + w.write_bytes
+    op_name = args.op
+    if op_name == "forward":
+        plan = L.lse_plan_query(xs[0])
+        bytes_per_step = in_bytes + w.write_bytes
 
-    def step(i, evb=0, eve=0):
-        xp, op = ptrs[i % copies]
-        L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, None, evb, eve)
+        def step(i, evb=0, eve=0):
+            xp, op = ptrs[i % copies]
+            L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, None, evb, eve)
+    elif op_name == "logprob":
+        # Targets drawn once per copy; only the log-probabilities are written.
+        rng = np.random.default_rng(w.seed + 1)
+        tgts = [torch.from_numpy(rng.integers(0, w.N, w.B).astype(np.int64)).to(dev)
+                for _ in range(copies)]
+        plan = L.lse_token_logprob_ptr(ptrs[0][0], dt, w.B, w.N, w.N, tgts[0].data_ptr(),
+                                       ptrs[0][1], 0, sh).as_dict()
+        bytes_per_step = in_bytes + 8 * w.B + 4 * w.B
+
+        def step(i, evb=0, eve=0):
+            xp, op = ptrs[i % copies]
+            L.lse_token_logprob_ptr(xp, dt, w.B, w.N, w.N, tgts[i % copies].data_ptr(), op, 0, sh)
+    else:  # backward
+        lses = [L.lse_forward(x) for x in xs]
+        gs = [torch.ones(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
+        dxs = [torch.empty_like(x) for x in xs]
+        plan = {"path": "backward", "launches": 1, "kernel": "lse_backward_kernel"}
+        bytes_per_step = 2 * in_bytes + 8 * w.B
+
+        def step(i, evb=0, eve=0):
+            c = i % copies
+            L.lse_backward_ptr(ptrs[c][0], dt, w.B, w.N, w.N, lses[c].data_ptr(), gs[c].data_ptr(),
+                               dxs[c].data_ptr(), w.N, sh)
 
     for i in range(args.warmup):
         step(i)
@@ -289,7 +327,8 @@ def run_native(args) -> None:
     # roofline's launch duration); the other steps run back to back untouched.
     # A one-kernel plan needs no per-step events: its launches are the whole
     # timed region.  Multi-kernel plans sample the main kernel's duration.
-    sampled = list(range(0, K, EVENT_EVERY)) if plan["launches"] > 1 else []
+    sampled = list(range(0, K, EVENT_EVERY)) \
+        if plan["launches"] > 1 and op_name == "forward" else []
     kb = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     ke = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     for e in list(kb.values()) + list(ke.values()):
@@ -319,7 +358,7 @@ def run_native(args) -> None:
 
     # Graph-replayed µs/call (launch overhead removed), same step.
     graph_us = None
-    if args.graph:
+    if args.graph and op_name == "forward":
         g = torch.cuda.CUDAGraph()
         s2 = torch.cuda.Stream(dev)
         s2.wait_stream(stream)
@@ -342,17 +381,23 @@ def run_native(args) -> None:
         graph_us = 1e3 * t0.elapsed_time(t1) / (10 * reps)
 
     # End to end through the host entry point: H2D of x, compute, D2H of out.
-    e2e_steps = max(1, min(K, args.e2e_steps))
-    x_pinned = xt_host.pin_memory()
-    L.lse_forward_host(x_pinned)  # warm-up
-    torch.cuda.synchronize(dev)
-    barrier(dev)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        res = L.lse_forward_host(x_pinned)
-    e2e_s = reduce_max(time.perf_counter() - t0, dev)
-    e2e_value = world * bytes_per_step * e2e_steps / e2e_s / 1e9
-    assert res.shape == (w.B,)
+    e2e = None
+    if op_name == "forward":
+        e2e_steps = max(1, min(K, args.e2e_steps))
+        x_pinned = xt_host.pin_memory()
+        L.lse_forward_host(x_pinned)  # warm-up
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            res = L.lse_forward_host(x_pinned)
+        e2e_s = reduce_max(time.perf_counter() - t0, dev)
+        assert res.shape == (w.B,)
+        e2e = {"value": world * bytes_per_step * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": w.write_bytes,
+               "steps": e2e_steps,
+               "call": "lse_forward_host on page-locked host x and out: the kernel "
+                       "streams x over NVLink-C2C in place (zero copy), writes out in place"}
 
     if rank != 0:
         return
@@ -368,8 +413,9 @@ def run_native(args) -> None:
                   f"timed region, divided by {K}")
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
     main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
-                   "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel"}[plan["path"]]
-    traffic = ncu_traffic(args.workload, plan["path"])
+                   "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
+                   "backward": "lse_backward_kernel"}[plan["path"]]
+    traffic = ncu_traffic(args.workload, plan["path"], op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
                 "peak_source": peak_src,
@@ -380,13 +426,14 @@ def run_native(args) -> None:
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rows = oracle_sample_rows(w, args.cpu_seconds / 4)
-        cpu = time_oracle(x_host[:rows], w, args.cpu_seconds)
+        cpu = time_oracle(x_host[:rows], w, args.cpu_seconds, op_name)
+    metric = METRIC if op_name == "forward" else f"{METRIC} [{OP_NAMES[op_name]}]"
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "B": w.B, "N": w.N, "input_dtype": w.dtype,
-                   "row_stride": w.N, "recipe": w.recipe, "plan": plan,
+        "config": {"workload": args.workload, "op": op_name, "B": w.B, "N": w.N,
+                   "input_dtype": w.dtype, "row_stride": w.N, "recipe": w.recipe, "plan": plan,
                    "bytes_per_step": bytes_per_step,
                    "l2": f"inputs larger than L2: {copies} rotating copies of "
                          f"{in_bytes / 1e6:.1f} MB (L2 {L2_BYTES / 1e6:.0f} MB)",
@@ -396,10 +443,7 @@ def run_native(args) -> None:
         "us_per_call_graph": graph_us,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": in_bytes,
-                "d2h_bytes_per_step": w.write_bytes, "steps": e2e_steps,
-                "call": "lse_forward_host on page-locked host x and out: the kernel "
-                        "streams x over NVLink-C2C in place (zero copy), writes out in place"},
+        "e2e": e2e,
         "gpu_launches": K * plan["launches"],
         "clocks": clocks.summary(),
     }
@@ -413,6 +457,8 @@ def main(argv=None) -> None:
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--op", choices=["forward", "logprob", "backward"], default="forward",
+                    help="row value (default), fused token log-probability, or backward")
     ap.add_argument("--graph", action="store_true", help="also time CUDA-graph replay")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

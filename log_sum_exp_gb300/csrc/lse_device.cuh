@@ -242,6 +242,38 @@ __device__ __forceinline__ float words_expsum(const uint32_t (&w)[W], float mu) 
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// Short rows with their shift mu known in advance: the same exp-sum with one
+// FFMA per element, t = x log2 e - c where c = fl(mu log2 e).  Every term then
+// carries the same factor 2^(mu log2 e - c); scaled_log corrects it exactly
+// with the rounding residual of c.  Valid while |mu| log2 e stays finite
+// (|mu| <= 2^126 is used as the bound).
+__device__ __forceinline__ bool ffma_shift_ok(float mu) { return fabsf(mu) <= 0x1.0p126f; }
+
+template <int DT, int W>
+__device__ __forceinline__ float words_expsum_scaled(const uint32_t (&w)[W], float c) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        if constexpr (DT == kF32) {
+            acc[i & 3] += ex2(fmaf(__uint_as_float(w[i]), kLog2e, -c));
+        } else {
+            acc[(2 * i) & 3] += ex2(fmaf(word_lo<DT>(w[i]), kLog2e, -c));
+            acc[(2 * i + 1) & 3] += ex2(fmaf(word_hi<DT>(w[i]), kLog2e, -c));
+        }
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// log(sum exp) from a maximum m and a sum s of 2^(x log2 e - c), c = fl(mu log2 e):
+// s = 2^r * sum 2^((x - mu) log2 e) with r = mu log2 e - c (exact by FMA).
+__device__ __forceinline__ float finalize_scaled(float m, float s, float mu, float c) {
+    if (s != s) return s;
+    if (m == __int_as_float(0x7f800000)) return m;
+    if (m == __int_as_float(kNegInfF32)) return m;
+    const float r = fmaf(mu, kLog2e, -c);
+    return m + kLn2 * (lg2(s) - r);
+}
+
 // Fold a chunk of W raw words into an accumulator.
 template <int DT, int W>
 __device__ __forceinline__ void acc_add_words(Acc& a, float& mu, const uint32_t (&w)[W]) {

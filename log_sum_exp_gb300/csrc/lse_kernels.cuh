@@ -119,7 +119,13 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                float s = words_expsum<DT, 4 * V>(w[r], shift_of(m));
+                const float mu = shift_of(m);
+                // FFMA form for the 4-slot variants (every row longer than two
+                // vectors); same decision for the whole group.
+                const bool scaled = V == 4 && ffma_shift_ok(mu);
+                const float c = mu * kLog2e;
+                float s = scaled ? words_expsum_scaled<DT, 4 * V>(w[r], c)
+                                 : words_expsum<DT, 4 * V>(w[r], mu);
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -139,7 +145,10 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                         xt += __shfl_xor_sync(0xffffffffu, xt, off);
                     if (!valid) xt = __int_as_float(0x7fc00000);
                 }
-                if (sub == 0 && row < B) store_row(out, TL ? logprob : nullptr, row, acc_finalize(Acc{m, s}), xt);
+                if (sub == 0 && row < B) {
+                    const float lse = scaled ? finalize_scaled(m, s, mu, c) : acc_finalize(Acc{m, s});
+                    store_row(out, TL ? logprob : nullptr, row, lse, xt);
+                }
             }
         } else {
             float v[R][V];

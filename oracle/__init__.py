@@ -64,6 +64,10 @@ class OracleLib:
                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_lse_backward.restype = ctypes.c_int
+        lib.oracle_lse_strided.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_void_p]
+        lib.oracle_lse_strided.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -81,6 +85,10 @@ class OracleLib:
     def backward(self, x: np.ndarray, lse: np.ndarray, grad: np.ndarray, dtype: str = "f32",
                  row_stride: int | None = None, N: int | None = None) -> np.ndarray:
         return _backward(self._lib, x, lse, grad, dtype, row_stride, N)
+
+    def lse_strided(self, x: np.ndarray, dtype: str, A: int, R: int, C: int, stride_a: int,
+                    stride_r: int) -> np.ndarray:
+        return _lse_strided(self._lib, x, dtype, A, R, C, stride_a, stride_r)
 
 
 def _load() -> OracleLib:
@@ -114,6 +122,28 @@ def backward(x: np.ndarray, lse: np.ndarray, grad: np.ndarray, dtype: str = "f32
              row_stride: int | None = None, N: int | None = None) -> np.ndarray:
     """dx[b, n] = grad[b] * exp(x[b, n] - lse[b]) in float64, dense [B, N]."""
     return _load().backward(x, lse, grad, dtype, row_stride, N)
+
+
+def lse_strided(x: np.ndarray, dtype: str, A: int, R: int, C: int, stride_a: int,
+                stride_r: int) -> np.ndarray:
+    """out[a, c] = log sum_r exp(x[a*stride_a + r*stride_r + c]) in float64, [A, C].
+
+    ``x`` is a flat buffer of raw elements (float32, or 16-bit patterns)."""
+    return _load().lse_strided(x, dtype, A, R, C, stride_a, stride_r)
+
+
+def _lse_strided(lib, x, dtype, A, R, C, stride_a, stride_r):
+    arr = _raw(x, dtype).reshape(-1)
+    if A > 0 and R > 0 and C > 0:
+        need = (A - 1) * stride_a + (R - 1) * stride_r + C
+        if arr.size < need:
+            raise ValueError(f"buffer of {arr.size} elements, need {need}")
+    out = np.empty((A, C), np.float64)
+    rc = lib.oracle_lse_strided(arr.ctypes.data if arr.size else None, DTYPE_CODES[dtype], A, R,
+                                C, stride_a, stride_r, out.ctypes.data if out.size else None)
+    if rc != 0:
+        raise ValueError("oracle_lse_strided rejected its arguments")
+    return out
 
 
 def _shape2d(arr: np.ndarray, row_stride, N):

@@ -37,6 +37,9 @@
  *       logprob[b] = x[b, target[b]] - lse[b]   (NaN if target[b] not in [0, N))
  *   gradient of the row value (backward support, Table 3):
  *       dx[b, n] = grad[b] * exp(x[b, n] - lse[b])
+ * and the same value over a non-last dimension (probabilistic-circuit sum
+ * layers, Sec. 5.2):
+ *       out[a, c] = log sum_r exp(x[a * stride_a + r * stride_r + c])
  */
 #include <math.h>
 #include <stdint.h>
@@ -98,15 +101,16 @@ static int64_t elem_size(int dtype)
     return dtype == ORACLE_F32 ? 4 : 2;
 }
 
-/* One row: max-subtract in double (Sec. 2.1), special values as above. */
-static double lse_row(int dtype, const unsigned char *row, int64_t N)
+/* LSE of count elements at element indices 0, step, 2*step, ... from base:
+ * max-subtract in double (Sec. 2.1), special values as above. */
+static double lse_strided(int dtype, const unsigned char *base, int64_t count, int64_t step)
 {
     int any_nan = 0, any_pos_inf = 0;
     double m = -INFINITY, s = 0.0;
     int64_t n;
 
-    for (n = 0; n < N; ++n) {
-        double v = decode(dtype, row, n);
+    for (n = 0; n < count; ++n) {
+        double v = decode(dtype, base, n * step);
         if (isnan(v))
             any_nan = 1;
         else if (v == INFINITY)
@@ -121,9 +125,15 @@ static double lse_row(int dtype, const unsigned char *row, int64_t N)
     if (m == -INFINITY)
         return -INFINITY;
 
-    for (n = 0; n < N; ++n)
-        s += exp(decode(dtype, row, n) - m);
+    for (n = 0; n < count; ++n)
+        s += exp(decode(dtype, base, n * step) - m);
     return m + log(s);
+}
+
+/* One contiguous row. */
+static double lse_row(int dtype, const unsigned char *row, int64_t N)
+{
+    return lse_strided(dtype, row, N, 1);
 }
 
 /*
@@ -218,5 +228,29 @@ int oracle_lse_backward(const void *x, int dtype, int64_t B, int64_t N,
         for (n = 0; n < N; ++n)
             dx[b * N + n] = grad[b] * exp(decode(dtype, row, n) - lse[b]);
     }
+    return 0;
+}
+
+/*
+ * oracle_lse_strided: out[a * C + c] = log sum_{r<R} exp(x[a*stride_a + r*stride_r + c])
+ * for a < A, c < C (element strides).  R = 0 gives -inf.  Returns 0, or -1 on
+ * an invalid argument.
+ */
+int oracle_lse_strided(const void *x, int dtype, int64_t A, int64_t R, int64_t C,
+                       int64_t stride_a, int64_t stride_r, double *out)
+{
+    const unsigned char *base = (const unsigned char *)x;
+    int64_t a, c, es;
+
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16)
+        return -1;
+    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0)
+        return -1;
+    if (A > 0 && C > 0 && (out == NULL || (R > 0 && x == NULL)))
+        return -1;
+    es = elem_size(dtype);
+    for (a = 0; a < A; ++a)
+        for (c = 0; c < C; ++c)
+            out[a * C + c] = lse_strided(dtype, base + (a * stride_a + c) * es, R, stride_r);
     return 0;
 }

@@ -381,6 +381,48 @@ def check_backward_special(orc) -> None:
     assert np.array_equal(dx[0], [0, 0, 0, 1.5, 0]) and np.all(np.isnan(dx[1]))
 
 
+# ---------------------------------------------------------------------------
+# Strided: out[a, c] = log sum_r exp(x[a*sa + r*sr + c])
+# ---------------------------------------------------------------------------
+def check_strided_against_scipy(orc) -> None:
+    """LSE over dim 1 of an [A, R, C] array, contiguous and padded, all dtypes."""
+    from scipy.special import logsumexp
+
+    rng = np.random.default_rng(47)
+    A, R, C = 3, 37, 21
+    x = (rng.normal(0, 6, (A, R, C)) + rng.uniform(-40, 40, (A, 1, C))).astype(np.float32)
+    want = logsumexp(x.astype(np.float64), axis=1)
+    got = orc.lse_strided(x.reshape(-1), "f32", A, R, C, R * C, C)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-13)
+    pad = np.full((A, R + 2, C + 5), np.nan, np.float32)  # padded strides: never read
+    pad[:, :R, :C] = x
+    got = orc.lse_strided(pad.reshape(-1), "f32", A, R, C, (R + 2) * (C + 5), C + 5)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-13)
+    h = x.astype(np.float16)
+    got = orc.lse_strided(h.reshape(-1), "f16", A, R, C, R * C, C)
+    assert np.allclose(got, logsumexp(h.astype(np.float64), axis=1), rtol=1e-14, atol=1e-13)
+
+
+def check_strided_matches_rows(orc) -> None:
+    """A column of a matrix is the row of its transpose; stride_r = 1 with C = 1
+    is a row; R = 0 gives -inf; special values per column."""
+    rng = np.random.default_rng(53)
+    m = rng.normal(0, 4, (50, 9)).astype(np.float32)
+    m[:, 2] = -np.inf
+    m[7, 3] = np.nan
+    m[9, 4] = np.inf
+    m[:, 5] = -np.inf
+    m[11, 5] = 1.5
+    cols = orc.lse_strided(m.reshape(-1), "f32", 1, 50, 9, 0, 9)[0]
+    rows = orc.lse(np.ascontiguousarray(m.T))
+    assert np.array_equal(np.isnan(cols), np.isnan(rows))
+    assert np.array_equal(cols[~np.isnan(cols)], rows[~np.isnan(rows)])
+    assert cols[2] == -np.inf and np.isnan(cols[3]) and cols[4] == np.inf and cols[5] == 1.5
+    r = rng.normal(0, 4, 30).astype(np.float32)
+    assert orc.lse_strided(r, "f32", 1, 30, 1, 0, 1)[0, 0] == orc.lse(r[None, :])[0]
+    assert np.all(orc.lse_strided(r, "f32", 2, 0, 3, 0, 0) == -np.inf)
+
+
 ALL_CHECKS = [
     check_golden, check_decode_all_patterns, check_single_element_rows,
     check_constant_rows, check_special_values, check_two_element_closed_form,
@@ -390,4 +432,5 @@ ALL_CHECKS = [
     check_logprob_against_scipy, check_logprob_shift_invariance,
     check_backward_sums_to_grad, check_backward_finite_difference,
     check_backward_against_scipy, check_backward_special,
+    check_strided_against_scipy, check_strided_matches_rows,
 ]

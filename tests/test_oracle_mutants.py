@@ -17,13 +17,12 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "lse_oracle.c")
 
 # (name, text in the oracle, replacement)
 MUTANTS = [
-    ("drop_first_term", "for (n = 0; n < N; ++n)\n        s += exp",
-     "for (n = 1; n < N; ++n)\n        s += exp"),
-    ("drop_last_term", "for (n = 0; n < N; ++n)\n        s += exp",
-     "for (n = 0; n + 1 < N; ++n)\n        s += exp"),
+    ("drop_first_term", "for (n = 0; n < count; ++n)\n        s += exp",
+     "for (n = 1; n < count; ++n)\n        s += exp"),
     ("wrong_sign_log", "return m + log(s);", "return m - log(s);"),
-    ("wrong_sign_shift", "- m);", "+ m);"),
+    ("wrong_sign_shift", "n * step) - m);", "n * step) + m);"),
     ("min_not_max", "else if (v > m)", "else if (v < m && v > -INFINITY)"),
+    ("row_step_two", "return lse_strided(dtype, row, N, 1);", "return lse_strided(dtype, row, N / 2, 2);"),
     ("missing_nan_rule", "    if (any_nan)\n        return NAN;\n", ""),
     ("missing_pos_inf_rule", "    if (any_pos_inf)\n        return INFINITY;\n", ""),
     ("log2_not_ln", "return m + log(s);", "return m + log2(s);"),
@@ -42,6 +41,10 @@ MUTANTS = [
     ("backward_no_grad", "= grad[b] * exp(decode", "= exp(decode"),
     ("backward_sign", "exp(decode(dtype, row, n) - lse[b])", "exp(lse[b] - decode(dtype, row, n))"),
     ("backward_first_row_lse", "n) - lse[b])", "n) - lse[0])"),
+    ("strided_ignores_step", "decode(dtype, base, n * step);", "decode(dtype, base, n);"),
+    ("strided_swaps_a_and_c", "base + (a * stride_a + c) * es", "base + (c * stride_a + a) * es"),
+    ("strided_drops_last", "for (n = 0; n < count; ++n)\n        s += exp",
+     "for (n = 0; n + 1 < count; ++n)\n        s += exp"),
 ]
 
 

@@ -31,15 +31,16 @@ from log_sum_exp_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "row-wise LSE achieved HBM GB/s (% of GB300 peak) and us/call, 1 GPU"
 DEFAULT_WORKLOAD = "vocab_512x128256_f32"
+DEFAULT_COLUMNS = "pcsum_512x64x1024_f32"
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 EVENT_EVERY = 16
 OP_NAMES = {"forward": "row value", "logprob": "fused token log-probability",
-            "backward": "backward dx = g exp(x - lse)"}
+            "backward": "backward dx = g exp(x - lse)", "columns": "value over a non-last dim"}
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
                   "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
-                  "lse_backward.cu"]
+                  "lse_backward.cu", "lse_strided.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -201,6 +202,27 @@ def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float, op: str = "forwa
             "seconds": elapsed, "rows": rows_done}
 
 
+def time_oracle_columns(x3: np.ndarray, cw, budget_s: float) -> dict:
+    """The oracle's strided value over the first slices of a column workload."""
+    import oracle
+
+    A = max(1, min(cw.A, int(budget_s / 4 / max(cw.R * cw.C * 8e-9, 1e-9))))
+    sample = np.ascontiguousarray(x3[:A]).reshape(-1)
+    bytes_per = A * (cw.R * cw.C * cw.elem_bytes + cw.C * 4)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.lse_strided(sample, cw.dtype, A, cw.R, cw.C, cw.R * cw.C, cw.C)
+        reps += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s:
+            break
+    return {"value": reps * bytes_per / elapsed / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} pass(es) of the oracle's strided value over {A} of {cw.A} slices "
+                      f"[{cw.R} x {cw.C}] ({elapsed:.1f} s single-threaded)",
+            "seconds": elapsed}
+
+
 def oracle_sample_rows(w: wl.Workload, target_s: float) -> int:
     """Rows of the workload that take roughly target_s of oracle time (~5 ns/elem)."""
     per_row = w.N * 5e-9
@@ -273,8 +295,15 @@ def run_native(args) -> None:
     lse_build.build()
     import log_sum_exp_gb300 as L
 
-    w = wl.WORKLOADS[args.workload]
-    x_host = wl.generate(args.workload, seed=rank_seed(w, rank))
+    if args.op == "columns":
+        cw = wl.COLUMN_WORKLOADS[args.workload]
+        x_host = wl.generate_columns(args.workload, seed=cw.seed + 7919 * rank)
+        # Seen as B = A*C outputs of R-long strided reductions.
+        w = wl.Workload(cw.key, cw.index, cw.A * cw.C, cw.R, cw.dtype, cw.recipe)
+    else:
+        cw = None
+        w = wl.WORKLOADS[args.workload]
+        x_host = wl.generate(args.workload, seed=rank_seed(w, rank))
     xt_host = to_torch(x_host, w.dtype)
     in_bytes = w.B * w.N * w.elem_bytes
     # Rotate over enough copies that consecutive steps never find their rows in L2.
@@ -306,6 +335,15 @@ def run_native(args) -> None:
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
             L.lse_token_logprob_ptr(xp, dt, w.B, w.N, w.N, tgts[i % copies].data_ptr(), op, 0, sh)
+    elif op_name == "columns":
+        A, R, C = cw.A, cw.R, cw.C
+        plan = {"path": "columns", "launches": 1, "kernel": "lse_cols_kernel",
+                "A": A, "R": R, "C": C}
+        bytes_per_step = in_bytes + w.write_bytes
+
+        def step(i, evb=0, eve=0):
+            xp, op = ptrs[i % copies]
+            L.lse_forward_strided_ptr(xp, dt, A, R, C, R * C, C, op, 0, sh)
     else:  # backward
         lses = [L.lse_forward(x) for x in xs]
         gs = [torch.ones(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
@@ -414,7 +452,7 @@ def run_native(args) -> None:
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
     main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
-                   "backward": "lse_backward_kernel"}[plan["path"]]
+                   "backward": "lse_backward_kernel", "columns": "lse_cols_kernel"}[plan["path"]]
     traffic = ncu_traffic(args.workload, plan["path"], op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
@@ -425,14 +463,18 @@ def run_native(args) -> None:
                 "kernel_timing": timing}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rows = oracle_sample_rows(w, args.cpu_seconds / 4)
-        cpu = time_oracle(x_host[:rows], w, args.cpu_seconds, op_name)
+        if op_name == "columns":
+            cpu = time_oracle_columns(x_host, cw, args.cpu_seconds)
+        else:
+            rows = oracle_sample_rows(w, args.cpu_seconds / 4)
+            cpu = time_oracle(x_host[:rows], w, args.cpu_seconds, op_name)
     metric = METRIC if op_name == "forward" else f"{METRIC} [{OP_NAMES[op_name]}]"
     line = {
         "metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "op": op_name, "B": w.B, "N": w.N,
+                   **({"A": cw.A, "R": cw.R, "C": cw.C} if cw else {}),
                    "input_dtype": w.dtype, "row_stride": w.N, "recipe": w.recipe, "plan": plan,
                    "bytes_per_step": bytes_per_step,
                    "l2": f"inputs larger than L2: {copies} rotating copies of "
@@ -456,9 +498,13 @@ def main(argv=None) -> None:
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=list(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--op", choices=["forward", "logprob", "backward"], default="forward",
-                    help="row value (default), fused token log-probability, or backward")
+    ap.add_argument("--workload", choices=list(wl.WORKLOADS) + list(wl.COLUMN_WORKLOADS),
+                    default=None, help=f"default {DEFAULT_WORKLOAD} ({DEFAULT_COLUMNS} for "
+                                       f"--op columns)")
+    ap.add_argument("--op", choices=["forward", "logprob", "backward", "columns"],
+                    default="forward",
+                    help="row value (default), fused token log-probability, backward, or the "
+                         "value over a non-last dimension (column workloads)")
     ap.add_argument("--graph", action="store_true", help="also time CUDA-graph replay")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -466,6 +512,10 @@ def main(argv=None) -> None:
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload is None:
+        args.workload = DEFAULT_COLUMNS if args.op == "columns" else DEFAULT_WORKLOAD
+    if (args.op == "columns") != (args.workload in wl.COLUMN_WORKLOADS):
+        ap.error("--op columns runs the column workloads, the other ops the row workloads")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -187,6 +187,27 @@ LSE_API lse_status lse_backward(const void *x, lse_dtype dtype, int64_t B, int64
                                 void *dx, int64_t dx_row_stride, lse_stream_t stream);
 
 /*
+ * lse_forward_strided -- the same value over a non-last dimension:
+ *
+ *     out[a * C + c] = log sum_{r < R} exp(x[a * stride_a + r * stride_r + c])
+ *
+ * for a < A, c < C (element strides; c is the contiguous index).  This is the
+ * reduction of a probabilistic-circuit sum layer over each node's children
+ * (Sec. 5.2), or a column LSE of a matrix (A = 1).  One pass over x.
+ *   out      device pointer to A * C floats (row-major [A, C]); must not
+ *            overlap x.
+ *   splits   rows per column split across CTAs: 0 = chosen to fill the GPU;
+ *            k >= 1 forces k (<= R, <= 65535).  With splits > 1 the call takes
+ *            A * C * splits * 8 bytes of stream-ordered scratch and a merge kernel.
+ * R == 0 gives -inf; A == 0 or C == 0 is a no-op.  Special values as in
+ * lse_forward, per (a, c).  16-byte aligned layouts with C a multiple of the
+ * elements per 16 bytes take vector loads; others element loads.
+ */
+LSE_API lse_status lse_forward_strided(const void *x, lse_dtype dtype, int64_t A, int64_t R,
+                                       int64_t C, int64_t stride_a, int64_t stride_r, float *out,
+                                       int64_t splits, lse_stream_t stream);
+
+/*
  * lse_trim_memory -- return the current device's cached stream-ordered memory
  * to the system.  Split-row scratch and lse_forward_host's staging buffers come
  * from a library-owned memory pool that keeps freed blocks mapped for reuse by

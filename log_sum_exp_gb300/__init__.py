@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     LsePlan,
     library_path,
     load,
+    logsumexp,
     lse_backward,
     lse_backward_ptr,
     lse_forward,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     lse_forward_plan_ptr,
     lse_forward_ptr,
     lse_forward_split_static_ptr,
+    lse_forward_strided_ptr,
     lse_plan_query,
     lse_plan_query_ptr,
     lse_token_logprob,

@@ -21,7 +21,8 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
-                 "lse_token_logprob", "lse_token_logprob_plan", "lse_backward", "lse_trim_memory",
+                 "lse_token_logprob", "lse_token_logprob_plan", "lse_backward",
+                 "lse_forward_strided", "lse_trim_memory",
                  "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
 
 
@@ -92,6 +93,8 @@ def load() -> ctypes.CDLL:
         lib.lse_token_logprob_plan.restype = i32
         lib.lse_backward.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, i64, vp]
         lib.lse_backward.restype = i32
+        lib.lse_forward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i64, vp]
+        lib.lse_forward_strided.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
@@ -165,6 +168,13 @@ def lse_backward_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, ls
     _check(load().lse_backward(x_ptr or None, DTYPES[dtype], B, N, row_stride, lse_ptr or None,
                                grad_ptr or None, dx_ptr or None, dx_row_stride, stream or None),
            "lse_backward")
+
+
+def lse_forward_strided_ptr(x_ptr: int, dtype: str, A: int, R: int, C: int, stride_a: int,
+                            stride_r: int, out_ptr: int, splits: int = 0, stream: int = 0) -> None:
+    _check(load().lse_forward_strided(x_ptr or None, DTYPES[dtype], A, R, C, stride_a, stride_r,
+                                      out_ptr or None, splits, stream or None),
+           "lse_forward_strided")
 
 
 def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
@@ -329,6 +339,43 @@ def lse_backward(x, lse, grad, dx=None, stream=None):
         lse_backward_ptr(x.data_ptr(), dt, B, N, row_stride, lse.data_ptr(), grad.data_ptr(),
                          dx.data_ptr(), dx_stride, _stream_handle(stream, x.device))
     return dx
+
+
+def logsumexp(x, dim=-1, stream=None):
+    """torch.logsumexp(x, dim) on liblse for CUDA tensors, computed in f32.
+
+    The reduced dimension may be any dimension; the tensor's other dimensions
+    must collapse to (outer, inner) with the inner one contiguous (any
+    contiguous tensor qualifies).  Returns float32 with ``dim`` removed.
+    """
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    dt = _dtype_name(x)
+    nd = x.dim()
+    if nd == 0:
+        raise ValueError("x must have at least one dimension")
+    d = dim % nd
+    shape = list(x.shape)
+    R = shape[d]
+    outer = 1
+    for n in shape[:d]:
+        outer *= n
+    inner = 1
+    for n in shape[d + 1:]:
+        inner *= n
+    out_shape = shape[:d] + shape[d + 1:]
+    if not x.is_contiguous():
+        raise ValueError("logsumexp needs a contiguous tensor")
+    out = torch.empty(out_shape, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        if inner == 1:
+            lse_forward_ptr(x.data_ptr(), dt, outer, R, R, out.data_ptr(),
+                            _stream_handle(stream, x.device))
+        else:
+            lse_forward_strided_ptr(x.data_ptr(), dt, outer, R, inner, R * inner, inner,
+                                    out.data_ptr(), 0, _stream_handle(stream, x.device))
+    return out
 
 
 def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,

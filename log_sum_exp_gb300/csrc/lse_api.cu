@@ -511,6 +511,85 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
+lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_t R, int64_t C,
+                               int64_t stride_a, int64_t stride_r, float* out, int64_t splits,
+                               lse_stream_t stream_) {
+    if (!valid_dtype(dtype)) return LSE_ERR_UNSUPPORTED_DTYPE;
+    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0 || splits < 0)
+        return LSE_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    int64_t outputs = 0, extent = 0, t = 0;
+    if (__builtin_mul_overflow(A, C, &outputs) || outputs > INT64_MAX / 8) return LSE_ERR_INVALID_ARG;
+    if (A > 0 && R > 0 && C > 0) {
+        if (__builtin_mul_overflow(A - 1, stride_a, &extent) ||
+            __builtin_mul_overflow(R - 1, stride_r, &t) || __builtin_add_overflow(extent, t, &extent) ||
+            __builtin_add_overflow(extent, C, &extent) ||
+            __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &extent))
+            return LSE_ERR_INVALID_ARG;
+    }
+    if (outputs == 0) return LSE_OK;
+    if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u)) return LSE_ERR_INVALID_ARG;
+    if (R > 0 && x == nullptr) return LSE_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    lse_status st = device_info(&dev, &info);
+    if (st != LSE_OK) return st;
+    if (R == 0) {
+        const cudaError_t e = launch_fill_neg_inf(out, nullptr, outputs, stream);
+        return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+    }
+    const int64_t epv16 = 16 / eb;
+    const bool vec = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (stride_r * eb) % 16 == 0 &&
+                     (stride_a * eb) % 16 == 0 && C % epv16 == 0;
+    const int64_t tiles = ceil_div(C, cols_columns_per_cta(vec, dtype));
+    const int64_t gy = A < 65535 ? A : 65535;
+    // Rows split across CTAs (blockIdx.z) when the column tiles alone do not
+    // cover the GPU ~8 times; each split keeps >= 2 batches of rows.
+    int64_t P = splits;
+    if (P == 0) {
+        const int64_t resident = static_cast<int64_t>(info->sms) * cols_occupancy(dtype, vec);
+        const int64_t ctas = tiles * gy;
+        P = ctas >= 8 * resident ? 1 : ceil_div(8 * resident, ctas);
+        const int64_t max_p = R / (2 * cols_rows_per_batch(vec));
+        if (P > max_p) P = max_p;
+        if (P < 1) P = 1;
+    }
+    if (P > R) return LSE_ERR_INVALID_ARG;
+    const int64_t rows_per_split = ceil_div(R, P);
+    P = ceil_div(R, rows_per_split);
+    if (P > 65535 || tiles > INT_MAX) return LSE_ERR_INVALID_ARG;
+    if (P > 1 && outputs > INT64_MAX / (8 * P)) return LSE_ERR_INVALID_ARG;
+
+    float2* scratch = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (P > 1) {
+        e = scratch_alloc(*info, reinterpret_cast<void**>(&scratch),
+                          static_cast<size_t>(outputs * P) * sizeof(float2), stream);
+        if (e != cudaSuccess) return cuda_fail(e, LSE_ERR_ALLOC);
+    }
+    StridedArgs a;
+    a.x = x;
+    a.A = A;
+    a.R = R;
+    a.C = C;
+    a.stride_a = stride_a;
+    a.stride_r = stride_r;
+    a.rows_per_split = rows_per_split;
+    a.out = out;
+    a.partial = scratch;
+    a.P = P;
+    a.grid = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(gy), static_cast<unsigned>(P));
+    a.stream = stream;
+    e = launch_cols(dtype, vec, a);
+    if (e == cudaSuccess && P > 1) e = launch_merge(scratch, nullptr, outputs, P, out, nullptr, stream);
+    if (scratch) {
+        const cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
 lse_status lse_token_logprob(const void* x, lse_dtype dtype, int64_t B, int64_t N,
                              int64_t row_stride, const int64_t* target, float* logprob,
                              float* lse_out, lse_stream_t stream) {

@@ -93,6 +93,26 @@ cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a);
 int backward_slots_per_thread();
 int backward_threads();
 
+// Strided / column reduction (lse_strided.cu).
+struct StridedArgs {
+    const void* x;
+    int64_t A;
+    int64_t R;
+    int64_t C;
+    int64_t stride_a;
+    int64_t stride_r;
+    int64_t rows_per_split;
+    float* out;
+    float2* partial;  // [A * C, P] when P > 1
+    int64_t P;
+    dim3 grid;
+    cudaStream_t stream;
+};
+cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a);
+int cols_occupancy(int dt, bool vec);
+int cols_columns_per_cta(bool vec, int dt);
+int cols_rows_per_batch(bool vec);
+
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);
 

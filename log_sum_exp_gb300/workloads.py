@@ -173,6 +173,67 @@ _GENERATORS = {1: _gen_small, 2: _gen_vocab128k, 3: _gen_vocab32k_bf16, 4: _gen_
                5: _gen_particles}
 
 
+@dataclasses.dataclass(frozen=True)
+class ColumnWorkload:
+    """x: [A, R, C]; the value is taken over R (a non-last dimension)."""
+    key: str
+    index: int
+    A: int
+    R: int
+    C: int
+    dtype: str
+    recipe: str
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def read_bytes(self) -> int:
+        return self.A * self.R * self.C * self.elem_bytes
+
+    @property
+    def write_bytes(self) -> int:
+        return self.A * self.C * 4
+
+    @property
+    def seed(self) -> int:
+        return SEED_BASE + self.index
+
+
+COLUMN_WORKLOADS = {
+    w.key: w for w in [
+        ColumnWorkload("pcsum_512x64x1024_f32", 11, 512, 64, 1024, "f32",
+                       "sum-layer log-weights: x[batch a, child r, node c] ~ U(-30,0), each entry "
+                       "-inf with p=0.1; the value is over the 64 children of each node"),
+        ColumnWorkload("columns_1x8192x16384_f32", 12, 1, 8192, 16384, "f32",
+                       "column LSE of a tall matrix: x ~ N(0, 3^2) + per-column offset U(-20,20)"),
+    ]
+}
+
+
+def generate_columns(key: str, A: int | None = None, R: int | None = None,
+                     C: int | None = None, seed: int | None = None) -> np.ndarray:
+    """A column workload's input as a contiguous [A, R, C] float32 array."""
+    w = COLUMN_WORKLOADS[key]
+    A = w.A if A is None else A
+    R = w.R if R is None else R
+    C = w.C if C is None else C
+    rng = _rng(w.seed if seed is None else seed)
+    x = np.empty((A, R, C), dtype=np.float32)
+    if w.index == 11:
+        _fill_uniform01(rng, x)
+        x *= np.float32(-30.0)
+        mask = np.empty_like(x)
+        _fill_uniform01(rng, mask)
+        x[mask < np.float32(0.1)] = -np.inf
+    else:
+        _fill_normal(rng, x)
+        x *= np.float32(3.0)
+        x += rng.uniform(-20.0, 20.0, size=(1, 1, C)).astype(np.float32)
+    return x
+
+
 def random_rows(B: int, N: int, dtype: str = "f32", seed: int = 0, scale: float = 4.0,
                 shift: float = 0.0) -> np.ndarray:
     """Generic seeded rows ``shift + scale * z`` for edge-shape tests.

@@ -1,0 +1,94 @@
+"""GPU parity of lse_forward_strided (the value over a non-last dimension)
+against the fp64 oracle: out[a, c] = log sum_r exp(x[a*sa + r*sr + c])."""
+import numpy as np
+import pytest
+
+import oracle
+from log_sum_exp_gb300 import workloads as wl
+from lse_testutil import canary_array, compare, torch_view
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import log_sum_exp_gb300 as L  # noqa: E402
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_strided(x3, dtype, pad_r=0, pad_c=0, pad_a=0, offset=0, splits=0):
+    """Place x [A, R, C] in a NaN-canaried buffer with padded strides and run."""
+    A, R, C = x3.shape
+    sr = C + pad_c
+    sa = R * sr + pad_a + pad_r * sr
+    total = offset + max(A, 1) * sa + 64
+    host = canary_array(total, dtype)
+    for a in range(A):
+        blk = host[offset + a * sa: offset + a * sa + R * sr].reshape(R, sr)
+        blk[:, :C] = x3[a] if dtype == "f32" else x3[a].view(np.uint16)
+    buf = torch_view(host, dtype).cuda()
+    eb = 4 if dtype == "f32" else 2
+    out = torch.full((A * C + 16,), float("nan"), device="cuda")
+    L.lse_forward_strided_ptr(buf.data_ptr() + offset * eb, dtype, A, R, C, sa, sr, out.data_ptr(),
+                              splits, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.all(np.isnan(o[A * C:])), "write past out[A*C-1]"
+    want = oracle.lse_strided(host[offset:], dtype, A, R, C, sa, sr)
+    return o[:A * C].reshape(A, C), want
+
+
+@pytest.mark.parametrize("key", list(wl.COLUMN_WORKLOADS))
+def test_column_workloads(key):
+    _need_gpu()
+    x = wl.generate_columns(key)
+    got, want = run_strided(x, "f32")
+    print(key, compare(got, want))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("A,R,C", [(1, 1, 1), (1, 5, 3), (2, 1, 64), (3, 7, 8), (2, 33, 129),
+                                   (5, 64, 1000), (1, 300, 256), (1, 1000, 17), (4, 2, 4096)])
+def test_strided_edge_shapes(dtype, A, R, C):
+    _need_gpu()
+    x = wl.random_rows(A * R, C, dtype, seed=A * 1000 + R * 10 + C, scale=5.0).reshape(A, R, C)
+    if R >= 3 and C >= 4:
+        xi = x.view(np.uint16) if dtype != "f32" else x
+        xi[0, :, 1] = {"f32": -np.inf, "bf16": 0xFF80, "f16": 0xFC00}[dtype]
+        xi[0, R // 2, 2] = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+        xi[A - 1, R - 1, 3] = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+    for lay in (dict(), dict(pad_c=8), dict(pad_c=3), dict(offset=1), dict(pad_a=8, pad_r=1)):
+        for splits in (0, 1, 2, 3):
+            if splits > R:
+                continue
+            got, want = run_strided(x, dtype, splits=splits, **lay)
+            try:
+                compare(got, want)
+            except AssertionError as e:
+                raise AssertionError(f"layout {lay} splits {splits}: {e}") from None
+
+
+def test_strided_degenerate():
+    _need_gpu()
+    out = torch.full((6,), 7.0, device="cuda")
+    x = torch.zeros(16, device="cuda")
+    L.lse_forward_strided_ptr(x.data_ptr(), "f32", 2, 0, 3, 0, 0, out.data_ptr())
+    torch.cuda.synchronize()
+    assert np.all(out.cpu().numpy() == -np.inf)
+    L.lse_forward_strided_ptr(x.data_ptr(), "f32", 0, 4, 3, 12, 3, out.data_ptr())  # no-op
+    with pytest.raises(L.LseError):
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, -3, out.data_ptr())
+    with pytest.raises(L.LseError):
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, 3, out.data_ptr(), splits=5)
+
+
+def test_logsumexp_any_dim():
+    _need_gpu()
+    x = wl.random_rows(6 * 40, 33, "f32", seed=9, scale=6.0).reshape(6, 40, 33)
+    xd = torch.from_numpy(x).cuda()
+    for dim in (0, 1, 2, -1):
+        got = L.logsumexp(xd, dim=dim).cpu().numpy()
+        want = torch.logsumexp(torch.from_numpy(x).double(), dim=dim).numpy()
+        compare(got, want)

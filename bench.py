@@ -337,13 +337,14 @@ def run_native(args) -> None:
             L.lse_token_logprob_ptr(xp, dt, w.B, w.N, w.N, tgts[i % copies].data_ptr(), op, 0, sh)
     elif op_name == "columns":
         A, R, C = cw.A, cw.R, cw.C
-        plan = {"path": "columns", "launches": 1, "kernel": "lse_cols_kernel",
-                "A": A, "R": R, "C": C}
+        plan = L.lse_forward_strided_ptr(ptrs[0][0], dt, A, R, C, R * C, C, ptrs[0][1], sh,
+                                         args.plan).as_dict()
         bytes_per_step = in_bytes + w.write_bytes
+        req = L._binding._as_plan(args.plan) if args.plan else None
 
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
-            L.lse_forward_strided_ptr(xp, dt, A, R, C, R * C, C, op, 0, sh)
+            L.lse_forward_strided_ptr(xp, dt, A, R, C, R * C, C, op, sh, req)
     else:  # backward
         lses = [L.lse_forward(x) for x in xs]
         gs = [torch.ones(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
@@ -452,7 +453,8 @@ def run_native(args) -> None:
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
     main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
-                   "backward": "lse_backward_kernel", "columns": "lse_cols_kernel"}[plan["path"]]
+                   "backward": "lse_backward_kernel", "columns_warp": "lse_cols_kernel",
+                   "columns_cta": "lse_cols_kernel"}[plan["path"]]
     traffic = ncu_traffic(args.workload, plan["path"], op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
@@ -506,6 +508,8 @@ def main(argv=None) -> None:
                     help="row value (default), fused token log-probability, backward, or the "
                          "value over a non-last dimension (column workloads)")
     ap.add_argument("--graph", action="store_true", help="also time CUDA-graph replay")
+    ap.add_argument("--plan", type=json.loads, default=None,
+                    help='forced plan for --op columns as JSON, e.g. {"path": "columns_cta"}')
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

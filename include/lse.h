@@ -75,8 +75,11 @@ typedef enum {
     LSE_PATH_EMPTY = 1,   /* N == 0: one fill kernel writes -inf           */
     LSE_PATH_SUBWARP = 2, /* short rows: a group of 1..32 lanes per row     */
     LSE_PATH_CTA = 3,     /* one CTA (1..8 warps) per row, online (m, s)    */
-    LSE_PATH_SPLIT = 4    /* `splits` CTAs per row write (m, s) partials;
+    LSE_PATH_SPLIT = 4,   /* `splits` CTAs per row write (m, s) partials;
                              a second small kernel merges them in order   */
+    LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
+    LSE_PATH_COLUMNS_CTA = 6   /* lse_forward_strided: a CTA's 8 warps share the
+                                  rows of one column tile                       */
 } lse_path;
 
 /*
@@ -196,16 +199,20 @@ LSE_API lse_status lse_backward(const void *x, lse_dtype dtype, int64_t B, int64
  * (Sec. 5.2), or a column LSE of a matrix (A = 1).  One pass over x.
  *   out      device pointer to A * C floats (row-major [A, C]); must not
  *            overlap x.
- *   splits   rows per column split across CTAs: 0 = chosen to fill the GPU;
- *            k >= 1 forces k (<= R, <= 65535).  With splits > 1 the call takes
- *            A * C * splits * 8 bytes of stream-ordered scratch and a merge kernel.
+ *   plan     NULL (automatic) or an lse_plan: path 0, LSE_PATH_COLUMNS_WARP
+ *            (one warp per 32-lane column tile, for short reductions) or
+ *            LSE_PATH_COLUMNS_CTA (a CTA's warps interleave the rows of one
+ *            tile); splits 0 (automatic) or k >= 1 (<= R, <= 65535) row splits
+ *            across CTAs -- with k > 1 the call takes A * C * k * 8 bytes of
+ *            stream-ordered scratch and a merge kernel; vector_bytes as for
+ *            lse_forward_plan.  On return *plan holds the plan that ran.
  * R == 0 gives -inf; A == 0 or C == 0 is a no-op.  Special values as in
  * lse_forward, per (a, c).  16-byte aligned layouts with C a multiple of the
  * elements per 16 bytes take vector loads; others element loads.
  */
 LSE_API lse_status lse_forward_strided(const void *x, lse_dtype dtype, int64_t A, int64_t R,
                                        int64_t C, int64_t stride_a, int64_t stride_r, float *out,
-                                       int64_t splits, lse_stream_t stream);
+                                       lse_stream_t stream, lse_plan *plan);
 
 /*
  * lse_trim_memory -- return the current device's cached stream-ordered memory

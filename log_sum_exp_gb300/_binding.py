@@ -16,7 +16,8 @@ LSE_OK = 0
 STATUS_NAMES = {0: "LSE_OK", 1: "LSE_ERR_INVALID_ARG", 2: "LSE_ERR_UNSUPPORTED_DTYPE",
                 3: "LSE_ERR_ALLOC", 4: "LSE_ERR_CUDA"}
 DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
-PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4}
+PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4, "columns_warp": 5,
+         "columns_cta": 6}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
@@ -93,7 +94,8 @@ def load() -> ctypes.CDLL:
         lib.lse_token_logprob_plan.restype = i32
         lib.lse_backward.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, i64, vp]
         lib.lse_backward.restype = i32
-        lib.lse_forward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i64, vp]
+        lib.lse_forward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, vp,
+                                            ctypes.POINTER(LsePlan)]
         lib.lse_forward_strided.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
@@ -171,10 +173,13 @@ def lse_backward_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, ls
 
 
 def lse_forward_strided_ptr(x_ptr: int, dtype: str, A: int, R: int, C: int, stride_a: int,
-                            stride_r: int, out_ptr: int, splits: int = 0, stream: int = 0) -> None:
+                            stride_r: int, out_ptr: int, stream: int = 0,
+                            plan: LsePlan | dict | None = None) -> LsePlan:
+    p = _as_plan(plan) if plan is not None else LsePlan()
     _check(load().lse_forward_strided(x_ptr or None, DTYPES[dtype], A, R, C, stride_a, stride_r,
-                                      out_ptr or None, splits, stream or None),
+                                      out_ptr or None, stream or None, ctypes.byref(p)),
            "lse_forward_strided")
+    return p
 
 
 def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
@@ -374,7 +379,7 @@ def logsumexp(x, dim=-1, stream=None):
                             _stream_handle(stream, x.device))
         else:
             lse_forward_strided_ptr(x.data_ptr(), dt, outer, R, inner, R * inner, inner,
-                                    out.data_ptr(), 0, _stream_handle(stream, x.device))
+                                    out.data_ptr(), _stream_handle(stream, x.device))
     return out
 
 

@@ -512,11 +512,10 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
 }
 
 lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_t R, int64_t C,
-                               int64_t stride_a, int64_t stride_r, float* out, int64_t splits,
-                               lse_stream_t stream_) {
+                               int64_t stride_a, int64_t stride_r, float* out,
+                               lse_stream_t stream_, lse_plan* plan) {
     if (!valid_dtype(dtype)) return LSE_ERR_UNSUPPORTED_DTYPE;
-    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0 || splits < 0)
-        return LSE_ERR_INVALID_ARG;
+    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0) return LSE_ERR_INVALID_ARG;
     const int eb = elem_bytes(dtype);
     int64_t outputs = 0, extent = 0, t = 0;
     if (__builtin_mul_overflow(A, C, &outputs) || outputs > INT64_MAX / 8) return LSE_ERR_INVALID_ARG;
@@ -527,6 +526,12 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
             __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &extent))
             return LSE_ERR_INVALID_ARG;
     }
+    const lse_plan* req = plan;
+    const int rpath = req ? req->path : LSE_PATH_AUTO;
+    if (rpath != LSE_PATH_AUTO && rpath != LSE_PATH_COLUMNS_WARP && rpath != LSE_PATH_COLUMNS_CTA &&
+        rpath != LSE_PATH_EMPTY)
+        return LSE_ERR_INVALID_ARG;
+    if (req && req->splits < 0) return LSE_ERR_INVALID_ARG;
     if (outputs == 0) return LSE_OK;
     if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u)) return LSE_ERR_INVALID_ARG;
     if (R > 0 && x == nullptr) return LSE_ERR_INVALID_ARG;
@@ -535,37 +540,76 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     const DeviceInfo* info = nullptr;
     lse_status st = device_info(&dev, &info);
     if (st != LSE_OK) return st;
+    lse_plan p;
+    std::memset(&p, 0, sizeof p);
     if (R == 0) {
+        if (rpath != LSE_PATH_AUTO && rpath != LSE_PATH_EMPTY) return LSE_ERR_INVALID_ARG;
+        p.path = LSE_PATH_EMPTY;
+        p.splits = 1;
+        p.launches = 1;
+        p.grid = ceil_div(outputs, 256);
+        if (plan) *plan = p;
         const cudaError_t e = launch_fill_neg_inf(out, nullptr, outputs, stream);
         return e == cudaSuccess ? LSE_OK : cuda_fail(e);
     }
+    if (rpath == LSE_PATH_EMPTY) return LSE_ERR_INVALID_ARG;
     const int64_t epv16 = 16 / eb;
-    const bool vec = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (stride_r * eb) % 16 == 0 &&
-                     (stride_a * eb) % 16 == 0 && C % epv16 == 0;
-    const int64_t tiles = ceil_div(C, cols_columns_per_cta(vec, dtype));
+    const bool aligned = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (stride_r * eb) % 16 == 0 &&
+                         (stride_a * eb) % 16 == 0 && C % epv16 == 0;
+    bool vec = aligned;
+    if (req && req->vector_bytes) {
+        if (req->vector_bytes == 16) {
+            if (!aligned) return LSE_ERR_INVALID_ARG;
+        } else if (req->vector_bytes != 1) {
+            return LSE_ERR_INVALID_ARG;
+        }
+        vec = req->vector_bytes == 16;
+    }
+    const int W = cols_warps_per_cta();
+    const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
     const int64_t gy = A < 65535 ? A : 65535;
-    // Rows split across CTAs (blockIdx.z) when the column tiles alone do not
-    // cover the GPU ~8 times; each split keeps >= 2 batches of rows.
-    int64_t P = splits;
+    const int64_t resident_warps = static_cast<int64_t>(info->sms) * W * cols_occupancy(dtype, vec);
+    const int64_t batch = cols_rows_per_batch(vec);
+    // One warp per tile when the reduction is short or the tiles alone fill
+    // the GPU; otherwise the CTA's warps share a tile's rows.
+    int path = rpath;
+    if (path == LSE_PATH_AUTO)
+        path = (R <= 256 || wtiles * gy >= 2 * resident_warps) ? LSE_PATH_COLUMNS_WARP
+                                                                  : LSE_PATH_COLUMNS_CTA;
+    const bool rowsplit = path == LSE_PATH_COLUMNS_CTA;
+    const int64_t gx = rowsplit ? wtiles : ceil_div(wtiles, W);
+    const int64_t warps_busy = rowsplit ? gx * gy * W : wtiles * gy;  // warps with work per split
+    const int64_t rows_per_warp_batch = rowsplit ? W * batch : batch;
+    int64_t P = req ? req->splits : 0;
     if (P == 0) {
-        const int64_t resident = static_cast<int64_t>(info->sms) * cols_occupancy(dtype, vec);
-        const int64_t ctas = tiles * gy;
-        P = ctas >= 8 * resident ? 1 : ceil_div(8 * resident, ctas);
-        const int64_t max_p = R / (2 * cols_rows_per_batch(vec));
+        // No split while the tiles keep half the resident warps busy (a split
+        // costs a merge kernel); otherwise just enough splits to cover the GPU
+        // once, keeping >= 4 batches per warp in every split.
+        P = 2 * warps_busy >= resident_warps ? 1 : ceil_div(resident_warps, warps_busy);
+        const int64_t max_p = R / (4 * rows_per_warp_batch);
         if (P > max_p) P = max_p;
         if (P < 1) P = 1;
     }
     if (P > R) return LSE_ERR_INVALID_ARG;
     const int64_t rows_per_split = ceil_div(R, P);
     P = ceil_div(R, rows_per_split);
-    if (P > 65535 || tiles > INT_MAX) return LSE_ERR_INVALID_ARG;
+    if (P > 65535 || gx > INT_MAX) return LSE_ERR_INVALID_ARG;
     if (P > 1 && outputs > INT64_MAX / (8 * P)) return LSE_ERR_INVALID_ARG;
+    p.path = path;
+    p.vector_bytes = vec ? 16 : 1;
+    p.threads = 32 * W;
+    p.splits = P;
+    p.segment_slots = rows_per_split;
+    p.grid = gx * gy * P;
+    p.scratch_bytes = P > 1 ? outputs * P * static_cast<int64_t>(sizeof(float2)) : 0;
+    p.launches = P > 1 ? 2 : 1;
+    if (plan) *plan = p;
 
     float2* scratch = nullptr;
     cudaError_t e = cudaSuccess;
     if (P > 1) {
         e = scratch_alloc(*info, reinterpret_cast<void**>(&scratch),
-                          static_cast<size_t>(outputs * P) * sizeof(float2), stream);
+                          static_cast<size_t>(p.scratch_bytes), stream);
         if (e != cudaSuccess) return cuda_fail(e, LSE_ERR_ALLOC);
     }
     StridedArgs a;
@@ -579,10 +623,11 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     a.out = out;
     a.partial = scratch;
     a.P = P;
-    a.grid = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(gy), static_cast<unsigned>(P));
+    a.rowsplit = rowsplit;
+    a.grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(P));
     a.stream = stream;
     e = launch_cols(dtype, vec, a);
-    if (e == cudaSuccess && P > 1) e = launch_merge(scratch, nullptr, outputs, P, out, nullptr, stream);
+    if (e == cudaSuccess && P > 1) e = launch_merge_columns(scratch, outputs, P, out, stream);
     if (scratch) {
         const cudaError_t ef = cudaFreeAsync(scratch, stream);
         if (e == cudaSuccess) e = ef;

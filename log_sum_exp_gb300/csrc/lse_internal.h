@@ -103,15 +103,19 @@ struct StridedArgs {
     int64_t stride_r;
     int64_t rows_per_split;
     float* out;
-    float2* partial;  // [A * C, P] when P > 1
+    float2* partial;  // [P, A * C] when P > 1
     int64_t P;
+    bool rowsplit;    // a CTA's warps share a column tile and split its rows
     dim3 grid;
     cudaStream_t stream;
 };
 cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a);
+cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t P, float* out,
+                                 cudaStream_t stream);
 int cols_occupancy(int dt, bool vec);
-int cols_columns_per_cta(bool vec, int dt);
-int cols_rows_per_batch(bool vec);
+int cols_columns_per_warp(bool vec, int dt);
+int cols_rows_per_batch(bool vec);  // per warp per iteration
+int cols_warps_per_cta();
 
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);

@@ -8,13 +8,15 @@
 // matrix.  One pass over x, per-column online (m, s) accumulators, the same
 // pairwise merge and finalize as the row kernels (lse_device.cuh).
 //
-// Mapping: a CTA of 8 warps covers one column tile of 32 lanes x EPV columns
-// (EPV = elements per 16-byte vector, or 1 when the layout is not 16-byte
-// aligned) of one index a.  Warp w reads rows w, w + 8, ... so each load
-// instruction covers one contiguous stretch of a row; a thread folds U rows
-// per batch into EPV accumulators with one rescale per batch.  Shared memory
-// merges the 8 warps.  With P > 1 the rows are split across blockIdx.z and
-// the (m, s) partials [A * C, P] go to the row path's merge kernel.
+// Mapping: a column tile is 32 lanes x EPV columns (EPV = elements per
+// 16-byte vector, or 1 when the layout is not 16-byte aligned) of one index a;
+// every load instruction of a warp covers one contiguous stretch of a row, and
+// a thread folds U rows per batch into EPV accumulators with one rescale per
+// batch.  Two ways to share the work (see lse_cols_kernel): one warp per tile
+// walking all rows, or a CTA's 8 warps interleaving the rows of one tile and
+// merging in shared memory.  With P > 1 the rows are also split across
+// blockIdx.z; the (m, s) partials are stored split-major, [P, A * C], and
+// merge_columns_kernel combines them with one thread per output.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -28,22 +30,29 @@ namespace {
 constexpr int kColWarps = 8;
 constexpr int kColThreads = 32 * kColWarps;
 
-template <int DT, bool VEC>
+// ROWSPLIT: the CTA's 8 warps share one column tile and interleave its rows
+// (merged in shared memory) -- for long reductions.  !ROWSPLIT: each warp owns
+// its own column tile (tile = blockIdx.x * 8 + warp) and walks all rows of the
+// split itself -- for short reductions, no cross-warp merge.
+template <int DT, bool VEC, bool ROWSPLIT>
 __global__ void __launch_bounds__(kColThreads)
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
-    constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
-    __shared__ float2 part[kColWarps][32][EPV];
+    constexpr int U = VEC ? 4 : 8;                    // rows per batch per thread
+    constexpr int RSTEP = ROWSPLIT ? kColWarps : 1;   // row interleave between warps
+    __shared__ float2 part[ROWSPLIT ? kColWarps : 1][32][EPV];
 
     pdl_trigger();
     pdl_wait();
 
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * EPV;
+    const int64_t tile = ROWSPLIT ? static_cast<int64_t>(blockIdx.x)
+                                  : static_cast<int64_t>(blockIdx.x) * kColWarps + wid;
+    const int64_t c0 = (tile * 32 + lane) * EPV;
     const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
     const int64_t split = blockIdx.z;
     const int64_t r_begin = split * rows_per_split;
@@ -59,11 +68,11 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             acc[e] = acc_identity();
             mu[e] = 0.0f;
         }
-        for (int64_t r = r_begin + wid; r < r_end; r += static_cast<int64_t>(kColWarps) * U) {
+        for (int64_t r = r_begin + (ROWSPLIT ? wid : 0); r < r_end; r += static_cast<int64_t>(RSTEP) * U) {
             float v[U][EPV];
 #pragma unroll
             for (int j = 0; j < U; ++j) {
-                const int64_t rr = r + j * kColWarps;
+                const int64_t rr = r + j * RSTEP;
                 const bool ok = active && rr < r_end;
                 if constexpr (VEC) {
                     uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
@@ -88,39 +97,70 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                 acc[e].s += sum;
             }
         }
+        if constexpr (ROWSPLIT) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) part[wid][lane][e] = make_float2(acc[e].m, acc[e].s);
-        __syncthreads();
-        if (wid == 0 && active) {
+            for (int e = 0; e < EPV; ++e) part[wid][lane][e] = make_float2(acc[e].m, acc[e].s);
+            __syncthreads();
+            if (wid == 0 && active) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    Acc t = acc_identity();
+#pragma unroll
+                    for (int w = 0; w < kColWarps; ++w)
+                        t = acc_merge(t, Acc{part[w][lane][e].x, part[w][lane][e].y});
+                    acc[e] = t;
+                }
+            }
+            __syncthreads();  // part[] is reused by the next a
+        }
+        if ((!ROWSPLIT || wid == 0) && active) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                Acc t = acc_identity();
-#pragma unroll
-                for (int w = 0; w < kColWarps; ++w) t = acc_merge(t, Acc{part[w][lane][e].x, part[w][lane][e].y});
                 const int64_t c = c0 + e;
                 if (c < C) {
                     if (P == 1)
-                        out[a * C + c] = acc_finalize(t);
-                    else
-                        partial[(a * C + c) * P + split] = make_float2(t.m, t.s);
+                        out[a * C + c] = acc_finalize(acc[e]);
+                    else  // split-major: coalesced here and in merge_columns_kernel
+                        partial[split * (A * C) + a * C + c] = make_float2(acc[e].m, acc[e].s);
                 }
             }
         }
-        __syncthreads();  // part[] is reused by the next a
+    }
+}
+
+// One thread per output (a, c): merges its P partials in split order.
+__global__ void __launch_bounds__(256)
+merge_columns_kernel(const float2* __restrict__ partial, int64_t outputs, int64_t P,
+                     float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < outputs;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        Acc t = acc_identity();
+        for (int64_t p = 0; p < P; ++p) {
+            const float2 v = partial[p * outputs + i];
+            t = acc_merge(t, Acc{v.x, v.y});
+        }
+        out[i] = acc_finalize(t);
     }
 }
 
 template <int DT, bool VEC>
 cudaError_t launch_cols_t(const StridedArgs& a) {
-    return launch_pdl(lse_cols_kernel<DT, VEC>, a.grid, dim3(kColThreads), a.stream, a.x, a.A, a.R,
-                      a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial, a.P);
+    if (a.rowsplit)
+        return launch_pdl(lse_cols_kernel<DT, VEC, true>, a.grid, dim3(kColThreads), a.stream, a.x,
+                          a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial,
+                          a.P);
+    return launch_pdl(lse_cols_kernel<DT, VEC, false>, a.grid, dim3(kColThreads), a.stream, a.x,
+                      a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial,
+                      a.P);
 }
 
 template <int DT, bool VEC>
 int cols_occupancy_t() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC>, kColThreads,
-                                                      0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, true>,
+                                                      kColThreads, 0) != cudaSuccess)
         return 1;
     return blocks > 0 ? blocks : 1;
 }
@@ -143,7 +183,16 @@ int cols_occupancy(int dt, bool vec) {
     }
 }
 
-int cols_columns_per_cta(bool vec, int dt) { return 32 * (vec ? 16 / (dt == kF32 ? 4 : 2) : 1); }
-int cols_rows_per_batch(bool vec) { return kColWarps * (vec ? 4 : 8); }
+cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t P, float* out,
+                                 cudaStream_t stream) {
+    int64_t grid = (outputs + 255) / 256;
+    if (grid > 1048576) grid = 1048576;
+    return launch_pdl(merge_columns_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), stream,
+                      partial, outputs, P, out);
+}
+
+int cols_columns_per_warp(bool vec, int dt) { return 32 * (vec ? 16 / (dt == kF32 ? 4 : 2) : 1); }
+int cols_rows_per_batch(bool vec) { return vec ? 4 : 8; }
+int cols_warps_per_cta() { return kColWarps; }
 
 }  // namespace lse

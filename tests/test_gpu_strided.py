@@ -18,7 +18,7 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def run_strided(x3, dtype, pad_r=0, pad_c=0, pad_a=0, offset=0, splits=0):
+def run_strided(x3, dtype, pad_r=0, pad_c=0, pad_a=0, offset=0, plan=None):
     """Place x [A, R, C] in a NaN-canaried buffer with padded strides and run."""
     A, R, C = x3.shape
     sr = C + pad_c
@@ -32,7 +32,7 @@ def run_strided(x3, dtype, pad_r=0, pad_c=0, pad_a=0, offset=0, splits=0):
     eb = 4 if dtype == "f32" else 2
     out = torch.full((A * C + 16,), float("nan"), device="cuda")
     L.lse_forward_strided_ptr(buf.data_ptr() + offset * eb, dtype, A, R, C, sa, sr, out.data_ptr(),
-                              splits, torch.cuda.current_stream().cuda_stream)
+                              torch.cuda.current_stream().cuda_stream, plan)
     torch.cuda.synchronize()
     o = out.cpu().numpy()
     assert np.all(np.isnan(o[A * C:])), "write past out[A*C-1]"
@@ -60,28 +60,34 @@ def test_strided_edge_shapes(dtype, A, R, C):
         xi[0, R // 2, 2] = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
         xi[A - 1, R - 1, 3] = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
     for lay in (dict(), dict(pad_c=8), dict(pad_c=3), dict(offset=1), dict(pad_a=8, pad_r=1)):
-        for splits in (0, 1, 2, 3):
-            if splits > R:
-                continue
-            got, want = run_strided(x, dtype, splits=splits, **lay)
-            try:
-                compare(got, want)
-            except AssertionError as e:
-                raise AssertionError(f"layout {lay} splits {splits}: {e}") from None
+        for path in ("auto", "columns_warp", "columns_cta"):
+            for splits in (0, 1, 2, 3):
+                if splits > R:
+                    continue
+                plan = {"path": path, "splits": splits}
+                got, want = run_strided(x, dtype, plan=plan, **lay)
+                try:
+                    compare(got, want)
+                except AssertionError as e:
+                    raise AssertionError(f"layout {lay} plan {plan}: {e}") from None
 
 
 def test_strided_degenerate():
     _need_gpu()
     out = torch.full((6,), 7.0, device="cuda")
     x = torch.zeros(16, device="cuda")
-    L.lse_forward_strided_ptr(x.data_ptr(), "f32", 2, 0, 3, 0, 0, out.data_ptr())
+    p = L.lse_forward_strided_ptr(x.data_ptr(), "f32", 2, 0, 3, 0, 0, out.data_ptr())
     torch.cuda.synchronize()
-    assert np.all(out.cpu().numpy() == -np.inf)
+    assert np.all(out.cpu().numpy() == -np.inf) and p.as_dict()["path"] == "empty"
     L.lse_forward_strided_ptr(x.data_ptr(), "f32", 0, 4, 3, 12, 3, out.data_ptr())  # no-op
     with pytest.raises(L.LseError):
         L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, -3, out.data_ptr())
     with pytest.raises(L.LseError):
-        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, 3, out.data_ptr(), splits=5)
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, 3, out.data_ptr(),
+                                  plan={"splits": 5})
+    with pytest.raises(L.LseError):
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 1, 4, 3, 12, 3, out.data_ptr(),
+                                  plan={"path": "split"})
 
 
 def test_logsumexp_any_dim():

@@ -578,14 +578,16 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
                                                                   : LSE_PATH_COLUMNS_CTA;
     const bool rowsplit = path == LSE_PATH_COLUMNS_CTA;
     const int64_t gx = rowsplit ? wtiles : ceil_div(wtiles, W);
-    const int64_t warps_busy = rowsplit ? gx * gy * W : wtiles * gy;  // warps with work per split
     const int64_t rows_per_warp_batch = rowsplit ? W * batch : batch;
+    const int64_t resident_ctas = resident_warps / W;
     int64_t P = req ? req->splits : 0;
     if (P == 0) {
-        // No split while the tiles keep half the resident warps busy (a split
-        // costs a merge kernel); otherwise just enough splits to cover the GPU
-        // once, keeping >= 4 batches per warp in every split.
-        P = 2 * warps_busy >= resident_warps ? 1 : ceil_div(resident_warps, warps_busy);
+        // No split while the CTAs already fill half the resident slots (a
+        // split costs a merge kernel); otherwise as many splits as fit in ONE
+        // wave of resident CTAs -- a partial second wave of these long-lived
+        // CTAs would nearly double the time -- keeping >= 4 batches per warp.
+        const int64_t base = gx * gy;
+        P = 2 * base >= resident_ctas ? 1 : resident_ctas / base;
         const int64_t max_p = R / (4 * rows_per_warp_batch);
         if (P > max_p) P = max_p;
         if (P < 1) P = 1;

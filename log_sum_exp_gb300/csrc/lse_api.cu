@@ -21,8 +21,12 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+// Report a CUDA failure through the status code and lse_last_cuda_error, and
+// clear the runtime's per-thread last error so it does not surface later in
+// the caller's own error checks (sticky device errors cannot be cleared).
 lse_status cuda_fail(cudaError_t e, lse_status st = LSE_ERR_CUDA) {
     g_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
     return st;
 }
 
@@ -314,7 +318,10 @@ merge_kernel(const float2* __restrict__ partial, const float* __restrict__ xt_bu
 
 }  // namespace
 
-void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+void record_cuda_error(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
+}
 
 cudaError_t launch_fill_neg_inf(float* out, float* logprob, int64_t B, cudaStream_t stream) {
     int64_t grid = ceil_div(B, 256);

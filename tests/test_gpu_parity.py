@@ -301,3 +301,84 @@ def test_tolerance_bar_is_met_with_margin():
     s = compare(run(torch.from_numpy(x).cuda())[0], oracle.lse(x))
     assert s["max_err_over_tol"] < 0.5, s
     assert math.isfinite(s["max_abs_err"])
+
+
+def test_concurrent_streams_split_scratch():
+    """Split-row calls on two streams at once: each gets its own stream-ordered
+    scratch, so neither disturbs the other."""
+    _need_gpu()
+    xs = [wl.generate("particles_16x16777216_f32", B=4, N=1 << 21, seed=s) for s in (1, 2)]
+    wants = [oracle.lse(x) for x in xs]
+    ds = [torch.from_numpy(x).cuda() for x in xs]
+    streams = [torch.cuda.Stream() for _ in ds]
+    outs = [torch.empty(4, device="cuda") for _ in ds]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for d, st, o in zip(ds, streams, outs):
+            L.lse_forward_plan(d, plan={"path": "split", "splits": 64}, out=o, stream=st)
+    torch.cuda.synchronize()
+    for o, w in zip(outs, wants):
+        compare(o.cpu().numpy(), w)
+
+
+def test_allocation_failure_is_reported():
+    """A staging allocation larger than the device reports LSE_ERR_ALLOC
+    (host-side failure: nothing is launched, the host buffer is not read)."""
+    _need_gpu()
+    small = np.zeros(16, np.float32)
+    out = np.zeros(1 << 10, np.float32)
+    free, total = torch.cuda.mem_get_info()
+    n = int(total // 4 * 2)  # twice the device memory, in f32 elements
+    with pytest.raises(L.LseError) as e:
+        L.lse_forward_host_ptr(small.ctypes.data, "f32", 1 << 10, n // (1 << 10), n // (1 << 10),
+                               out.ctypes.data)
+    assert e.value.status == 3
+    # The failure is reported once, by status; the runtime is left clean for
+    # the caller's next CUDA call.
+    torch.ones(3, device="cuda").sum().item()
+
+
+def test_graph_capture_all_ops():
+    """lse_token_logprob, lse_backward and lse_forward_strided replay correctly
+    from a CUDA graph (split plans included)."""
+    _need_gpu()
+    x = wl.generate("particles_16x16777216_f32", B=3, N=1 << 20)
+    t = np.array([0, 5, (1 << 20) - 1], np.int64)
+    xd = torch.from_numpy(x).cuda()
+    td = torch.from_numpy(t).cuda()
+    lse_d = torch.from_numpy(oracle.lse(x).astype(np.float32)).cuda()
+    g_d = torch.ones(3, device="cuda")
+    x3 = wl.generate_columns("pcsum_512x64x1024_f32", A=8)
+    x3d = torch.from_numpy(x3).cuda()
+    lp = torch.empty(3, device="cuda")
+    dx = torch.empty_like(xd)
+    col = torch.empty(8 * 1024, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def ops(stream):
+        h = stream.cuda_stream
+        L.lse_token_logprob_ptr(xd.data_ptr(), "f32", 3, 1 << 20, 1 << 20, td.data_ptr(),
+                                lp.data_ptr(), 0, h, L._binding._as_plan({"path": "split", "splits": 8}))
+        L.lse_backward_ptr(xd.data_ptr(), "f32", 3, 1 << 20, 1 << 20, lse_d.data_ptr(),
+                           g_d.data_ptr(), dx.data_ptr(), 1 << 20, h)
+        L.lse_forward_strided_ptr(x3d.data_ptr(), "f32", 8, 64, 1024, 64 * 1024, 1024,
+                                  col.data_ptr(), h, {"path": "columns_warp", "splits": 2})
+
+    with torch.cuda.stream(s):
+        ops(s)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ops(torch.cuda.current_stream())
+    lp.fill_(0)
+    dx.fill_(0)
+    col.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    want_lp, want_lse = oracle.token_logprob(x, t)
+    compare(lp.cpu().numpy(), want_lp, scale=np.abs(want_lp) + np.abs(want_lse))
+    compare(col.cpu().numpy().reshape(8, 1024),
+            oracle.lse_strided(x3.reshape(-1), "f32", 8, 64, 1024, 64 * 1024, 1024))
+    assert np.allclose(dx.sum(dim=1).cpu().numpy(), 1.0, rtol=1e-4)

@@ -40,7 +40,7 @@ OP_NAMES = {"forward": "row value", "logprob": "fused token log-probability",
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
                   "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
-                  "lse_backward.cu", "lse_strided.cu"]
+                  "lse_backward.cu", "lse_strided.cu", "lse_rowtile.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -451,7 +451,8 @@ def run_native(args) -> None:
         timing = (f"one-kernel plan: CUDA events around the {K} back-to-back launches of the "
                   f"timed region, divided by {K}")
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
-    main_kernel = {"subwarp": "lse_subwarp_kernel", "cta": "lse_segment_kernel",
+    main_kernel = {"subwarp": "lse_subwarp_kernel", "rowtile": "lse_rowtile_kernel",
+                   "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
                    "backward": "lse_backward_kernel", "columns_warp": "lse_cols_kernel",
                    "columns_cta": "lse_cols_kernel"}[plan["path"]]

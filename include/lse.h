@@ -78,8 +78,12 @@ typedef enum {
     LSE_PATH_SPLIT = 4,   /* `splits` CTAs per row write (m, s) partials;
                              a second small kernel merges them in order   */
     LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
-    LSE_PATH_COLUMNS_CTA = 6   /* lse_forward_strided: a CTA's 8 warps share the
+    LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: a CTA's 8 warps share the
                                   rows of one column tile                       */
+    LSE_PATH_ROWTILE = 7       /* short back-to-back rows (16..128 bytes, 16-byte
+                                  aligned): 32 KB chunks of rows streamed into
+                                  shared memory by bulk copies (TMA), one thread
+                                  per row; row value only                      */
 } lse_path;
 
 /*
@@ -223,6 +227,15 @@ LSE_API lse_status lse_forward_strided(const void *x, lse_dtype dtype, int64_t A
  * stream that used the library on this device.
  */
 LSE_API lse_status lse_trim_memory(void);
+
+/*
+ * lse_wait_timeouts -- number of bounded device-side waits that gave up since
+ * the library was loaded, on the current device (synchronous read).  Kernels
+ * that wait for their own asynchronous copies (LSE_PATH_ROWTILE) stop and
+ * count here instead of waiting forever; a non-zero count means results of
+ * such a launch are incomplete.  Zero in correct operation.
+ */
+LSE_API lse_status lse_wait_timeouts(unsigned long long *count);
 
 /* Short English description of a status code (static storage). */
 LSE_API const char *lse_status_string(lse_status status);

@@ -29,5 +29,6 @@ from ._binding import (  # noqa: F401
     lse_token_logprob,
     lse_token_logprob_ptr,
     lse_trim_memory,
+    lse_wait_timeouts,
     status_string,
 )

@@ -17,13 +17,13 @@ STATUS_NAMES = {0: "LSE_OK", 1: "LSE_ERR_INVALID_ARG", 2: "LSE_ERR_UNSUPPORTED_D
                 3: "LSE_ERR_ALLOC", 4: "LSE_ERR_CUDA"}
 DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
 PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4, "columns_warp": 5,
-         "columns_cta": 6}
+         "columns_cta": 6, "rowtile": 7}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
                  "lse_token_logprob", "lse_token_logprob_plan", "lse_backward",
-                 "lse_forward_strided", "lse_trim_memory",
+                 "lse_forward_strided", "lse_trim_memory", "lse_wait_timeouts",
                  "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
 
 
@@ -97,6 +97,8 @@ def load() -> ctypes.CDLL:
         lib.lse_forward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, vp,
                                             ctypes.POINTER(LsePlan)]
         lib.lse_forward_strided.restype = i32
+        lib.lse_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+        lib.lse_wait_timeouts.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
@@ -117,6 +119,13 @@ def _check(status: int, where: str) -> None:
 def lse_trim_memory() -> None:
     """Release the library's cached device memory on the current device."""
     _check(load().lse_trim_memory(), "lse_trim_memory")
+
+
+def lse_wait_timeouts() -> int:
+    """Bounded device-side waits that gave up so far (0 in correct operation)."""
+    v = ctypes.c_ulonglong(0)
+    _check(load().lse_wait_timeouts(ctypes.byref(v)), "lse_wait_timeouts")
+    return v.value
 
 
 def status_string(status: int) -> str:

@@ -165,10 +165,39 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         *plan = p;
         return LSE_OK;
     }
-    if (path == LSE_PATH_EMPTY || path < 0 || path > LSE_PATH_SPLIT) return LSE_ERR_INVALID_ARG;
+    if (path == LSE_PATH_EMPTY || path < 0 || path > LSE_PATH_ROWTILE ||
+        path == LSE_PATH_COLUMNS_WARP || path == LSE_PATH_COLUMNS_CTA)
+        return LSE_ERR_INVALID_ARG;
 
     const int64_t sub_capacity = 32 * kSubwarpMaxSlots;  // slots per row
-    if (path == LSE_PATH_AUTO) path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
+    // Bulk-copy ring for short back-to-back rows: row value only, contiguous
+    // 16-byte aligned rows of 16..128 bytes, enough rows for every CTA.
+    const int64_t row_bytes = N * eb;
+    const bool rowtile_ok = vec && !with_logprob && row_stride == N && row_bytes % 16 == 0 &&
+                            (row_bytes == 16 || row_bytes == 32 || row_bytes == 64 ||
+                             row_bytes == 128);
+    if (path == LSE_PATH_AUTO) {
+        const int64_t chunk_rows = rowtile_ok ? rowtile_rows_per_chunk(static_cast<int>(row_bytes / 16)) : 1;
+        if (rowtile_ok && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
+            path = LSE_PATH_ROWTILE;
+        else
+            path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
+    }
+    if (path == LSE_PATH_ROWTILE) {
+        if (!rowtile_ok) return LSE_ERR_INVALID_ARG;
+        const int nvec = static_cast<int>(row_bytes / 16);
+        const int64_t chunks = ceil_div(B, rowtile_rows_per_chunk(nvec));
+        int64_t grid = static_cast<int64_t>(info.sms) * rowtile_ctas_per_sm();
+        if (grid > chunks) grid = chunks;
+        p.path = LSE_PATH_ROWTILE;
+        p.threads = 256;
+        p.slots_per_lane = nvec;
+        p.splits = 1;
+        p.grid = grid;
+        p.launches = B > 0 ? 1 : 0;
+        *plan = p;
+        return LSE_OK;
+    }
 
     if (path == LSE_PATH_SUBWARP) {
         if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
@@ -413,6 +442,9 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
         break;
     case LSE_PATH_SUBWARP:
         e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
+        break;
+    case LSE_PATH_ROWTILE:
+        e = launch_rowtile(dtype, p.slots_per_lane, x, B, out, static_cast<int>(p.grid), stream);
         break;
     default:
         e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,
@@ -716,6 +748,12 @@ lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int6
     if (e != cudaSuccess) return cuda_fail(e);
     if (es != cudaSuccess) return cuda_fail(es);
     return LSE_OK;
+}
+
+lse_status lse_wait_timeouts(unsigned long long* count) {
+    if (count == nullptr) return LSE_ERR_INVALID_ARG;
+    const cudaError_t e = read_wait_timeouts(count);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
 lse_status lse_trim_memory(void) {

@@ -53,6 +53,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStre
     return cudaGetLastError();
 }
 
+// launch_pdl with dynamic shared memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Per element type (f32 / bf16 / f16): launchers and occupancy queries.
 #define LSE_DECLARE_TYPE_ENTRY_POINTS(SUFFIX)                                                  \
     cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
@@ -116,6 +136,13 @@ int cols_occupancy(int dt, bool vec);
 int cols_columns_per_warp(bool vec, int dt);
 int cols_rows_per_batch(bool vec);  // per warp per iteration
 int cols_warps_per_cta();
+
+// Short contiguous rows through the bulk-copy ring (lse_rowtile.cu).
+cudaError_t launch_rowtile(int dt, int nv, const void* x, int64_t B, float* out, int grid,
+                           cudaStream_t stream);
+int rowtile_ctas_per_sm();
+int rowtile_rows_per_chunk(int nv);
+cudaError_t read_wait_timeouts(unsigned long long* count);
 
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);

@@ -1,0 +1,210 @@
+// lse_rowtile.cu -- short contiguous rows fed by 1-D bulk copies (sm_103a).
+//
+// For rows of 16, 32, 64 or 128 bytes stored back to back (row_stride == N,
+// 16-byte aligned), a persistent CTA streams 32 KB chunks of whole rows from
+// HBM into a ring of shared-memory stages with cp.async.bulk (the Tensor
+// Memory Accelerator's 1-D copy; one instruction per chunk, completion tracked
+// by an mbarrier transaction count), and each of its 256 threads reduces whole
+// rows out of shared memory: max, then one FFMA + ex2 per element, then the
+// finalize of lse_device.cuh.  Memory traffic never waits for the arithmetic:
+// while one stage is consumed the others are in flight.  ("Speeding up
+// Log-Sum-Exp ...", Sec. 3.1: one pass, a register accumulator per row.)
+//
+// Waits are bounded: a stage that does not complete within kWaitPolls polls
+// counts a timeout in a device counter (read by lse_wait_timeouts), the whole
+// CTA stops, waits (also bounded) for its own copies still in flight, and
+// returns.  Such a timeout does not happen in correct operation.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "lse_device.cuh"
+#include "lse_internal.h"
+
+namespace lse {
+namespace {
+
+constexpr int kTileThreads = 256;
+constexpr int kChunkBytes = 32 * 1024;  // per stage
+constexpr int kStages = 2;
+constexpr uint32_t kWaitPolls = 1u << 26;
+
+__device__ unsigned long long g_wait_timeouts;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// false when the phase did not complete within `polls` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// NV 16-byte vectors per row; RPT = 8 / NV rows per thread per chunk, so a
+// chunk is 256 * RPT rows = 32 KB.  Chunks are dealt round-robin to the CTAs.
+template <int DT, int NV>
+__global__ void __launch_bounds__(kTileThreads)
+lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ out) {
+    constexpr int RB = NV * 16;                // bytes per row
+    constexpr int RPT = 8 / NV;                // rows per thread per chunk
+    constexpr int CR = kTileThreads * RPT;     // rows per chunk
+    extern __shared__ __align__(128) unsigned char stage[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    const int tid = threadIdx.x;
+    const int64_t nchunks = (B + CR - 1) / CR;
+    const char* xb = reinterpret_cast<const char*>(x);
+
+    pdl_trigger();
+    pdl_wait();
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int64_t chunk, int s) {  // thread 0 only
+        const int64_t r0 = chunk * CR;
+        const int64_t rows = B - r0 < CR ? B - r0 : CR;
+        const uint32_t bytes = static_cast<uint32_t>(rows * RB);
+        mbar_expect_tx(&full[s], bytes);
+        bulk_load(stage + s * kChunkBytes, xb + r0 * RB, bytes, &full[s]);
+    };
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (c < nchunks) issue(c, s);
+        }
+
+    int64_t k = 0;  // chunks consumed by this CTA
+    bool timed_out = false;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % kStages);
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((k / kStages) & 1), kWaitPolls);
+        uint32_t w[RPT][4 * NV];
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const uint4* rp =
+                reinterpret_cast<const uint4*>(stage + s * kChunkBytes + (q * kTileThreads + tid) * RB);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                // Rotated reads: consecutive threads start at different 16-byte
+                // bank groups.  Max and sum do not depend on the order.
+                const uint4 u = ok ? rp[(j + tid) % NV] : make_uint4(0, 0, 0, 0);
+                w[q][4 * j] = u.x; w[q][4 * j + 1] = u.y; w[q][4 * j + 2] = u.z; w[q][4 * j + 3] = u.w;
+            }
+        }
+        // Every thread has read stage s: it may be refilled.  A timed-out wait
+        // in any thread stops the whole CTA.
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            break;
+        }
+        if (tid == 0) {
+            const int64_t cn = c + static_cast<int64_t>(kStages) * gridDim.x;
+            if (cn < nchunks) issue(cn, s);
+        }
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const int64_t row = c * CR + q * kTileThreads + tid;
+            if (row < B) {
+                const float m = words_max<DT, 4 * NV>(w[q]);
+                const float mu = shift_of(m);
+                float lse;
+                if (ffma_shift_ok(mu)) {
+                    const float cc = mu * kLog2e;
+                    lse = finalize_scaled(m, words_expsum_scaled<DT, 4 * NV>(w[q], cc), mu, cc);
+                } else {
+                    lse = acc_finalize(Acc{m, words_expsum<DT, 4 * NV>(w[q], mu)});
+                }
+                out[row] = lse;
+            }
+        }
+    }
+    if (timed_out) {
+        if (tid == 0) {
+            atomicAdd(&g_wait_timeouts, 1ull);
+            // Let every copy this CTA may still have in flight land (bounded)
+            // before the shared memory is released.
+            for (int s = 0; s < kStages; ++s) {
+                mbar_wait(&full[s], 0, kWaitPolls);
+                mbar_wait(&full[s], 1, kWaitPolls);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int DT, int NV>
+cudaError_t launch_rowtile_t(const void* x, int64_t B, float* out, int grid, cudaStream_t stream) {
+    const int smem = kStages * kChunkBytes;
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_smem(lse_rowtile_kernel<DT, NV>, dim3(static_cast<unsigned>(grid)),
+                           dim3(kTileThreads), static_cast<size_t>(smem), stream, x, B, out);
+}
+
+template <int DT>
+cudaError_t launch_rowtile_dt(int nv, const void* x, int64_t B, float* out, int grid,
+                              cudaStream_t stream) {
+    switch (nv) {
+    case 1: return launch_rowtile_t<DT, 1>(x, B, out, grid, stream);
+    case 2: return launch_rowtile_t<DT, 2>(x, B, out, grid, stream);
+    case 4: return launch_rowtile_t<DT, 4>(x, B, out, grid, stream);
+    case 8: return launch_rowtile_t<DT, 8>(x, B, out, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rowtile(int dt, int nv, const void* x, int64_t B, float* out, int grid,
+                           cudaStream_t stream) {
+    switch (dt) {
+    case kF32: return launch_rowtile_dt<kF32>(nv, x, B, out, grid, stream);
+    case kBF16: return launch_rowtile_dt<kBF16>(nv, x, B, out, grid, stream);
+    default: return launch_rowtile_dt<kF16>(nv, x, B, out, grid, stream);
+    }
+}
+
+int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
+int rowtile_rows_per_chunk(int nv) { return kTileThreads * (8 / nv); }
+
+cudaError_t read_wait_timeouts(unsigned long long* count) {
+    return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));
+}
+
+}  // namespace lse

@@ -104,7 +104,10 @@ def test_edge_shapes(dtype, N):
     for row_stride, offset in layouts:
         buf, xv = device_rows(x, dtype, row_stride=row_stride, offset=offset)
         vec = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
-        for plan in plans_for(N, dtype, vec):
+        plans = plans_for(N, dtype, vec)
+        if vec and row_stride == N and N * eb in (16, 32, 64, 128):
+            plans.append({"path": "rowtile"})
+        for plan in plans:
             got, p = run(xv, plan)
             try:
                 compare(got, want)
@@ -219,7 +222,7 @@ def test_plan_query_matches_forward():
         q = L.lse_plan_query(dtype=w.dtype, B=w.B, N=w.N)
         assert q["launches"] in (1, 2)
         if key.startswith("short"):
-            assert q["path"] == "subwarp"
+            assert q["path"] == "rowtile"
         if key.startswith("particles"):
             assert q["path"] == "split"
 
@@ -382,3 +385,37 @@ def test_graph_capture_all_ops():
     compare(col.cpu().numpy().reshape(8, 1024),
             oracle.lse_strided(x3.reshape(-1), "f32", 8, 64, 1024, 64 * 1024, 1024))
     assert np.allclose(dx.sum(dim=1).cpu().numpy(), 1.0, rtol=1e-4)
+
+
+def test_short_rows_both_mappings_full_size():
+    """The 1048576 x 32 workload through the bulk-copy ring (default) and the
+    register sub-warp kernel (forced)."""
+    _need_gpu()
+    x = wl.generate("short_1048576x32_f32")
+    want = oracle.lse(x)
+    xd = torch.from_numpy(x).cuda()
+    for plan in (None, {"path": "rowtile"}, {"path": "subwarp"}):
+        got, p = run(xd, plan)
+        if plan is None:
+            assert p.as_dict()["path"] == "rowtile"
+        compare(got, want)
+
+
+def test_rowtile_ragged_chunks_and_dtypes():
+    """Row counts that leave a partial last chunk, for every row size and dtype."""
+    _need_gpu()
+    for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
+        for rb in (16, 32, 64, 128):
+            N = rb // eb
+            for B in (1, 255, 2049, 100003):
+                x = wl.random_rows(B, N, dtype, seed=B + rb, scale=8.0)
+                got, p = run(torch_view(x, dtype).cuda(), {"path": "rowtile"})
+                assert p.as_dict()["path"] == "rowtile"
+                compare(got, oracle.lse(x, dtype))
+
+
+def test_no_wait_timed_out():
+    """No bounded device-side wait gave up during the tests above."""
+    _need_gpu()
+    torch.cuda.synchronize()
+    assert L.lse_wait_timeouts() == 0

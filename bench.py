@@ -78,9 +78,10 @@ def barrier(device=None) -> None:
             dist.barrier()
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files: list[str] | None = None) -> str:
+    """sha256 (16 hex digits) of kernel source files under the package's csrc/."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (KERNEL_SOURCES if files is None else files):
         with open(os.path.join(ROOT, "log_sum_exp_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -95,20 +96,29 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
-def ncu_traffic(workload_key: str, kernel_path: str, op: str = "forward") -> float | None:
-    """DRAM bytes per launch of the main kernel from the committed ncu summary,
-    or None when there is none for this workload or the kernels changed since."""
+def ncu_traffic(workload_key: str, plan: dict, op: str = "forward") -> float | None:
+    """DRAM bytes per launch of the main kernel from the committed ncu record,
+    or None when there is none for this workload, op and plan, or when the
+    files that define the kernel changed since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             entries = json.load(f)["entries"]
     except (OSError, KeyError, ValueError):
         return None
-    src = kernel_source_hash()
     for e in entries:
-        if e.get("workload") == workload_key and e.get("source_hash") == src \
-                and e.get("path") == kernel_path and e.get("op", "forward") == op:
-            return float(e["dram_bytes_per_launch"])
+        if e.get("workload") != workload_key or e.get("op", "forward") != op:
+            continue
+        if e.get("path") != plan.get("path"):
+            continue
+        if any(k in plan and e.get(k) != plan[k] for k in ("grid", "threads")):
+            continue
+        try:
+            if kernel_source_hash(e["sources"]) != e["source_hash"]:
+                continue
+        except (KeyError, OSError):
+            continue
+        return float(e["dram_bytes_per_launch"])
     return None
 
 
@@ -456,7 +466,7 @@ def run_native(args) -> None:
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
                    "backward": "lse_backward_kernel", "columns_warp": "lse_cols_kernel",
                    "columns_cta": "lse_cols_kernel"}[plan["path"]]
-    traffic = ncu_traffic(args.workload, plan["path"], op_name)
+    traffic = ncu_traffic(args.workload, plan, op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
                 "peak_source": peak_src,

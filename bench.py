@@ -526,7 +526,9 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+        print(f"bench.py: --warmup {args.warmup} raised to 3 (at least 3 warm-up steps)",
+              file=sys.stderr)
+        args.warmup = 3
     if args.workload is None:
         args.workload = DEFAULT_COLUMNS if args.op == "columns" else DEFAULT_WORKLOAD
     if (args.op == "columns") != (args.workload in wl.COLUMN_WORKLOADS):

@@ -355,8 +355,8 @@ def lse_backward(x, lse, grad, dx=None, stream=None):
     return dx
 
 
-def logsumexp(x, dim=-1, stream=None):
-    """torch.logsumexp(x, dim) on liblse for CUDA tensors, computed in f32.
+def logsumexp(x, dim=-1, keepdim=False, stream=None):
+    """torch.logsumexp(x, dim, keepdim) on liblse for CUDA tensors, computed in f32.
 
     The reduced dimension may be any dimension; the tensor's other dimensions
     must collapse to (outer, inner) with the inner one contiguous (any
@@ -389,7 +389,7 @@ def logsumexp(x, dim=-1, stream=None):
         else:
             lse_forward_strided_ptr(x.data_ptr(), dt, outer, R, inner, R * inner, inner,
                                     out.data_ptr(), _stream_handle(stream, x.device))
-    return out
+    return out.unsqueeze(d) if keepdim else out
 
 
 def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,

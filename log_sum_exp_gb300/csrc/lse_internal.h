@@ -79,8 +79,7 @@ cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
                                         int64_t grid);                                         \
     cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
                                         int64_t seg_slots, float2* partial, float* xt_buf);    \
-    int segment_occupancy_##SUFFIX(bool vec, int threads);                                     \
-    int subwarp_occupancy_##SUFFIX(bool vec);
+    int segment_occupancy_##SUFFIX(bool vec, int threads);
 
 LSE_DECLARE_TYPE_ENTRY_POINTS(f32)
 LSE_DECLARE_TYPE_ENTRY_POINTS(bf16)

@@ -1,18 +1,21 @@
-// lse_kernels.cuh -- the row-wise log-sum-exp kernels (sm_103a).
+// lse_kernels.cuh -- the row-wise log-sum-exp kernels over strided rows (sm_103a).
 //
 // One pass over x: every element is loaded once with coalesced 128-bit loads
 // (scalar loads when rows are not 16-byte aligned), folded into a register
 // accumulator, and each row writes one float ("Speeding up Log-Sum-Exp ...",
-// Sec. 3.1).  Three mappings:
+// Sec. 3.1).  Two mappings live here:
 //   subwarp  rows of at most 32*4 vectors: G lanes per row hold the whole row
 //            in registers; max first, then the exp-sum (two passes over
 //            registers, one over HBM); lanes combine by xor shuffles.
 //   segment  one CTA per (row, segment): online (m, s) accumulation over
 //            batches of 8 vectors per thread, then warp shuffles and shared
 //            memory.  With one segment per row it writes out[row]; with P > 1
-//            segments it writes an (m, s) partial that lse_merge_kernel
-//            combines (the split-row mapping for long rows or few rows).
-// This header is included by one translation unit per element type.
+//            segments it writes an (m, s) partial that merge_kernel
+//            (lse_api.cu) combines -- the split-row mapping for long or few rows.
+// Both take an optional fused epilogue (TL) for the token log-probability.
+// Back-to-back short rows have a bulk-copy mapping of their own
+// (lse_rowtile.cu).  This header is included by one translation unit per
+// element type and epilogue.
 #pragma once
 
 #include "lse_device.cuh"
@@ -364,15 +367,6 @@ int segment_occupancy_t() {
     return blocks;
 }
 
-template <int DT, int G, int V, bool VEC, bool TL>
-int subwarp_occupancy_gv() {
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_subwarp_kernel<DT, G, V, VEC, TL>,
-                                                      kSubwarpThreads, 0) != cudaSuccess)
-        return 0;
-    return blocks;
-}
-
 }  // namespace lse
 
 // Instantiates the per-type entry points declared in lse_internal.h; TL selects
@@ -414,9 +408,5 @@ int subwarp_occupancy_gv() {
                              : segment_occupancy_t<DT, 512, false, TL>();                          \
         default: return 0;                                                                     \
         }                                                                                      \
-    }                                                                                          \
-    int subwarp_occupancy_##SUFFIX(bool vec) {                                                 \
-        return vec ? subwarp_occupancy_gv<DT, 8, 1, true, TL>()                                    \
-                   : subwarp_occupancy_gv<DT, 8, 1, false, TL>();                                  \
     }                                                                                          \
     }

@@ -98,3 +98,5 @@ def test_logsumexp_any_dim():
         got = L.logsumexp(xd, dim=dim).cpu().numpy()
         want = torch.logsumexp(torch.from_numpy(x).double(), dim=dim).numpy()
         compare(got, want)
+        kd = L.logsumexp(xd, dim=dim, keepdim=True)
+        assert kd.shape == torch.logsumexp(torch.from_numpy(x), dim=dim, keepdim=True).shape

@@ -518,7 +518,8 @@ def main(argv=None) -> None:
                     default="forward",
                     help="row value (default), fused token log-probability, backward, or the "
                          "value over a non-last dimension (column workloads)")
-    ap.add_argument("--graph", action="store_true", help="also time CUDA-graph replay")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="skip the CUDA-graph replay timing (us_per_call_graph)")
     ap.add_argument("--plan", type=json.loads, default=None,
                     help='forced plan for --op columns as JSON, e.g. {"path": "columns_cta"}')
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -95,7 +95,8 @@ typedef struct {
     int32_t path;           /* lse_path                                              */
     int32_t vector_bytes;   /* 16: 128-bit loads; 1: element loads (unaligned rows);
                                0 in a request: let the library choose              */
-    int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32         */
+    int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32;
+                               column paths: warps sharing one column tile, 1/2/4/8 */
     int32_t slots_per_lane; /* SUBWARP: vectors (or elements) per lane (output)      */
     int32_t threads;        /* CTA / SPLIT: threads per CTA, 32/64/128/256/512      */
     int32_t launches;       /* kernels launched per call (output)                    */
@@ -204,9 +205,10 @@ LSE_API lse_status lse_backward(const void *x, lse_dtype dtype, int64_t B, int64
  *   out      device pointer to A * C floats (row-major [A, C]); must not
  *            overlap x.
  *   plan     NULL (automatic) or an lse_plan: path 0, LSE_PATH_COLUMNS_WARP
- *            (one warp per 32-lane column tile, for short reductions) or
- *            LSE_PATH_COLUMNS_CTA (a CTA's warps interleave the rows of one
- *            tile); splits 0 (automatic) or k >= 1 (<= R, <= 65535) row splits
+ *            (one warp per 32-lane column tile walks all its rows) or
+ *            LSE_PATH_COLUMNS_CTA (lanes_per_row = 2, 4 or 8 warps interleave
+ *            the rows of one tile, merged in shared memory; 0 = 8);
+ *            splits 0 (automatic) or k >= 1 (<= R, <= 65535) row splits
  *            across CTAs -- with k > 1 the call takes A * C * k * 8 bytes of
  *            stream-ordered scratch and a merge kernel; vector_bytes as for
  *            lse_forward_plan.  On return *plan holds the plan that ran.

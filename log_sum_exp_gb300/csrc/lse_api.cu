@@ -609,15 +609,25 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     const int64_t gy = A < 65535 ? A : 65535;
     const int64_t resident_warps = static_cast<int64_t>(info->sms) * W * cols_occupancy(dtype, vec);
     const int64_t batch = cols_rows_per_batch(vec);
-    // One warp per tile when the reduction is short or the tiles alone fill
-    // the GPU; otherwise the CTA's warps share a tile's rows.
+    // Warps per tile (measured): short reductions walk each tile with one
+    // warp and no merge; longer ones share a tile between 4 warps and fill
+    // the GPU with row splits below.
+    int WT = req && req->lanes_per_row ? req->lanes_per_row : 0;
     int path = rpath;
-    if (path == LSE_PATH_AUTO)
-        path = (R <= 256 || wtiles * gy >= 2 * resident_warps) ? LSE_PATH_COLUMNS_WARP
-                                                                  : LSE_PATH_COLUMNS_CTA;
-    const bool rowsplit = path == LSE_PATH_COLUMNS_CTA;
-    const int64_t gx = rowsplit ? wtiles : ceil_div(wtiles, W);
-    const int64_t rows_per_warp_batch = rowsplit ? W * batch : batch;
+    if (path == LSE_PATH_COLUMNS_WARP) {
+        if (WT > 1) return LSE_ERR_INVALID_ARG;
+        WT = 1;
+    }
+    if (WT == 0) {
+        if (path == LSE_PATH_COLUMNS_CTA)
+            WT = W;
+        else
+            WT = (R <= 256 || wtiles * gy >= 2 * resident_warps) ? 1 : 4;
+    }
+    if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
+    path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
+    const int64_t gx = ceil_div(wtiles, W / WT);
+    const int64_t rows_per_warp_batch = WT * batch;
     const int64_t resident_ctas = resident_warps / W;
     int64_t P = req ? req->splits : 0;
     if (P == 0) {
@@ -639,6 +649,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     p.path = path;
     p.vector_bytes = vec ? 16 : 1;
     p.threads = 32 * W;
+    p.lanes_per_row = WT;
     p.splits = P;
     p.segment_slots = rows_per_split;
     p.grid = gx * gy * P;
@@ -664,7 +675,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     a.out = out;
     a.partial = scratch;
     a.P = P;
-    a.rowsplit = rowsplit;
+    a.warps_per_tile = WT;
     a.grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(P));
     a.stream = stream;
     e = launch_cols(dtype, vec, a);

@@ -124,7 +124,7 @@ struct StridedArgs {
     float* out;
     float2* partial;  // [P, A * C] when P > 1
     int64_t P;
-    bool rowsplit;    // a CTA's warps share a column tile and split its rows
+    int warps_per_tile;  // 1, 2, 4 or 8 warps interleave the rows of one column tile
     dim3 grid;
     cudaStream_t stream;
 };

@@ -12,9 +12,8 @@
 // 16-byte vector, or 1 when the layout is not 16-byte aligned) of one index a;
 // every load instruction of a warp covers one contiguous stretch of a row, and
 // a thread folds U rows per batch into EPV accumulators with one rescale per
-// batch.  Two ways to share the work (see lse_cols_kernel): one warp per tile
-// walking all rows, or a CTA's 8 warps interleaving the rows of one tile and
-// merging in shared memory.  With P > 1 the rows are also split across
+// batch.  WT = 1, 2, 4 or 8 warps share a tile, interleaving its rows and
+// merging in shared memory (see lse_cols_kernel).  With P > 1 the rows are also split across
 // blockIdx.z; the (m, s) partials are stored split-major, [P, A * C], and
 // merge_columns_kernel combines them with one thread per output.
 #include <cstdint>
@@ -30,28 +29,28 @@ namespace {
 constexpr int kColWarps = 8;
 constexpr int kColThreads = 32 * kColWarps;
 
-// ROWSPLIT: the CTA's 8 warps share one column tile and interleave its rows
-// (merged in shared memory) -- for long reductions.  !ROWSPLIT: each warp owns
-// its own column tile (tile = blockIdx.x * 8 + warp) and walks all rows of the
-// split itself -- for short reductions, no cross-warp merge.
-template <int DT, bool VEC, bool ROWSPLIT>
+// WT warps share one column tile and interleave its rows (merged in shared
+// memory); the CTA's 8 warps cover 8 / WT tiles.  WT = 1: each warp walks all
+// rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
+// works on one tile (long reductions with few tiles).
+template <int DT, bool VEC, int WT>
 __global__ void __launch_bounds__(kColThreads)
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
-    constexpr int U = VEC ? 4 : 8;                    // rows per batch per thread
-    constexpr int RSTEP = ROWSPLIT ? kColWarps : 1;   // row interleave between warps
-    __shared__ float2 part[ROWSPLIT ? kColWarps : 1][32][EPV];
+    constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
+    constexpr int TPC = kColWarps / WT;  // tiles per CTA
+    __shared__ float2 part[WT > 1 ? kColWarps : 1][32][EPV];
 
     pdl_trigger();
     pdl_wait();
 
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    const int64_t tile = ROWSPLIT ? static_cast<int64_t>(blockIdx.x)
-                                  : static_cast<int64_t>(blockIdx.x) * kColWarps + wid;
+    const int phase = wid % WT;  // row interleave position within the tile's warps
+    const int64_t tile = static_cast<int64_t>(blockIdx.x) * TPC + wid / WT;
     const int64_t c0 = (tile * 32 + lane) * EPV;
     const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
     const int64_t split = blockIdx.z;
@@ -68,11 +67,11 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             acc[e] = acc_identity();
             mu[e] = 0.0f;
         }
-        for (int64_t r = r_begin + (ROWSPLIT ? wid : 0); r < r_end; r += static_cast<int64_t>(RSTEP) * U) {
+        for (int64_t r = r_begin + phase; r < r_end; r += static_cast<int64_t>(WT) * U) {
             float v[U][EPV];
 #pragma unroll
             for (int j = 0; j < U; ++j) {
-                const int64_t rr = r + j * RSTEP;
+                const int64_t rr = r + j * WT;
                 const bool ok = active && rr < r_end;
                 if constexpr (VEC) {
                     uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
@@ -97,23 +96,23 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                 acc[e].s += sum;
             }
         }
-        if constexpr (ROWSPLIT) {
+        if constexpr (WT > 1) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) part[wid][lane][e] = make_float2(acc[e].m, acc[e].s);
             __syncthreads();
-            if (wid == 0 && active) {
+            if (phase == 0 && active) {
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
                     Acc t = acc_identity();
 #pragma unroll
-                    for (int w = 0; w < kColWarps; ++w)
-                        t = acc_merge(t, Acc{part[w][lane][e].x, part[w][lane][e].y});
+                    for (int w = 0; w < WT; ++w)
+                        t = acc_merge(t, Acc{part[wid + w][lane][e].x, part[wid + w][lane][e].y});
                     acc[e] = t;
                 }
             }
             __syncthreads();  // part[] is reused by the next a
         }
-        if ((!ROWSPLIT || wid == 0) && active) {
+        if (phase == 0 && active) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
                 const int64_t c = c0 + e;
@@ -147,19 +146,23 @@ merge_columns_kernel(const float2* __restrict__ partial, int64_t outputs, int64_
 
 template <int DT, bool VEC>
 cudaError_t launch_cols_t(const StridedArgs& a) {
-    if (a.rowsplit)
-        return launch_pdl(lse_cols_kernel<DT, VEC, true>, a.grid, dim3(kColThreads), a.stream, a.x,
-                          a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial,
-                          a.P);
-    return launch_pdl(lse_cols_kernel<DT, VEC, false>, a.grid, dim3(kColThreads), a.stream, a.x,
-                      a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial,
-                      a.P);
+#define LSE_COLS_LAUNCH(WT)                                                                        \
+    return launch_pdl(lse_cols_kernel<DT, VEC, WT>, a.grid, dim3(kColThreads), a.stream, a.x, a.A, \
+                      a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial, a.P)
+    switch (a.warps_per_tile) {
+    case 1: LSE_COLS_LAUNCH(1);
+    case 2: LSE_COLS_LAUNCH(2);
+    case 4: LSE_COLS_LAUNCH(4);
+    case 8: LSE_COLS_LAUNCH(8);
+    default: return cudaErrorInvalidValue;
+    }
+#undef LSE_COLS_LAUNCH
 }
 
 template <int DT, bool VEC>
 int cols_occupancy_t() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, true>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, 8>,
                                                       kColThreads, 0) != cudaSuccess)
         return 1;
     return blocks > 0 ? blocks : 1;

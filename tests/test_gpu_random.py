@@ -110,8 +110,9 @@ def test_random_strided(seed):
     want = oracle.lse_strided(flat, dtype, A, R, C, sa, sr)
     buf = torch_view(flat, dtype).cuda()
     out = torch.empty(A * C, device="cuda")
-    plan = [None, {"path": "columns_warp"}, {"path": "columns_cta"},
-            {"path": "columns_warp", "splits": 2}, {"path": "columns_cta", "splits": 3}][seed % 5]
+    plan = [None, {"path": "columns_warp"}, {"path": "columns_cta", "lanes_per_row": 2},
+            {"path": "columns_warp", "splits": 2}, {"path": "columns_cta", "splits": 3},
+            {"path": "columns_cta", "lanes_per_row": 4, "splits": 2}][seed % 6]
     if plan and plan.get("splits", 0) > R:
         plan = None
     L.lse_forward_strided_ptr(buf.data_ptr(), dtype, A, R, C, sa, sr, out.data_ptr(),

@@ -60,11 +60,12 @@ def test_strided_edge_shapes(dtype, A, R, C):
         xi[0, R // 2, 2] = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
         xi[A - 1, R - 1, 3] = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
     for lay in (dict(), dict(pad_c=8), dict(pad_c=3), dict(offset=1), dict(pad_a=8, pad_r=1)):
-        for path in ("auto", "columns_warp", "columns_cta"):
+        for path, wt in (("auto", 0), ("columns_warp", 0), ("columns_cta", 2), ("columns_cta", 4),
+                         ("columns_cta", 8)):
             for splits in (0, 1, 2, 3):
                 if splits > R:
                     continue
-                plan = {"path": path, "splits": splits}
+                plan = {"path": path, "splits": splits, "lanes_per_row": wt}
                 got, want = run_strided(x, dtype, plan=plan, **lay)
                 try:
                     compare(got, want)

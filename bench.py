@@ -35,12 +35,14 @@ DEFAULT_COLUMNS = "pcsum_512x64x1024_f32"
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
 EVENT_EVERY = 16
-OP_NAMES = {"forward": "row value", "logprob": "fused token log-probability",
+OP_NAMES = {"forward": "row value", "forward16": "row value, reduced-bit exponentials",
+            "logprob": "fused token log-probability",
             "backward": "backward dx = g exp(x - lse)", "columns": "value over a non-last dim"}
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
                   "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
-                  "lse_backward.cu", "lse_strided.cu", "lse_rowtile.cu"]
+                  "lse_backward.cu", "lse_strided.cu", "lse_rowtile.cu", "lse_ex16_f32.cu",
+                  "lse_ex16_bf16.cu", "lse_ex16_f16.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -333,6 +335,13 @@ def run_native(args) -> None:
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
             L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, None, evb, eve)
+    elif op_name == "forward16":
+        plan = L.lse_forward16_ptr(ptrs[0][0], dt, w.B, w.N, w.N, ptrs[0][1], sh).as_dict()
+        bytes_per_step = in_bytes + w.write_bytes
+
+        def step(i, evb=0, eve=0):
+            xp, op = ptrs[i % copies]
+            L.lse_forward16_ptr(xp, dt, w.B, w.N, w.N, op, sh)
     elif op_name == "logprob":
         # Targets drawn once per copy; only the log-probabilities are written.
         rng = np.random.default_rng(w.seed + 1)
@@ -459,7 +468,9 @@ def run_native(args) -> None:
     else:
         kmean_ms = kmed_ms = ms_per_step
         timing = (f"one-kernel plan: CUDA events around the {K} back-to-back launches of the "
-                  f"timed region, divided by {K}")
+                  f"timed region, divided by {K}") if plan["launches"] == 1 else \
+                 (f"{plan['launches']} kernels per step: CUDA events around the {K} steps of the "
+                  f"timed region, divided by {K} (main kernel and merge together)")
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
     main_kernel = {"subwarp": "lse_subwarp_kernel", "rowtile": "lse_rowtile_kernel",
                    "cta": "lse_segment_kernel",
@@ -485,7 +496,9 @@ def run_native(args) -> None:
     line = {
         "metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 sums, bf16 exponentials" if op_name == "forward16" else "f32",
+        "data": "synthetic",
         "config": {"workload": args.workload, "op": op_name, "B": w.B, "N": w.N,
                    **({"A": cw.A, "R": cw.R, "C": cw.C} if cw else {}),
                    "input_dtype": w.dtype, "row_stride": w.N, "recipe": w.recipe, "plan": plan,
@@ -514,7 +527,7 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", choices=list(wl.WORKLOADS) + list(wl.COLUMN_WORKLOADS),
                     default=None, help=f"default {DEFAULT_WORKLOAD} ({DEFAULT_COLUMNS} for "
                                        f"--op columns)")
-    ap.add_argument("--op", choices=["forward", "logprob", "backward", "columns"],
+    ap.add_argument("--op", choices=["forward", "forward16", "logprob", "backward", "columns"],
                     default="forward",
                     help="row value (default), fused token log-probability, backward, or the "
                          "value over a non-last dimension (column workloads)")

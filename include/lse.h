@@ -137,6 +137,35 @@ LSE_API lse_status lse_forward_plan(const void *x, lse_dtype dtype, int64_t B, i
                             lse_plan *plan, lse_event_t ev_begin, lse_event_t ev_end);
 
 /*
+ * lse_forward16 -- lse_forward with reduced-bit exponentials, the paper's
+ * 16-bit compute variant ("Speeding up Log-Sum-Exp ...", Sec. 4.3 and Fig. 5:
+ * FuseLSE16, faster on V100 at a mean absolute error below 3e-3).  The same
+ * single pass, mappings and plans (plan as for lse_forward_plan, NULL =
+ * automatic), except for the terms exp(x - max): each base-2 argument
+ * a = (x - max) log2 e is formed in f32 plus a constant d = 0.00407 (below),
+ * rounded to bf16, and two of them are exponentiated by one packed bf16 SFU
+ * instruction; sums, merges and the final log stay in f32, and special values
+ * follow lse_forward exactly.  The SFU rounds its bf16 result toward zero,
+ * half a bf16 ulp low on average (2^-8 / (2 ln 2) of the value); d scales every
+ * term up by that much first, so terms are unbiased on average, while the
+ * maximum's own term (2^d = 1.0028) still truncates to exactly 1.
+ * Accuracy: the argument moves by d plus at most (|a| + d) 2^-8 in rounding, and
+ * truncation takes off less than a factor (1 - 2^-7), so each term is within a
+ * relative r_n = 2^(d + (|a_n| + d) 2^-8) - 1 + 2^-7 of exp(x_n - max), and
+ *     |result - lse| <= -log(1 - e),  e = sum_n p_n r_n
+ * (p_n the row's softmax) plus the f32 rounding of lse_forward.  To first
+ * order e <= 2^-7 + 2^-8 ln N + 0.003, since sum_n p_n |a_n| ln 2 <= ln N; far
+ * less in practice, as rounding errors of different terms do not line up.
+ * It halves the SFU operations per element; the f32 path is already bound by
+ * HBM bandwidth on this GPU at full clocks, so the gain is SFU headroom (at
+ * lower clocks, with 16-bit input).  The pages do not give FuseLSE16's kernel:
+ * this is the plain reading of a 16-bit exponent evaluation with f32 sums.
+ */
+LSE_API lse_status lse_forward16(const void *x, lse_dtype dtype, int64_t B, int64_t N,
+                                 int64_t row_stride, float *out, lse_stream_t stream,
+                                 lse_plan *plan);
+
+/*
  * lse_forward_host -- the same result from HOST buffers, synchronising
  * `stream` before returning.  A page-locked x (cudaHostAlloc'ed or registered)
  * is read in place by the kernel over the host link (zero copy; the bytes

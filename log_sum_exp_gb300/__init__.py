@@ -17,6 +17,8 @@ from ._binding import (  # noqa: F401
     lse_backward,
     lse_backward_ptr,
     lse_forward,
+    lse_forward16,
+    lse_forward16_ptr,
     lse_forward_host,
     lse_forward_host_ptr,
     lse_forward_plan,

@@ -21,7 +21,8 @@ PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4, "columns_war
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
-ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward_host",
+ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward16",
+                 "lse_forward_host",
                  "lse_token_logprob", "lse_token_logprob_plan", "lse_backward",
                  "lse_forward_strided", "lse_trim_memory", "lse_wait_timeouts",
                  "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
@@ -85,6 +86,8 @@ def load() -> ctypes.CDLL:
         lib.lse_forward_plan.argtypes = [vp, i32, i64, i64, i64, vp, vp,
                                          ctypes.POINTER(LsePlan), vp, vp]
         lib.lse_forward_plan.restype = i32
+        lib.lse_forward16.argtypes = [vp, i32, i64, i64, i64, vp, vp, ctypes.POINTER(LsePlan)]
+        lib.lse_forward16.restype = i32
         lib.lse_forward_host.argtypes = [vp, i32, i64, i64, i64, vp, vp]
         lib.lse_forward_host.restype = i32
         lib.lse_token_logprob.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, vp]
@@ -148,6 +151,14 @@ def lse_forward_plan_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int
     _check(load().lse_forward_plan(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
                                    stream or None, ctypes.byref(p), ev_begin or None,
                                    ev_end or None), "lse_forward_plan")
+    return p
+
+
+def lse_forward16_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int, out_ptr: int,
+                      stream: int = 0, plan: LsePlan | None = None) -> LsePlan:
+    p = plan if plan is not None else LsePlan()
+    _check(load().lse_forward16(x_ptr or None, DTYPES[dtype], B, N, row_stride, out_ptr or None,
+                                stream or None, ctypes.byref(p)), "lse_forward16")
     return p
 
 
@@ -279,6 +290,28 @@ def lse_forward_plan(x, plan: LsePlan | dict | None = None, out=None, stream=Non
         eve = _event_handle(ev_end)
         p = lse_forward_plan_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
                                  _stream_handle(stream, x.device), p, evb, eve)
+    if x.dim() == 1:
+        return out.reshape(()), p
+    return out, p
+
+
+def lse_forward16(x, plan: LsePlan | dict | None = None, out=None, stream=None):
+    """``lse_forward`` with reduced-bit exponentials (two terms per packed bf16
+    SFU operation; f32 sums).  Returns (out, plan_that_ran)."""
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    if out is None:
+        out = torch.empty(B, dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or out.numel() != B or not out.is_contiguous() \
+            or out.device != x.device:
+        raise ValueError("out must be a contiguous float32 tensor of B elements on x's device")
+    p = _as_plan(plan)
+    with torch.cuda.device(x.device):
+        p = lse_forward16_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
+                              _stream_handle(stream, x.device), p)
     if x.dim() == 1:
         return out.reshape(()), p
     return out, p

@@ -290,6 +290,13 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
 
 cudaError_t launch_subwarp(lse_dtype dt, const LaunchArgs& a, bool vec, int G, int V, int64_t grid) {
     const bool tl = a.tl.logprob != nullptr;
+    if (a.e16) {
+        switch (dt) {
+        case LSE_F32: return launch_subwarp_e16_f32(a, vec, G, V, grid);
+        case LSE_BF16: return launch_subwarp_e16_bf16(a, vec, G, V, grid);
+        default: return launch_subwarp_e16_f16(a, vec, G, V, grid);
+        }
+    }
     switch (dt) {
     case LSE_F32: return tl ? launch_subwarp_lp_f32(a, vec, G, V, grid) : launch_subwarp_f32(a, vec, G, V, grid);
     case LSE_BF16: return tl ? launch_subwarp_lp_bf16(a, vec, G, V, grid) : launch_subwarp_bf16(a, vec, G, V, grid);
@@ -300,6 +307,13 @@ cudaError_t launch_subwarp(lse_dtype dt, const LaunchArgs& a, bool vec, int G, i
 cudaError_t launch_segment(lse_dtype dt, const LaunchArgs& a, bool vec, int T, int64_t P,
                            int64_t seg_slots, float2* partial, float* xt_buf) {
     const bool tl = a.tl.logprob != nullptr;
+    if (a.e16) {
+        switch (dt) {
+        case LSE_F32: return launch_segment_e16_f32(a, vec, T, P, seg_slots, partial, xt_buf);
+        case LSE_BF16: return launch_segment_e16_bf16(a, vec, T, P, seg_slots, partial, xt_buf);
+        default: return launch_segment_e16_f16(a, vec, T, P, seg_slots, partial, xt_buf);
+        }
+    }
     switch (dt) {
     case LSE_F32:
         return tl ? launch_segment_lp_f32(a, vec, T, P, seg_slots, partial, xt_buf)
@@ -405,11 +419,12 @@ lse_status lse_plan_query(const void* x, lse_dtype dtype, int64_t B, int64_t N,
 
 namespace {
 
-// The forward pass behind lse_forward_plan and lse_token_logprob_plan.  `out`
-// may be null when `tl.logprob` is set; arguments are already checked.
+// The forward pass behind lse_forward_plan, lse_token_logprob_plan and
+// lse_forward16 (e16: reduced-bit exponentials).  `out` may be null when
+// `tl.logprob` is set; arguments are already checked.
 lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,
                        float* out, TokenLogprob tl, cudaStream_t stream, lse_plan* plan,
-                       lse_event_t ev_begin, lse_event_t ev_end) {
+                       lse_event_t ev_begin, lse_event_t ev_end, bool e16 = false) {
     if (B == 0) return LSE_OK;  // no work, no device access
     int dev = 0;
     const DeviceInfo* info = nullptr;
@@ -423,6 +438,7 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
 
     LaunchArgs a{x, B, N, row_stride, out, stream};
     a.tl = tl;
+    a.e16 = e16;
     cudaError_t e = cudaSuccess;
     char* scratch = nullptr;
     if (p.scratch_bytes > 0) {
@@ -444,7 +460,8 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
         e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
         break;
     case LSE_PATH_ROWTILE:
-        e = launch_rowtile(dtype, p.slots_per_lane, x, B, out, static_cast<int>(p.grid), stream);
+        e = launch_rowtile(dtype, p.slots_per_lane, e16, x, B, out, static_cast<int>(p.grid),
+                           stream);
         break;
     default:
         e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,
@@ -477,6 +494,14 @@ lse_status lse_forward_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N
     if (st != LSE_OK) return st;
     return run_forward(x, dtype, B, N, row_stride, out, TokenLogprob{},
                        reinterpret_cast<cudaStream_t>(stream), plan, ev_begin, ev_end);
+}
+
+lse_status lse_forward16(const void* x, lse_dtype dtype, int64_t B, int64_t N, int64_t row_stride,
+                         float* out, lse_stream_t stream, lse_plan* plan) {
+    const lse_status st = check_args(x, dtype, B, N, row_stride, out);
+    if (st != LSE_OK) return st;
+    return run_forward(x, dtype, B, N, row_stride, out, TokenLogprob{},
+                       reinterpret_cast<cudaStream_t>(stream), plan, nullptr, nullptr, true);
 }
 
 lse_status lse_token_logprob_plan(const void* x, lse_dtype dtype, int64_t B, int64_t N,

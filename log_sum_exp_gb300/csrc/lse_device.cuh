@@ -274,29 +274,113 @@ __device__ __forceinline__ float finalize_scaled(float m, float s, float mu, flo
     return m + kLn2 * (lg2(s) - r);
 }
 
-// Fold a chunk of W raw words into an accumulator.
+// ---------------------------------------------------------------------------
+// Reduced-bit exponentials (E16), the 16-bit compute variant of the method
+// ("Speeding up Log-Sum-Exp ...", Sec. 4.3, Fig. 5).  Each term's argument is
+// formed in f32 exactly as above; two arguments are rounded to bf16 (nearest
+// even) and exponentiated by one packed SFU operation, ex2.approx.ftz.bf16x2;
+// the two bf16 terms are added into the f32 sum by mixed-precision adds
+// (add.rn.f32.bf16, sm_100+).  Half the SFU operations of the f32 path.  bf16
+// keeps the f32 exponent range, so terms down to 2^-126 of the maximum still
+// count; the error comes from rounding the argument a to 8 significant bits
+// (a term is off by a factor 2^(|a| * 2^-8) at most) and from the bf16 result.
+// Special values behave as in the f32 path: ex2(-inf) = 0, ex2(+inf) = +inf,
+// NaN stays NaN through the conversion, the SFU and the adds.
+//
+// The packed instruction rounds its bf16 result toward zero (measured: every
+// result is the bf16 value at or below 2^a over the whole argument grid), which
+// lowers a term by half a bf16 ulp on average, 2^-8 / (2 ln 2) = 0.28 % of its
+// value for mantissas spread evenly on a log scale.  Every argument therefore
+// carries kE16Bias = -log2(1 - 2^-8 / (2 ln 2)): each term is scaled up by that
+// amount before the truncation takes it back off, so terms are unbiased on
+// average.  The maximum's own term, 2^kE16Bias = 1.0028, still truncates to
+// exactly 1, so one-element and constant rows stay exact.
+// ---------------------------------------------------------------------------
+constexpr float kE16Bias = 0.0040709119f;
+
+// The E16 argument of element x under shift mu.
+__device__ __forceinline__ float e16_arg(float x, float mu) {
+    return fmaf(x - mu, kLog2e, kE16Bias);
+}
+
+// 2^lo and 2^hi as a bf16 pair (lo in the low half).
+__device__ __forceinline__ uint32_t ex2_bf16_pair(float lo, float hi) {
+    uint32_t p, e;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p) : "f"(hi), "f"(lo));
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(p));
+    return e;
+}
+
+// acc + lo + hi for a bf16 pair, in f32.
+__device__ __forceinline__ float add_bf16_pair(float acc, uint32_t e) {
+    float d;
+    asm("{\n .reg .b16 lo, hi;\n .reg .f32 t;\n mov.b32 {lo, hi}, %1;\n"
+        " add.rn.f32.bf16 t, lo, %2;\n add.rn.f32.bf16 %0, hi, t;\n}\n"
+        : "=f"(d)
+        : "r"(e), "f"(acc));
+    return d;
+}
+
+// words_expsum with E16 exponentials: pairs are two f32 words, or the two
+// 16-bit halves of one word.
 template <int DT, int W>
+__device__ __forceinline__ float words_expsum16(const uint32_t (&w)[W], float mu) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if constexpr (DT == kF32) {
+        static_assert(W % 2 == 0, "f32 words are taken in pairs");
+#pragma unroll
+        for (int i = 0; i < W / 2; ++i)
+            acc[i & 3] = add_bf16_pair(acc[i & 3], ex2_bf16_pair(e16_arg(__uint_as_float(w[2 * i]), mu),
+                                                                 e16_arg(__uint_as_float(w[2 * i + 1]), mu)));
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            acc[i & 3] = add_bf16_pair(acc[i & 3], ex2_bf16_pair(e16_arg(word_lo<DT>(w[i]), mu),
+                                                                 e16_arg(word_hi<DT>(w[i]), mu)));
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// Exp-sum of raw words with f32 (E16 = false) or reduced-bit exponentials.
+template <int DT, int W, bool E16>
+__device__ __forceinline__ float expsum_words(const uint32_t (&w)[W], float mu) {
+    if constexpr (E16) return words_expsum16<DT, W>(w, mu);
+    else return words_expsum<DT, W>(w, mu);
+}
+
+// Fold a chunk of W raw words into an accumulator.
+template <int DT, int W, bool E16 = false>
 __device__ __forceinline__ void acc_add_words(Acc& a, float& mu, const uint32_t (&w)[W]) {
     acc_raise(a, mu, words_max<DT, W>(w));
-    a.s += words_expsum<DT, W>(w, mu);
+    a.s += expsum_words<DT, W, E16>(w, mu);
 }
 
 // Fold a chunk of K converted floats into an accumulator.
-template <int K>
+template <int K, bool E16 = false>
 __device__ __forceinline__ void acc_add_floats(Acc& a, float& mu, const float (&v)[K]) {
     float cm = v[0];
 #pragma unroll
     for (int i = 1; i < K; ++i) cm = fmaxf(cm, v[i]);
     acc_raise(a, mu, cm);
-    float e[K];
+    if constexpr (E16) {
+        static_assert(K % 2 == 0, "elements are taken in pairs");
+        float acc[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < K; ++i) e[i] = ex2((v[i] - mu) * kLog2e);
+        for (int i = 0; i < K / 2; ++i)
+            acc[i & 1] = add_bf16_pair(acc[i & 1], ex2_bf16_pair(e16_arg(v[2 * i], mu),
+                                                                 e16_arg(v[2 * i + 1], mu)));
+        a.s += acc[0] + acc[1];
+    } else {
+        float e[K];
 #pragma unroll
-    for (int stride = 1; stride < K; stride *= 2) {
+        for (int i = 0; i < K; ++i) e[i] = ex2((v[i] - mu) * kLog2e);
 #pragma unroll
-        for (int i = 0; i + stride < K; i += 2 * stride) e[i] += e[i + stride];
+        for (int stride = 1; stride < K; stride *= 2) {
+#pragma unroll
+            for (int i = 0; i + stride < K; i += 2 * stride) e[i] += e[i + stride];
+        }
+        a.s += e[0];
     }
-    a.s += e[0];
 }
 
 }  // namespace lse

@@ -30,6 +30,7 @@ struct LaunchArgs {
     float* out;          // row values; may be nullptr when tl.logprob is set
     cudaStream_t stream;
     TokenLogprob tl;
+    bool e16 = false;  // reduced-bit exponentials (row value only)
 };
 
 // Launch with programmatic stream serialization (see pdl_trigger / pdl_wait in
@@ -88,6 +89,10 @@ LSE_DECLARE_TYPE_ENTRY_POINTS(f16)
 LSE_DECLARE_TYPE_ENTRY_POINTS(lp_f32)
 LSE_DECLARE_TYPE_ENTRY_POINTS(lp_bf16)
 LSE_DECLARE_TYPE_ENTRY_POINTS(lp_f16)
+// The same kernels with reduced-bit (packed bf16) exponentials.
+LSE_DECLARE_TYPE_ENTRY_POINTS(e16_f32)
+LSE_DECLARE_TYPE_ENTRY_POINTS(e16_bf16)
+LSE_DECLARE_TYPE_ENTRY_POINTS(e16_f16)
 
 // Type-independent kernels (lse_api.cu).
 cudaError_t launch_fill_neg_inf(float* out, float* logprob, int64_t B, cudaStream_t stream);
@@ -137,8 +142,8 @@ int cols_rows_per_batch(bool vec);  // per warp per iteration
 int cols_warps_per_cta();
 
 // Short contiguous rows through the bulk-copy ring (lse_rowtile.cu).
-cudaError_t launch_rowtile(int dt, int nv, const void* x, int64_t B, float* out, int grid,
-                           cudaStream_t stream);
+cudaError_t launch_rowtile(int dt, int nv, bool e16, const void* x, int64_t B, float* out,
+                           int grid, cudaStream_t stream);
 int rowtile_ctas_per_sm();
 int rowtile_rows_per_chunk(int nv);
 cudaError_t read_wait_timeouts(unsigned long long* count);

@@ -12,7 +12,9 @@
 //            memory.  With one segment per row it writes out[row]; with P > 1
 //            segments it writes an (m, s) partial that merge_kernel
 //            (lse_api.cu) combines -- the split-row mapping for long or few rows.
-// Both take an optional fused epilogue (TL) for the token log-probability.
+// Both take an optional fused epilogue (TL) for the token log-probability, and
+// E16 selects the reduced-bit exponentials of lse_device.cuh (two terms per
+// packed bf16 SFU operation) in place of the f32 ones.
 // Back-to-back short rows have a bulk-copy mapping of their own
 // (lse_rowtile.cu).  This header is included by one translation unit per
 // element type and epilogue.
@@ -54,7 +56,7 @@ __device__ __forceinline__ void load_tail_words(const void* row, int64_t start, 
 // VEC: a slot is one 16-byte vector (the lane holding vector index N/EPV also
 // loads the < EPV tail elements); !VEC: a slot is one element.
 // ---------------------------------------------------------------------------
-template <int DT, int G, int V, bool VEC, bool TL>
+template <int DT, int G, int V, bool VEC, bool TL, bool E16>
 __global__ void __launch_bounds__(kSubwarpThreads, kSubwarpMinBlocks)
 lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                    float* __restrict__ out, const int64_t* __restrict__ target,
@@ -124,11 +126,13 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                 const float mu = shift_of(m);
                 // FFMA form for the 4-slot variants (every row longer than two
-                // vectors); same decision for the whole group.
-                const bool scaled = V == 4 && ffma_shift_ok(mu);
+                // vectors); same decision for the whole group.  Not with E16:
+                // there the maximum's own argument must be exactly 0 (its bf16
+                // term exactly 1), not the rounding residual of mu log2 e.
+                const bool scaled = !E16 && V == 4 && ffma_shift_ok(mu);
                 const float c = mu * kLog2e;
                 float s = scaled ? words_expsum_scaled<DT, 4 * V>(w[r], c)
-                                 : words_expsum<DT, 4 * V>(w[r], mu);
+                                 : expsum_words<DT, 4 * V, E16>(w[r], mu);
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -177,8 +181,17 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                 const float mu = shift_of(m);
                 float s = 0.0f;
+                if constexpr (E16) {
 #pragma unroll
-                for (int j = 0; j < V; ++j) s += ex2((v[r][j] - mu) * kLog2e);
+                    for (int j = 0; j < V; j += 2) {
+                        const float hi = j + 1 < V ? e16_arg(v[r][j + 1], mu)
+                                                   : __int_as_float(kNegInfF32);
+                        s = add_bf16_pair(s, ex2_bf16_pair(e16_arg(v[r][j], mu), hi));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < V; ++j) s += ex2((v[r][j] - mu) * kLog2e);
+                }
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -206,7 +219,7 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 // ---------------------------------------------------------------------------
 template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
 
-template <int DT, int T, bool VEC, bool TL>
+template <int DT, int T, bool VEC, bool TL, bool E16>
 __global__ void __launch_bounds__(T, SegmentOccupancy<T>::min_blocks)
 lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, int64_t P,
                    int64_t seg_slots, float* __restrict__ out, float2* __restrict__ partial,
@@ -251,7 +264,7 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
                 if (t >= 0 && t < N) xt = load_elem<DT>(rp, t);
                 xt_pending = false;
             }
-            acc_add_words<DT, 4 * U>(acc, mu, w);
+            acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
         if (k < s_end) {
             uint32_t w[4 * U];
@@ -266,20 +279,20 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
                     for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
                 }
             }
-            acc_add_words<DT, 4 * U>(acc, mu, w);
+            acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
         const int tail = static_cast<int>(N - nv * EPV);
         if (tail > 0 && seg == P - 1 && threadIdx.x == 0) {
             uint32_t w[4];
             load_tail_words<DT>(rp, nv * EPV, tail, w);
-            acc_add_words<DT, 4>(acc, mu, w);
+            acc_add_words<DT, 4, E16>(acc, mu, w);
         }
     } else {
         for (; k + (U - 1) * T < s_end; k += U * T) {
             float v[U];
 #pragma unroll
             for (int j = 0; j < U; ++j) v[j] = load_elem<DT>(rp, k + j * T);
-            acc_add_floats<U>(acc, mu, v);
+            acc_add_floats<U, E16>(acc, mu, v);
         }
         if (k < s_end) {
             float v[U];
@@ -288,7 +301,7 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
                 const int64_t kk = k + j * T;
                 v[j] = kk < s_end ? load_elem<DT>(rp, kk) : __int_as_float(kNegInfF32);
             }
-            acc_add_floats<U>(acc, mu, v);
+            acc_add_floats<U, E16>(acc, mu, v);
         }
     }
 
@@ -319,49 +332,50 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
 // ---------------------------------------------------------------------------
 // Host-side launchers for one element type.
 // ---------------------------------------------------------------------------
-template <int DT, int G, int V, bool VEC, bool TL>
+template <int DT, int G, int V, bool VEC, bool TL, bool E16>
 cudaError_t launch_subwarp_gv(const LaunchArgs& a, int64_t grid) {
-    return launch_pdl(lse_subwarp_kernel<DT, G, V, VEC, TL>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl(lse_subwarp_kernel<DT, G, V, VEC, TL, E16>, dim3(static_cast<unsigned>(grid)),
                       dim3(kSubwarpThreads), a.stream, a.x, a.B, a.N, a.row_stride, a.out,
                       a.tl.target, a.tl.logprob);
 }
 
-template <int DT, int G, bool VEC, bool TL>
+template <int DT, int G, bool VEC, bool TL, bool E16>
 cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     switch (V) {
-    case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL>(a, grid);
-    case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL>(a, grid);
-    case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL>(a, grid);
+    case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL, E16>(a, grid);
+    case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL, E16>(a, grid);
+    case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL, E16>(a, grid);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int DT, bool VEC, bool TL>
+template <int DT, bool VEC, bool TL, bool E16>
 cudaError_t launch_subwarp_dt(const LaunchArgs& a, int G, int V, int64_t grid) {
     switch (G) {
-    case 1: return launch_subwarp_g<DT, 1, VEC, TL>(a, V, grid);
-    case 2: return launch_subwarp_g<DT, 2, VEC, TL>(a, V, grid);
-    case 4: return launch_subwarp_g<DT, 4, VEC, TL>(a, V, grid);
-    case 8: return launch_subwarp_g<DT, 8, VEC, TL>(a, V, grid);
-    case 16: return launch_subwarp_g<DT, 16, VEC, TL>(a, V, grid);
-    case 32: return launch_subwarp_g<DT, 32, VEC, TL>(a, V, grid);
+    case 1: return launch_subwarp_g<DT, 1, VEC, TL, E16>(a, V, grid);
+    case 2: return launch_subwarp_g<DT, 2, VEC, TL, E16>(a, V, grid);
+    case 4: return launch_subwarp_g<DT, 4, VEC, TL, E16>(a, V, grid);
+    case 8: return launch_subwarp_g<DT, 8, VEC, TL, E16>(a, V, grid);
+    case 16: return launch_subwarp_g<DT, 16, VEC, TL, E16>(a, V, grid);
+    case 32: return launch_subwarp_g<DT, 32, VEC, TL, E16>(a, V, grid);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int DT, int T, bool VEC, bool TL>
+template <int DT, int T, bool VEC, bool TL, bool E16>
 cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial,
                              float* xt_buf) {
     const int64_t grid = a.B * P;
-    return launch_pdl(lse_segment_kernel<DT, T, VEC, TL>, dim3(static_cast<unsigned>(grid)), dim3(T),
+    return launch_pdl(lse_segment_kernel<DT, T, VEC, TL, E16>, dim3(static_cast<unsigned>(grid)), dim3(T),
                       a.stream, a.x, a.N, a.row_stride, P, seg_slots, a.out, partial,
                       a.tl.target, a.tl.logprob, xt_buf);
 }
 
-template <int DT, int T, bool VEC, bool TL>
+template <int DT, int T, bool VEC, bool TL, bool E16>
 int segment_occupancy_t() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC, TL>, T, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC, TL, E16>, T,
+                                                      0) !=
         cudaSuccess)
         return 0;
     return blocks;
@@ -370,42 +384,43 @@ int segment_occupancy_t() {
 }  // namespace lse
 
 // Instantiates the per-type entry points declared in lse_internal.h; TL selects
-// the kernels with the fused token log-probability epilogue.
-#define LSE_DEFINE_TYPE_ENTRY_POINTS(DT, SUFFIX, TL)                                               \
+// the kernels with the fused token log-probability epilogue, E16 the
+// reduced-bit exponentials.
+#define LSE_DEFINE_TYPE_ENTRY_POINTS(DT, SUFFIX, TL, E16)                                               \
     namespace lse {                                                                            \
     cudaError_t launch_subwarp_##SUFFIX(const LaunchArgs& a, bool vec, int G, int V,           \
                                         int64_t grid) {                                        \
-        return vec ? launch_subwarp_dt<DT, true, TL>(a, G, V, grid)                                \
-                   : launch_subwarp_dt<DT, false, TL>(a, G, V, grid);                              \
+        return vec ? launch_subwarp_dt<DT, true, TL, E16>(a, G, V, grid)                                \
+                   : launch_subwarp_dt<DT, false, TL, E16>(a, G, V, grid);                              \
     }                                                                                          \
     cudaError_t launch_segment_##SUFFIX(const LaunchArgs& a, bool vec, int threads, int64_t P, \
                                         int64_t seg_slots, float2* partial, float* xt_buf) {   \
         switch (threads) {                                                                     \
-        case 32: return vec ? launch_segment_t<DT, 32, true, TL>(a, P, seg_slots, partial, xt_buf)         \
-                            : launch_segment_t<DT, 32, false, TL>(a, P, seg_slots, partial, xt_buf);       \
-        case 64: return vec ? launch_segment_t<DT, 64, true, TL>(a, P, seg_slots, partial, xt_buf)         \
-                            : launch_segment_t<DT, 64, false, TL>(a, P, seg_slots, partial, xt_buf);       \
-        case 128: return vec ? launch_segment_t<DT, 128, true, TL>(a, P, seg_slots, partial, xt_buf)       \
-                             : launch_segment_t<DT, 128, false, TL>(a, P, seg_slots, partial, xt_buf);     \
-        case 256: return vec ? launch_segment_t<DT, 256, true, TL>(a, P, seg_slots, partial, xt_buf)       \
-                             : launch_segment_t<DT, 256, false, TL>(a, P, seg_slots, partial, xt_buf);     \
-        case 512: return vec ? launch_segment_t<DT, 512, true, TL>(a, P, seg_slots, partial, xt_buf)       \
-                             : launch_segment_t<DT, 512, false, TL>(a, P, seg_slots, partial, xt_buf);     \
+        case 32: return vec ? launch_segment_t<DT, 32, true, TL, E16>(a, P, seg_slots, partial, xt_buf)         \
+                            : launch_segment_t<DT, 32, false, TL, E16>(a, P, seg_slots, partial, xt_buf);       \
+        case 64: return vec ? launch_segment_t<DT, 64, true, TL, E16>(a, P, seg_slots, partial, xt_buf)         \
+                            : launch_segment_t<DT, 64, false, TL, E16>(a, P, seg_slots, partial, xt_buf);       \
+        case 128: return vec ? launch_segment_t<DT, 128, true, TL, E16>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 128, false, TL, E16>(a, P, seg_slots, partial, xt_buf);     \
+        case 256: return vec ? launch_segment_t<DT, 256, true, TL, E16>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 256, false, TL, E16>(a, P, seg_slots, partial, xt_buf);     \
+        case 512: return vec ? launch_segment_t<DT, 512, true, TL, E16>(a, P, seg_slots, partial, xt_buf)       \
+                             : launch_segment_t<DT, 512, false, TL, E16>(a, P, seg_slots, partial, xt_buf);     \
         default: return cudaErrorInvalidValue;                                                 \
         }                                                                                      \
     }                                                                                          \
     int segment_occupancy_##SUFFIX(bool vec, int threads) {                                    \
         switch (threads) {                                                                     \
-        case 32: return vec ? segment_occupancy_t<DT, 32, true, TL>()                              \
-                            : segment_occupancy_t<DT, 32, false, TL>();                            \
-        case 64: return vec ? segment_occupancy_t<DT, 64, true, TL>()                              \
-                            : segment_occupancy_t<DT, 64, false, TL>();                            \
-        case 128: return vec ? segment_occupancy_t<DT, 128, true, TL>()                            \
-                             : segment_occupancy_t<DT, 128, false, TL>();                          \
-        case 256: return vec ? segment_occupancy_t<DT, 256, true, TL>()                            \
-                             : segment_occupancy_t<DT, 256, false, TL>();                          \
-        case 512: return vec ? segment_occupancy_t<DT, 512, true, TL>()                            \
-                             : segment_occupancy_t<DT, 512, false, TL>();                          \
+        case 32: return vec ? segment_occupancy_t<DT, 32, true, TL, E16>()                              \
+                            : segment_occupancy_t<DT, 32, false, TL, E16>();                            \
+        case 64: return vec ? segment_occupancy_t<DT, 64, true, TL, E16>()                              \
+                            : segment_occupancy_t<DT, 64, false, TL, E16>();                            \
+        case 128: return vec ? segment_occupancy_t<DT, 128, true, TL, E16>()                            \
+                             : segment_occupancy_t<DT, 128, false, TL, E16>();                          \
+        case 256: return vec ? segment_occupancy_t<DT, 256, true, TL, E16>()                            \
+                             : segment_occupancy_t<DT, 256, false, TL, E16>();                          \
+        case 512: return vec ? segment_occupancy_t<DT, 512, true, TL, E16>()                            \
+                             : segment_occupancy_t<DT, 512, false, TL, E16>();                          \
         default: return 0;                                                                     \
         }                                                                                      \
     }                                                                                          \

@@ -2,4 +2,4 @@
 // epilogue, for bf16 elements (see lse_kernels.cuh).
 #include "lse_kernels.cuh"
 
-LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kBF16, lp_bf16, true)
+LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kBF16, lp_bf16, true, false)

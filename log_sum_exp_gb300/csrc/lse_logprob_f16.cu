@@ -2,4 +2,4 @@
 // epilogue, for f16 elements (see lse_kernels.cuh).
 #include "lse_kernels.cuh"
 
-LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kF16, lp_f16, true)
+LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kF16, lp_f16, true, false)

@@ -2,4 +2,4 @@
 // epilogue, for f32 elements (see lse_kernels.cuh).
 #include "lse_kernels.cuh"
 
-LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kF32, lp_f32, true)
+LSE_DEFINE_TYPE_ENTRY_POINTS(lse::kF32, lp_f32, true, false)

@@ -5,8 +5,9 @@
 // HBM into a ring of shared-memory stages with cp.async.bulk (the Tensor
 // Memory Accelerator's 1-D copy; one instruction per chunk, completion tracked
 // by an mbarrier transaction count), and each of its 256 threads reduces whole
-// rows out of shared memory: max, then one FFMA + ex2 per element, then the
-// finalize of lse_device.cuh.  Memory traffic never waits for the arithmetic:
+// rows out of shared memory: max, then one FFMA + ex2 per element (or, with
+// E16, one packed bf16 ex2 per two elements), then the finalize of
+// lse_device.cuh.  Memory traffic never waits for the arithmetic:
 // while one stage is consumed the others are in flight.  ("Speeding up
 // Log-Sum-Exp ...", Sec. 3.1: one pass, a register accumulator per row.)
 //
@@ -75,7 +76,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // NV 16-byte vectors per row; RPT = 8 / NV rows per thread per chunk, so a
 // chunk is 256 * RPT rows = 32 KB.  Chunks are dealt round-robin to the CTAs.
-template <int DT, int NV>
+template <int DT, int NV, bool E16>
 __global__ void __launch_bounds__(kTileThreads)
 lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ out) {
     constexpr int RB = NV * 16;                // bytes per row
@@ -143,11 +144,11 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
                 const float m = words_max<DT, 4 * NV>(w[q]);
                 const float mu = shift_of(m);
                 float lse;
-                if (ffma_shift_ok(mu)) {
+                if (!E16 && ffma_shift_ok(mu)) {  // E16: exact 0 argument for the maximum
                     const float cc = mu * kLog2e;
                     lse = finalize_scaled(m, words_expsum_scaled<DT, 4 * NV>(w[q], cc), mu, cc);
                 } else {
-                    lse = acc_finalize(Acc{m, words_expsum<DT, 4 * NV>(w[q], mu)});
+                    lse = acc_finalize(Acc{m, expsum_words<DT, 4 * NV, E16>(w[q], mu)});
                 }
                 out[row] = lse;
             }
@@ -167,37 +168,44 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     }
 }
 
-template <int DT, int NV>
+template <int DT, int NV, bool E16>
 cudaError_t launch_rowtile_t(const void* x, int64_t B, float* out, int grid, cudaStream_t stream) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV>,
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV, E16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_kernel<DT, NV>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl_smem(lse_rowtile_kernel<DT, NV, E16>, dim3(static_cast<unsigned>(grid)),
                            dim3(kTileThreads), static_cast<size_t>(smem), stream, x, B, out);
 }
 
-template <int DT>
+template <int DT, bool E16>
 cudaError_t launch_rowtile_dt(int nv, const void* x, int64_t B, float* out, int grid,
                               cudaStream_t stream) {
     switch (nv) {
-    case 1: return launch_rowtile_t<DT, 1>(x, B, out, grid, stream);
-    case 2: return launch_rowtile_t<DT, 2>(x, B, out, grid, stream);
-    case 4: return launch_rowtile_t<DT, 4>(x, B, out, grid, stream);
-    case 8: return launch_rowtile_t<DT, 8>(x, B, out, grid, stream);
+    case 1: return launch_rowtile_t<DT, 1, E16>(x, B, out, grid, stream);
+    case 2: return launch_rowtile_t<DT, 2, E16>(x, B, out, grid, stream);
+    case 4: return launch_rowtile_t<DT, 4, E16>(x, B, out, grid, stream);
+    case 8: return launch_rowtile_t<DT, 8, E16>(x, B, out, grid, stream);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool E16>
+cudaError_t launch_rowtile_e(int dt, int nv, const void* x, int64_t B, float* out, int grid,
+                             cudaStream_t stream) {
+    switch (dt) {
+    case kF32: return launch_rowtile_dt<kF32, E16>(nv, x, B, out, grid, stream);
+    case kBF16: return launch_rowtile_dt<kBF16, E16>(nv, x, B, out, grid, stream);
+    default: return launch_rowtile_dt<kF16, E16>(nv, x, B, out, grid, stream);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_rowtile(int dt, int nv, const void* x, int64_t B, float* out, int grid,
-                           cudaStream_t stream) {
-    switch (dt) {
-    case kF32: return launch_rowtile_dt<kF32>(nv, x, B, out, grid, stream);
-    case kBF16: return launch_rowtile_dt<kBF16>(nv, x, B, out, grid, stream);
-    default: return launch_rowtile_dt<kF16>(nv, x, B, out, grid, stream);
-    }
+cudaError_t launch_rowtile(int dt, int nv, bool e16, const void* x, int64_t B, float* out,
+                           int grid, cudaStream_t stream) {
+    return e16 ? launch_rowtile_e<true>(dt, nv, x, B, out, grid, stream)
+               : launch_rowtile_e<false>(dt, nv, x, B, out, grid, stream);
 }
 
 int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM

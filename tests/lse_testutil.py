@@ -95,3 +95,56 @@ def device_rows(x: np.ndarray, dtype: str, row_stride: int | None = None, offset
         return buf, buf[offset:offset].reshape(0, N)
     view = buf[offset:offset + B * row_stride].reshape(B, row_stride)[:, :N]
     return buf, view
+
+
+# Reduced-bit exponentials (lse_forward16): a term with base-2 argument a is
+# within a relative r(a) = 2^(E16_BIAS + (|a| + E16_BIAS) E16_ARG) - 1 + E16_OUT
+# of its exact value (the accuracy statement of lse_forward16 in include/lse.h):
+# the argument carries the constant E16_BIAS and is rounded to bf16, and the
+# SFU's bf16 result is truncated (by less than a factor 1 - E16_OUT).
+E16_ARG = 2.0 ** -8 + 2.0 ** -22  # bf16 rounding of the argument, plus its f32 steps
+E16_OUT = 2.0 ** -7               # truncation of the packed bf16 exponential's result
+E16_BIAS = 0.0040709119223702435  # -log2(1 - 2^-8 / (2 ln 2))
+LOG2E = 1.4426950408889634
+
+
+def e16_bound(x: np.ndarray, dtype: str, want: np.ndarray, block_elems: int = 1 << 24):
+    """Per-row bound on |lse_forward16 - oracle|: -log(1 - e) + ATOL + RTOL |want|
+    with e = sum_n p_n r(a_n), p the oracle's softmax of the row (its backward
+    with unit gradient) and |a_n| = (max - x_n) log2 e.  inf for non-finite rows
+    (those must match exactly)."""
+    import oracle
+
+    B = want.shape[0]
+    N = x.shape[1] if x.ndim == 2 else 0
+    out = np.full(B, np.inf)
+    rows = max(1, block_elems // max(N, 1))
+    for b0 in range(0, B, rows):
+        xb = np.ascontiguousarray(x[b0:b0 + rows])
+        wb = np.asarray(want[b0:b0 + rows], dtype=np.float64)
+        fin = np.isfinite(wb)
+        if not fin.any() or N == 0:
+            continue
+        xd = oracle.decode(xb, dtype).reshape(xb.shape[0], N)
+        p = oracle.backward(xb, np.where(fin, wb, 0.0), np.ones(len(wb)), dtype)
+        p = p.reshape(xb.shape[0], N)
+        m = np.max(np.where(np.isnan(xd), -np.inf, xd), axis=1)
+        with np.errstate(invalid="ignore", over="ignore"):
+            a = (m[:, None] - xd) * LOG2E
+            r = np.exp2(E16_BIAS + (a + E16_BIAS) * E16_ARG) - 1.0 + E16_OUT
+            r = np.where(a > 125.0, 1.0, r)  # flushed below 2^-126 of the maximum
+            e = np.where(p > 0, p * r, 0.0).sum(axis=1)
+            bnd = np.where(e < 1.0, -np.log1p(-np.minimum(e, 0.999999)), np.inf)
+        out[b0:b0 + len(wb)] = np.where(fin, bnd + ATOL + RTOL * np.abs(wb), np.inf)
+    return out
+
+
+def compare_e16(got: np.ndarray, want: np.ndarray, bound: np.ndarray) -> dict:
+    """Special values exactly, finite rows within their e16_bound; the summary
+    adds the mean absolute and mean signed errors."""
+    s = compare(got, want, atol=0.0, rtol=1.0, scale=bound)
+    fin = np.isfinite(np.asarray(want, dtype=np.float64))
+    d = np.asarray(got, dtype=np.float64)[fin] - np.asarray(want, dtype=np.float64)[fin]
+    s["mean_abs_err"] = float(np.abs(d).mean()) if d.size else 0.0
+    s["mean_err"] = float(d.mean()) if d.size else 0.0
+    return s

@@ -328,38 +328,44 @@ def run_native(args) -> None:
     dt = w.dtype
     ptrs = [(t.data_ptr(), o.data_ptr()) for t, o in zip(xs, outs)]
     op_name = args.op
+    # A forced plan (--plan) is resolved by its first call and then reused.
+    req = L._binding._as_plan(args.plan) if args.plan else None
     if op_name == "forward":
-        plan = L.lse_plan_query(xs[0])
+        if req is None:
+            plan = L.lse_plan_query(xs[0])
+        else:
+            plan = L.lse_forward_plan_ptr(ptrs[0][0], dt, w.B, w.N, w.N, ptrs[0][1], sh,
+                                          req).as_dict()
         bytes_per_step = in_bytes + w.write_bytes
 
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
-            L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, None, evb, eve)
+            L.lse_forward_plan_ptr(xp, dt, w.B, w.N, w.N, op, sh, req, evb, eve)
     elif op_name == "forward16":
-        plan = L.lse_forward16_ptr(ptrs[0][0], dt, w.B, w.N, w.N, ptrs[0][1], sh).as_dict()
+        plan = L.lse_forward16_ptr(ptrs[0][0], dt, w.B, w.N, w.N, ptrs[0][1], sh, req).as_dict()
         bytes_per_step = in_bytes + w.write_bytes
 
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
-            L.lse_forward16_ptr(xp, dt, w.B, w.N, w.N, op, sh)
+            L.lse_forward16_ptr(xp, dt, w.B, w.N, w.N, op, sh, req)
     elif op_name == "logprob":
         # Targets drawn once per copy; only the log-probabilities are written.
         rng = np.random.default_rng(w.seed + 1)
         tgts = [torch.from_numpy(rng.integers(0, w.N, w.B).astype(np.int64)).to(dev)
                 for _ in range(copies)]
         plan = L.lse_token_logprob_ptr(ptrs[0][0], dt, w.B, w.N, w.N, tgts[0].data_ptr(),
-                                       ptrs[0][1], 0, sh).as_dict()
+                                       ptrs[0][1], 0, sh, req).as_dict()
         bytes_per_step = in_bytes + 8 * w.B + 4 * w.B
 
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
-            L.lse_token_logprob_ptr(xp, dt, w.B, w.N, w.N, tgts[i % copies].data_ptr(), op, 0, sh)
+            L.lse_token_logprob_ptr(xp, dt, w.B, w.N, w.N, tgts[i % copies].data_ptr(), op, 0, sh,
+                                    req)
     elif op_name == "columns":
         A, R, C = cw.A, cw.R, cw.C
         plan = L.lse_forward_strided_ptr(ptrs[0][0], dt, A, R, C, R * C, C, ptrs[0][1], sh,
-                                         args.plan).as_dict()
+                                         req).as_dict()
         bytes_per_step = in_bytes + w.write_bytes
-        req = L._binding._as_plan(args.plan) if args.plan else None
 
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
@@ -421,12 +427,12 @@ def run_native(args) -> None:
         s2 = torch.cuda.Stream(dev)
         s2.wait_stream(stream)
         with torch.cuda.stream(s2):
-            L.lse_forward(xs[0], out=outs[0])
+            L.lse_forward_plan(xs[0], plan=args.plan, out=outs[0])
         stream.wait_stream(s2)
         reps = 100
         with torch.cuda.graph(g):
             for i in range(reps):
-                L.lse_forward(xs[i % copies], out=outs[i % copies])
+                L.lse_forward_plan(xs[i % copies], plan=args.plan, out=outs[i % copies])
         g.replay()
         torch.cuda.synchronize(dev)
         t0 = torch.cuda.Event(enable_timing=True)
@@ -534,7 +540,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip the CUDA-graph replay timing (us_per_call_graph)")
     ap.add_argument("--plan", type=json.loads, default=None,
-                    help='forced plan for --op columns as JSON, e.g. {"path": "columns_cta"}')
+                    help='forced plan as JSON (fields of lse_plan, path by name), e.g. '
+                         '{"path": "subwarp"} or, for --op columns, {"path": "columns_cta"}')
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

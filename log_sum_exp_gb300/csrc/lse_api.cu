@@ -629,10 +629,11 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
         }
         vec = req->vector_bytes == 16;
     }
-    const int W = cols_warps_per_cta();
     const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
     const int64_t gy = A < 65535 ? A : 65535;
-    const int64_t resident_warps = static_cast<int64_t>(info->sms) * W * cols_occupancy(dtype, vec);
+    // Resident warps of the single-warp-tile variant (used to pick WT).
+    const int64_t resident_warps = static_cast<int64_t>(info->sms) * cols_warps_per_cta(1) *
+                                   cols_occupancy(dtype, vec, 1);
     const int64_t batch = cols_rows_per_batch(vec);
     // Warps per tile (measured): short reductions walk each tile with one
     // warp and no merge; longer ones share a tile between 4 warps and fill
@@ -645,15 +646,16 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     }
     if (WT == 0) {
         if (path == LSE_PATH_COLUMNS_CTA)
-            WT = W;
+            WT = 8;
         else
             WT = (R <= 256 || wtiles * gy >= 2 * resident_warps) ? 1 : 4;
     }
     if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
     path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
+    const int W = cols_warps_per_cta(WT);
     const int64_t gx = ceil_div(wtiles, W / WT);
     const int64_t rows_per_warp_batch = WT * batch;
-    const int64_t resident_ctas = resident_warps / W;
+    const int64_t resident_ctas = static_cast<int64_t>(info->sms) * cols_occupancy(dtype, vec, WT);
     int64_t P = req ? req->splits : 0;
     if (P == 0) {
         // No split while the CTAs already fill half the resident slots (a

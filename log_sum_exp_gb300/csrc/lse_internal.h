@@ -136,10 +136,10 @@ struct StridedArgs {
 cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a);
 cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t P, float* out,
                                  cudaStream_t stream);
-int cols_occupancy(int dt, bool vec);
+int cols_occupancy(int dt, bool vec, int warps_per_tile);  // CTAs per SM
 int cols_columns_per_warp(bool vec, int dt);
 int cols_rows_per_batch(bool vec);  // per warp per iteration
-int cols_warps_per_cta();
+int cols_warps_per_cta(int warps_per_tile);
 
 // Short contiguous rows through the bulk-copy ring (lse_rowtile.cu).
 cudaError_t launch_rowtile(int dt, int nv, bool e16, const void* x, int64_t B, float* out,

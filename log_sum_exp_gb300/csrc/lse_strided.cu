@@ -26,23 +26,25 @@
 namespace lse {
 namespace {
 
-constexpr int kColWarps = 8;
-constexpr int kColThreads = 32 * kColWarps;
+// Warps per CTA for WT warps per tile: 4 (small CTAs balance better across
+// SMs) unless the tile itself takes 8.
+template <int WT> struct ColCta { static constexpr int warps = WT > 4 ? WT : 4; };
 
 // WT warps share one column tile and interleave its rows (merged in shared
-// memory); the CTA's 8 warps cover 8 / WT tiles.  WT = 1: each warp walks all
-// rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
+// memory); the CTA's warps cover warps / WT tiles.  WT = 1: each warp walks
+// all rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
 // works on one tile (long reductions with few tiles).
 template <int DT, bool VEC, int WT>
-__global__ void __launch_bounds__(kColThreads)
+__global__ void __launch_bounds__(32 * ColCta<WT>::warps)
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
-    constexpr int TPC = kColWarps / WT;  // tiles per CTA
-    __shared__ float2 part[WT > 1 ? kColWarps : 1][32][EPV];
+    constexpr int NW = ColCta<WT>::warps;
+    constexpr int TPC = NW / WT;  // tiles per CTA
+    __shared__ float2 part[WT > 1 ? NW : 1][32][EPV];
 
     pdl_trigger();
     pdl_wait();
@@ -58,6 +60,7 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
     const int64_t r_end = r_begin + rows_per_split < R ? r_begin + rows_per_split : R;
     const char* xb = reinterpret_cast<const char*>(x);
 
+    constexpr int64_t kStep = static_cast<int64_t>(WT) * U;  // rows per batch of one warp
     for (int64_t a = blockIdx.y; a < A; a += gridDim.y) {
         const char* base = xb + (a * stride_a + c0) * EB;
         Acc acc[EPV];
@@ -67,21 +70,48 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             acc[e] = acc_identity();
             mu[e] = 0.0f;
         }
-        for (int64_t r = r_begin + phase; r < r_end; r += static_cast<int64_t>(WT) * U) {
-            float v[U][EPV];
+        // PIPE: the next batch's loads are issued before the current batch is
+        // folded, so two batches per warp are in flight.  For one warp per
+        // tile (short reductions, which otherwise wait a full memory round
+        // trip per batch) on 4-byte elements, where the second buffer still
+        // fits 4 CTAs per SM.
+        constexpr bool PIPE = VEC && WT == 1 && EB == 4;
+        uint4 nxt[U];
+        auto load_batch = [&](int64_t r, uint4 (&u)[U]) {
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 const int64_t rr = r + j * WT;
-                const bool ok = active && rr < r_end;
-                if constexpr (VEC) {
-                    uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
-                                         neg_inf_word<DT>());
-                    if (ok) u = ldg_stream16(base + rr * stride_r * EB);
-                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                u[j] = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                  neg_inf_word<DT>());
+                if (active && rr < r_end) u[j] = ldg_stream16(base + rr * stride_r * EB);
+            }
+        };
+        if constexpr (PIPE) {
+            if (r_begin + phase < r_end) load_batch(r_begin + phase, nxt);
+        }
+        for (int64_t r = r_begin + phase; r < r_end; r += kStep) {
+            float v[U][EPV];
+            if constexpr (VEC) {
+                uint4 cur[U];
+                if constexpr (PIPE) {
+#pragma unroll
+                    for (int j = 0; j < U; ++j) cur[j] = nxt[j];
+                    if (r + kStep < r_end) load_batch(r + kStep, nxt);  // uniform per warp
+                } else {
+                    load_batch(r, cur);
+                }
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const uint32_t w4[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) v[j][e] = word_elem<DT>(w4, e);
-                } else {
-                    v[j][0] = ok ? load_elem<DT>(base, rr * stride_r) : __int_as_float(kNegInfF32);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const int64_t rr = r + j * WT;
+                    v[j][0] = active && rr < r_end ? load_elem<DT>(base, rr * stride_r)
+                                                   : __int_as_float(kNegInfF32);
                 }
             }
 #pragma unroll
@@ -146,9 +176,10 @@ merge_columns_kernel(const float2* __restrict__ partial, int64_t outputs, int64_
 
 template <int DT, bool VEC>
 cudaError_t launch_cols_t(const StridedArgs& a) {
-#define LSE_COLS_LAUNCH(WT)                                                                        \
-    return launch_pdl(lse_cols_kernel<DT, VEC, WT>, a.grid, dim3(kColThreads), a.stream, a.x, a.A, \
-                      a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out, a.partial, a.P)
+#define LSE_COLS_LAUNCH(WT)                                                                     \
+    return launch_pdl(lse_cols_kernel<DT, VEC, WT>, a.grid, dim3(32 * ColCta<WT>::warps), a.stream, \
+                      a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out,          \
+                      a.partial, a.P)
     switch (a.warps_per_tile) {
     case 1: LSE_COLS_LAUNCH(1);
     case 2: LSE_COLS_LAUNCH(2);
@@ -159,13 +190,23 @@ cudaError_t launch_cols_t(const StridedArgs& a) {
 #undef LSE_COLS_LAUNCH
 }
 
-template <int DT, bool VEC>
-int cols_occupancy_t() {
+template <int DT, bool VEC, int WT>
+int cols_occupancy_w() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, 8>,
-                                                      kColThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, WT>,
+                                                      32 * ColCta<WT>::warps, 0) != cudaSuccess)
         return 1;
     return blocks > 0 ? blocks : 1;
+}
+
+template <int DT, bool VEC>
+int cols_occupancy_t(int wt) {
+    switch (wt) {
+    case 1: return cols_occupancy_w<DT, VEC, 1>();
+    case 2: return cols_occupancy_w<DT, VEC, 2>();
+    case 4: return cols_occupancy_w<DT, VEC, 4>();
+    default: return cols_occupancy_w<DT, VEC, 8>();
+    }
 }
 
 }  // namespace
@@ -178,11 +219,11 @@ cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a) {
     }
 }
 
-int cols_occupancy(int dt, bool vec) {
+int cols_occupancy(int dt, bool vec, int wt) {
     switch (dt) {
-    case kF32: return vec ? cols_occupancy_t<kF32, true>() : cols_occupancy_t<kF32, false>();
-    case kBF16: return vec ? cols_occupancy_t<kBF16, true>() : cols_occupancy_t<kBF16, false>();
-    default: return vec ? cols_occupancy_t<kF16, true>() : cols_occupancy_t<kF16, false>();
+    case kF32: return vec ? cols_occupancy_t<kF32, true>(wt) : cols_occupancy_t<kF32, false>(wt);
+    case kBF16: return vec ? cols_occupancy_t<kBF16, true>(wt) : cols_occupancy_t<kBF16, false>(wt);
+    default: return vec ? cols_occupancy_t<kF16, true>(wt) : cols_occupancy_t<kF16, false>(wt);
     }
 }
 
@@ -196,6 +237,6 @@ cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t
 
 int cols_columns_per_warp(bool vec, int dt) { return 32 * (vec ? 16 / (dt == kF32 ? 4 : 2) : 1); }
 int cols_rows_per_batch(bool vec) { return vec ? 4 : 8; }
-int cols_warps_per_cta() { return kColWarps; }
+int cols_warps_per_cta(int wt) { return wt > 4 ? wt : 4; }
 
 }  // namespace lse

@@ -1,10 +1,12 @@
 /*
  * abi_smoke.c -- liblse called from plain C, with no Python and no torch:
- * device buffers from the CUDA runtime, one lse_forward call.
+ * device buffers from the CUDA runtime, one lse_forward call and one
+ * lse_forward16 call.
  *
  * Usage: abi_smoke <dtype 0=f32|1=bf16|2=f16> <B> <N> <seed> <x_out_path>
- * Writes the raw input elements it generated to x_out_path and prints one
- * float result per row (%.9g), so a test can check them against the oracle.
+ * Writes the raw input elements it generated to x_out_path and prints, per
+ * row, the lse_forward and the lse_forward16 results (%.9g %.9g), so a test
+ * can check them against the oracle.
  */
 #include <stdint.h>
 #include <stdio.h>
@@ -33,7 +35,8 @@ int main(int argc, char **argv)
     const size_t eb = dt == 0 ? 4 : 2, n = (size_t)(B * N);
     unsigned char *h = malloc(n * eb + 1);
     float *out = malloc((size_t)B * sizeof(float) + 1);
-    if (!h || !out)
+    float *out16 = malloc((size_t)B * sizeof(float) + 1);
+    if (!h || !out || !out16)
         return 3;
     for (size_t i = 0; i < n; ++i) {
         const uint32_t r = lcg(&s);
@@ -68,11 +71,19 @@ int main(int argc, char **argv)
     }
     if (cudaMemcpy(out, dout, (size_t)B * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
         return 8;
+    const lse_status st16 = lse_forward16(dx, (lse_dtype)dt, B, N, N, dout, NULL, NULL);
+    if (st16 != LSE_OK) {
+        fprintf(stderr, "lse_forward16: %s\n", lse_status_string(st16));
+        return 9;
+    }
+    if (cudaMemcpy(out16, dout, (size_t)B * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return 10;
     for (int64_t b = 0; b < B; ++b)
-        printf("%.9g\n", out[b]);
+        printf("%.9g %.9g\n", out[b], out16[b]);
     cudaFree(dx);
     cudaFree(dout);
     free(h);
     free(out);
+    free(out16);
     return 0;
 }

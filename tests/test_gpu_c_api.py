@@ -1,5 +1,6 @@
 """liblse from plain C (tests/c/abi_smoke.c, compiled with gcc against
-include/lse.h and the CUDA runtime): results checked against the oracle."""
+include/lse.h and the CUDA runtime): lse_forward and lse_forward16 results
+checked against the oracle."""
 import os
 import subprocess
 
@@ -7,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from lse_testutil import compare
+from lse_testutil import compare, compare_e16, e16_bound
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -39,7 +40,9 @@ def test_c_program(exe, tmp_path, dt, B, N):
     xfile = tmp_path / "x.bin"
     res = subprocess.run([exe, str(dt), str(B), str(N), "7", str(xfile)], capture_output=True,
                          text=True, check=True)
-    got = np.array([float(v) for v in res.stdout.split()])
+    vals = np.array([[float(v) for v in ln.split()] for ln in res.stdout.splitlines()])
     dtype = ["f32", "bf16", "f16"][dt]
     raw = np.fromfile(xfile, dtype=np.float32 if dt == 0 else np.uint16).reshape(B, N)
-    compare(got, oracle.lse(raw, dtype))
+    want = oracle.lse(raw, dtype)
+    compare(vals[:, 0], want)
+    compare_e16(vals[:, 1], want, e16_bound(raw, dtype, want))

@@ -78,12 +78,12 @@ typedef enum {
     LSE_PATH_SPLIT = 4,   /* `splits` CTAs per row write (m, s) partials;
                              a second small kernel merges them in order   */
     LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
-    LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: a CTA's 8 warps share the
+    LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: 2, 4 or 8 warps share the
                                   rows of one column tile                       */
     LSE_PATH_ROWTILE = 7       /* short back-to-back rows (16..128 bytes, 16-byte
                                   aligned): 32 KB chunks of rows streamed into
                                   shared memory by bulk copies (TMA), one thread
-                                  per row; row value only                      */
+                                  per row; row value and token log-probability */
 } lse_path;
 
 /*
@@ -184,7 +184,8 @@ LSE_API lse_status lse_forward_host(const void *x_host, lse_dtype dtype, int64_t
  *     logprob[b] = x[b, target[b]] - log sum_n exp(x[b, n])
  *
  * in the same single pass over x as lse_forward (x[b, target[b]] is taken
- * from registers on short rows and gathered once per row on long ones).
+ * from registers or from the row staged in shared memory on short rows, and
+ * gathered once per row on long ones).
  *   target   device pointer to B int64 column indices, 8-byte aligned; a
  *            target outside [0, N) gives logprob NaN (it is never read).
  *   logprob  device pointer to B floats, 4-byte aligned.

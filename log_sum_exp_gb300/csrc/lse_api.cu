@@ -170,10 +170,10 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         return LSE_ERR_INVALID_ARG;
 
     const int64_t sub_capacity = 32 * kSubwarpMaxSlots;  // slots per row
-    // Bulk-copy ring for short back-to-back rows: row value only, contiguous
-    // 16-byte aligned rows of 16..128 bytes, enough rows for every CTA.
+    // Bulk-copy ring for short back-to-back rows: contiguous 16-byte aligned
+    // rows of 16..128 bytes, enough rows for every CTA.
     const int64_t row_bytes = N * eb;
-    const bool rowtile_ok = vec && !with_logprob && row_stride == N && row_bytes % 16 == 0 &&
+    const bool rowtile_ok = vec && row_stride == N && row_bytes % 16 == 0 &&
                             (row_bytes == 16 || row_bytes == 32 || row_bytes == 64 ||
                              row_bytes == 128);
     if (path == LSE_PATH_AUTO) {
@@ -460,8 +460,7 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
         e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
         break;
     case LSE_PATH_ROWTILE:
-        e = launch_rowtile(dtype, p.slots_per_lane, e16, x, B, out, static_cast<int>(p.grid),
-                           stream);
+        e = launch_rowtile(dtype, p.slots_per_lane, a, static_cast<int>(p.grid));
         break;
     default:
         e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,

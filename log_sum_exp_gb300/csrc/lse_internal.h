@@ -142,8 +142,9 @@ int cols_rows_per_batch(bool vec);  // per warp per iteration
 int cols_warps_per_cta(int warps_per_tile);
 
 // Short contiguous rows through the bulk-copy ring (lse_rowtile.cu).
-cudaError_t launch_rowtile(int dt, int nv, bool e16, const void* x, int64_t B, float* out,
-                           int grid, cudaStream_t stream);
+// Reads a.x, a.B, a.out, a.tl (token log-probability) and a.e16 (reduced-bit
+// exponentials; not together with a.tl).
+cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid);
 int rowtile_ctas_per_sm();
 int rowtile_rows_per_chunk(int nv);
 cudaError_t read_wait_timeouts(unsigned long long* count);

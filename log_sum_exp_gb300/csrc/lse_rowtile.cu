@@ -11,6 +11,10 @@
 // while one stage is consumed the others are in flight.  ("Speeding up
 // Log-Sum-Exp ...", Sec. 3.1: one pass, a register accumulator per row.)
 //
+// With TL the same pass writes the token log-probability x[row, target[row]] -
+// lse[row]: each thread loads its rows' targets before the chunk lands and
+// reads the target element from the staged row in shared memory.
+//
 // Waits are bounded: a stage that does not complete within kWaitPolls polls
 // counts a timeout in a device counter (read by lse_wait_timeouts), the whole
 // CTA stops, waits (also bounded) for its own copies still in flight, and
@@ -74,14 +78,31 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Element i of a row staged in shared memory (plain loads: the read-only
+// global path must not see a shared-memory address).
+template <int DT>
+__device__ __forceinline__ float staged_elem(const unsigned char* row, int i) {
+    if constexpr (DT == kF32) {
+        return reinterpret_cast<const float*>(row)[i];
+    } else {
+        const unsigned short h = reinterpret_cast<const unsigned short*>(row)[i];
+        if constexpr (DT == kBF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+        else return __half2float(__ushort_as_half(h));
+    }
+}
+
 // NV 16-byte vectors per row; RPT = 8 / NV rows per thread per chunk, so a
 // chunk is 256 * RPT rows = 32 KB.  Chunks are dealt round-robin to the CTAs.
-template <int DT, int NV, bool E16>
+// E16: reduced-bit exponentials; TL: token log-probability epilogue (out may
+// then be null).
+template <int DT, int NV, bool E16, bool TL>
 __global__ void __launch_bounds__(kTileThreads)
-lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ out) {
+lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ out,
+                   const int64_t* __restrict__ target, float* __restrict__ logprob) {
     constexpr int RB = NV * 16;                // bytes per row
     constexpr int RPT = 8 / NV;                // rows per thread per chunk
     constexpr int CR = kTileThreads * RPT;     // rows per chunk
+    constexpr int NE = RB / DType<DT>::bytes;  // elements per row
     extern __shared__ __align__(128) unsigned char stage[];
     __shared__ __align__(8) uint64_t full[kStages];
     const int tid = threadIdx.x;
@@ -113,12 +134,23 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     bool timed_out = false;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
         const int s = static_cast<int>(k % kStages);
+        // Targets of this thread's rows (coalesced), loaded while the chunk lands.
+        int tq[TL ? RPT : 1];
+        if constexpr (TL) {
+#pragma unroll
+            for (int q = 0; q < RPT; ++q) {
+                const int64_t row = c * CR + q * kTileThreads + tid;
+                const int64_t t = row < B ? __ldg(target + row) : -1;
+                tq[q] = (t >= 0 && t < NE) ? static_cast<int>(t) : -1;
+            }
+        }
         const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((k / kStages) & 1), kWaitPolls);
         uint32_t w[RPT][4 * NV];
+        float xt[TL ? RPT : 1];
 #pragma unroll
         for (int q = 0; q < RPT; ++q) {
-            const uint4* rp =
-                reinterpret_cast<const uint4*>(stage + s * kChunkBytes + (q * kTileThreads + tid) * RB);
+            const unsigned char* rowp = stage + s * kChunkBytes + (q * kTileThreads + tid) * RB;
+            const uint4* rp = reinterpret_cast<const uint4*>(rowp);
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 // Rotated reads: consecutive threads start at different 16-byte
@@ -126,6 +158,8 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
                 const uint4 u = ok ? rp[(j + tid) % NV] : make_uint4(0, 0, 0, 0);
                 w[q][4 * j] = u.x; w[q][4 * j + 1] = u.y; w[q][4 * j + 2] = u.z; w[q][4 * j + 3] = u.w;
             }
+            if constexpr (TL)
+                xt[q] = ok && tq[q] >= 0 ? staged_elem<DT>(rowp, tq[q]) : __int_as_float(0x7fc00000);
         }
         // Every thread has read stage s: it may be refilled.  A timed-out wait
         // in any thread stops the whole CTA.
@@ -150,7 +184,7 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
                 } else {
                     lse = acc_finalize(Acc{m, expsum_words<DT, 4 * NV, E16>(w[q], mu)});
                 }
-                out[row] = lse;
+                store_row(out, TL ? logprob : nullptr, row, lse, TL ? xt[TL ? q : 0] : 0.0f);
             }
         }
     }
@@ -168,44 +202,43 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     }
 }
 
-template <int DT, int NV, bool E16>
-cudaError_t launch_rowtile_t(const void* x, int64_t B, float* out, int grid, cudaStream_t stream) {
+template <int DT, int NV, bool E16, bool TL>
+cudaError_t launch_rowtile_t(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV, E16>,
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV, E16, TL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_kernel<DT, NV, E16>, dim3(static_cast<unsigned>(grid)),
-                           dim3(kTileThreads), static_cast<size_t>(smem), stream, x, B, out);
+    return launch_pdl_smem(lse_rowtile_kernel<DT, NV, E16, TL>, dim3(static_cast<unsigned>(grid)),
+                           dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B,
+                           a.out, a.tl.target, a.tl.logprob);
 }
 
-template <int DT, bool E16>
-cudaError_t launch_rowtile_dt(int nv, const void* x, int64_t B, float* out, int grid,
-                              cudaStream_t stream) {
+template <int DT, bool E16, bool TL>
+cudaError_t launch_rowtile_dt(int nv, const LaunchArgs& a, int grid) {
     switch (nv) {
-    case 1: return launch_rowtile_t<DT, 1, E16>(x, B, out, grid, stream);
-    case 2: return launch_rowtile_t<DT, 2, E16>(x, B, out, grid, stream);
-    case 4: return launch_rowtile_t<DT, 4, E16>(x, B, out, grid, stream);
-    case 8: return launch_rowtile_t<DT, 8, E16>(x, B, out, grid, stream);
+    case 1: return launch_rowtile_t<DT, 1, E16, TL>(a, grid);
+    case 2: return launch_rowtile_t<DT, 2, E16, TL>(a, grid);
+    case 4: return launch_rowtile_t<DT, 4, E16, TL>(a, grid);
+    case 8: return launch_rowtile_t<DT, 8, E16, TL>(a, grid);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <bool E16>
-cudaError_t launch_rowtile_e(int dt, int nv, const void* x, int64_t B, float* out, int grid,
-                             cudaStream_t stream) {
+template <bool E16, bool TL>
+cudaError_t launch_rowtile_e(int dt, int nv, const LaunchArgs& a, int grid) {
     switch (dt) {
-    case kF32: return launch_rowtile_dt<kF32, E16>(nv, x, B, out, grid, stream);
-    case kBF16: return launch_rowtile_dt<kBF16, E16>(nv, x, B, out, grid, stream);
-    default: return launch_rowtile_dt<kF16, E16>(nv, x, B, out, grid, stream);
+    case kF32: return launch_rowtile_dt<kF32, E16, TL>(nv, a, grid);
+    case kBF16: return launch_rowtile_dt<kBF16, E16, TL>(nv, a, grid);
+    default: return launch_rowtile_dt<kF16, E16, TL>(nv, a, grid);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_rowtile(int dt, int nv, bool e16, const void* x, int64_t B, float* out,
-                           int grid, cudaStream_t stream) {
-    return e16 ? launch_rowtile_e<true>(dt, nv, x, B, out, grid, stream)
-               : launch_rowtile_e<false>(dt, nv, x, B, out, grid, stream);
+cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid) {
+    if (a.tl.logprob) return launch_rowtile_e<false, true>(dt, nv, a, grid);
+    return a.e16 ? launch_rowtile_e<true, false>(dt, nv, a, grid)
+                 : launch_rowtile_e<false, false>(dt, nv, a, grid);
 }
 
 int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM

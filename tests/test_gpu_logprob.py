@@ -92,6 +92,8 @@ def test_logprob_edge_shapes(dtype, N):
         if -(-N // epv) <= 128:
             plans += [{"path": "subwarp", "lanes_per_row": G} for G in (1, 2, 4, 8, 16, 32)
                       if -(-(-(-N // epv)) // G) <= 4]
+        if vec and row_stride == N and N * eb in (16, 32, 64, 128):
+            plans.append({"path": "rowtile"})
         for plan in plans:
             if plan and plan.get("path") == "split" and slots < plan["splits"]:
                 continue
@@ -104,6 +106,26 @@ def test_logprob_edge_shapes(dtype, N):
                 except AssertionError as e:
                     raise AssertionError(f"stride={row_stride} offset={offset} plan={plan} "
                                          f"ran={p.as_dict()}: {e}") from None
+
+
+def test_logprob_rowtile_ragged_chunks_and_dtypes():
+    """The bulk-copy mapping's epilogue: row counts leaving a partial last
+    chunk, every row size and dtype, targets in and out of range."""
+    _need_gpu()
+    for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
+        for rb in (16, 32, 64, 128):
+            N = rb // eb
+            for B in (1, 255, 2049, 100003):
+                x = wl.random_rows(B, N, dtype, seed=3 * B + rb, scale=8.0)
+                t = _targets(B, N, seed=B + rb)
+                want_lp, want_lse = oracle.token_logprob(x, t, dtype)
+                for with_lse in (True, False):
+                    lp, lse, p = run_logprob(torch_view(x, dtype).cuda(), t, {"path": "rowtile"},
+                                             with_lse)
+                    assert p.as_dict()["path"] == "rowtile"
+                    compare_logprob(lp, want_lp, want_lse)
+                    if with_lse:
+                        compare(lse, want_lse)
 
 
 def test_logprob_empty_rows():

@@ -110,14 +110,26 @@ LOG2E = 1.4426950408889634
 
 def e16_bound(x: np.ndarray, dtype: str, want: np.ndarray, block_elems: int = 1 << 24):
     """Per-row bound on |lse_forward16 - oracle|: -log(1 - e) + ATOL + RTOL |want|
-    with e = sum_n p_n r(a_n), p the oracle's softmax of the row (its backward
-    with unit gradient) and |a_n| = (max - x_n) log2 e.  inf for non-finite rows
-    (those must match exactly)."""
+    with e = e16_error_sum(...).  inf for non-finite rows (those must match
+    exactly)."""
+    e = e16_error_sum(x, dtype, want, block_elems)
+    want = np.asarray(want, dtype=np.float64)
+    with np.errstate(invalid="ignore"):
+        bnd = np.where(e < 1.0, -np.log1p(-np.minimum(e, 0.999999)), np.inf)
+    return np.where(np.isfinite(want), bnd + ATOL + RTOL * np.abs(want), np.inf)
+
+
+def e16_error_sum(x: np.ndarray, dtype: str, want: np.ndarray, block_elems: int = 1 << 24,
+                  row_max: np.ndarray | None = None):
+    """e = sum_n p_n r(a_n) per row: p the oracle's softmax of the row (its
+    backward with unit gradient, against the row value ``want``) and
+    |a_n| = (max - x_n) log2 e.  ``row_max`` overrides the maximum (for a
+    slice of a longer row).  nan for non-finite rows."""
     import oracle
 
     B = want.shape[0]
     N = x.shape[1] if x.ndim == 2 else 0
-    out = np.full(B, np.inf)
+    out = np.full(B, np.nan)
     rows = max(1, block_elems // max(N, 1))
     for b0 in range(0, B, rows):
         xb = np.ascontiguousarray(x[b0:b0 + rows])
@@ -128,14 +140,14 @@ def e16_bound(x: np.ndarray, dtype: str, want: np.ndarray, block_elems: int = 1 
         xd = oracle.decode(xb, dtype).reshape(xb.shape[0], N)
         p = oracle.backward(xb, np.where(fin, wb, 0.0), np.ones(len(wb)), dtype)
         p = p.reshape(xb.shape[0], N)
-        m = np.max(np.where(np.isnan(xd), -np.inf, xd), axis=1)
+        m = np.max(np.where(np.isnan(xd), -np.inf, xd), axis=1) if row_max is None \
+            else np.asarray(row_max, dtype=np.float64)[b0:b0 + len(wb)]
         with np.errstate(invalid="ignore", over="ignore"):
             a = (m[:, None] - xd) * LOG2E
             r = np.exp2(E16_BIAS + (a + E16_BIAS) * E16_ARG) - 1.0 + E16_OUT
             r = np.where(a > 125.0, 1.0, r)  # flushed below 2^-126 of the maximum
             e = np.where(p > 0, p * r, 0.0).sum(axis=1)
-            bnd = np.where(e < 1.0, -np.log1p(-np.minimum(e, 0.999999)), np.inf)
-        out[b0:b0 + len(wb)] = np.where(fin, bnd + ATOL + RTOL * np.abs(wb), np.inf)
+        out[b0:b0 + len(wb)] = np.where(fin, e, np.nan)
     return out
 
 
@@ -148,3 +160,30 @@ def compare_e16(got: np.ndarray, want: np.ndarray, bound: np.ndarray) -> dict:
     s["mean_abs_err"] = float(np.abs(d).mean()) if d.size else 0.0
     s["mean_err"] = float(d.mean()) if d.size else 0.0
     return s
+
+
+# Backward: dx = g exp(x - lse) computed in f32 and rounded once to the element
+# type.  Relative bar per element: the f32 steps (2^-21 plus 2^-23 per unit of
+# |lse| and |x - lse|, the argument's rounding) plus the output rounding q, an
+# absolute 1e-37 |g| for flushed results and 2^-24 for f16 subnormals.
+BWD_Q = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+
+
+def compare_backward(got: np.ndarray, xv: np.ndarray, dtype: str, lse64: np.ndarray,
+                     g: np.ndarray, want: np.ndarray) -> float:
+    """got, xv: decoded float64 [B, n] dx and x; want: the oracle's dx.  Special
+    values exactly; returns the largest error / bar."""
+    nan_w, nan_g = np.isnan(want), np.isnan(got)
+    assert np.array_equal(nan_w, nan_g), f"NaN mismatch at {np.argwhere(nan_w != nan_g)[:5]}"
+    inf_w = np.isinf(want)
+    assert np.array_equal(got[inf_w], want[inf_w])
+    fin = ~nan_w & ~inf_w
+    lse_b = np.broadcast_to(np.abs(np.nan_to_num(lse64, posinf=0, neginf=0))[:, None], want.shape)
+    dist = np.abs(np.nan_to_num(xv - lse64[:, None], posinf=0, neginf=0))
+    rel = 2.0 ** -21 + 2.0 ** -23 * (lse_b + dist) + BWD_Q[dtype]
+    lim = np.abs(g)[:, None] * 1e-37 + np.abs(want) * rel + (2.0 ** -24 if dtype == "f16" else 0)
+    err = np.abs(got - want)
+    bad = fin & ~(err <= lim)
+    assert not bad.any(), (f"{bad.sum()} out of tolerance; first "
+                           f"{[(tuple(i), got[tuple(i)], want[tuple(i)]) for i in np.argwhere(bad)[:4]]}")
+    return float((err[fin] / np.maximum(lim[fin], 1e-300)).max()) if fin.any() else 0.0

@@ -14,15 +14,12 @@ import pytest
 
 import oracle
 from log_sum_exp_gb300 import workloads as wl
-from lse_testutil import canary_array, torch_view
+from lse_testutil import canary_array, compare_backward, torch_view
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 import log_sum_exp_gb300 as L  # noqa: E402
-
-Q = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
-
 
 def _need_gpu():
     if not torch.cuda.is_available():
@@ -34,22 +31,7 @@ def _decode(x, dtype):
 
 
 def _check(got_raw, x, dtype, lse64, g, want):
-    got = _decode(got_raw, dtype)
-    xv = _decode(x, dtype)
-    nan_w, nan_g = np.isnan(want), np.isnan(got)
-    assert np.array_equal(nan_w, nan_g), f"NaN mismatch at {np.argwhere(nan_w != nan_g)[:5]}"
-    inf_w = np.isinf(want)
-    assert np.array_equal(got[inf_w], want[inf_w])
-    fin = ~nan_w & ~inf_w
-    lse_b = np.broadcast_to(np.abs(np.nan_to_num(lse64, posinf=0, neginf=0))[:, None], want.shape)
-    dist = np.abs(np.nan_to_num(xv - lse64[:, None], posinf=0, neginf=0))
-    rel = 2.0 ** -21 + 2.0 ** -23 * (lse_b + dist) + Q[dtype]
-    lim = np.abs(g)[:, None] * 1e-37 + np.abs(want) * rel + (2.0 ** -24 if dtype == "f16" else 0)
-    err = np.abs(got - want)
-    bad = fin & ~(err <= lim)
-    assert not bad.any(), (f"{bad.sum()} out of tolerance; first "
-                           f"{[(tuple(i), got[tuple(i)], want[tuple(i)]) for i in np.argwhere(bad)[:4]]}")
-    return float((err[fin] / np.maximum(lim[fin], 1e-300)).max()) if fin.any() else 0.0
+    return compare_backward(_decode(got_raw, dtype), _decode(x, dtype), dtype, lse64, g, want)
 
 
 def _run(x, dtype, g, row_stride=None, offset=0, dx_row_stride=None, dx_offset=0, inplace=False):

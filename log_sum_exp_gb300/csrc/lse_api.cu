@@ -436,9 +436,7 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
         return st;
     if (plan) *plan = p;
 
-    LaunchArgs a{x, B, N, row_stride, out, stream};
-    a.tl = tl;
-    a.e16 = e16;
+    const LaunchArgs a{x, B, N, row_stride, out, stream, tl, e16};
     cudaError_t e = cudaSuccess;
     char* scratch = nullptr;
     if (p.scratch_bytes > 0) {

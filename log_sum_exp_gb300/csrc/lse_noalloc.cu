@@ -21,7 +21,6 @@
 // Calls on one stream are ordered and safe.  Nothing in the array needs to
 // start at zero: each call writes every partial slot it later reads.
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -132,7 +131,7 @@ extern "C" lse_status lse_forward_split_static(const void* x, lse_dtype dtype, i
     P = ceil_div(slots, seg_slots);
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const LaunchArgs a{x, B, N, row_stride, out, stream};
+    const LaunchArgs a{x, B, N, row_stride, out, stream, TokenLogprob{}, false};
     cudaError_t e;
     switch (dtype) {
     case LSE_F32: e = launch_segment_f32(a, vec, kThreads, P, seg_slots, s->ptr, nullptr); break;

@@ -391,18 +391,27 @@ def lse_backward(x, lse, grad, dx=None, stream=None):
 def logsumexp(x, dim=-1, keepdim=False, stream=None):
     """torch.logsumexp(x, dim, keepdim) on liblse for CUDA tensors, computed in f32.
 
-    The reduced dimension may be any dimension; the tensor's other dimensions
-    must collapse to (outer, inner) with the inner one contiguous (any
-    contiguous tensor qualifies).  Returns float32 with ``dim`` removed.
+    The reduced dimension may be any dimension; the tensor must be contiguous
+    (its other dimensions collapse to (outer, inner)).  Returns float32 with
+    ``dim`` removed.  When x requires a gradient the result is differentiable
+    over the last dimension: the gradient g * exp(x - lse) comes from
+    lse_backward (there is no strided backward kernel, so a gradient over
+    another dimension raises).
     """
     torch = _torch()
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor")
-    dt = _dtype_name(x)
-    nd = x.dim()
-    if nd == 0:
+    if x.dim() == 0:
         raise ValueError("x must have at least one dimension")
-    d = dim % nd
+    d = dim % x.dim()
+    if torch.is_grad_enabled() and x.requires_grad:
+        return _logsumexp_function().apply(x, d, keepdim, stream)
+    return _logsumexp_value(x, d, keepdim, stream)
+
+
+def _logsumexp_value(x, d, keepdim, stream):
+    torch = _torch()
+    dt = _dtype_name(x)
     shape = list(x.shape)
     R = shape[d]
     outer = 1
@@ -423,6 +432,40 @@ def logsumexp(x, dim=-1, keepdim=False, stream=None):
             lse_forward_strided_ptr(x.data_ptr(), dt, outer, R, inner, R * inner, inner,
                                     out.data_ptr(), _stream_handle(stream, x.device))
     return out.unsqueeze(d) if keepdim else out
+
+
+_LSE_FUNCTION = None
+
+
+def _logsumexp_function():
+    """The torch.autograd.Function behind a differentiable logsumexp (built on
+    first use, since torch is imported lazily)."""
+    global _LSE_FUNCTION
+    if _LSE_FUNCTION is None:
+        torch = _torch()
+
+        class LogSumExp(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, x, d, keepdim, stream):
+                out = _logsumexp_value(x, d, keepdim, stream)
+                ctx.save_for_backward(x, out)
+                ctx.d, ctx.stream = d, stream
+                return out
+
+            @staticmethod
+            def backward(ctx, grad_out):
+                x, out = ctx.saved_tensors
+                if ctx.d != x.dim() - 1:
+                    raise NotImplementedError(
+                        "liblse has no backward kernel for a reduction over a non-last dimension")
+                N = x.shape[-1]
+                B = x.numel() // N if N else 0
+                g = grad_out.reshape(B).to(torch.float32).contiguous()
+                dx = lse_backward(x.reshape(B, N), out.reshape(B), g, stream=ctx.stream)
+                return dx.reshape(x.shape), None, None, None
+
+        _LSE_FUNCTION = LogSumExp
+    return _LSE_FUNCTION
 
 
 def lse_plan_query(x=None, dtype: str | None = None, B: int | None = None, N: int | None = None,

@@ -34,6 +34,7 @@ DEFAULT_WORKLOAD = "vocab_512x128256_f32"
 DEFAULT_COLUMNS = "pcsum_512x64x1024_f32"
 L2_BYTES = 129 * 10**6
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0  # public HBM3e bandwidth of the part, for a labelled second percentage
 EVENT_EVERY = 16
 OP_NAMES = {"forward": "row value", "forward16": "row value, reduced-bit exponentials",
             "logprob": "fused token log-probability",
@@ -208,7 +209,7 @@ def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float, op: str = "forwa
         if elapsed >= budget_s:
             break
     gbs = rows_done * bytes_per_row / elapsed / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_info(),
             "sample": f"{reps} pass(es) of the oracle's {OP_NAMES[op]} over {rows} rows x "
                       f"{w.N} {w.dtype} of the workload ({elapsed:.1f} s single-threaded)",
             "seconds": elapsed, "rows": rows_done}
@@ -229,10 +230,35 @@ def time_oracle_columns(x3: np.ndarray, cw, budget_s: float) -> dict:
         if elapsed >= budget_s:
             break
     return {"value": reps * bytes_per / elapsed / 1e9, "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", "host": host_info(),
             "sample": f"{reps} pass(es) of the oracle's strided value over {A} of {cw.A} slices "
                       f"[{cw.R} x {cw.C}] ({elapsed:.1f} s single-threaded)",
             "seconds": elapsed}
+
+
+def host_info() -> dict:
+    """CPU model and logical core count of the machine the oracle runs on."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"cpu": model or platform.processor() or platform.machine(),
+            "arch": platform.machine(), "nproc": os.cpu_count()}
 
 
 def oracle_sample_rows(w: wl.Workload, target_s: float) -> int:
@@ -274,7 +300,7 @@ def run_reference(args) -> None:
         "config": {"workload": args.workload, "B": w.B, "N": w.N, "input_dtype": w.dtype,
                    "rows_per_step": rows, "recipe": w.recipe},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_info()},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -514,6 +540,10 @@ def run_native(args) -> None:
                    "parallelism": f"replicas x{world}, rows independent, no collective"},
         "us_per_call": 1e3 * ms_per_step,
         "pct_of_peak": 100.0 * value / peak,
+        # x alone (the per-row outputs, targets or dx left out), and against
+        # the public HBM3e figure rather than the measured copy peak.
+        "read_gbs": world * in_bytes / (ms_per_step * 1e-3) / 1e9,
+        "pct_of_spec_8tbs": 100.0 * value / SPEC_HBM_GBS,
         "us_per_call_graph": graph_us,
         "roofline": roofline,
         "cpu_baseline": cpu,

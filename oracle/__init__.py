@@ -68,6 +68,10 @@ class OracleLib:
                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64, ctypes.c_void_p]
         lib.oracle_lse_strided.restype = ctypes.c_int
+        lib.oracle_lse_backward_strided.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_lse_backward_strided.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -89,6 +93,11 @@ class OracleLib:
     def lse_strided(self, x: np.ndarray, dtype: str, A: int, R: int, C: int, stride_a: int,
                     stride_r: int) -> np.ndarray:
         return _lse_strided(self._lib, x, dtype, A, R, C, stride_a, stride_r)
+
+    def backward_strided(self, x: np.ndarray, dtype: str, A: int, R: int, C: int,
+                         stride_a: int, stride_r: int, lse: np.ndarray,
+                         grad: np.ndarray) -> np.ndarray:
+        return _backward_strided(self._lib, x, dtype, A, R, C, stride_a, stride_r, lse, grad)
 
 
 def _load() -> OracleLib:
@@ -130,6 +139,34 @@ def lse_strided(x: np.ndarray, dtype: str, A: int, R: int, C: int, stride_a: int
 
     ``x`` is a flat buffer of raw elements (float32, or 16-bit patterns)."""
     return _load().lse_strided(x, dtype, A, R, C, stride_a, stride_r)
+
+
+def backward_strided(x: np.ndarray, dtype: str, A: int, R: int, C: int, stride_a: int,
+                     stride_r: int, lse: np.ndarray, grad: np.ndarray) -> np.ndarray:
+    """dx[a, r, c] = grad[a, c] * exp(x[a*stride_a + r*stride_r + c] - lse[a, c]) in
+    float64, [A, R, C]: the gradient of lse_strided's value.  ``lse`` and ``grad``
+    are [A, C]."""
+    return _load().backward_strided(x, dtype, A, R, C, stride_a, stride_r, lse, grad)
+
+
+def _backward_strided(lib, x, dtype, A, R, C, stride_a, stride_r, lse, grad):
+    arr = _raw(x, dtype).reshape(-1)
+    if A > 0 and R > 0 and C > 0:
+        need = (A - 1) * stride_a + (R - 1) * stride_r + C
+        if arr.size < need:
+            raise ValueError(f"buffer of {arr.size} elements, need {need}")
+    lse = np.ascontiguousarray(lse, dtype=np.float64).reshape(-1)
+    grad = np.ascontiguousarray(grad, dtype=np.float64).reshape(-1)
+    if lse.size != A * C or grad.size != A * C:
+        raise ValueError("lse and grad hold one value per (a, c)")
+    dx = np.empty((A, R, C), np.float64)
+    if dx.size:
+        rc = lib.oracle_lse_backward_strided(arr.ctypes.data, DTYPE_CODES[dtype], A, R, C,
+                                             stride_a, stride_r, lse.ctypes.data,
+                                             grad.ctypes.data, dx.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_lse_backward_strided rejected its arguments")
+    return dx
 
 
 def _lse_strided(lib, x, dtype, A, R, C, stride_a, stride_r):

@@ -38,8 +38,9 @@
  *   gradient of the row value (backward support, Table 3):
  *       dx[b, n] = grad[b] * exp(x[b, n] - lse[b])
  * and the same value over a non-last dimension (probabilistic-circuit sum
- * layers, Sec. 5.2):
+ * layers, Sec. 5.2) with its gradient:
  *       out[a, c] = log sum_r exp(x[a * stride_a + r * stride_r + c])
+ *       dx[a, r, c] = grad[a, c] * exp(x[a * stride_a + r * stride_r + c] - lse[a, c])
  */
 #include <math.h>
 #include <stdint.h>
@@ -252,5 +253,36 @@ int oracle_lse_strided(const void *x, int dtype, int64_t A, int64_t R, int64_t C
     for (a = 0; a < A; ++a)
         for (c = 0; c < C; ++c)
             out[a * C + c] = lse_strided(dtype, base + (a * stride_a + c) * es, R, stride_r);
+    return 0;
+}
+
+/*
+ * oracle_lse_backward_strided: gradient of oracle_lse_strided's value,
+ *     dx[(a * R + r) * C + c] = grad[a * C + c]
+ *                               * exp(x[a*stride_a + r*stride_r + c] - lse[a * C + c])
+ * for a dense [A, R, C] double output; lse and grad are [A, C] (lse normally
+ * from oracle_lse_strided).  Returns 0, or -1 on an invalid argument.
+ */
+int oracle_lse_backward_strided(const void *x, int dtype, int64_t A, int64_t R, int64_t C,
+                                int64_t stride_a, int64_t stride_r, const double *lse,
+                                const double *grad, double *dx)
+{
+    const unsigned char *base = (const unsigned char *)x;
+    int64_t a, r, c, es;
+
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16)
+        return -1;
+    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0)
+        return -1;
+    if (A > 0 && R > 0 && C > 0 && (x == NULL || lse == NULL || grad == NULL || dx == NULL))
+        return -1;
+    es = elem_size(dtype);
+    for (a = 0; a < A; ++a)
+        for (r = 0; r < R; ++r) {
+            const unsigned char *row = base + (a * stride_a + r * stride_r) * es;
+            for (c = 0; c < C; ++c)
+                dx[(a * R + r) * C + c] =
+                    grad[a * C + c] * exp(decode(dtype, row, c) - lse[a * C + c]);
+        }
     return 0;
 }

@@ -423,6 +423,74 @@ def check_strided_matches_rows(orc) -> None:
     assert np.all(orc.lse_strided(r, "f32", 2, 0, 3, 0, 0) == -np.inf)
 
 
+def check_strided_backward_sums_to_grad(orc) -> None:
+    """Over the reduced dimension exp(x - lse) sums to 1: sum_r dx[a, r, c] = g[a, c];
+    -inf entries get 0."""
+    rng = np.random.default_rng(59)
+    A, R, C = 3, 41, 17
+    x = (rng.normal(0, 5, (A, R, C)) + rng.uniform(-30, 30, (A, 1, C))).astype(np.float32)
+    x[1, ::5, 4] = -np.inf
+    lse = orc.lse_strided(x.reshape(-1), "f32", A, R, C, R * C, C)
+    g = rng.normal(0, 2, (A, C))
+    dx = orc.backward_strided(x.reshape(-1), "f32", A, R, C, R * C, C, lse, g)
+    assert np.allclose(dx.sum(axis=1), g, rtol=1e-13, atol=1e-13)
+    assert np.all(dx[1, ::5, 4] == 0.0)
+
+
+def check_strided_backward_finite_difference(orc) -> None:
+    """d out[a, c] / d x[a, r, c] by central differences of the strided forward
+    oracle (x on a 2^-10 grid, step 2^-10, exact in f32), on a padded layout;
+    other columns do not move."""
+    rng = np.random.default_rng(61)
+    A, R, C = 2, 5, 3
+    sa, sr = R * (C + 2) + 3, C + 2
+    x = (np.round(rng.uniform(-4, 4, (A, R, C)) * 1024) / 1024).astype(np.float32)
+    buf = np.full((A - 1) * sa + (R - 1) * sr + C + 4, np.nan, np.float32)
+    for a in range(A):
+        for r in range(R):
+            buf[a * sa + r * sr:a * sa + r * sr + C] = x[a, r]
+    lse = orc.lse_strided(buf, "f32", A, R, C, sa, sr)
+    dx = orc.backward_strided(buf, "f32", A, R, C, sa, sr, lse, np.ones((A, C)))
+    h = 2.0 ** -10
+    for a in range(A):
+        for r in range(R):
+            for c in range(C):
+                bp, bm = buf.copy(), buf.copy()
+                bp[a * sa + r * sr + c] += np.float32(h)
+                bm[a * sa + r * sr + c] -= np.float32(h)
+                lp = orc.lse_strided(bp, "f32", A, R, C, sa, sr)
+                lm = orc.lse_strided(bm, "f32", A, R, C, sa, sr)
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd[a, c] - dx[a, r, c]) <= 2e-7, (a, r, c)
+                others = np.ones((A, C), bool)
+                others[a, c] = False
+                assert np.all(fd[others] == 0.0)
+
+
+def check_strided_backward_matches_rows(orc) -> None:
+    """A column's gradient is the row gradient of the transpose, special values
+    included; bf16 and f16 decode as in the row oracle."""
+    rng = np.random.default_rng(67)
+    m = rng.normal(0, 4, (30, 7)).astype(np.float32)
+    m[:, 2] = -np.inf
+    m[4, 3] = np.nan
+    m[6, 5] = np.inf
+    g = rng.normal(0, 1, 7)
+    lse = orc.lse_strided(m.reshape(-1), "f32", 1, 30, 7, 0, 7)
+    cols = orc.backward_strided(m.reshape(-1), "f32", 1, 30, 7, 0, 7, lse, g[None, :])[0]
+    rows = orc.backward(np.ascontiguousarray(m.T), lse[0], g)
+    assert np.array_equal(np.isnan(cols), np.isnan(rows.T))
+    ok = ~np.isnan(cols)
+    assert np.array_equal(cols[ok], rows.T[ok])
+    for dt in ("f16", "bf16"):
+        h = m.astype(np.float16) if dt == "f16" else (m.view(np.uint32) >> 16).astype(np.uint16)
+        lh = orc.lse_strided(h.reshape(-1), dt, 1, 30, 7, 0, 7)
+        ch = orc.backward_strided(h.reshape(-1), dt, 1, 30, 7, 0, 7, lh, g[None, :])[0]
+        rh = orc.backward(np.ascontiguousarray(h.T), lh[0], g, dt)
+        ok = ~np.isnan(ch)
+        assert np.array_equal(np.isnan(ch), np.isnan(rh.T)) and np.array_equal(ch[ok], rh.T[ok])
+
+
 ALL_CHECKS = [
     check_golden, check_decode_all_patterns, check_single_element_rows,
     check_constant_rows, check_special_values, check_two_element_closed_form,
@@ -433,4 +501,6 @@ ALL_CHECKS = [
     check_backward_sums_to_grad, check_backward_finite_difference,
     check_backward_against_scipy, check_backward_special,
     check_strided_against_scipy, check_strided_matches_rows,
+    check_strided_backward_sums_to_grad, check_strided_backward_finite_difference,
+    check_strided_backward_matches_rows,
 ]

@@ -45,6 +45,10 @@ MUTANTS = [
     ("strided_swaps_a_and_c", "base + (a * stride_a + c) * es", "base + (c * stride_a + a) * es"),
     ("strided_drops_last", "for (n = 0; n < count; ++n)\n        s += exp",
      "for (n = 0; n + 1 < count; ++n)\n        s += exp"),
+    ("strided_backward_row_lse", "- lse[a * C + c]);", "- lse[a * C]);"),
+    ("strided_backward_ignores_step", "base + (a * stride_a + r * stride_r) * es",
+     "base + (a * stride_a + r * C) * es"),
+    ("strided_backward_no_grad", "grad[a * C + c] * exp(", "exp("),
 ]
 
 

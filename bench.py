@@ -38,7 +38,9 @@ SPEC_HBM_GBS = 8000.0  # public HBM3e bandwidth of the part, for a labelled seco
 EVENT_EVERY = 16
 OP_NAMES = {"forward": "row value", "forward16": "row value, reduced-bit exponentials",
             "logprob": "fused token log-probability",
-            "backward": "backward dx = g exp(x - lse)", "columns": "value over a non-last dim"}
+            "backward": "backward dx = g exp(x - lse)", "columns": "value over a non-last dim",
+            "columns_backward": "backward of the value over a non-last dim"}
+COLUMN_OPS = ("columns", "columns_backward")
 KERNEL_SOURCES = ["lse_api.cu", "lse_kernels.cuh", "lse_device.cuh", "lse_internal.h",
                   "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kernels_f16.cu",
                   "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu",
@@ -215,23 +217,32 @@ def time_oracle(x: np.ndarray, w: wl.Workload, budget_s: float, op: str = "forwa
             "seconds": elapsed, "rows": rows_done}
 
 
-def time_oracle_columns(x3: np.ndarray, cw, budget_s: float) -> dict:
-    """The oracle's strided value over the first slices of a column workload."""
+def time_oracle_columns(x3: np.ndarray, cw, budget_s: float, op: str = "columns") -> dict:
+    """The oracle's strided value (or its gradient) over the first slices of a
+    column workload."""
     import oracle
 
     A = max(1, min(cw.A, int(budget_s / 4 / max(cw.R * cw.C * 8e-9, 1e-9))))
     sample = np.ascontiguousarray(x3[:A]).reshape(-1)
-    bytes_per = A * (cw.R * cw.C * cw.elem_bytes + cw.C * 4)
+    args = (cw.dtype, A, cw.R, cw.C, cw.R * cw.C, cw.C)
+    if op == "columns_backward":
+        lse = oracle.lse_strided(sample, *args)
+        g = np.ones((A, cw.C))
+        fn = lambda: oracle.backward_strided(sample, *args, lse, g)  # noqa: E731
+        bytes_per = A * (2 * cw.R * cw.C * cw.elem_bytes + cw.C * 8)
+    else:
+        fn = lambda: oracle.lse_strided(sample, *args)  # noqa: E731
+        bytes_per = A * (cw.R * cw.C * cw.elem_bytes + cw.C * 4)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.lse_strided(sample, cw.dtype, A, cw.R, cw.C, cw.R * cw.C, cw.C)
+        fn()
         reps += 1
         elapsed = time.perf_counter() - t0
         if elapsed >= budget_s:
             break
     return {"value": reps * bytes_per / elapsed / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle", "host": host_info(),
-            "sample": f"{reps} pass(es) of the oracle's strided value over {A} of {cw.A} slices "
+            "sample": f"{reps} pass(es) of the oracle's {OP_NAMES[op]} over {A} of {cw.A} slices "
                       f"[{cw.R} x {cw.C}] ({elapsed:.1f} s single-threaded)",
             "seconds": elapsed}
 
@@ -333,7 +344,7 @@ def run_native(args) -> None:
     lse_build.build()
     import log_sum_exp_gb300 as L
 
-    if args.op == "columns":
+    if args.op in COLUMN_OPS:
         cw = wl.COLUMN_WORKLOADS[args.workload]
         x_host = wl.generate_columns(args.workload, seed=cw.seed + 7919 * rank)
         # Seen as B = A*C outputs of R-long strided reductions.
@@ -396,6 +407,19 @@ def run_native(args) -> None:
         def step(i, evb=0, eve=0):
             xp, op = ptrs[i % copies]
             L.lse_forward_strided_ptr(xp, dt, A, R, C, R * C, C, op, sh, req)
+    elif op_name == "columns_backward":
+        A, R, C = cw.A, cw.R, cw.C
+        for t, o in ptrs:  # the saved forward values, one set per copy
+            L.lse_forward_strided_ptr(t, dt, A, R, C, R * C, C, o, sh)
+        gs = [torch.ones(A * C, dtype=torch.float32, device=dev) for _ in range(copies)]
+        dxs = [torch.empty_like(x) for x in xs]
+        plan = {"path": "columns_backward", "launches": 1}
+        bytes_per_step = 2 * in_bytes + 8 * A * C
+
+        def step(i, evb=0, eve=0):
+            c = i % copies
+            L.lse_backward_strided_ptr(ptrs[c][0], dt, A, R, C, R * C, C, ptrs[c][1],
+                                       gs[c].data_ptr(), dxs[c].data_ptr(), R * C, C, sh)
     else:  # backward
         lses = [L.lse_forward(x) for x in xs]
         gs = [torch.ones(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
@@ -508,7 +532,8 @@ def run_native(args) -> None:
                    "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
                    "backward": "lse_backward_kernel", "columns_warp": "lse_cols_kernel",
-                   "columns_cta": "lse_cols_kernel"}[plan["path"]]
+                   "columns_cta": "lse_cols_kernel",
+                   "columns_backward": "lse_backward_strided_kernel"}[plan["path"]]
     traffic = ncu_traffic(args.workload, plan, op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
@@ -519,8 +544,8 @@ def run_native(args) -> None:
                 "kernel_timing": timing}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        if op_name == "columns":
-            cpu = time_oracle_columns(x_host, cw, args.cpu_seconds)
+        if op_name in COLUMN_OPS:
+            cpu = time_oracle_columns(x_host, cw, args.cpu_seconds, op_name)
         else:
             rows = oracle_sample_rows(w, args.cpu_seconds / 4)
             cpu = time_oracle(x_host[:rows], w, args.cpu_seconds, op_name)
@@ -563,7 +588,8 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", choices=list(wl.WORKLOADS) + list(wl.COLUMN_WORKLOADS),
                     default=None, help=f"default {DEFAULT_WORKLOAD} ({DEFAULT_COLUMNS} for "
                                        f"--op columns)")
-    ap.add_argument("--op", choices=["forward", "forward16", "logprob", "backward", "columns"],
+    ap.add_argument("--op", choices=["forward", "forward16", "logprob", "backward", "columns",
+                                     "columns_backward"],
                     default="forward",
                     help="row value (default), fused token log-probability, backward, or the "
                          "value over a non-last dimension (column workloads)")
@@ -581,9 +607,10 @@ def main(argv=None) -> None:
               file=sys.stderr)
         args.warmup = 3
     if args.workload is None:
-        args.workload = DEFAULT_COLUMNS if args.op == "columns" else DEFAULT_WORKLOAD
-    if (args.op == "columns") != (args.workload in wl.COLUMN_WORKLOADS):
-        ap.error("--op columns runs the column workloads, the other ops the row workloads")
+        args.workload = DEFAULT_COLUMNS if args.op in COLUMN_OPS else DEFAULT_WORKLOAD
+    if (args.op in COLUMN_OPS) != (args.workload in wl.COLUMN_WORKLOADS):
+        ap.error("--op columns / columns_backward run the column workloads, the other ops "
+                 "the row workloads")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -251,6 +251,33 @@ LSE_API lse_status lse_forward_strided(const void *x, lse_dtype dtype, int64_t A
                                        lse_stream_t stream, lse_plan *plan);
 
 /*
+ * lse_backward_strided -- gradient of lse_forward_strided's value:
+ *
+ *     dx[a, r, c] = grad[a, c] * exp(x[a * stride_a + r * stride_r + c] - lse[a, c])
+ *
+ * (d out[a, c] / d x[a, r, c] is the softmax over r; the backward of the
+ * value over a non-last dimension, as lse_backward is for rows).  One pass:
+ * x read once, dx written once; lse and grad are read once per column tile.
+ *   x        as for lse_forward_strided (element strides stride_a, stride_r;
+ *            c contiguous).
+ *   lse      device pointer to A * C floats ([A, C]): the saved forward values.
+ *   grad     device pointer to A * C floats ([A, C]): upstream gradients.
+ *   dx       device pointer, x's element type, element (a, r, c) at
+ *            a * dx_stride_a + r * dx_stride_r + c; computed in f32 and
+ *            rounded to nearest-even on store.  dx may be x itself (same
+ *            strides); other overlaps are undefined.
+ * A, R or C == 0 is a no-op.  Special values follow IEEE arithmetic on the
+ * formula.  16-byte aligned layouts (x, dx, every stride) with C a multiple of
+ * the elements per 16 bytes take vector loads; others element loads.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+LSE_API lse_status lse_backward_strided(const void *x, lse_dtype dtype, int64_t A, int64_t R,
+                                        int64_t C, int64_t stride_a, int64_t stride_r,
+                                        const float *lse, const float *grad, void *dx,
+                                        int64_t dx_stride_a, int64_t dx_stride_r,
+                                        lse_stream_t stream);
+
+/*
  * lse_trim_memory -- return the current device's cached stream-ordered memory
  * to the system.  Split-row scratch and lse_forward_host's staging buffers come
  * from a library-owned memory pool that keeps freed blocks mapped for reuse by

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     logsumexp,
     lse_backward,
     lse_backward_ptr,
+    lse_backward_strided_ptr,
     lse_forward,
     lse_forward16,
     lse_forward16_ptr,

@@ -22,10 +22,10 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward16",
-                 "lse_forward_host",
-                 "lse_token_logprob", "lse_token_logprob_plan", "lse_backward",
-                 "lse_forward_strided", "lse_trim_memory", "lse_wait_timeouts",
-                 "lse_status_string", "lse_last_cuda_error", "lse_forward_split_static"]
+                 "lse_forward_host", "lse_token_logprob", "lse_token_logprob_plan",
+                 "lse_backward", "lse_forward_strided", "lse_backward_strided",
+                 "lse_trim_memory", "lse_wait_timeouts", "lse_status_string",
+                 "lse_last_cuda_error", "lse_forward_split_static"]
 
 
 class LsePlan(ctypes.Structure):
@@ -100,6 +100,9 @@ def load() -> ctypes.CDLL:
         lib.lse_forward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, vp,
                                             ctypes.POINTER(LsePlan)]
         lib.lse_forward_strided.restype = i32
+        lib.lse_backward_strided.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, vp, vp, i64,
+                                             i64, vp]
+        lib.lse_backward_strided.restype = i32
         lib.lse_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
         lib.lse_wait_timeouts.restype = i32
         lib.lse_trim_memory.argtypes = []
@@ -200,6 +203,15 @@ def lse_forward_strided_ptr(x_ptr: int, dtype: str, A: int, R: int, C: int, stri
                                       out_ptr or None, stream or None, ctypes.byref(p)),
            "lse_forward_strided")
     return p
+
+
+def lse_backward_strided_ptr(x_ptr: int, dtype: str, A: int, R: int, C: int, stride_a: int,
+                             stride_r: int, lse_ptr: int, grad_ptr: int, dx_ptr: int,
+                             dx_stride_a: int, dx_stride_r: int, stream: int = 0) -> None:
+    _check(load().lse_backward_strided(x_ptr or None, DTYPES[dtype], A, R, C, stride_a, stride_r,
+                                       lse_ptr or None, grad_ptr or None, dx_ptr or None,
+                                       dx_stride_a, dx_stride_r, stream or None),
+           "lse_backward_strided")
 
 
 def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_stride: int,
@@ -393,10 +405,9 @@ def logsumexp(x, dim=-1, keepdim=False, stream=None):
 
     The reduced dimension may be any dimension; the tensor must be contiguous
     (its other dimensions collapse to (outer, inner)).  Returns float32 with
-    ``dim`` removed.  When x requires a gradient the result is differentiable
-    over the last dimension: the gradient g * exp(x - lse) comes from
-    lse_backward (there is no strided backward kernel, so a gradient over
-    another dimension raises).
+    ``dim`` removed.  When x requires a gradient the result is differentiable:
+    the gradient g * exp(x - lse) comes from lse_backward (last dimension) or
+    lse_backward_strided (any other).
     """
     torch = _torch()
     if not x.is_cuda:
@@ -455,14 +466,24 @@ def _logsumexp_function():
             @staticmethod
             def backward(ctx, grad_out):
                 x, out = ctx.saved_tensors
-                if ctx.d != x.dim() - 1:
-                    raise NotImplementedError(
-                        "liblse has no backward kernel for a reduction over a non-last dimension")
-                N = x.shape[-1]
-                B = x.numel() // N if N else 0
-                g = grad_out.reshape(B).to(torch.float32).contiguous()
-                dx = lse_backward(x.reshape(B, N), out.reshape(B), g, stream=ctx.stream)
-                return dx.reshape(x.shape), None, None, None
+                d = ctx.d
+                R = x.shape[d]
+                inner = 1
+                for n in x.shape[d + 1:]:
+                    inner *= n
+                outer = x.numel() // (R * inner) if R * inner else 0
+                g = grad_out.reshape(outer * inner).to(torch.float32).contiguous()
+                lse = out.reshape(outer * inner)
+                if inner == 1:
+                    dx = lse_backward(x.reshape(outer, R), lse, g, stream=ctx.stream)
+                    return dx.reshape(x.shape), None, None, None
+                dx = torch.empty_like(x)
+                with torch.cuda.device(x.device):
+                    lse_backward_strided_ptr(x.data_ptr(), _dtype_name(x), outer, R, inner,
+                                             R * inner, inner, lse.data_ptr(), g.data_ptr(),
+                                             dx.data_ptr(), R * inner, inner,
+                                             _stream_handle(ctx.stream, x.device))
+                return dx, None, None, None
 
         _LSE_FUNCTION = LogSumExp
     return _LSE_FUNCTION

@@ -572,6 +572,87 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
+namespace {
+
+// Elements spanned by an [A, R, C] layout with the given strides (0 when
+// empty), or -1 when its byte extent overflows.
+int64_t strided_extent(int64_t A, int64_t R, int64_t C, int64_t sa, int64_t sr, int eb) {
+    if (A == 0 || R == 0 || C == 0) return 0;
+    int64_t extent = 0, t = 0;
+    if (__builtin_mul_overflow(A - 1, sa, &extent) || __builtin_mul_overflow(R - 1, sr, &t) ||
+        __builtin_add_overflow(extent, t, &extent) || __builtin_add_overflow(extent, C, &extent) ||
+        __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &t))
+        return -1;
+    return extent;
+}
+
+}  // namespace
+
+lse_status lse_backward_strided(const void* x, lse_dtype dtype, int64_t A, int64_t R, int64_t C,
+                                int64_t stride_a, int64_t stride_r, const float* lse_in,
+                                const float* grad, void* dx, int64_t dx_stride_a,
+                                int64_t dx_stride_r, lse_stream_t stream) {
+    if (!valid_dtype(dtype)) return LSE_ERR_UNSUPPORTED_DTYPE;
+    if (A < 0 || R < 0 || C < 0 || stride_a < 0 || stride_r < 0 || dx_stride_a < 0 ||
+        dx_stride_r < 0)
+        return LSE_ERR_INVALID_ARG;
+    const int eb = elem_bytes(dtype);
+    int64_t outputs = 0;
+    if (__builtin_mul_overflow(A, C, &outputs) || outputs > INT64_MAX / 8) return LSE_ERR_INVALID_ARG;
+    if (strided_extent(A, R, C, stride_a, stride_r, eb) < 0 ||
+        strided_extent(A, R, C, dx_stride_a, dx_stride_r, eb) < 0)
+        return LSE_ERR_INVALID_ARG;
+    if (A == 0 || R == 0 || C == 0) return LSE_OK;
+    if (x == nullptr || lse_in == nullptr || grad == nullptr || dx == nullptr)
+        return LSE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lse_in) & 3u) || (reinterpret_cast<uintptr_t>(grad) & 3u) ||
+        (reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(eb)) ||
+        (reinterpret_cast<uintptr_t>(dx) % static_cast<uintptr_t>(eb)))
+        return LSE_ERR_INVALID_ARG;
+    int dev = 0;
+    const DeviceInfo* info = nullptr;
+    lse_status st = device_info(&dev, &info);
+    if (st != LSE_OK) return st;
+
+    const int64_t epv16 = 16 / eb;
+    const auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16u == 0; };
+    const bool vec = al16(x) && al16(dx) && C % epv16 == 0 && (stride_a * eb) % 16 == 0 &&
+                     (stride_r * eb) % 16 == 0 && (dx_stride_a * eb) % 16 == 0 &&
+                     (dx_stride_r * eb) % 16 == 0;
+    const int64_t gx = ceil_div(C, 32 * (vec ? epv16 : 1));  // 32-lane column tiles
+    const int64_t gy = A < 65535 ? A : 65535;
+    // Row splits until the grid covers the GPU 4x (CTAs of backward_strided_warps()
+    // warps), keeping >= 2 batches of rows per warp.
+    const int64_t W = backward_strided_warps();
+    const int64_t target = static_cast<int64_t>(info->sms) * 4 * (64 / W);
+    int64_t P = ceil_div(target, gx * gy);
+    const int64_t max_p = ceil_div(R, 2 * W * backward_slots_per_thread());
+    if (P > max_p) P = max_p;
+    if (P > 65535) P = 65535;
+    if (P < 1) P = 1;
+    const int64_t rows_per_split = ceil_div(R, P);
+    P = ceil_div(R, rows_per_split);
+    if (gx > INT_MAX) return LSE_ERR_INVALID_ARG;
+
+    BackwardStridedArgs a;
+    a.x = x;
+    a.A = A;
+    a.R = R;
+    a.C = C;
+    a.stride_a = stride_a;
+    a.stride_r = stride_r;
+    a.lse = lse_in;
+    a.grad = grad;
+    a.dx = dx;
+    a.dx_stride_a = dx_stride_a;
+    a.dx_stride_r = dx_stride_r;
+    a.rows_per_split = rows_per_split;
+    a.grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(P));
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = launch_backward_strided(dtype, vec, a);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
 lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_t R, int64_t C,
                                int64_t stride_a, int64_t stride_r, float* out,
                                lse_stream_t stream_, lse_plan* plan) {

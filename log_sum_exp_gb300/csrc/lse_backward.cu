@@ -11,6 +11,9 @@
 // ex2.approx.ftz on (x - lse) * log2 e, computed in f32 and rounded once to
 // the element type (nearest-even) on store.
 //
+// lse_backward_strided_kernel is the same gradient for the value over a
+// non-last dimension (lse_forward_strided), with lse and grad per column.
+//
 // Mapping: a CTA is TX x TY threads; TY rows, TX threads across a row, each
 // thread moving U = 4 slots (16-byte vectors, or single elements when rows are
 // not 16-byte aligned) per iteration with every load issued before any store.
@@ -132,6 +135,102 @@ lse_backward_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t ro
     }
 }
 
+// One 16-byte vector whose elements belong to different columns, each with
+// its own lse and gradient.
+template <int DT, int EPV>
+__device__ __forceinline__ uint4 grad_vector_cols(uint4 u, const float (&l)[EPV],
+                                                  const float (&g)[EPV]) {
+    if constexpr (DT == kF32) {
+        return make_uint4(__float_as_uint(grad_term(__uint_as_float(u.x), l[0], g[0])),
+                          __float_as_uint(grad_term(__uint_as_float(u.y), l[1], g[1])),
+                          __float_as_uint(grad_term(__uint_as_float(u.z), l[2], g[2])),
+                          __float_as_uint(grad_term(__uint_as_float(u.w), l[3], g[3])));
+    } else {
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack2<DT>(grad_term(word_lo<DT>(in[i]), l[2 * i], g[2 * i]),
+                             grad_term(word_hi<DT>(in[i]), l[2 * i + 1], g[2 * i + 1]));
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Gradient of the value over a non-last dimension:
+//     dx[a, r, c] = grad[a, c] * exp(x[a, r, c] - lse[a, c]),
+// lse and grad dense [A, C].  A lane owns EPV columns of one a (a 16-byte
+// vector, or one element when the layout is not 16-byte aligned) and loads
+// their lse and gradient once; the CTA's kStrWarps warps interleave the rows
+// of blockIdx.z's split, each with kBwdU rows in flight (all loads before any
+// store, so dx may be x itself).  blockIdx.x is the 32-lane column tile,
+// blockIdx.y the index a (grid-stride beyond gridDim.y).
+constexpr int kStrWarps = 4;
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(32 * kStrWarps)
+lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C,
+                            int64_t stride_a, int64_t stride_r, const float* __restrict__ lse,
+                            const float* __restrict__ grad, void* __restrict__ dx,
+                            int64_t dx_stride_a, int64_t dx_stride_r, int64_t rows_per_split) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = VEC ? 16 / EB : 1;
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * EPV;
+    const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.z) * rows_per_split;
+    const int64_t r_end = r_begin + rows_per_split < R ? r_begin + rows_per_split : R;
+    for (int64_t a = blockIdx.y; a < A; a += gridDim.y) {
+        float l[EPV], g[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            l[e] = active ? __ldg(lse + a * C + c0 + e) : 0.0f;
+            g[e] = active ? __ldg(grad + a * C + c0 + e) : 0.0f;
+        }
+        const char* xa = reinterpret_cast<const char*>(x) + (a * stride_a + c0) * EB;
+        char* da = reinterpret_cast<char*>(dx) + (a * dx_stride_a + c0) * EB;
+        for (int64_t r = r_begin + wid; r < r_end; r += static_cast<int64_t>(kStrWarps) * kBwdU) {
+            if constexpr (VEC) {
+                uint4 v[kBwdU];
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    const int64_t rr = r + j * kStrWarps;
+                    if (active && rr < r_end) v[j] = ldg_stream16(xa + rr * stride_r * EB);
+                }
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    const int64_t rr = r + j * kStrWarps;
+                    if (active && rr < r_end)
+                        __stcs(reinterpret_cast<uint4*>(da + rr * dx_stride_r * EB),
+                               grad_vector_cols<DT, EPV>(v[j], l, g));
+                }
+            } else {
+                float v[kBwdU];
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    const int64_t rr = r + j * kStrWarps;
+                    if (active && rr < r_end) v[j] = load_elem<DT>(xa, rr * stride_r);
+                }
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    const int64_t rr = r + j * kStrWarps;
+                    if (active && rr < r_end)
+                        store_elem<DT>(da, rr * dx_stride_r, grad_term(v[j], l[0], g[0]));
+                }
+            }
+        }
+    }
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_backward_strided_t(const BackwardStridedArgs& a) {
+    return launch_pdl(lse_backward_strided_kernel<DT, VEC>, a.grid, dim3(32 * kStrWarps), a.stream,
+                      a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad, a.dx,
+                      a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
+}
+
 template <int DT, bool VEC>
 cudaError_t launch_backward_t(const BackwardArgs& a) {
     return launch_pdl(lse_backward_kernel<DT, VEC>, a.grid, a.block, a.stream, a.x, a.B, a.N,
@@ -148,6 +247,19 @@ cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a) {
     }
 }
 
+cudaError_t launch_backward_strided(int dt, bool vec, const BackwardStridedArgs& a) {
+    switch (dt) {
+    case kF32:
+        return vec ? launch_backward_strided_t<kF32, true>(a) : launch_backward_strided_t<kF32, false>(a);
+    case kBF16:
+        return vec ? launch_backward_strided_t<kBF16, true>(a)
+                   : launch_backward_strided_t<kBF16, false>(a);
+    default:
+        return vec ? launch_backward_strided_t<kF16, true>(a) : launch_backward_strided_t<kF16, false>(a);
+    }
+}
+
+int backward_strided_warps() { return kStrWarps; }
 int backward_slots_per_thread() { return kBwdU; }
 int backward_threads() { return kBwdThreads; }
 

@@ -100,6 +100,25 @@ struct BackwardArgs {
     cudaStream_t stream;
 };
 cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a);
+// Backward of the value over a non-last dimension (lse_backward.cu).
+struct BackwardStridedArgs {
+    const void* x;
+    int64_t A;
+    int64_t R;
+    int64_t C;
+    int64_t stride_a;
+    int64_t stride_r;
+    const float* lse;   // [A, C]
+    const float* grad;  // [A, C]
+    void* dx;
+    int64_t dx_stride_a;
+    int64_t dx_stride_r;
+    int64_t rows_per_split;
+    dim3 grid;  // (column tiles, a, row splits)
+    cudaStream_t stream;
+};
+cudaError_t launch_backward_strided(int dt, bool vec, const BackwardStridedArgs& a);
+int backward_strided_warps();
 int backward_slots_per_thread();
 int backward_threads();
 

@@ -89,3 +89,27 @@ def test_last_cuda_error_null(lib):
     assert lib.lse_last_cuda_error(None) == 1
     v = ctypes.c_int(-1)
     assert lib.lse_last_cuda_error(ctypes.byref(v)) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    # x, dtype, A, R, C, sa, sr, lse, grad, dx, dsa, dsr
+    ((16, 0, -1, 2, 4, 8, 4, 16, 16, 16, 8, 4), 1),     # A < 0
+    ((16, 0, 2, 2, 4, -8, 4, 16, 16, 16, 8, 4), 1),     # negative stride
+    ((16, 0, 2, 2, 4, 8, 4, 16, 16, 16, 8, -4), 1),     # negative dx stride
+    ((0, 0, 2, 2, 4, 8, 4, 16, 16, 16, 8, 4), 1),       # x NULL with work to do
+    ((16, 0, 2, 2, 4, 8, 4, 0, 16, 16, 8, 4), 1),       # lse NULL
+    ((16, 0, 2, 2, 4, 8, 4, 16, 16, 0, 8, 4), 1),       # dx NULL
+    ((16, 0, 2, 2, 4, 8, 4, 18, 16, 16, 8, 4), 1),      # lse not 4-byte aligned
+    ((16, 1, 2, 2, 4, 8, 4, 16, 16, 17, 8, 4), 1),      # dx not element aligned
+    ((16, 5, 2, 2, 4, 8, 4, 16, 16, 16, 8, 4), 2),      # unknown dtype
+    ((16, 0, 2, 1 << 40, 4, 8, 1 << 30, 16, 16, 16, 8, 4), 1),  # x extent overflows
+])
+def test_backward_strided_bad_arguments_rejected_before_cuda(lib, args, status):
+    x, dt, A, R, C, sa, sr, lse, grad, dx, dsa, dsr = args
+    assert lib.lse_backward_strided(x or None, dt, A, R, C, sa, sr, lse or None, grad or None,
+                                    dx or None, dsa, dsr, None) == status
+
+
+def test_backward_strided_empty_is_ok_without_device(lib):
+    assert lib.lse_backward_strided(None, 0, 0, 3, 4, 12, 4, None, None, None, 12, 4, None) == 0
+    assert lib.lse_backward_strided(None, 0, 2, 0, 4, 0, 4, None, None, None, 0, 4, None) == 0

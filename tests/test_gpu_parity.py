@@ -342,8 +342,8 @@ def test_allocation_failure_is_reported():
 
 
 def test_graph_capture_all_ops():
-    """lse_token_logprob, lse_backward and lse_forward_strided replay correctly
-    from a CUDA graph (split plans included)."""
+    """lse_token_logprob, lse_backward, lse_forward_strided, lse_backward_strided
+    and lse_forward16 replay correctly from a CUDA graph (split plans included)."""
     _need_gpu()
     x = wl.generate("particles_16x16777216_f32", B=3, N=1 << 20)
     t = np.array([0, 5, (1 << 20) - 1], np.int64)
@@ -356,6 +356,11 @@ def test_graph_capture_all_ops():
     lp = torch.empty(3, device="cuda")
     dx = torch.empty_like(xd)
     col = torch.empty(8 * 1024, device="cuda")
+    col_lse = torch.from_numpy(oracle.lse_strided(x3.reshape(-1), "f32", 8, 64, 1024, 64 * 1024,
+                                                  1024).astype(np.float32)).cuda()
+    col_g = torch.ones(8 * 1024, device="cuda")
+    dx3 = torch.empty_like(x3d)
+    v16 = torch.empty(3, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
 
@@ -367,6 +372,11 @@ def test_graph_capture_all_ops():
                            g_d.data_ptr(), dx.data_ptr(), 1 << 20, h)
         L.lse_forward_strided_ptr(x3d.data_ptr(), "f32", 8, 64, 1024, 64 * 1024, 1024,
                                   col.data_ptr(), h, {"path": "columns_warp", "splits": 2})
+        L.lse_backward_strided_ptr(x3d.data_ptr(), "f32", 8, 64, 1024, 64 * 1024, 1024,
+                                   col_lse.data_ptr(), col_g.data_ptr(), dx3.data_ptr(),
+                                   64 * 1024, 1024, h)
+        L.lse_forward16_ptr(xd.data_ptr(), "f32", 3, 1 << 20, 1 << 20, v16.data_ptr(), h,
+                            L._binding._as_plan({"path": "split", "splits": 8}))
 
     with torch.cuda.stream(s):
         ops(s)  # warm-up outside capture
@@ -378,6 +388,8 @@ def test_graph_capture_all_ops():
     lp.fill_(0)
     dx.fill_(0)
     col.fill_(0)
+    dx3.fill_(0)
+    v16.fill_(0)
     g.replay()
     torch.cuda.synchronize()
     want_lp, want_lse = oracle.token_logprob(x, t)
@@ -385,6 +397,9 @@ def test_graph_capture_all_ops():
     compare(col.cpu().numpy().reshape(8, 1024),
             oracle.lse_strided(x3.reshape(-1), "f32", 8, 64, 1024, 64 * 1024, 1024))
     assert np.allclose(dx.sum(dim=1).cpu().numpy(), 1.0, rtol=1e-4)
+    assert np.allclose(dx3.sum(dim=1).cpu().numpy(), 1.0, rtol=1e-4)
+    want = oracle.lse(x)
+    assert np.all(np.abs(v16.cpu().numpy() - want) < 3e-3)
 
 
 def test_short_rows_both_mappings_full_size():

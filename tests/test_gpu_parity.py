@@ -275,6 +275,37 @@ def test_host_entry_point_pinned_and_pageable():
     compare(L.lse_forward_host(torch.from_numpy(x)).numpy(), want)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_host_entry_point_dtypes(dtype):
+    """lse_forward_host for every element type, page-locked and pageable input."""
+    _need_gpu()
+    x = wl.random_rows(64, 1000, dtype, seed=17, scale=7.0)
+    want = oracle.lse(x, dtype)
+    for pin in (True, False):
+        xt = torch_view(x.copy(), dtype)
+        if pin:
+            xt = xt.pin_memory()
+        out = torch.full((64,), 7.0, dtype=torch.float32).pin_memory()
+        L.lse_forward_host_ptr(xt.data_ptr(), dtype, 64, 1000, 1000, out.data_ptr())
+        compare(out.numpy(), want)
+
+
+def test_host_entry_point_short_rows_bulk_copy():
+    """Short back-to-back rows from page-locked host memory take the bulk-copy
+    mapping, whose copies then read host memory in place: full short-row
+    workload against the oracle, and no bounded wait gave up."""
+    _need_gpu()
+    x = wl.generate("short_1048576x32_f32")
+    B, N = x.shape
+    assert L.lse_plan_query(dtype="f32", B=B, N=N, row_stride=N)["path"] == "rowtile"
+    before = L.lse_wait_timeouts()
+    xt = torch.from_numpy(x).pin_memory()
+    out = torch.empty(B, dtype=torch.float32).pin_memory()
+    L.lse_forward_host_ptr(xt.data_ptr(), "f32", B, N, N, out.data_ptr())
+    compare(out.numpy(), oracle.lse(x))
+    assert L.lse_wait_timeouts() == before
+
+
 def test_cuda_graph_capture_and_replay():
     _need_gpu()
     for key, B in (("small_64x4096_f32", None), ("particles_16x16777216_f32", 2)):

@@ -70,6 +70,8 @@ def library_path() -> str:
 def load() -> ctypes.CDLL:
     """Load liblse.so; raise if it has not been built."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -233,17 +235,48 @@ def lse_forward_split_static_ptr(x_ptr: int, dtype: str, B: int, N: int, row_str
 # ---------------------------------------------------------------------------
 # torch-tensor conveniences: torch supplies device memory and the stream only.
 # ---------------------------------------------------------------------------
+_TORCH = None
+_DTYPE_NAMES = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _dtype_name(t) -> str:
-    torch = _torch()
-    names = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
-    if t.dtype not in names:
+    global _DTYPE_NAMES
+    if _DTYPE_NAMES is None:
+        torch = _torch()
+        _DTYPE_NAMES = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    name = _DTYPE_NAMES.get(t.dtype)
+    if name is None:
         raise TypeError(f"unsupported dtype {t.dtype}; expected float32, bfloat16 or float16")
-    return names[t.dtype]
+    return name
+
+
+class _on_device:
+    """Make ``device`` current for the block, switching only when it is not
+    current already (torch.cuda.device always switches)."""
+
+    __slots__ = ("index", "prev")
+
+    def __init__(self, device):
+        self.index = device.index
+
+    def __enter__(self):
+        cuda = _torch().cuda
+        cur = cuda.current_device()
+        self.prev = cur if self.index is not None and cur != self.index else None
+        if self.prev is not None:
+            cuda.set_device(self.index)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            _torch().cuda.set_device(self.prev)
 
 
 def _rows(x):
@@ -263,10 +296,22 @@ def _rows(x):
     return B, N, row_stride
 
 
+_RAW_STREAM = None
+
+
 def _stream_handle(stream, device):
+    """cudaStream_t of ``stream``, or of the device's current stream.  The raw
+    getter avoids building a torch Stream object on every call."""
+    global _RAW_STREAM
+    if stream is not None:
+        return stream.cuda_stream
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream(device)
-    return s.cuda_stream
+    if _RAW_STREAM is None:
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    if _RAW_STREAM:
+        return _RAW_STREAM(index)
+    return torch.cuda.current_stream(index).cuda_stream
 
 
 def lse_forward(x, out=None, stream=None):
@@ -274,7 +319,31 @@ def lse_forward(x, out=None, stream=None):
 
     Returns a float32 tensor of shape [B] (a 0-d tensor for 1-D input).
     """
-    out, _ = lse_forward_plan(x, out=out, stream=stream)
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (use lse_forward_host for host memory)")
+    dt = _dtype_name(x)
+    B, N, row_stride = _rows(x)
+    out = _out_rows(out, B, x)
+    device = x.device
+    args = (x.data_ptr() or None, DTYPES[dt], B, N, row_stride, out.data_ptr() or None,
+            _stream_handle(stream, device) or None)
+    if torch.cuda.current_device() == device.index:
+        _check(load().lse_forward(*args), "lse_forward")
+    else:
+        with _on_device(device):
+            _check(load().lse_forward(*args), "lse_forward")
+    return out.reshape(()) if x.dim() == 1 else out
+
+
+def _out_rows(out, B, x):
+    """A float32 [B] output on x's device: new, or the caller's after checks."""
+    torch = _torch()
+    if out is None:
+        return torch.empty(B, dtype=torch.float32, device=x.device)
+    if out.dtype != torch.float32 or out.numel() != B or not out.is_contiguous() \
+            or out.device != x.device:
+        raise ValueError("out must be a contiguous float32 tensor of B elements on x's device")
     return out
 
 
@@ -297,7 +366,7 @@ def lse_forward_plan(x, plan: LsePlan | dict | None = None, out=None, stream=Non
             or out.device != x.device:
         raise ValueError("out must be a contiguous float32 tensor of B elements on x's device")
     p = _as_plan(plan)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         evb = _event_handle(ev_begin)
         eve = _event_handle(ev_end)
         p = lse_forward_plan_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
@@ -321,7 +390,7 @@ def lse_forward16(x, plan: LsePlan | dict | None = None, out=None, stream=None):
             or out.device != x.device:
         raise ValueError("out must be a contiguous float32 tensor of B elements on x's device")
     p = _as_plan(plan)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         p = lse_forward16_ptr(x.data_ptr(), dt, B, N, row_stride, out.data_ptr(),
                               _stream_handle(stream, x.device), p)
     if x.dim() == 1:
@@ -369,7 +438,7 @@ def lse_token_logprob(x, target, lse_out=None, plan=None, stream=None, return_pl
     if lse_out is not None and (lse_out.dtype != torch.float32 or lse_out.numel() != B
                                 or not lse_out.is_contiguous() or lse_out.device != x.device):
         raise ValueError("lse_out must be a contiguous float32 tensor of B elements on x's device")
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         p = lse_token_logprob_ptr(x.data_ptr(), dt, B, N, row_stride, target.data_ptr(),
                                   logprob.data_ptr(), lse_out.data_ptr() if lse_out is not None else 0,
                                   _stream_handle(stream, x.device), _as_plan(plan))
@@ -394,7 +463,7 @@ def lse_backward(x, lse, grad, dx=None, stream=None):
     if dx.shape != (B, N) or dx.dtype != x.dtype or (N > 1 and dx.stride(1) != 1):
         raise ValueError("dx must match x's shape and dtype with unit last stride")
     dx_stride = dx.stride(0) if B > 1 else N
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         lse_backward_ptr(x.data_ptr(), dt, B, N, row_stride, lse.data_ptr(), grad.data_ptr(),
                          dx.data_ptr(), dx_stride, _stream_handle(stream, x.device))
     return dx
@@ -434,14 +503,15 @@ def _logsumexp_value(x, d, keepdim, stream):
     out_shape = shape[:d] + shape[d + 1:]
     if not x.is_contiguous():
         raise ValueError("logsumexp needs a contiguous tensor")
-    out = torch.empty(out_shape, dtype=torch.float32, device=x.device)
-    with torch.cuda.device(x.device):
+    device = x.device
+    out = torch.empty(out_shape, dtype=torch.float32, device=device)
+    h = _stream_handle(stream, device)
+    with _on_device(device):
         if inner == 1:
-            lse_forward_ptr(x.data_ptr(), dt, outer, R, R, out.data_ptr(),
-                            _stream_handle(stream, x.device))
+            lse_forward_ptr(x.data_ptr(), dt, outer, R, R, out.data_ptr(), h)
         else:
             lse_forward_strided_ptr(x.data_ptr(), dt, outer, R, inner, R * inner, inner,
-                                    out.data_ptr(), _stream_handle(stream, x.device))
+                                    out.data_ptr(), h)
     return out.unsqueeze(d) if keepdim else out
 
 
@@ -478,7 +548,7 @@ def _logsumexp_function():
                     dx = lse_backward(x.reshape(outer, R), lse, g, stream=ctx.stream)
                     return dx.reshape(x.shape), None, None, None
                 dx = torch.empty_like(x)
-                with torch.cuda.device(x.device):
+                with _on_device(x.device):
                     lse_backward_strided_ptr(x.data_ptr(), _dtype_name(x), outer, R, inner,
                                              R * inner, inner, lse.data_ptr(), g.data_ptr(),
                                              dx.data_ptr(), R * inner, inner,

@@ -171,14 +171,21 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
 
     const int64_t sub_capacity = 32 * kSubwarpMaxSlots;  // slots per row
     // Bulk-copy ring for short back-to-back rows: contiguous 16-byte aligned
-    // rows of 16..128 bytes, enough rows for every CTA.
+    // rows of 16..128 bytes, enough rows for every CTA.  Chosen automatically
+    // where it measured faster than the sub-warp mapping (256 MB of rows):
+    // rows of 3, 5, 6 or 7 vectors (the sub-warp mapping pads those to 4 or 8
+    // slots) and f32 rows of 4 or 8; the sub-warp mapping keeps rows of 1 or 2
+    // vectors and 16-bit rows of 4 or 8, where one thread per row would fold
+    // 32 or 64 elements alone.
     const int64_t row_bytes = N * eb;
-    const bool rowtile_ok = vec && row_stride == N && row_bytes % 16 == 0 &&
-                            (row_bytes == 16 || row_bytes == 32 || row_bytes == 64 ||
-                             row_bytes == 128);
+    const bool rowtile_ok = vec && row_stride == N && row_bytes % 16 == 0 && row_bytes >= 16 &&
+                            row_bytes <= 128;
+    const int64_t row_vecs = row_bytes / 16;
+    const bool rowtile_auto =
+        row_vecs > 2 && !(eb == 2 && (row_vecs == 4 || row_vecs == 8));
     if (path == LSE_PATH_AUTO) {
         const int64_t chunk_rows = rowtile_ok ? rowtile_rows_per_chunk(static_cast<int>(row_bytes / 16)) : 1;
-        if (rowtile_ok && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
+        if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
         else
             path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;

@@ -1,7 +1,7 @@
 // lse_rowtile.cu -- short contiguous rows fed by 1-D bulk copies (sm_103a).
 //
-// For rows of 16, 32, 64 or 128 bytes stored back to back (row_stride == N,
-// 16-byte aligned), a persistent CTA streams 32 KB chunks of whole rows from
+// For rows of 16..128 bytes (a multiple of 16) stored back to back
+// (row_stride == N, 16-byte aligned), a persistent CTA streams 32 KB chunks of whole rows from
 // HBM into a ring of shared-memory stages with cp.async.bulk (the Tensor
 // Memory Accelerator's 1-D copy; one instruction per chunk, completion tracked
 // by an mbarrier transaction count), and each of its 256 threads reduces whole
@@ -91,8 +91,9 @@ __device__ __forceinline__ float staged_elem(const unsigned char* row, int i) {
     }
 }
 
-// NV 16-byte vectors per row; RPT = 8 / NV rows per thread per chunk, so a
-// chunk is 256 * RPT rows = 32 KB.  Chunks are dealt round-robin to the CTAs.
+// NV (1..8) 16-byte vectors per row; RPT = floor(8 / NV) rows per thread per
+// chunk, so a chunk is 256 * RPT rows of at most 32 KB (exactly 32 KB when NV
+// divides 8).  Chunks are dealt round-robin to the CTAs.
 // E16: reduced-bit exponentials; TL: token log-probability epilogue (out may
 // then be null).
 template <int DT, int NV, bool E16, bool TL>
@@ -103,6 +104,7 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     constexpr int RPT = 8 / NV;                // rows per thread per chunk
     constexpr int CR = kTileThreads * RPT;     // rows per chunk
     constexpr int NE = RB / DType<DT>::bytes;  // elements per row
+    static_assert(NV >= 1 && NV <= 8 && CR * RB <= kChunkBytes, "a chunk must fit one stage");
     extern __shared__ __align__(128) unsigned char stage[];
     __shared__ __align__(8) uint64_t full[kStages];
     const int tid = threadIdx.x;
@@ -218,7 +220,11 @@ cudaError_t launch_rowtile_dt(int nv, const LaunchArgs& a, int grid) {
     switch (nv) {
     case 1: return launch_rowtile_t<DT, 1, E16, TL>(a, grid);
     case 2: return launch_rowtile_t<DT, 2, E16, TL>(a, grid);
+    case 3: return launch_rowtile_t<DT, 3, E16, TL>(a, grid);
     case 4: return launch_rowtile_t<DT, 4, E16, TL>(a, grid);
+    case 5: return launch_rowtile_t<DT, 5, E16, TL>(a, grid);
+    case 6: return launch_rowtile_t<DT, 6, E16, TL>(a, grid);
+    case 7: return launch_rowtile_t<DT, 7, E16, TL>(a, grid);
     case 8: return launch_rowtile_t<DT, 8, E16, TL>(a, grid);
     default: return cudaErrorInvalidValue;
     }

@@ -151,7 +151,7 @@ def _plans(rng, N, dtype, vec, rs):
         out.append({"path": "cta", "threads": int(32 * 2 ** rng.integers(0, 5))})
     if slots >= 2:
         out.append({"path": "split", "splits": int(rng.integers(2, min(slots, 40) + 1))})
-    if vec and rs == N and N * eb in (16, 32, 64, 128):
+    if vec and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
         out.append({"path": "rowtile"})
     return out
 

@@ -92,7 +92,7 @@ def test_logprob_edge_shapes(dtype, N):
         if -(-N // epv) <= 128:
             plans += [{"path": "subwarp", "lanes_per_row": G} for G in (1, 2, 4, 8, 16, 32)
                       if -(-(-(-N // epv)) // G) <= 4]
-        if vec and row_stride == N and N * eb in (16, 32, 64, 128):
+        if vec and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             plans.append({"path": "rowtile"})
         for plan in plans:
             if plan and plan.get("path") == "split" and slots < plan["splits"]:
@@ -113,7 +113,7 @@ def test_logprob_rowtile_ragged_chunks_and_dtypes():
     chunk, every row size and dtype, targets in and out of range."""
     _need_gpu()
     for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
-        for rb in (16, 32, 64, 128):
+        for rb in range(16, 129, 16):
             N = rb // eb
             for B in (1, 255, 2049, 100003):
                 x = wl.random_rows(B, N, dtype, seed=3 * B + rb, scale=8.0)

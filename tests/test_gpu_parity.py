@@ -105,7 +105,7 @@ def test_edge_shapes(dtype, N):
         buf, xv = device_rows(x, dtype, row_stride=row_stride, offset=offset)
         vec = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
         plans = plans_for(N, dtype, vec)
-        if vec and row_stride == N and N * eb in (16, 32, 64, 128):
+        if vec and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             plans.append({"path": "rowtile"})
         for plan in plans:
             got, p = run(xv, plan)
@@ -433,6 +433,23 @@ def test_graph_capture_all_ops():
     assert np.all(np.abs(v16.cpu().numpy() - want) < 3e-3)
 
 
+def test_short_row_mapping_rule():
+    """Automatic choice between the bulk-copy ring and the sub-warp mapping for
+    back-to-back rows of 16..128 bytes (the measured rule): the ring for rows
+    of 3, 5, 6 or 7 vectors and f32 rows of 4 or 8, sub-warp otherwise."""
+    _need_gpu()
+    for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
+        for nv in range(1, 9):
+            N = nv * 16 // eb
+            q = L.lse_plan_query(dtype=dtype, B=1 << 20, N=N, row_stride=N)
+            ring = nv > 2 and not (eb == 2 and nv in (4, 8))
+            assert q["path"] == ("rowtile" if ring else "subwarp"), (dtype, nv, q)
+            # not back to back, or too few rows: never the ring
+            assert L.lse_plan_query(dtype=dtype, B=1 << 20, N=N, row_stride=N + 16 // eb)["path"] \
+                == "subwarp"
+            assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
+
+
 def test_short_rows_both_mappings_full_size():
     """The 1048576 x 32 workload through the bulk-copy ring (default) and the
     register sub-warp kernel (forced)."""
@@ -451,7 +468,7 @@ def test_rowtile_ragged_chunks_and_dtypes():
     """Row counts that leave a partial last chunk, for every row size and dtype."""
     _need_gpu()
     for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
-        for rb in (16, 32, 64, 128):
+        for rb in range(16, 129, 16):
             N = rb // eb
             for B in (1, 255, 2049, 100003):
                 x = wl.random_rows(B, N, dtype, seed=B + rb, scale=8.0)

@@ -54,7 +54,7 @@ def _random_plan(rng, N, dtype, vec, rs):
         if slots >= 2:
             choices.append({"path": "split", "splits": int(rng.integers(2, min(slots, 50) + 1)),
                             "threads": int(32 * 2 ** rng.integers(0, 5))})
-        if vec and rs == N and N * eb in (16, 32, 64, 128):
+        if vec and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             choices.append({"path": "rowtile"})
     return choices[int(rng.integers(len(choices)))]
 

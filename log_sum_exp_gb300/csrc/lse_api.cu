@@ -31,7 +31,8 @@ lse_status cuda_fail(cudaError_t e, lse_status st = LSE_ERR_CUDA) {
 }
 
 constexpr int kMaxDevices = 64;
-constexpr int kSubwarpMaxSlots = 4;    // slots per lane in the subwarp kernel
+constexpr int kSubwarpMaxSlots = 4;    // slots per lane in the subwarp kernel (G < 32)
+constexpr int kSubwarpWarpSlots = 8;   // slots per lane when a whole warp holds a row
 constexpr int kSegmentBatchVec = 8;    // slots per thread per batch (16-byte loads)
 constexpr int kSegmentBatchScalar = 16;
 constexpr int kMergeRowsPerCta = 8;    // one warp per row
@@ -169,7 +170,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         path == LSE_PATH_COLUMNS_WARP || path == LSE_PATH_COLUMNS_CTA)
         return LSE_ERR_INVALID_ARG;
 
-    const int64_t sub_capacity = 32 * kSubwarpMaxSlots;  // slots per row
+    const int64_t sub_capacity = 32 * kSubwarpWarpSlots;  // slots per row
     // Bulk-copy ring for short back-to-back rows: contiguous 16-byte aligned
     // rows of 16..128 bytes, enough rows for every CTA.  Chosen automatically
     // where it measured faster than the sub-warp mapping (256 MB of rows):
@@ -210,12 +211,16 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
         // Fewest lanes per row that keep <= kSubwarpMaxSlots slots per lane:
         // four independent 16-byte loads per thread (V * R = 4 in the kernel).
-        int G = req && req->lanes_per_row ? req->lanes_per_row
-                                          : pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
+        // Rows of more than 32 * 4 slots take a whole warp with up to 8 each.
+        int G = req && req->lanes_per_row ? req->lanes_per_row : 0;
+        if (G == 0) {
+            G = pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
+            if (G > 32) G = 32;
+        }
         if (G < 1 || G > 32 || (G & (G - 1)) != 0) return LSE_ERR_INVALID_ARG;
         int64_t V = ceil_div(nvt, G);
-        if (V > kSubwarpMaxSlots) return LSE_ERR_INVALID_ARG;
-        V = V <= 1 ? 1 : (V <= 2 ? 2 : 4);
+        if (V > (G == 32 ? kSubwarpWarpSlots : kSubwarpMaxSlots)) return LSE_ERR_INVALID_ARG;
+        V = V <= 1 ? 1 : (V <= 2 ? 2 : (V <= 4 ? 4 : 8));
         const int64_t R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
         const int64_t rows_per_warp_iter = (32 / G) * R;
         const int64_t warps = ceil_div(B, rows_per_warp_iter);

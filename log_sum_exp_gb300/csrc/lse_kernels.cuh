@@ -54,10 +54,14 @@ __device__ __forceinline__ void load_tail_words(const void* row, int64_t start, 
 // ---------------------------------------------------------------------------
 // subwarp: G lanes per row, V slots per lane, R row-groups per warp iteration.
 // VEC: a slot is one 16-byte vector (the lane holding vector index N/EPV also
-// loads the < EPV tail elements); !VEC: a slot is one element.
+// loads the < EPV tail elements); !VEC: a slot is one element.  V = 8 (only
+// with G = 32: a whole warp per row of up to 256 slots) keeps 32 words per
+// lane and runs at 4 CTAs per SM.
 // ---------------------------------------------------------------------------
+template <int V> struct SubwarpOccupancy { static constexpr int min_blocks = V >= 8 ? 4 : kSubwarpMinBlocks; };
+
 template <int DT, int G, int V, bool VEC, bool TL, bool E16>
-__global__ void __launch_bounds__(kSubwarpThreads, kSubwarpMinBlocks)
+__global__ void __launch_bounds__(kSubwarpThreads, SubwarpOccupancy<V>::min_blocks)
 lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                    float* __restrict__ out, const int64_t* __restrict__ target,
                    float* __restrict__ logprob) {
@@ -78,7 +82,7 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 
     for (int64_t row0 = warp * (RPW * R); row0 < B; row0 += nwarps * (RPW * R)) {
         // Targets, loaded with the rows (token log-probability only); rows on
-        // this path hold at most 32 * 4 * 8 elements, so an in-range target
+        // this path hold at most 32 * 8 * 8 elements, so an in-range target
         // fits in 32 bits and -1 marks an invalid one.
         int t[R];
 #pragma unroll
@@ -125,11 +129,11 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                 for (int off = G / 2; off > 0; off >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                 const float mu = shift_of(m);
-                // FFMA form for the 4-slot variants (every row longer than two
-                // vectors); same decision for the whole group.  Not with E16:
+                // FFMA form for the 4- and 8-slot variants (every row longer than
+                // two vectors); same decision for the whole group.  Not with E16:
                 // there the maximum's own argument must be exactly 0 (its bf16
                 // term exactly 1), not the rounding residual of mu log2 e.
-                const bool scaled = !E16 && V == 4 && ffma_shift_ok(mu);
+                const bool scaled = !E16 && V >= 4 && ffma_shift_ok(mu);
                 const float c = mu * kLog2e;
                 float s = scaled ? words_expsum_scaled<DT, 4 * V>(w[r], c)
                                  : expsum_words<DT, 4 * V, E16>(w[r], mu);
@@ -345,6 +349,9 @@ cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL, E16>(a, grid);
     case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL, E16>(a, grid);
     case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL, E16>(a, grid);
+    case 8:
+        if constexpr (G == 32) return launch_subwarp_gv<DT, G, 8, VEC, TL, E16>(a, grid);
+        else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }
 }

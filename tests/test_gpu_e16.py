@@ -147,6 +147,8 @@ def _plans(rng, N, dtype, vec, rs):
         G = int(2 ** rng.integers(0, 6))
         if -(-nvt // G) <= 4:
             out.append({"path": "subwarp", "lanes_per_row": G})
+    elif nvt <= 256:
+        out.append({"path": "subwarp", "lanes_per_row": 32})
     if slots >= 1:
         out.append({"path": "cta", "threads": int(32 * 2 ** rng.integers(0, 5))})
     if slots >= 2:

@@ -65,7 +65,8 @@ PLANS = [None, {"path": "cta", "threads": 32}, {"path": "cta", "threads": 512},
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 31, 33, 127, 129, 1000, 4097, 20001])
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 31, 33, 127, 129, 200, 1000, 1024, 2047, 4097,
+                               20001])
 def test_logprob_edge_shapes(dtype, N):
     _need_gpu()
     B = 9
@@ -92,6 +93,8 @@ def test_logprob_edge_shapes(dtype, N):
         if -(-N // epv) <= 128:
             plans += [{"path": "subwarp", "lanes_per_row": G} for G in (1, 2, 4, 8, 16, 32)
                       if -(-(-(-N // epv)) // G) <= 4]
+        elif -(-N // epv) <= 256:
+            plans.append({"path": "subwarp", "lanes_per_row": 32})
         if vec and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             plans.append({"path": "rowtile"})
         for plan in plans:

@@ -36,6 +36,7 @@ constexpr int kSubwarpWarpSlots = 8;   // slots per lane when a whole warp holds
 constexpr int kSegmentBatchVec = 8;    // slots per thread per batch (16-byte loads)
 constexpr int kSegmentBatchScalar = 16;
 constexpr int kMergeRowsPerCta = 8;    // one warp per row
+constexpr int kSplitMinBatches = 8;    // batches per thread a split segment keeps (when it can)
 
 struct DeviceInfo {
     bool ready = false;
@@ -241,7 +242,10 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     // that still give every thread >= 2 batches; at most 128 when rows are
     // plentiful (B >= 16 per SM), at least 256 when there are fewer rows than
     // SMs.  Rows are split only when B * threads would not cover half the
-    // GPU's resident threads (a split adds a merge kernel).
+    // GPU's resident threads (a split adds a merge kernel).  Splits (measured
+    // on 256 MB - 1 GB of few long rows): up to 8x the resident threads, but
+    // every thread keeps >= kSplitMinBatches batches (short-lived CTAs cost
+    // 5-15 %), and never fewer CTAs than one full wave.
     const int U = vec ? kSegmentBatchVec : kSegmentBatchScalar;
     const int64_t slots = vec ? nv : N;  // slots the segments cover (tail handled separately)
     int T = req && req->threads ? req->threads : 0;
@@ -275,7 +279,10 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         if (req && req->splits > 1) return LSE_ERR_INVALID_ARG;
         if ((!req || req->path == LSE_PATH_AUTO) && 2 * B * T < resident_threads) {
             int64_t want = ceil_div(8 * resident_threads, B * T);
-            const int64_t max_p = slots / (2 * batch);
+            const int64_t long_p = slots / (kSplitMinBatches * batch);  // long-lived CTAs
+            const int64_t wave_p = ceil_div(resident_threads, B * T);    // one full wave
+            if (want > long_p) want = long_p > wave_p ? long_p : wave_p;
+            const int64_t max_p = slots / (2 * batch);  // >= 2 batches per thread at least
             if (want > max_p) want = max_p;
             if (want >= 2) P = want;
         }

@@ -727,14 +727,17 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
         vec = req->vector_bytes == 16;
     }
     const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
-    const int64_t gy = A < 65535 ? A : 65535;
+    int64_t units = 0;  // (a, tile) pairs
+    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
     // Resident warps of the single-warp-tile variant (used to pick WT).
     const int64_t resident_warps = static_cast<int64_t>(info->sms) * cols_warps_per_cta(1) *
                                    cols_occupancy(dtype, vec, 1);
     const int64_t batch = cols_rows_per_batch(vec);
-    // Warps per tile (measured): short reductions walk each tile with one
-    // warp and no merge; longer ones share a tile between 4 warps and fill
-    // the GPU with row splits below.
+    // Warps per tile (measured on 256 MB of [A, R, C] for R = 2..4096, C =
+    // 128..16384): one warp walks each tile up to R = 64, or whenever the
+    // units alone give every resident warp two; 2 warps up to R = 128 and 4
+    // beyond share a tile (a shared-memory merge is cheaper than a split);
+    // row splits below fill the GPU only where that is still not enough.
     int WT = req && req->lanes_per_row ? req->lanes_per_row : 0;
     int path = rpath;
     if (path == LSE_PATH_COLUMNS_WARP) {
@@ -745,12 +748,12 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
         if (path == LSE_PATH_COLUMNS_CTA)
             WT = 8;
         else
-            WT = (R <= 256 || wtiles * gy >= 2 * resident_warps) ? 1 : 4;
+            WT = (R <= 64 || units >= 2 * resident_warps) ? 1 : (R <= 128 ? 2 : 4);
     }
     if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
     path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
     const int W = cols_warps_per_cta(WT);
-    const int64_t gx = ceil_div(wtiles, W / WT);
+    int64_t gx = ceil_div(units, W / WT);  // CTAs if each took one group of units
     const int64_t rows_per_warp_batch = WT * batch;
     const int64_t resident_ctas = static_cast<int64_t>(info->sms) * cols_occupancy(dtype, vec, WT);
     int64_t P = req ? req->splits : 0;
@@ -759,7 +762,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
         // split costs a merge kernel); otherwise as many splits as fit in ONE
         // wave of resident CTAs -- a partial second wave of these long-lived
         // CTAs would nearly double the time -- keeping >= 4 batches per warp.
-        const int64_t base = gx * gy;
+        const int64_t base = gx;
         P = 2 * base >= resident_ctas ? 1 : resident_ctas / base;
         const int64_t max_p = R / (4 * rows_per_warp_batch);
         if (P > max_p) P = max_p;
@@ -768,7 +771,10 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     if (P > R) return LSE_ERR_INVALID_ARG;
     const int64_t rows_per_split = ceil_div(R, P);
     P = ceil_div(R, rows_per_split);
-    if (P > 65535 || gx > INT_MAX) return LSE_ERR_INVALID_ARG;
+    if (P > 65535) return LSE_ERR_INVALID_ARG;
+    // Beyond a few waves CTAs loop over the units instead of being launched
+    // one per group (tiny groups made the launch itself the bottleneck).
+    if (gx > 4 * resident_ctas) gx = 4 * resident_ctas;
     if (P > 1 && outputs > INT64_MAX / (8 * P)) return LSE_ERR_INVALID_ARG;
     p.path = path;
     p.vector_bytes = vec ? 16 : 1;
@@ -776,7 +782,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     p.lanes_per_row = WT;
     p.splits = P;
     p.segment_slots = rows_per_split;
-    p.grid = gx * gy * P;
+    p.grid = gx * P;
     p.scratch_bytes = P > 1 ? outputs * P * static_cast<int64_t>(sizeof(float2)) : 0;
     p.launches = P > 1 ? 2 : 1;
     if (plan) *plan = p;
@@ -800,7 +806,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     a.partial = scratch;
     a.P = P;
     a.warps_per_tile = WT;
-    a.grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(P));
+    a.grid = dim3(static_cast<unsigned>(gx), 1, static_cast<unsigned>(P));
     a.stream = stream;
     e = launch_cols(dtype, vec, a);
     if (e == cudaSuccess && P > 1) e = launch_merge_columns(scratch, outputs, P, out, stream);

@@ -135,7 +135,7 @@ struct StridedArgs {
     float2* partial;  // [P, A * C] when P > 1
     int64_t P;
     int warps_per_tile;  // 1, 2, 4 or 8 warps interleave the rows of one column tile
-    dim3 grid;
+    dim3 grid;           // (CTAs striding over the (a, tile) units, 1, row splits)
     cudaStream_t stream;
 };
 cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a);

@@ -13,8 +13,10 @@
 // every load instruction of a warp covers one contiguous stretch of a row, and
 // a thread folds U rows per batch into EPV accumulators with one rescale per
 // batch.  WT = 1, 2, 4 or 8 warps share a tile, interleaving its rows and
-// merging in shared memory (see lse_cols_kernel).  With P > 1 the rows are also split across
-// blockIdx.z; the (m, s) partials are stored split-major, [P, A * C], and
+// merging in shared memory (see lse_cols_kernel).  The (a, tile) pairs are
+// flattened into units; a CTA's warps take consecutive units and CTAs stride
+// over them.  With P > 1 the rows are also split across blockIdx.z; the
+// (m, s) partials are stored split-major, [P, A * C], and
 // merge_columns_kernel combines them with one thread per output.
 #include <cstdint>
 
@@ -27,15 +29,23 @@ namespace lse {
 namespace {
 
 // Warps per CTA for WT warps per tile: 4 (small CTAs balance better across
-// SMs) unless the tile itself takes 8.
-template <int WT> struct ColCta { static constexpr int warps = WT > 4 ? WT : 4; };
+// SMs) unless the tile itself takes 8.  f32 variants and one-warp tiles keep
+// 32 warps per SM resident (<= 64 registers per thread); 16-bit tiles shared
+// by several warps hold 8 accumulators per lane and keep 24 (<= 85 registers;
+// capping them at 64 measured 15 % slower on long reductions).
+template <int WT> struct ColCta {
+    static constexpr int warps = WT > 4 ? WT : 4;
+    static constexpr int min_blocks(int elem_bytes) {
+        return (elem_bytes == 4 || WT == 1) ? 1024 / (32 * warps) : 896 / (32 * warps);
+    }
+};
 
 // WT warps share one column tile and interleave its rows (merged in shared
 // memory); the CTA's warps cover warps / WT tiles.  WT = 1: each warp walks
 // all rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
 // works on one tile (long reductions with few tiles).
 template <int DT, bool VEC, int WT>
-__global__ void __launch_bounds__(32 * ColCta<WT>::warps)
+__global__ void __launch_bounds__(32 * ColCta<WT>::warps, ColCta<WT>::min_blocks(DType<DT>::bytes))
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
@@ -52,17 +62,26 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     const int phase = wid % WT;  // row interleave position within the tile's warps
-    const int64_t tile = static_cast<int64_t>(blockIdx.x) * TPC + wid / WT;
-    const int64_t c0 = (tile * 32 + lane) * EPV;
-    const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
     const int64_t split = blockIdx.z;
     const int64_t r_begin = split * rows_per_split;
     const int64_t r_end = r_begin + rows_per_split < R ? r_begin + rows_per_split : R;
     const char* xb = reinterpret_cast<const char*>(x);
+    // Work units are (a, tile) pairs in a-major order; a CTA's TPC tile slots
+    // take consecutive units (several a when C is narrow), and CTAs stride
+    // over the units (the loop bound is the same for every warp of the CTA).
+    const int64_t wtiles = (C + 32 * EPV - 1) / (32 * EPV);
+    const int64_t units = A * wtiles;
 
     constexpr int64_t kStep = static_cast<int64_t>(WT) * U;  // rows per batch of one warp
-    for (int64_t a = blockIdx.y; a < A; a += gridDim.y) {
-        const char* base = xb + (a * stride_a + c0) * EB;
+#pragma unroll 1
+    for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * TPC; u0 < units;
+         u0 += static_cast<int64_t>(gridDim.x) * TPC) {
+        const int64_t unit = u0 + wid / WT;
+        const int64_t a = unit < units ? unit / wtiles : 0;
+        const int64_t tile = unit - a * wtiles;
+        const int64_t c0 = (tile * 32 + lane) * EPV;
+        const bool active = unit < units && c0 < C;  // VEC: whole vectors only (C % EPV == 0)
+        const char* base = xb + (a * stride_a + (active ? c0 : 0)) * EB;
         Acc acc[EPV];
         float mu[EPV];
 #pragma unroll

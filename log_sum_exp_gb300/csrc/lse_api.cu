@@ -638,20 +638,27 @@ lse_status lse_backward_strided(const void* x, lse_dtype dtype, int64_t A, int64
     const bool vec = al16(x) && al16(dx) && C % epv16 == 0 && (stride_a * eb) % 16 == 0 &&
                      (stride_r * eb) % 16 == 0 && (dx_stride_a * eb) % 16 == 0 &&
                      (dx_stride_r * eb) % 16 == 0;
-    const int64_t gx = ceil_div(C, 32 * (vec ? epv16 : 1));  // 32-lane column tiles
-    const int64_t gy = A < 65535 ? A : 65535;
-    // Row splits until the grid covers the GPU 4x (CTAs of backward_strided_warps()
-    // warps), keeping >= 2 batches of rows per warp.
+    const int64_t wtiles = ceil_div(C, 32 * (vec ? epv16 : 1));  // 32-lane column tiles
+    int64_t units = 0;  // (a, tile) pairs
+    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
+    // Warps per unit: a warp takes a whole unit when rows are few (one batch
+    // of rows per warp would leave a shared unit's warps idle), else the CTA's
+    // warps share it.  Row splits only while the units cannot cover the GPU
+    // 4x, keeping >= 2 batches per warp; beyond 4 waves CTAs loop over units.
     const int64_t W = backward_strided_warps();
-    const int64_t target = static_cast<int64_t>(info->sms) * 4 * (64 / W);
-    int64_t P = ceil_div(target, gx * gy);
-    const int64_t max_p = ceil_div(R, 2 * W * backward_slots_per_thread());
+    const int64_t U = backward_slots_per_thread();
+    const int wpu = R <= 2 * W * U ? 1 : static_cast<int>(W);
+    const int64_t upc = W / wpu;  // units per CTA
+    const int64_t resident_ctas = static_cast<int64_t>(info->sms) * (64 / W);
+    int64_t gx = ceil_div(units, upc);
+    int64_t P = ceil_div(4 * resident_ctas, gx);
+    const int64_t max_p = ceil_div(R, 2 * wpu * U);
     if (P > max_p) P = max_p;
     if (P > 65535) P = 65535;
     if (P < 1) P = 1;
     const int64_t rows_per_split = ceil_div(R, P);
     P = ceil_div(R, rows_per_split);
-    if (gx > INT_MAX) return LSE_ERR_INVALID_ARG;
+    if (gx > 4 * resident_ctas) gx = 4 * resident_ctas;
 
     BackwardStridedArgs a;
     a.x = x;
@@ -666,7 +673,8 @@ lse_status lse_backward_strided(const void* x, lse_dtype dtype, int64_t A, int64
     a.dx_stride_a = dx_stride_a;
     a.dx_stride_r = dx_stride_r;
     a.rows_per_split = rows_per_split;
-    a.grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(P));
+    a.warps_per_unit = wpu;
+    a.grid = dim3(static_cast<unsigned>(gx), 1, static_cast<unsigned>(P));
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = launch_backward_strided(dtype, vec, a);
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);

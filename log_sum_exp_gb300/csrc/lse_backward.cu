@@ -158,15 +158,17 @@ __device__ __forceinline__ uint4 grad_vector_cols(uint4 u, const float (&l)[EPV]
 
 // Gradient of the value over a non-last dimension:
 //     dx[a, r, c] = grad[a, c] * exp(x[a, r, c] - lse[a, c]),
-// lse and grad dense [A, C].  A lane owns EPV columns of one a (a 16-byte
-// vector, or one element when the layout is not 16-byte aligned) and loads
-// their lse and gradient once; the CTA's kStrWarps warps interleave the rows
-// of blockIdx.z's split, each with kBwdU rows in flight (all loads before any
-// store, so dx may be x itself).  blockIdx.x is the 32-lane column tile,
-// blockIdx.y the index a (grid-stride beyond gridDim.y).
+// lse and grad dense [A, C].  A unit is one (a, column tile) pair, the tile
+// 32 lanes x EPV columns (a 16-byte vector per lane, or one element when the
+// layout is not 16-byte aligned); a lane loads its columns' lse and gradient
+// once per unit.  WT warps (1 or kStrWarps) share a unit and interleave the
+// rows of blockIdx.z's split, each with kBwdU rows in flight (all loads before
+// any store, so dx may be x).  A CTA's warps take consecutive units (several
+// a when C is narrow) and CTAs stride over the units; nothing is merged, so
+// every warp loops on its own.
 constexpr int kStrWarps = 4;
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, int WT>
 __global__ void __launch_bounds__(32 * kStrWarps)
 lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C,
                             int64_t stride_a, int64_t stride_r, const float* __restrict__ lse,
@@ -174,34 +176,40 @@ lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, in
                             int64_t dx_stride_a, int64_t dx_stride_r, int64_t rows_per_split) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
+    constexpr int UPC = kStrWarps / WT;  // units per CTA
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + lane) * EPV;
-    const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
+    const int phase = wid % WT;
     const int64_t r_begin = static_cast<int64_t>(blockIdx.z) * rows_per_split;
     const int64_t r_end = r_begin + rows_per_split < R ? r_begin + rows_per_split : R;
-    for (int64_t a = blockIdx.y; a < A; a += gridDim.y) {
+    const int64_t wtiles = (C + 32 * EPV - 1) / (32 * EPV);
+    const int64_t units = A * wtiles;
+    for (int64_t unit = static_cast<int64_t>(blockIdx.x) * UPC + wid / WT; unit < units;
+         unit += static_cast<int64_t>(gridDim.x) * UPC) {
+        const int64_t a = unit / wtiles;
+        const int64_t c0 = ((unit - a * wtiles) * 32 + lane) * EPV;
+        const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
         float l[EPV], g[EPV];
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
             l[e] = active ? __ldg(lse + a * C + c0 + e) : 0.0f;
             g[e] = active ? __ldg(grad + a * C + c0 + e) : 0.0f;
         }
-        const char* xa = reinterpret_cast<const char*>(x) + (a * stride_a + c0) * EB;
-        char* da = reinterpret_cast<char*>(dx) + (a * dx_stride_a + c0) * EB;
-        for (int64_t r = r_begin + wid; r < r_end; r += static_cast<int64_t>(kStrWarps) * kBwdU) {
+        const char* xa = reinterpret_cast<const char*>(x) + (a * stride_a + (active ? c0 : 0)) * EB;
+        char* da = reinterpret_cast<char*>(dx) + (a * dx_stride_a + (active ? c0 : 0)) * EB;
+        for (int64_t r = r_begin + phase; r < r_end; r += static_cast<int64_t>(WT) * kBwdU) {
             if constexpr (VEC) {
                 uint4 v[kBwdU];
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const int64_t rr = r + j * kStrWarps;
+                    const int64_t rr = r + j * WT;
                     if (active && rr < r_end) v[j] = ldg_stream16(xa + rr * stride_r * EB);
                 }
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const int64_t rr = r + j * kStrWarps;
+                    const int64_t rr = r + j * WT;
                     if (active && rr < r_end)
                         __stcs(reinterpret_cast<uint4*>(da + rr * dx_stride_r * EB),
                                grad_vector_cols<DT, EPV>(v[j], l, g));
@@ -210,12 +218,12 @@ lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, in
                 float v[kBwdU];
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const int64_t rr = r + j * kStrWarps;
+                    const int64_t rr = r + j * WT;
                     if (active && rr < r_end) v[j] = load_elem<DT>(xa, rr * stride_r);
                 }
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const int64_t rr = r + j * kStrWarps;
+                    const int64_t rr = r + j * WT;
                     if (active && rr < r_end)
                         store_elem<DT>(da, rr * dx_stride_r, grad_term(v[j], l[0], g[0]));
                 }
@@ -226,8 +234,12 @@ lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, in
 
 template <int DT, bool VEC>
 cudaError_t launch_backward_strided_t(const BackwardStridedArgs& a) {
-    return launch_pdl(lse_backward_strided_kernel<DT, VEC>, a.grid, dim3(32 * kStrWarps), a.stream,
-                      a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad, a.dx,
+    if (a.warps_per_unit == 1)
+        return launch_pdl(lse_backward_strided_kernel<DT, VEC, 1>, a.grid, dim3(32 * kStrWarps),
+                          a.stream, a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad,
+                          a.dx, a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
+    return launch_pdl(lse_backward_strided_kernel<DT, VEC, kStrWarps>, a.grid, dim3(32 * kStrWarps),
+                      a.stream, a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad, a.dx,
                       a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
 }
 

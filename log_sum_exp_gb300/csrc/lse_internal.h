@@ -114,7 +114,8 @@ struct BackwardStridedArgs {
     int64_t dx_stride_a;
     int64_t dx_stride_r;
     int64_t rows_per_split;
-    dim3 grid;  // (column tiles, a, row splits)
+    int warps_per_unit;  // 1, or backward_strided_warps(): warps sharing one (a, tile) unit
+    dim3 grid;           // (CTAs striding over the (a, tile) units, 1, row splits)
     cudaStream_t stream;
 };
 cudaError_t launch_backward_strided(int dt, bool vec, const BackwardStridedArgs& a);

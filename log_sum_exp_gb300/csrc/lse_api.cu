@@ -586,6 +586,16 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
     a.seg_slots = seg;
     a.grid = dim3(static_cast<unsigned>(P), static_cast<unsigned>(gy));
     a.block = dim3(static_cast<unsigned>(TX), static_cast<unsigned>(TY));
+    // Rows of at most U slots: flattened (row, slot) pairs, U per thread in
+    // flight, at most 4 waves of 256-thread CTAs striding over them.
+    a.small = nvt <= U;
+    if (a.small) {
+        int64_t ctas = ceil_div(ceil_div(B * nvt, U), threads);
+        const int64_t cap = static_cast<int64_t>(info->sms) * 8 * 4;
+        if (ctas > cap) ctas = cap;
+        a.grid = dim3(static_cast<unsigned>(ctas));
+        a.block = dim3(static_cast<unsigned>(threads));
+    }
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = launch_backward(dtype, vec, a);
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);

@@ -243,6 +243,75 @@ cudaError_t launch_backward_strided_t(const BackwardStridedArgs& a) {
                       a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
 }
 
+// Rows of at most kBwdU slots: the (row, slot) pairs are flattened and each
+// thread keeps kBwdU of them in flight (slot q, q + stride, ...), so
+// consecutive threads touch consecutive vectors whatever the row length.  A
+// slot is a 16-byte vector (VEC; the slot index nv of a row holds its < EPV
+// tail elements) or one element.  lse and grad are read per slot; a row's
+// slots share them in L1.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kBwdThreads)
+lse_backward_small_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
+                          const float* __restrict__ lse, const float* __restrict__ grad,
+                          void* __restrict__ dx, int64_t dx_row_stride) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = VEC ? 16 / EB : 1;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t nv = N / EPV;
+    const int tail = static_cast<int>(N - nv * EPV);
+    const int64_t nvt = nv + (tail > 0 ? 1 : 0);  // slots per row, <= kBwdU
+    const int64_t slots = B * nvt;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const char* xb = reinterpret_cast<const char*>(x);
+    char* db = reinterpret_cast<char*>(dx);
+    for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q0 < slots;
+         q0 += stride * kBwdU) {
+        int64_t row[kBwdU], k[kBwdU];
+        float l[kBwdU], g[kBwdU];
+        uint4 v[kBwdU];
+#pragma unroll
+        for (int j = 0; j < kBwdU; ++j) {
+            const int64_t q = q0 + j * stride;
+            row[j] = q < slots ? q / nvt : -1;
+            k[j] = q - row[j] * nvt;
+            if (row[j] >= 0) {
+                l[j] = __ldg(lse + row[j]);
+                g[j] = __ldg(grad + row[j]);
+                if constexpr (VEC) {
+                    if (k[j] < nv) v[j] = ldg_stream16(xb + (row[j] * row_stride + k[j] * EPV) * EB);
+                } else {
+                    v[j].x = __float_as_uint(load_elem<DT>(xb + row[j] * row_stride * EB, k[j]));
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBwdU; ++j) {
+            if (row[j] < 0) continue;
+            char* dr = db + row[j] * dx_row_stride * EB;
+            if constexpr (VEC) {
+                if (k[j] < nv) {
+                    __stcs(reinterpret_cast<uint4*>(dr + k[j] * EPV * EB),
+                           grad_vector<DT>(v[j], l[j], g[j]));
+                } else {  // the < EPV tail elements
+                    const char* xr = xb + row[j] * row_stride * EB;
+                    for (int i = 0; i < tail; ++i)
+                        store_elem<DT>(dr, nv * EPV + i,
+                                       grad_term(load_elem<DT>(xr, nv * EPV + i), l[j], g[j]));
+                }
+            } else {
+                store_elem<DT>(dr, k[j], grad_term(__uint_as_float(v[j].x), l[j], g[j]));
+            }
+        }
+    }
+}
+
+template <int DT, bool VEC>
+cudaError_t launch_backward_small_t(const BackwardArgs& a) {
+    return launch_pdl(lse_backward_small_kernel<DT, VEC>, a.grid, a.block, a.stream, a.x, a.B,
+                      a.N, a.row_stride, a.lse, a.grad, a.dx, a.dx_row_stride);
+}
+
 template <int DT, bool VEC>
 cudaError_t launch_backward_t(const BackwardArgs& a) {
     return launch_pdl(lse_backward_kernel<DT, VEC>, a.grid, a.block, a.stream, a.x, a.B, a.N,
@@ -252,6 +321,13 @@ cudaError_t launch_backward_t(const BackwardArgs& a) {
 }  // namespace
 
 cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a) {
+    if (a.small) {
+        switch (dt) {
+        case kF32: return vec ? launch_backward_small_t<kF32, true>(a) : launch_backward_small_t<kF32, false>(a);
+        case kBF16: return vec ? launch_backward_small_t<kBF16, true>(a) : launch_backward_small_t<kBF16, false>(a);
+        default: return vec ? launch_backward_small_t<kF16, true>(a) : launch_backward_small_t<kF16, false>(a);
+        }
+    }
     switch (dt) {
     case kF32: return vec ? launch_backward_t<kF32, true>(a) : launch_backward_t<kF32, false>(a);
     case kBF16: return vec ? launch_backward_t<kBF16, true>(a) : launch_backward_t<kBF16, false>(a);

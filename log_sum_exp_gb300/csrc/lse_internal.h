@@ -95,6 +95,7 @@ struct BackwardArgs {
     void* dx;
     int64_t dx_row_stride;
     int64_t seg_slots;  // slots (16-byte vectors or elements) per blockIdx.x segment
+    bool small;         // rows of <= backward_slots_per_thread() slots: flattened mapping
     dim3 grid;
     dim3 block;
     cudaStream_t stream;

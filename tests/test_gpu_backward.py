@@ -90,7 +90,8 @@ def test_workload_backward(key, B, N):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 33, 1000, 4097, 20001])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 8, 9, 12, 15, 16, 17, 31, 32, 33, 1000, 4097,
+                               20001])
 def test_backward_edge_shapes(dtype, N):
     _need_gpu()
     B = 7

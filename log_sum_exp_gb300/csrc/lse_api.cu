@@ -135,16 +135,20 @@ int pow2_ceil(int64_t v) {
 // Fill in (or check) a plan.  `req` may be null (automatic).
 lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t row_stride,
                      const DeviceInfo& info, const lse_plan* req, bool with_logprob,
-                     lse_plan* plan) {
+                     lse_plan* plan, bool e16 = false) {
     lse_plan p;
     std::memset(&p, 0, sizeof p);
     const int eb = elem_bytes(dt);
+    // Every row starts on a 16-byte boundary when x and the row stride do;
+    // otherwise the vector path peels each row's head (and tail) into scalar
+    // loads, which needs only element-aligned x.
     const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16u == 0) &&
                          ((row_stride * eb) % 16 == 0);
-    bool vec = aligned;
+    const bool peelable = reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(eb) == 0;
+    bool vec = peelable;
     if (req && req->vector_bytes != 0) {
         if (req->vector_bytes == 16) {
-            if (!aligned) return LSE_ERR_INVALID_ARG;
+            if (!peelable) return LSE_ERR_INVALID_ARG;
             vec = true;
         } else if (req->vector_bytes == 1) {
             vec = false;
@@ -154,8 +158,9 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     }
     p.vector_bytes = vec ? 16 : 1;
     const int64_t epv = vec ? 16 / eb : 1;
-    const int64_t nv = N / epv;               // full slots per row
-    const int64_t nvt = ceil_div(N, epv);     // slots including the tail vector
+    const int64_t nv = N / epv;  // full slots per row (at most)
+    // Slots including the tail vector, and the head slot of peeled rows.
+    const int64_t nvt = vec && !aligned ? nv + 2 : ceil_div(N, epv);
     int path = req ? req->path : LSE_PATH_AUTO;
 
     if (N == 0) {
@@ -180,17 +185,45 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     // vectors and 16-bit rows of 4 or 8, where one thread per row would fold
     // 32 or 64 elements alone.
     const int64_t row_bytes = N * eb;
-    const bool rowtile_ok = vec && row_stride == N && row_bytes % 16 == 0 && row_bytes >= 16 &&
-                            row_bytes <= 128;
+    const bool rowtile_ok = vec && aligned && row_stride == N && row_bytes % 16 == 0 &&
+                            row_bytes >= 16 && row_bytes <= 128;
     const int64_t row_vecs = row_bytes / 16;
     const bool rowtile_auto =
         row_vecs > 2 && !(eb == 2 && (row_vecs == 4 || row_vecs == 8));
+    // Rows of other widths up to 128 bytes, still back to back from a 16-byte
+    // aligned base: the same ring with element reads (row value with f32
+    // exponentials only).  Chosen automatically: it measured 1.15-2.9x the
+    // sub-warp mapping (with the head peel) on every such width but f32 rows
+    // of 7, where the two are even.
+    const bool rowtile_any_ok = !rowtile_ok && !with_logprob && !e16 && row_stride == N &&
+                                row_bytes <= 128 &&
+                                reinterpret_cast<uintptr_t>(x) % 16u == 0 &&
+                                (!req || req->vector_bytes != 16);
     if (path == LSE_PATH_AUTO) {
         const int64_t chunk_rows = rowtile_ok ? rowtile_rows_per_chunk(static_cast<int>(row_bytes / 16)) : 1;
+        const int64_t any_rows =
+            rowtile_any_ok ? rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)) : 1;
         if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
+            path = LSE_PATH_ROWTILE;
+        else if (rowtile_any_ok && B >= any_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
         else
             path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
+    }
+    if (path == LSE_PATH_ROWTILE && !rowtile_ok && rowtile_any_ok) {
+        const int64_t chunks = ceil_div(B, rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)));
+        int64_t grid = static_cast<int64_t>(info.sms) * rowtile_ctas_per_sm();
+        if (grid > chunks) grid = chunks;
+        if (grid < 1) grid = 1;
+        p.path = LSE_PATH_ROWTILE;
+        p.vector_bytes = 1;
+        p.threads = 256;
+        p.slots_per_lane = 0;  // any row width
+        p.splits = 1;
+        p.grid = grid;
+        p.launches = B > 0 ? 1 : 0;
+        *plan = p;
+        return LSE_OK;
     }
     if (path == LSE_PATH_ROWTILE) {
         if (!rowtile_ok) return LSE_ERR_INVALID_ARG;
@@ -450,7 +483,7 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
     lse_status st = device_info(&dev, &info);
     if (st != LSE_OK) return st;
     lse_plan p;
-    if ((st = make_plan(x, dtype, B, N, row_stride, *info, plan, tl.logprob != nullptr, &p)) !=
+    if ((st = make_plan(x, dtype, B, N, row_stride, *info, plan, tl.logprob != nullptr, &p, e16)) !=
         LSE_OK)
         return st;
     if (plan) *plan = p;

@@ -51,17 +51,33 @@ __device__ __forceinline__ void load_tail_words(const void* row, int64_t start, 
     }
 }
 
+// Elements of a row before its first 16-byte boundary (the scalar head peel
+// of a row that does not start on one); the vectors start right after.
+template <int DT>
+__device__ __forceinline__ int head_elems(const void* row, int64_t N) {
+    const int h = static_cast<int>((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row)) & 15u)) & 15u) /
+                  DType<DT>::bytes;
+    return N < h ? static_cast<int>(N) : h;
+}
+
 // ---------------------------------------------------------------------------
 // subwarp: G lanes per row, V slots per lane, R row-groups per warp iteration.
-// VEC: a slot is one 16-byte vector (the lane holding vector index N/EPV also
-// loads the < EPV tail elements); !VEC: a slot is one element.  V = 8 (only
+// VEC: a slot is one 16-byte vector of the row's aligned part; a row that does
+// not start on a 16-byte boundary peels its head (< EPV elements) and tail
+// (< EPV elements) into two more slots: slot nv holds the tail, the slot after
+// it the head (nv = full vectors of that row).  !VEC: a slot is one element.
+// V = 8 (only
 // with G = 32: a whole warp per row of up to 256 slots) keeps 32 words per
 // lane and runs at 4 CTAs per SM.
 // ---------------------------------------------------------------------------
-template <int V> struct SubwarpOccupancy { static constexpr int min_blocks = V >= 8 ? 4 : kSubwarpMinBlocks; };
+// The token log-probability epilogue keeps the targets and the peel state of
+// every row group live: one CTA per SM less, so it does not spill.
+template <int V, bool TL> struct SubwarpOccupancy {
+    static constexpr int min_blocks = (V >= 8 ? 4 : kSubwarpMinBlocks) - (TL ? 1 : 0);
+};
 
 template <int DT, int G, int V, bool VEC, bool TL, bool E16>
-__global__ void __launch_bounds__(kSubwarpThreads, SubwarpOccupancy<V>::min_blocks)
+__global__ void __launch_bounds__(kSubwarpThreads, SubwarpOccupancy<V, TL>::min_blocks)
 lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                    float* __restrict__ out, const int64_t* __restrict__ target,
                    float* __restrict__ logprob) {
@@ -74,8 +90,6 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
     const int grp = lane / G;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t nv = N / EPV;                        // full slots per row
-    const int tail = static_cast<int>(N - nv * EPV);   // VEC only: 0 .. EPV-1
     const char* xb = reinterpret_cast<const char*>(x);
     pdl_trigger();
     pdl_wait();
@@ -93,31 +107,37 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
         }
         if constexpr (VEC) {
             uint32_t w[R][4 * V];
+            int head[R], tail[R], nv[R];  // per row: peeled head, tail, full vectors
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int64_t row = row0 + r * RPW + grp;
-                const char* rp = xb + row * row_stride * EB;
+                const char* rp = xb + (row < B ? row : 0) * row_stride * EB;
+                head[r] = head_elems<DT>(rp, N);
+                const char* rv = rp + head[r] * EB;  // 16-byte aligned
+                nv[r] = static_cast<int>((N - head[r]) / EPV);
+                tail[r] = static_cast<int>(N - head[r] - static_cast<int64_t>(nv[r]) * EPV);
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
-                    const int64_t k = sub + j * G;
+                    const int k = sub + j * G;
                     uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
                                          neg_inf_word<DT>());
-                    if (row < B && k < nv) u = ldg_stream16(rp + k * 16);
+                    if (row < B && k < nv[r]) u = ldg_stream16(rv + k * 16);
                     w[r][4 * j] = u.x; w[r][4 * j + 1] = u.y; w[r][4 * j + 2] = u.z; w[r][4 * j + 3] = u.w;
                 }
-            }
-            if (tail > 0) {  // same for every lane: depends on N only
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int64_t row = row0 + r * RPW + grp;
+                if (row < B && (tail[r] > 0 || head[r] > 0)) {
 #pragma unroll
                     for (int j = 0; j < V; ++j) {
-                        if (row < B && sub + j * G == nv) {
-                            uint32_t q[4];
-                            load_tail_words<DT>(xb + row * row_stride * EB, nv * EPV, tail, q);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                        const int k = sub + j * G;
+                        uint32_t q[4];
+                        if (tail[r] > 0 && k == nv[r]) {
+                            load_tail_words<DT>(rv, static_cast<int64_t>(nv[r]) * EPV, tail[r], q);
+                        } else if (head[r] > 0 && k == nv[r] + (tail[r] > 0 ? 1 : 0)) {
+                            load_tail_words<DT>(rp, 0, head[r], q);
+                        } else {
+                            continue;
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
                     }
                 }
             }
@@ -146,10 +166,19 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                 if constexpr (TL) {
                     const bool valid = t[r] >= 0;
                     if (valid) {
-                        const int kv = t[r] / EPV;
+                        // slot and position of x[row, t]: head slot, a vector, or the tail slot
+                        int slot, pos;
+                        if (t[r] < head[r]) {
+                            slot = nv[r] + (tail[r] > 0 ? 1 : 0);
+                            pos = t[r];
+                        } else {
+                            const int t2 = t[r] - head[r];
+                            slot = t2 / EPV < nv[r] ? t2 / EPV : nv[r];
+                            pos = t2 - slot * EPV;
+                        }
 #pragma unroll
                         for (int j = 0; j < V; ++j)
-                            if (sub + j * G == kv) xt = word_elem<DT>(&w[r][4 * j], t[r] - kv * EPV);
+                            if (sub + j * G == slot) xt = word_elem<DT>(&w[r][4 * j], pos);
                     }
 #pragma unroll
                     for (int off = G / 2; off > 0; off >>= 1)
@@ -219,7 +248,8 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 // ---------------------------------------------------------------------------
 // segment: blockIdx.x = row * P + seg.  Segment seg covers slots
 // [seg * seg_slots, min(nv, (seg + 1) * seg_slots)) of its row; the last
-// segment also takes the < EPV tail elements (VEC only).
+// segment also takes the < EPV tail elements and the first segment the < EPV
+// head elements before the row's first 16-byte boundary (VEC only).
 // ---------------------------------------------------------------------------
 template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
 
@@ -240,10 +270,12 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
     const int64_t unit = blockIdx.x;
     const int64_t row = unit / P;
     const int64_t seg = unit - row * P;
-    const int64_t nv = N / EPV;
+    const char* rp = reinterpret_cast<const char*>(x) + row * row_stride * EB;
+    const int head = VEC ? head_elems<DT>(rp, N) : 0;
+    const char* rv = rp + head * EB;  // VEC: 16-byte aligned vectors from here
+    const int64_t nv = (N - head) / EPV;
     const int64_t s_begin = seg * seg_slots;
     const int64_t s_end = s_begin + seg_slots < nv ? s_begin + seg_slots : nv;
-    const char* rp = reinterpret_cast<const char*>(x) + row * row_stride * EB;
 
     Acc acc = acc_identity();
     float mu = 0.0f;
@@ -261,7 +293,7 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             uint32_t w[4 * U];
 #pragma unroll
             for (int j = 0; j < U; ++j) {
-                const uint4 u = ldg_stream16(rp + (k + j * T) * 16);
+                const uint4 u = ldg_stream16(rv + (k + j * T) * 16);
                 w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
             }
             if (xt_pending) {
@@ -276,7 +308,7 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             for (int j = 0; j < U; ++j) {
                 const int64_t kk = k + j * T;
                 if (kk < s_end) {
-                    const uint4 u = ldg_stream16(rp + kk * 16);
+                    const uint4 u = ldg_stream16(rv + kk * 16);
                     w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
                 } else {
 #pragma unroll
@@ -285,10 +317,15 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             }
             acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
-        const int tail = static_cast<int>(N - nv * EPV);
+        const int tail = static_cast<int>(N - head - nv * EPV);
         if (tail > 0 && seg == P - 1 && threadIdx.x == 0) {
             uint32_t w[4];
-            load_tail_words<DT>(rp, nv * EPV, tail, w);
+            load_tail_words<DT>(rv, nv * EPV, tail, w);
+            acc_add_words<DT, 4, E16>(acc, mu, w);
+        }
+        if (head > 0 && seg == 0 && threadIdx.x == 0) {
+            uint32_t w[4];
+            load_tail_words<DT>(rp, 0, head, w);
             acc_add_words<DT, 4, E16>(acc, mu, w);
         }
     } else {

@@ -204,6 +204,117 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     }
 }
 
+// Back-to-back rows of any width RB = N * elem <= 128 bytes that is not a
+// multiple of 16 (row value only).  Chunks hold CR = 256 * floor(32 KB / (256
+// * RB)) rows, a multiple of 16, so every chunk starts and ends on a 16-byte
+// boundary as long as it has a multiple of k = 16 / gcd(RB, 16) rows: the
+// copies cover the first Bm = B - B % k rows, and the < k rows after them are
+// read from global memory by CTA 0 at the end.  A thread folds each of its
+// rows straight from shared memory (max, then the exp-sum) before the stage
+// is released for the next copy.
+template <int DT>
+__global__ void __launch_bounds__(kTileThreads)
+lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out) {
+    constexpr int EB = DType<DT>::bytes;
+    extern __shared__ __align__(128) unsigned char stage[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    const int tid = threadIdx.x;
+    const int RB = static_cast<int>(N) * EB;  // <= 128
+    const int RPT = kChunkBytes / (kTileThreads * RB);
+    const int64_t CR = static_cast<int64_t>(kTileThreads) * RPT;
+    int g = RB;  // gcd(RB, 16)
+    for (int t = 16; t != 0;) {
+        const int r = g % t;
+        g = t;
+        t = r;
+    }
+    const int64_t k = 16 / g;
+    const int64_t Bm = B - B % k;
+    const int64_t nchunks = (Bm + CR - 1) / CR;
+    const char* xb = reinterpret_cast<const char*>(x);
+
+    pdl_trigger();
+    pdl_wait();
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int64_t chunk, int s) {  // thread 0 only
+        const int64_t r0 = chunk * CR;
+        const int64_t rows = Bm - r0 < CR ? Bm - r0 : CR;
+        const uint32_t bytes = static_cast<uint32_t>(rows * RB);  // a multiple of 16
+        mbar_expect_tx(&full[s], bytes);
+        bulk_load(stage + s * kChunkBytes, xb + r0 * RB, bytes, &full[s]);
+    };
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (c < nchunks) issue(c, s);
+        }
+
+    auto fold = [&](auto elem) {  // elem(n) -> float; the row value
+        float m = __int_as_float(kNegInfF32);
+        for (int n = 0; n < N; ++n) m = fmaxf(m, elem(n));
+        const float mu = shift_of(m);
+        float acc[2] = {0.0f, 0.0f};
+        for (int n = 0; n < N; ++n) acc[n & 1] += ex2((elem(n) - mu) * kLog2e);
+        return acc_finalize(Acc{m, acc[0] + acc[1]});
+    };
+
+    int64_t kc = 0;  // chunks consumed by this CTA
+    bool timed_out = false;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++kc) {
+        const int s = static_cast<int>(kc % kStages);
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((kc / kStages) & 1), kWaitPolls);
+        // Results are stored as soon as they are computed; the stage is only
+        // read before the barrier below.
+        for (int q = 0; q < RPT; ++q) {
+            const int64_t row = c * CR + q * kTileThreads + tid;
+            if (ok && row < Bm) {
+                const unsigned char* rowp = stage + s * kChunkBytes + (q * kTileThreads + tid) * RB;
+                out[row] = fold([&](int n) { return staged_elem<DT>(rowp, n); });
+            }
+        }
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            break;
+        }
+        if (tid == 0) {
+            const int64_t cn = c + static_cast<int64_t>(kStages) * gridDim.x;
+            if (cn < nchunks) issue(cn, s);
+        }
+    }
+    if (timed_out) {
+        if (tid == 0) {
+            atomicAdd(&g_wait_timeouts, 1ull);
+            for (int s = 0; s < kStages; ++s) {
+                mbar_wait(&full[s], 0, kWaitPolls);
+                mbar_wait(&full[s], 1, kWaitPolls);
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    if (blockIdx.x == 0 && Bm + tid < B) {  // the < k rows after the last copy
+        const int64_t row = Bm + tid;
+        const char* rowp = xb + row * RB;
+        out[row] = fold([&](int n) { return load_elem<DT>(rowp, n); });
+    }
+}
+
+template <int DT>
+cudaError_t launch_rowtile_any_t(const LaunchArgs& a, int grid) {
+    const int smem = kStages * kChunkBytes;
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_smem(lse_rowtile_any_kernel<DT>, dim3(static_cast<unsigned>(grid)),
+                           dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B, a.N,
+                           a.out);
+}
+
 template <int DT, int NV, bool E16, bool TL>
 cudaError_t launch_rowtile_t(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
@@ -242,6 +353,14 @@ cudaError_t launch_rowtile_e(int dt, int nv, const LaunchArgs& a, int grid) {
 }  // namespace
 
 cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid) {
+    if (nv == 0) {  // any row width: row value with f32 exponentials only
+        if (a.tl.logprob || a.e16) return cudaErrorInvalidValue;
+        switch (dt) {
+        case kF32: return launch_rowtile_any_t<kF32>(a, grid);
+        case kBF16: return launch_rowtile_any_t<kBF16>(a, grid);
+        default: return launch_rowtile_any_t<kF16>(a, grid);
+        }
+    }
     if (a.tl.logprob) return launch_rowtile_e<false, true>(dt, nv, a, grid);
     return a.e16 ? launch_rowtile_e<true, false>(dt, nv, a, grid)
                  : launch_rowtile_e<false, false>(dt, nv, a, grid);
@@ -249,6 +368,9 @@ cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid) {
 
 int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
 int rowtile_rows_per_chunk(int nv) { return kTileThreads * (8 / nv); }
+int rowtile_any_rows_per_chunk(int row_bytes) {
+    return kTileThreads * (kChunkBytes / (kTileThreads * row_bytes));
+}
 
 cudaError_t read_wait_timeouts(unsigned long long* count) {
     return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));

@@ -137,11 +137,11 @@ def test_special_values(dtype, N):
     compare_e16(got.cpu().numpy(), want, e16_bound(x, dtype, want))
 
 
-def _plans(rng, N, dtype, vec, rs):
+def _plans(rng, N, dtype, aligned, rs):
     eb = 4 if dtype == "f32" else 2
-    epv = 16 // eb if vec else 1
-    slots = N // epv if vec else N
-    nvt = -(-N // epv)
+    epv = 16 // eb  # vector slots; rows off a 16-byte boundary peel a head and a tail slot
+    slots = N // epv
+    nvt = -(-N // epv) if aligned else N // epv + 2
     out = [None]
     if nvt <= 128:
         G = int(2 ** rng.integers(0, 6))
@@ -153,7 +153,7 @@ def _plans(rng, N, dtype, vec, rs):
         out.append({"path": "cta", "threads": int(32 * 2 ** rng.integers(0, 5))})
     if slots >= 2:
         out.append({"path": "split", "splits": int(rng.integers(2, min(slots, 40) + 1))})
-    if vec and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
+    if aligned and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
         out.append({"path": "rowtile"})
     return out
 
@@ -173,10 +173,10 @@ def test_random_layouts_and_plans(seed):
     x = wl.random_rows(B, N, dtype, seed=int(rng.integers(1 << 30)), scale=scale, shift=shift)
     _, xv = device_rows(x, dtype, row_stride=rs, offset=off)
     eb = 4 if dtype == "f32" else 2
-    vec = xv.data_ptr() % 16 == 0 and (rs * eb) % 16 == 0
+    aligned = xv.data_ptr() % 16 == 0 and (rs * eb) % 16 == 0
     want = oracle.lse(x, dtype)
     bound = e16_bound(x, dtype, want)
-    for plan in _plans(rng, N, dtype, vec, rs):
+    for plan in _plans(rng, N, dtype, aligned, rs):
         try:
             got, p = L.lse_forward16(xv, plan=plan)
         except L.LseError:

@@ -86,19 +86,28 @@ def test_logprob_edge_shapes(dtype, N):
     eb = 4 if dtype == "f32" else 2
     for row_stride, offset in ((N, 0), (N + 5, 1), (N + 8, 0)):
         _, xv = device_rows(x, dtype, row_stride=row_stride, offset=offset)
-        vec = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
-        epv = 16 // eb if vec else 1
-        slots = N // epv if vec else N
+        # Vector slots on every layout: rows off a 16-byte boundary peel a head
+        # and a tail slot; the element mappings are forced on those too.
+        aligned = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
+        epv = 16 // eb
+        slots = N // epv
+        nvt = -(-N // epv) if aligned else N // epv + 2
         plans = list(PLANS)
-        if -(-N // epv) <= 128:
+        if nvt <= 128:
             plans += [{"path": "subwarp", "lanes_per_row": G} for G in (1, 2, 4, 8, 16, 32)
-                      if -(-(-(-N // epv)) // G) <= 4]
-        elif -(-N // epv) <= 256:
+                      if -(-nvt // G) <= 4]
+        elif nvt <= 256:
             plans.append({"path": "subwarp", "lanes_per_row": 32})
-        if vec and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
+        if aligned and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             plans.append({"path": "rowtile"})
+        if not aligned:
+            plans += [{"path": "cta", "threads": 128, "vector_bytes": 1},
+                      {"path": "split", "splits": 3, "threads": 64, "vector_bytes": 1}]
+            if N <= 128:
+                plans.append({"path": "subwarp", "lanes_per_row": 32, "vector_bytes": 1})
         for plan in plans:
-            if plan and plan.get("path") == "split" and slots < plan["splits"]:
+            if plan and plan.get("path") == "split" and \
+                    (N if plan.get("vector_bytes") == 1 else slots) < plan["splits"]:
                 continue
             for with_lse in (True, False):
                 lp, lse, p = run_logprob(xv, t, plan, with_lse)

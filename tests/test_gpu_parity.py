@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from log_sum_exp_gb300 import workloads as wl
-from lse_testutil import compare, device_rows, torch_view
+from lse_testutil import compare, compare_e16, compare_logprob, device_rows, e16_bound, torch_view
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -60,10 +60,12 @@ LENGTHS = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128,
            8191, 12345, 65537, 131073]
 
 
-def plans_for(N, dtype, vec):
+def plans_for(N, dtype, vec, aligned=True):
+    """Forced plans for rows of N elements.  vec: 16-byte vector slots; rows
+    that are not 16-byte aligned (aligned=False) peel a head and a tail slot."""
     eb = 4 if dtype == "f32" else 2
     epv = 16 // eb if vec else 1
-    nvt = -(-N // epv)
+    nvt = -(-N // epv) if aligned or not vec else N // epv + 2
     slots = N // epv if vec else N
     plans = [None]
     vb = 16 if vec else 1
@@ -105,10 +107,12 @@ def test_edge_shapes(dtype, N):
     layouts = [(N, 0), (N + 8, 0), (N + 1, 0), (N, 1)]
     for row_stride, offset in layouts:
         buf, xv = device_rows(x, dtype, row_stride=row_stride, offset=offset)
-        vec = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
-        plans = plans_for(N, dtype, vec)
-        if vec and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
-            plans.append({"path": "rowtile"})
+        aligned = (xv.data_ptr() % 16 == 0) and (row_stride * eb) % 16 == 0
+        plans = plans_for(N, dtype, aligned)
+        if not aligned:  # the vector mappings with the head and tail peeled
+            plans += plans_for(N, dtype, True, aligned=False)[1:]
+        if row_stride == N and N * eb <= 128 and xv.data_ptr() % 16 == 0:
+            plans.append({"path": "rowtile"})  # vector ring, or element reads for other widths
         for plan in plans:
             got, p = run(xv, plan)
             try:
@@ -435,6 +439,24 @@ def test_graph_capture_all_ops():
     assert np.all(np.abs(v16.cpu().numpy() - want) < 3e-3)
 
 
+def test_rowtile_any_width_ragged():
+    """The bulk-copy ring for back-to-back rows whose width is not a multiple of
+    16 bytes (element reads from shared memory; the last < 16/gcd(width, 16)
+    rows come from global memory), every dtype, odd widths and row counts."""
+    _need_gpu()
+    for dtype, eb, Ns in (("f32", 4, (1, 2, 3, 5, 6, 7, 9, 13, 17, 31)),
+                          ("bf16", 2, (1, 2, 3, 5, 7, 9, 12, 17, 33, 63)),
+                          ("f16", 2, (3, 5, 12, 31))):
+        for N in Ns:
+            for B in (1, 7, 255, 2049, 100003):
+                x = wl.random_rows(B, N, dtype, seed=B + 7 * N, scale=8.0)
+                got, p = run(torch_view(x, dtype).cuda(), {"path": "rowtile"})
+                d = p.as_dict()
+                assert d["path"] == "rowtile" and d["slots_per_lane"] == 0, d
+                compare(got, oracle.lse(x, dtype))
+    assert L.lse_wait_timeouts() == 0
+
+
 def test_short_row_mapping_rule():
     """Automatic choice between the bulk-copy ring and the sub-warp mapping for
     back-to-back rows of 16..128 bytes (the measured rule): the ring for rows
@@ -450,6 +472,36 @@ def test_short_row_mapping_rule():
             assert L.lse_plan_query(dtype=dtype, B=1 << 20, N=N, row_stride=N + 16 // eb)["path"] \
                 == "subwarp"
             assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
+
+
+def test_any_width_ring_rule():
+    """Back-to-back rows of other widths up to 128 bytes take the element-read
+    ring when there are rows for every CTA (row value only); the 16-bit
+    exponential and token log-probability entry points keep the register
+    mappings for them."""
+    _need_gpu()
+    for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
+        for N in (1, 3, 5, 7, 9, 17, 128 // eb - 1):
+            # (a query only: 2^26 rows fill every CTA's chunk for any width)
+            q = L.lse_plan_query(dtype=dtype, B=1 << 26, N=N, row_stride=N)
+            assert q["path"] == "rowtile" and q["slots_per_lane"] == 0, (dtype, N, q)
+            assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
+            assert L.lse_plan_query(dtype=dtype, B=1 << 26, N=N, row_stride=N + 1)["path"] \
+                == "subwarp"
+    x = wl.random_rows(1 << 20, 5, "f32", seed=55, scale=4.0)  # >= 1536 rows per CTA
+    xd = torch.from_numpy(x).cuda()
+    want = oracle.lse(x, "f32")
+    got, p = run(xd, None)
+    assert p.as_dict()["path"] == "rowtile"
+    compare(got, want)
+    g16, p16 = L.lse_forward16(xd)
+    assert p16.as_dict()["path"] == "subwarp"
+    compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
+    t = np.arange(x.shape[0], dtype=np.int64) % 5
+    lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
+    assert pl.as_dict()["path"] == "subwarp"
+    want_lp, want_lse = oracle.token_logprob(x, t, "f32")
+    compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
 
 
 def test_short_rows_both_mappings_full_size():

@@ -38,25 +38,29 @@ def _random_rows(rng, B, N, dtype):
     return x
 
 
-def _random_plan(rng, N, dtype, vec, rs):
+def _random_plan(rng, N, dtype, aligned, rs):
+    """A random plan: vector slots (rows off a 16-byte boundary peel a head and
+    a tail slot) or, one time in four, element slots."""
     eb = 4 if dtype == "f32" else 2
-    epv = 16 // eb if vec else 1
-    slots = N // epv if vec else N
-    nvt = -(-N // epv)
+    vb = 1 if rng.random() < 0.25 else 16
+    epv = 16 // eb if vb == 16 else 1
+    slots = N // epv
+    nvt = -(-N // epv) if aligned or vb == 1 else N // epv + 2
     choices = [None]
     if N > 0:
         if nvt <= 128:
             G = int(2 ** rng.integers(0, 6))
             if -(-nvt // G) <= 4:
-                choices.append({"path": "subwarp", "lanes_per_row": G})
+                choices.append({"path": "subwarp", "lanes_per_row": G, "vector_bytes": vb})
         elif nvt <= 256:
-            choices.append({"path": "subwarp", "lanes_per_row": 32})
+            choices.append({"path": "subwarp", "lanes_per_row": 32, "vector_bytes": vb})
         if slots >= 1:
-            choices.append({"path": "cta", "threads": int(32 * 2 ** rng.integers(0, 5))})
+            choices.append({"path": "cta", "threads": int(32 * 2 ** rng.integers(0, 5)),
+                            "vector_bytes": vb})
         if slots >= 2:
             choices.append({"path": "split", "splits": int(rng.integers(2, min(slots, 50) + 1)),
-                            "threads": int(32 * 2 ** rng.integers(0, 5))})
-        if vec and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
+                            "threads": int(32 * 2 ** rng.integers(0, 5)), "vector_bytes": vb})
+        if aligned and rs == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             choices.append({"path": "rowtile"})
     return choices[int(rng.integers(len(choices)))]
 
@@ -73,8 +77,8 @@ def test_random_forward_and_logprob(seed):
     x = _random_rows(rng, B, N, dtype)
     _, xv = device_rows(x, dtype, row_stride=rs, offset=off)
     eb = 4 if dtype == "f32" else 2
-    vec = xv.data_ptr() % 16 == 0 and (rs * eb) % 16 == 0
-    plan = _random_plan(rng, N, dtype, vec, rs)
+    aligned = xv.data_ptr() % 16 == 0 and (rs * eb) % 16 == 0
+    plan = _random_plan(rng, N, dtype, aligned, rs)
     want = oracle.lse(x, dtype)
     out = torch.full((B + 4,), float("nan"), device="cuda")
     try:

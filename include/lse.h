@@ -14,9 +14,12 @@
  *   x           device pointer (host pointer for lse_forward_host) to B rows;
  *               row b starts at element b * row_stride.  Elements are f32,
  *               bf16 or f16 (lse_dtype).  Read-only; not retained.
- *   row_stride  distance between row starts, in ELEMENTS, >= N.  Any
- *               alignment of x and row_stride is accepted; 16-byte aligned
- *               rows take the vectorised path.
+ *               x must be aligned to its element size (4 bytes for f32,
+ *               2 for bf16 and f16).
+ *   row_stride  distance between row starts, in ELEMENTS, >= N; any value.
+ *               Rows are read as 16-byte vectors; a row that does not start
+ *               on a 16-byte boundary reads its head and tail (< 16 bytes
+ *               each) element by element.
  *   out         device pointer (host pointer for lse_forward_host) to B
  *               floats, 4-byte aligned.  Written once per row; not retained.
  *   stream      CUDA stream for all work (0 = legacy default stream).  The
@@ -29,7 +32,7 @@
  *   lse_forward_host.
  *
  * Errors: every call returns an lse_status.  LSE_ERR_INVALID_ARG for B < 0,
- * N < 0, row_stride < N, a NULL x (N > 0) or out (B > 0), a misaligned out, or
+ * N < 0, row_stride < N, a NULL x (N > 0) or out (B > 0), a misaligned x or out, or
  * sizes whose byte extent overflows int64; LSE_ERR_UNSUPPORTED_DTYPE for an
  * unknown dtype; LSE_ERR_ALLOC when stream-ordered scratch cannot be
  * allocated; LSE_ERR_CUDA when a CUDA call fails (lse_last_cuda_error gives
@@ -80,10 +83,15 @@ typedef enum {
     LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
     LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: 2, 4 or 8 warps share the
                                   rows of one column tile                       */
-    LSE_PATH_ROWTILE = 7       /* short back-to-back rows (16..128 bytes, 16-byte
-                                  aligned): 32 KB chunks of rows streamed into
-                                  shared memory by bulk copies (TMA), one thread
-                                  per row; row value and token log-probability */
+    LSE_PATH_ROWTILE = 7       /* short back-to-back rows (<= 128 bytes) from a
+                                  16-byte aligned base: 32 KB chunks of rows
+                                  streamed into shared memory by bulk copies
+                                  (TMA), one thread per row.  Rows of 16..128
+                                  bytes in multiples of 16 (slots_per_lane =
+                                  vectors per row): row value and token
+                                  log-probability; rows of other widths
+                                  (slots_per_lane = 0, vector_bytes = 1): row
+                                  value with f32 exponentials only            */
 } lse_path;
 
 /*
@@ -93,7 +101,9 @@ typedef enum {
  */
 typedef struct {
     int32_t path;           /* lse_path                                              */
-    int32_t vector_bytes;   /* 16: 128-bit loads; 1: element loads (unaligned rows);
+    int32_t vector_bytes;   /* 16: 128-bit loads (a row that does not start on a
+                               16-byte boundary peels its head and tail into
+                               element loads); 1: element loads only;
                                0 in a request: let the library choose              */
     int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32;
                                column paths: warps sharing one column tile, 1/2/4/8 */

@@ -15,10 +15,14 @@
 // non-last dimension (lse_forward_strided), with lse and grad per column.
 //
 // Mapping: a CTA is TX x TY threads; TY rows, TX threads across a row, each
-// thread moving U = 4 slots (16-byte vectors, or single elements when rows are
-// not 16-byte aligned) per iteration with every load issued before any store.
-// blockIdx.x picks a segment of seg_slots slots of the row; rows beyond
-// gridDim.y * TY are covered by a grid-stride loop.
+// thread moving U = 4 slots per iteration with every load issued before any
+// store.  A slot is a 16-byte vector, or a single element when x and dx rows
+// do not share their offset from a 16-byte boundary.  With PEEL, rows that do
+// share it but do not start on a boundary read and write their head (the
+// elements before the first boundary) and their tail element by element, in
+// two more slots, and the rest as aligned vectors.  blockIdx.x picks a segment
+// of seg_slots slots of the row; rows beyond gridDim.y * TY are covered by a
+// grid-stride loop.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -76,8 +80,33 @@ __device__ __forceinline__ uint4 grad_vector(uint4 u, float lse, float g) {
     }
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kBwdThreads)
+// Elements of row `rp` before its first 16-byte boundary, at most N.
+template <int DT>
+__device__ __forceinline__ int64_t head_elems_of(const void* rp, int64_t N) {
+    const int64_t h = static_cast<int64_t>((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(rp)) & 15u)) & 15u) /
+                      DType<DT>::bytes;
+    return N < h ? N : h;
+}
+
+// The elements [i0, i0 + n) of a row, n < 16 / element bytes (a head or a
+// tail): every load issued before the first store, so the loads overlap and
+// dx may be x.
+template <int DT>
+__device__ __forceinline__ void grad_elems(const char* xr, char* dr, int64_t i0, int n,
+                                           float l, float g) {
+    constexpr int M = 16 / DType<DT>::bytes - 1;
+    float v[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (i < n) v[i] = load_elem<DT>(xr, i0 + i);
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (i < n) store_elem<DT>(dr, i0 + i, grad_term(v[i], l, g));
+}
+
+// At most 64 registers: 4 CTAs (32 warps) per SM.
+template <int DT, bool VEC, bool PEEL>
+__global__ void __launch_bounds__(kBwdThreads, 4)
 lse_backward_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                     const float* __restrict__ lse, const float* __restrict__ grad,
                     void* __restrict__ dx, int64_t dx_row_stride, int64_t seg_slots) {
@@ -86,11 +115,12 @@ lse_backward_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t ro
     pdl_trigger();
     pdl_wait();
     const int TX = blockDim.x;
-    const int64_t nv = N / EPV;            // full slots per row
-    const int tail = static_cast<int>(N - nv * EPV);
+    const int64_t nv0 = N / EPV;  // full slots of a row on a 16-byte boundary
+    const int tail0 = static_cast<int>(N - nv0 * EPV);
+    // Slots per row: full vectors, then the tail slot, then (PEEL) the head slot.
+    const int64_t nvt = PEEL ? nv0 + 2 : nv0 + (tail0 > 0 ? 1 : 0);
     const int64_t k_begin = static_cast<int64_t>(blockIdx.x) * seg_slots;
     int64_t k_end = k_begin + seg_slots;
-    const int64_t nvt = nv + (tail > 0 ? 1 : 0);
     if (k_end > nvt) k_end = nvt;
 
     for (int64_t row = static_cast<int64_t>(blockIdx.y) * blockDim.y + threadIdx.y; row < B;
@@ -99,24 +129,34 @@ lse_backward_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t ro
         const float g = __ldg(grad + row);
         const char* xr = reinterpret_cast<const char*>(x) + row * row_stride * EB;
         char* dr = reinterpret_cast<char*>(dx) + row * dx_row_stride * EB;
+        int head = 0;
+        int64_t nv = nv0;
+        int tail = tail0;
+        if constexpr (PEEL) {
+            head = static_cast<int>(head_elems_of<DT>(xr, N));
+            nv = (N - head) / EPV;
+            tail = static_cast<int>(N - head - nv * EPV);
+        }
+        const char* xv = xr + head * EB;  // 16-byte aligned, as is dv
+        char* dv = dr + head * EB;
         for (int64_t k = k_begin + threadIdx.x; k < k_end; k += static_cast<int64_t>(TX) * kBwdU) {
             if constexpr (VEC) {
                 uint4 v[kBwdU];
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     const int64_t kk = k + j * TX;
-                    if (kk < nv && kk < k_end) v[j] = ldg_stream16(xr + kk * 16);
+                    if (kk < nv && kk < k_end) v[j] = ldg_stream16(xv + kk * 16);
                 }
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     const int64_t kk = k + j * TX;
-                    if (kk < nv && kk < k_end) {
-                        __stcs(reinterpret_cast<uint4*>(dr + kk * 16), grad_vector<DT>(v[j], l, g));
-                    } else if (kk == nv && kk < k_end) {  // the < EPV tail elements
-                        for (int i = 0; i < tail; ++i)
-                            store_elem<DT>(dr, nv * EPV + i,
-                                           grad_term(load_elem<DT>(xr, nv * EPV + i), l, g));
-                    }
+                    if (kk >= k_end) continue;
+                    if (kk < nv)
+                        __stcs(reinterpret_cast<uint4*>(dv + kk * 16), grad_vector<DT>(v[j], l, g));
+                    else if (kk == nv && tail > 0)  // the < EPV tail elements
+                        grad_elems<DT>(xv, dv, nv * EPV, tail, l, g);
+                    else if (PEEL && kk == nv + (tail > 0 ? 1 : 0) && head > 0)  // the head
+                        grad_elems<DT>(xr, dr, 0, head, l, g);
                 }
             } else {
                 float v[kBwdU];
@@ -246,11 +286,11 @@ cudaError_t launch_backward_strided_t(const BackwardStridedArgs& a) {
 // Rows of at most kBwdU slots: the (row, slot) pairs are flattened and each
 // thread keeps kBwdU of them in flight (slot q, q + stride, ...), so
 // consecutive threads touch consecutive vectors whatever the row length.  A
-// slot is a 16-byte vector (VEC; the slot index nv of a row holds its < EPV
-// tail elements) or one element.  lse and grad are read per slot; a row's
-// slots share them in L1.
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kBwdThreads)
+// slot is a 16-byte vector (VEC; slot nv of a row holds its < EPV tail
+// elements and, with PEEL, the next one its head) or one element.  lse and
+// grad are read per slot; a row's slots share them in L1.
+template <int DT, bool VEC, bool PEEL>
+__global__ void __launch_bounds__(kBwdThreads, PEEL ? 3 : 4)
 lse_backward_small_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride,
                           const float* __restrict__ lse, const float* __restrict__ grad,
                           void* __restrict__ dx, int64_t dx_row_stride) {
@@ -258,30 +298,35 @@ lse_backward_small_kernel(const void* __restrict__ x, int64_t B, int64_t N, int6
     constexpr int EPV = VEC ? 16 / EB : 1;
     pdl_trigger();
     pdl_wait();
-    const int64_t nv = N / EPV;
-    const int tail = static_cast<int>(N - nv * EPV);
-    const int64_t nvt = nv + (tail > 0 ? 1 : 0);  // slots per row, <= kBwdU
+    const int nv0 = static_cast<int>(N / EPV);  // full slots of a row on a 16-byte boundary
+    const int tail0 = static_cast<int>(N - static_cast<int64_t>(nv0) * EPV);
+    const int nvt = PEEL ? nv0 + 2 : nv0 + (tail0 > 0 ? 1 : 0);  // slots per row (a few)
     const int64_t slots = B * nvt;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const char* xb = reinterpret_cast<const char*>(x);
     char* db = reinterpret_cast<char*>(dx);
     for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q0 < slots;
          q0 += stride * kBwdU) {
-        int64_t row[kBwdU], k[kBwdU];
+        int64_t row[kBwdU];
+        int k[kBwdU], head[kBwdU];
         float l[kBwdU], g[kBwdU];
         uint4 v[kBwdU];
 #pragma unroll
         for (int j = 0; j < kBwdU; ++j) {
             const int64_t q = q0 + j * stride;
             row[j] = q < slots ? q / nvt : -1;
-            k[j] = q - row[j] * nvt;
+            k[j] = static_cast<int>(q - row[j] * nvt);
+            head[j] = 0;
             if (row[j] >= 0) {
                 l[j] = __ldg(lse + row[j]);
                 g[j] = __ldg(grad + row[j]);
+                const char* xr = xb + row[j] * row_stride * EB;
                 if constexpr (VEC) {
-                    if (k[j] < nv) v[j] = ldg_stream16(xb + (row[j] * row_stride + k[j] * EPV) * EB);
+                    if constexpr (PEEL) head[j] = static_cast<int>(head_elems_of<DT>(xr, N));
+                    const int nv = PEEL ? static_cast<int>((N - head[j]) / EPV) : nv0;
+                    if (k[j] < nv) v[j] = ldg_stream16(xr + head[j] * EB + k[j] * 16);
                 } else {
-                    v[j].x = __float_as_uint(load_elem<DT>(xb + row[j] * row_stride * EB, k[j]));
+                    v[j].x = __float_as_uint(load_elem<DT>(xr, k[j]));
                 }
             }
         }
@@ -290,15 +335,16 @@ lse_backward_small_kernel(const void* __restrict__ x, int64_t B, int64_t N, int6
             if (row[j] < 0) continue;
             char* dr = db + row[j] * dx_row_stride * EB;
             if constexpr (VEC) {
-                if (k[j] < nv) {
-                    __stcs(reinterpret_cast<uint4*>(dr + k[j] * EPV * EB),
+                const char* xr = xb + row[j] * row_stride * EB;
+                const int nv = PEEL ? static_cast<int>((N - head[j]) / EPV) : nv0;
+                const int tail = PEEL ? static_cast<int>(N - head[j] - nv * EPV) : tail0;
+                if (k[j] < nv)
+                    __stcs(reinterpret_cast<uint4*>(dr + head[j] * EB + k[j] * 16),
                            grad_vector<DT>(v[j], l[j], g[j]));
-                } else {  // the < EPV tail elements
-                    const char* xr = xb + row[j] * row_stride * EB;
-                    for (int i = 0; i < tail; ++i)
-                        store_elem<DT>(dr, nv * EPV + i,
-                                       grad_term(load_elem<DT>(xr, nv * EPV + i), l[j], g[j]));
-                }
+                else if (k[j] == nv && tail > 0)  // the < EPV tail elements
+                    grad_elems<DT>(xr, dr, head[j] + nv * EPV, tail, l[j], g[j]);
+                else if (PEEL && k[j] == nv + (tail > 0 ? 1 : 0) && head[j] > 0)  // the head
+                    grad_elems<DT>(xr, dr, 0, head[j], l[j], g[j]);
             } else {
                 store_elem<DT>(dr, k[j], grad_term(__uint_as_float(v[j].x), l[j], g[j]));
             }
@@ -306,32 +352,132 @@ lse_backward_small_kernel(const void* __restrict__ x, int64_t B, int64_t N, int6
     }
 }
 
-template <int DT, bool VEC>
-cudaError_t launch_backward_small_t(const BackwardArgs& a) {
-    return launch_pdl(lse_backward_small_kernel<DT, VEC>, a.grid, a.block, a.stream, a.x, a.B,
-                      a.N, a.row_stride, a.lse, a.grad, a.dx, a.dx_row_stride);
+// One 16-byte vector whose elements [0, sp) belong to one row (l0, g0) and
+// [sp, EPV) to the next (l1, g1).
+template <int DT>
+__device__ __forceinline__ uint4 grad_vector_split(uint4 u, int sp, float l0, float g0, float l1,
+                                                   float g1) {
+    if constexpr (DT == kF32) {
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o[e] = __float_as_uint(grad_term(__uint_as_float(in[e]), e < sp ? l0 : l1,
+                                             e < sp ? g0 : g1));
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 2 * i;
+            o[i] = pack2<DT>(grad_term(word_lo<DT>(in[i]), e < sp ? l0 : l1, e < sp ? g0 : g1),
+                             grad_term(word_hi<DT>(in[i]), e + 1 < sp ? l0 : l1,
+                                       e + 1 < sp ? g0 : g1));
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
-template <int DT, bool VEC>
-cudaError_t launch_backward_t(const BackwardArgs& a) {
-    return launch_pdl(lse_backward_kernel<DT, VEC>, a.grid, a.block, a.stream, a.x, a.B, a.N,
+constexpr int kFlatU = 4;  // vectors in flight per thread in the flat backward
+
+// Back-to-back rows of x and dx (row stride N for both) at the same offset
+// from a 16-byte boundary, N >= EPV: the [B, N] block is one flat array of
+// B*N elements streamed as 16-byte vectors, whatever N is; the < EPV elements
+// before the array's first boundary (all in row 0) and after its last one
+// (all in row B - 1) are done element by element.  A vector holds elements of
+// at most two rows.  One wave of CTAs strides through the vectors; each
+// thread finds the row and in-row offset of its first vector with one
+// division and then steps them by the stride incrementally.
+// kFlatU vectors are in flight per thread, all loads before any store, so dx
+// may be x.
+template <int DT>
+__global__ void __launch_bounds__(kBwdThreads, 4)
+lse_backward_flat_kernel(const void* __restrict__ x, int64_t B, int64_t N,
+                         const float* __restrict__ lse, const float* __restrict__ grad,
+                         void* __restrict__ dx) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = 16 / EB;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t total = B * N;
+    const int64_t head = head_elems_of<DT>(x, total);
+    const int64_t nvec = (total - head) / EPV;
+    const int tail = static_cast<int>(total - head - nvec * EPV);
+    const char* xv = reinterpret_cast<const char*>(x) + head * EB;  // 16-byte aligned, as is dv
+    char* dv = reinterpret_cast<char*>(dx) + head * EB;
+    const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t == 0) {
+        if (head > 0) grad_elems<DT>(reinterpret_cast<const char*>(x), reinterpret_cast<char*>(dx),
+                                     0, static_cast<int>(head), __ldg(lse), __ldg(grad));
+        if (tail > 0) grad_elems<DT>(reinterpret_cast<const char*>(x), reinterpret_cast<char*>(dx),
+                                     total - tail, tail, __ldg(lse + B - 1), __ldg(grad + B - 1));
+    }
+    int64_t row = (head + t * EPV) / N;
+    int64_t off = head + t * EPV - row * N;
+    const int64_t qS = T * EPV / N;
+    const int64_t rS = T * EPV - qS * N;  // a stride of T vectors: qS rows and rS elements
+    for (int64_t v = t; v < nvec; v += kFlatU * T) {
+        uint4 u[kFlatU];
+        float l0[kFlatU], g0[kFlatU], l1[kFlatU], g1[kFlatU];
+        int sp[kFlatU];
+#pragma unroll
+        for (int j = 0; j < kFlatU; ++j) {
+            const int64_t vj = v + j * T;
+            if (vj < nvec) {
+                u[j] = ldg_stream16(xv + vj * 16);
+                sp[j] = off + EPV > N ? static_cast<int>(N - off) : EPV;
+                l0[j] = __ldg(lse + row);
+                g0[j] = __ldg(grad + row);
+                l1[j] = sp[j] < EPV ? __ldg(lse + row + 1) : l0[j];
+                g1[j] = sp[j] < EPV ? __ldg(grad + row + 1) : g0[j];
+            }
+            row += qS;
+            off += rS;
+            if (off >= N) {
+                off -= N;
+                ++row;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kFlatU; ++j) {
+            const int64_t vj = v + j * T;
+            if (vj < nvec)
+                __stcs(reinterpret_cast<uint4*>(dv + vj * 16),
+                       grad_vector_split<DT>(u[j], sp[j], l0[j], g0[j], l1[j], g1[j]));
+        }
+    }
+}
+
+template <int DT, bool VEC, bool PEEL>
+cudaError_t launch_backward_dt(const BackwardArgs& a) {
+    if (a.small)
+        return launch_pdl(lse_backward_small_kernel<DT, VEC, PEEL>, a.grid, a.block, a.stream, a.x,
+                          a.B, a.N, a.row_stride, a.lse, a.grad, a.dx, a.dx_row_stride);
+    return launch_pdl(lse_backward_kernel<DT, VEC, PEEL>, a.grid, a.block, a.stream, a.x, a.B, a.N,
                       a.row_stride, a.lse, a.grad, a.dx, a.dx_row_stride, a.seg_slots);
+}
+
+template <int DT>
+cudaError_t launch_backward_mode(int mode, const BackwardArgs& a) {
+    switch (mode) {
+    case kBwdFlat:
+        return launch_pdl(lse_backward_flat_kernel<DT>, a.grid, a.block, a.stream, a.x, a.B, a.N,
+                          a.lse, a.grad, a.dx);
+    case kBwdVector: return launch_backward_dt<DT, true, false>(a);
+    case kBwdPeel: return launch_backward_dt<DT, true, true>(a);
+    default: return launch_backward_dt<DT, false, false>(a);
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a) {
-    if (a.small) {
-        switch (dt) {
-        case kF32: return vec ? launch_backward_small_t<kF32, true>(a) : launch_backward_small_t<kF32, false>(a);
-        case kBF16: return vec ? launch_backward_small_t<kBF16, true>(a) : launch_backward_small_t<kBF16, false>(a);
-        default: return vec ? launch_backward_small_t<kF16, true>(a) : launch_backward_small_t<kF16, false>(a);
-        }
-    }
+cudaError_t launch_backward(int dt, int mode, const BackwardArgs& a) {
     switch (dt) {
-    case kF32: return vec ? launch_backward_t<kF32, true>(a) : launch_backward_t<kF32, false>(a);
-    case kBF16: return vec ? launch_backward_t<kBF16, true>(a) : launch_backward_t<kBF16, false>(a);
-    default: return vec ? launch_backward_t<kF16, true>(a) : launch_backward_t<kF16, false>(a);
+    case kF32: return launch_backward_mode<kF32>(mode, a);
+    case kBF16: return launch_backward_mode<kBF16>(mode, a);
+    default: return launch_backward_mode<kF16>(mode, a);
     }
 }
 
@@ -350,5 +496,6 @@ cudaError_t launch_backward_strided(int dt, bool vec, const BackwardStridedArgs&
 int backward_strided_warps() { return kStrWarps; }
 int backward_slots_per_thread() { return kBwdU; }
 int backward_threads() { return kBwdThreads; }
+int backward_flat_vectors_per_thread() { return kFlatU; }
 
 }  // namespace lse

@@ -100,7 +100,12 @@ struct BackwardArgs {
     dim3 block;
     cudaStream_t stream;
 };
-cudaError_t launch_backward(int dt, bool vec, const BackwardArgs& a);
+// Slots of the row backward: elements (x and dx rows at different offsets
+// from a 16-byte boundary), 16-byte vectors (every row on a boundary),
+// vectors with each row's head and tail peeled into element slots, or (flat)
+// back-to-back rows streamed as one array of vectors that may span two rows.
+enum BackwardMode { kBwdScalar = 0, kBwdVector = 1, kBwdPeel = 2, kBwdFlat = 3 };
+cudaError_t launch_backward(int dt, int mode, const BackwardArgs& a);
 // Backward of the value over a non-last dimension (lse_backward.cu).
 struct BackwardStridedArgs {
     const void* x;
@@ -123,6 +128,7 @@ cudaError_t launch_backward_strided(int dt, bool vec, const BackwardStridedArgs&
 int backward_strided_warps();
 int backward_slots_per_thread();
 int backward_threads();
+int backward_flat_vectors_per_thread();
 
 // Strided / column reduction (lse_strided.cu).
 struct StridedArgs {

@@ -103,15 +103,19 @@ extern "C" lse_status lse_forward_split_static(const void* x, lse_dtype dtype, i
     if (B == 0) return LSE_OK;
     if (x == nullptr || out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
         return LSE_ERR_INVALID_ARG;
-    if (B > kScratchPartials / 2) return LSE_ERR_INVALID_ARG;  // needs >= 2 partials per row
     const int eb = dtype == LSE_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(eb) != 0) return LSE_ERR_INVALID_ARG;
+    if (B > kScratchPartials / 2) return LSE_ERR_INVALID_ARG;  // needs >= 2 partials per row
     int64_t extent = 0;
     if (__builtin_mul_overflow(B - 1, row_stride, &extent) ||
         __builtin_add_overflow(extent, N, &extent) ||
         __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &extent))
         return LSE_ERR_INVALID_ARG;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) % 16u == 0) && ((row_stride * eb) % 16 == 0);
-    const int64_t slots = vec ? N / (16 / eb) : N;  // segments cover these; the tail rides along
+    // 16-byte vectors; rows off a 16-byte boundary peel their head and tail
+    // into element loads, unless they hold fewer than two vectors.
+    const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16u == 0) && ((row_stride * eb) % 16 == 0);
+    const bool vec = aligned || N / (16 / eb) >= 2;
+    const int64_t slots = vec ? N / (16 / eb) : N;  // segments cover these; head and tail ride along
     if (slots < 2) return LSE_ERR_INVALID_ARG;     // too short to split
 
     const StaticScratch* s = nullptr;

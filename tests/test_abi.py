@@ -70,6 +70,8 @@ def test_status_strings(lib):
     ((0, 0, 4, 8, 8, 16), 1),              # x NULL with work to do
     ((16, 0, 4, 8, 8, 0), 1),              # out NULL
     ((16, 0, 4, 8, 8, 18), 1),             # out not 4-byte aligned
+    ((18, 0, 4, 8, 8, 16), 1),             # f32 x not element aligned
+    ((17, 1, 4, 8, 8, 16), 1),             # bf16 x not element aligned
     ((16, 3, 4, 8, 8, 16), 2),             # unknown dtype
     ((16, 0, 1 << 40, 1 << 30, 1 << 30, 16), 1),  # byte extent overflows int64
 ])
@@ -113,3 +115,19 @@ def test_backward_strided_bad_arguments_rejected_before_cuda(lib, args, status):
 def test_backward_strided_empty_is_ok_without_device(lib):
     assert lib.lse_backward_strided(None, 0, 0, 3, 4, 12, 4, None, None, None, 12, 4, None) == 0
     assert lib.lse_backward_strided(None, 0, 2, 0, 4, 0, 4, None, None, None, 0, 4, None) == 0
+
+
+@pytest.mark.parametrize("dt,x", [(0, 18), (0, 17), (1, 17), (2, 33)])
+def test_misaligned_x_rejected_before_cuda(lib, dt, x):
+    """Every load is at least one whole element: an x that is not element
+    aligned is refused by every entry point, before any device work."""
+    B, N, out, t, lp = 4, 8, 256, 512, 1024
+    assert lib.lse_forward(x, dt, B, N, N, out, None) == 1
+    assert lib.lse_forward_host(x, dt, B, N, N, out, None) == 1
+    assert lib.lse_forward_plan(x, dt, B, N, N, out, None, None, None, None) == 1
+    assert lib.lse_forward16(x, dt, B, N, N, out, None, None) == 1
+    assert lib.lse_forward_split_static(x, dt, B, N, N, out, None) == 1
+    assert lib.lse_token_logprob(x, dt, B, N, N, t, lp, None, None) == 1
+    assert lib.lse_backward(x, dt, B, N, N, out, out, 2048, N, None) == 1
+    assert lib.lse_forward_strided(x, dt, 2, 3, N, 3 * N, N, out, None, None) == 1
+    assert lib.lse_backward_strided(x, dt, 2, 3, N, 3 * N, N, out, out, 2048, 3 * N, N, None) == 1

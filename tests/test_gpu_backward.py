@@ -105,8 +105,15 @@ def test_backward_edge_shapes(dtype, N):
         xi[4, ::2] = ninf         # zeros in the gradient
     g = np.random.default_rng(N).normal(0, 3, B)
     g[5] = 0.0
+    eb = 4 if dtype == "f32" else 2
+    # Element slots where x and dx rows sit at different offsets from a 16-byte
+    # boundary; vectors with a peeled head and tail where they share it.
     layouts = [dict(), dict(row_stride=N + 8, dx_row_stride=N + 8), dict(row_stride=N + 3),
-               dict(offset=1), dict(dx_offset=1), dict(inplace=True)]
+               dict(offset=1), dict(dx_offset=1), dict(inplace=True),
+               dict(offset=1, dx_offset=1), dict(row_stride=N + 3, dx_row_stride=N + 3),
+               dict(offset=3, dx_offset=3 + 16 // eb, row_stride=N + 1,
+                    dx_row_stride=N + 1 + 16 // eb),
+               dict(inplace=True, offset=1, row_stride=N + 1)]
     for lay in layouts:
         got, lse64, want = _run(x, dtype, g, **lay)
         try:
@@ -130,3 +137,50 @@ def test_backward_tensor_api_and_bad_args():
     with pytest.raises(L.LseError):
         L.lse_backward_ptr(x.data_ptr(), "f32", 8, 100, 100, lse.data_ptr(), g.data_ptr(),
                            dx.data_ptr() + 2, 100)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_backward_random_layouts(seed):
+    """Random dtype, shape, offsets and strides of x and dx: element slots,
+    16-byte vectors, or vectors with a peeled head and tail, against the
+    oracle, with nothing written outside dx's rows."""
+    _need_gpu()
+    rng = np.random.default_rng(7000 + seed)
+    dtype = ["f32", "bf16", "f16"][seed % 3]
+    N = int(np.exp(rng.uniform(0, np.log(30000))))
+    B = int(rng.integers(1, 64)) if N > 256 else int(rng.integers(1, 3000))
+    off = int(rng.choice([0, 1, 2, 5]))
+    rs = N + int(rng.choice([0, 0, 1, 3, 8]))
+    if rng.random() < 0.5:  # dx at the same offset from a 16-byte boundary as x
+        eb = 4 if dtype == "f32" else 2
+        lay = dict(offset=off, row_stride=rs, dx_offset=off + int(rng.choice([0, 16 // eb])),
+                   dx_row_stride=rs + int(rng.choice([0, 16 // eb])))
+    else:
+        lay = dict(offset=off, row_stride=rs, dx_offset=int(rng.choice([0, 1, 3])),
+                   dx_row_stride=N + int(rng.choice([0, 1, 2])))
+    x = wl.random_rows(B, N, dtype, seed=int(rng.integers(1 << 30)),
+                       scale=float(rng.choice([0.5, 4.0, 20.0])))
+    g = rng.normal(0, 2, B)
+    got, lse64, want = _run(x, dtype, g, **lay)
+    try:
+        _check(got, x, dtype, lse64, g, want)
+    except AssertionError as e:
+        raise AssertionError(f"B={B} N={N} layout {lay}: {e}") from None
+
+
+@pytest.mark.parametrize("dtype,B,N,off", [("bf16", 100003, 37, 0), ("f32", 30001, 129, 1),
+                                           ("f16", 4099, 1001, 3), ("f32", 3, 8, 1),
+                                           ("bf16", 1, 8, 5)])
+def test_backward_flat_rows(dtype, B, N, off):
+    """Back-to-back rows whose starts are not all on a 16-byte boundary: the
+    whole block streamed as one array of vectors spanning row ends, with many
+    CTAs striding through it (and in place)."""
+    _need_gpu()
+    x = wl.random_rows(B, N, dtype, seed=B + N, scale=6.0)
+    g = np.random.default_rng(N).normal(0, 2, B)
+    for lay in (dict(offset=off, dx_offset=off), dict(inplace=True, offset=off)):
+        got, lse64, want = _run(x, dtype, g, **lay)
+        try:
+            _check(got, x, dtype, lse64, g, want)
+        except AssertionError as e:
+            raise AssertionError(f"layout {lay}: {e}") from None

@@ -66,9 +66,9 @@ __device__ __forceinline__ int head_elems(const void* row, int64_t N) {
 // not start on a 16-byte boundary peels its head (< EPV elements) and tail
 // (< EPV elements) into two more slots: slot nv holds the tail, the slot after
 // it the head (nv = full vectors of that row).  !VEC: a slot is one element.
-// V = 8 (only
-// with G = 32: a whole warp per row of up to 256 slots) keeps 32 words per
-// lane and runs at 4 CTAs per SM.
+// V = 8 (a whole warp per row of up to 256 slots, or 4-16 lanes per row of
+// vectors: twice the rows in flight of V = 4 with half the lanes) keeps 32
+// words per lane and runs at 4 CTAs per SM.
 // ---------------------------------------------------------------------------
 // The token log-probability epilogue keeps the targets and the peel state of
 // every row group live: one CTA per SM less, so it does not spill.
@@ -386,8 +386,8 @@ cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL, E16>(a, grid);
     case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL, E16>(a, grid);
     case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL, E16>(a, grid);
-    case 8:
-        if constexpr (G == 32) return launch_subwarp_gv<DT, G, 8, VEC, TL, E16>(a, grid);
+    case 8:  // a whole warp per row, or 4-16 lanes per row of 16-byte vectors
+        if constexpr (G == 32 || (VEC && G >= 4)) return launch_subwarp_gv<DT, G, 8, VEC, TL, E16>(a, grid);
         else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }

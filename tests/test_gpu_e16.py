@@ -145,7 +145,7 @@ def _plans(rng, N, dtype, aligned, rs):
     out = [None]
     if nvt <= 128:
         G = int(2 ** rng.integers(0, 6))
-        if -(-nvt // G) <= 4:
+        if -(-nvt // G) <= 4 or (G >= 4 and -(-nvt // G) <= 8):
             out.append({"path": "subwarp", "lanes_per_row": G})
     elif nvt <= 256:
         out.append({"path": "subwarp", "lanes_per_row": 32})

@@ -98,6 +98,8 @@ def test_logprob_edge_shapes(dtype, N):
                       if -(-nvt // G) <= 4]
         elif nvt <= 256:
             plans.append({"path": "subwarp", "lanes_per_row": 32})
+        plans += [{"path": "subwarp", "lanes_per_row": G} for G in (4, 8, 16)
+                  if 4 < -(-nvt // G) <= 8]  # 8 vectors per lane
         if aligned and row_stride == N and N * eb % 16 == 0 and 16 <= N * eb <= 128:
             plans.append({"path": "rowtile"})
         if not aligned:

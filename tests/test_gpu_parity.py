@@ -77,6 +77,10 @@ def plans_for(N, dtype, vec, aligned=True):
             G *= 2
     if 4 < -(-nvt // 32) <= 8:  # a whole warp per row, up to 8 slots per lane
         plans.append({"path": "subwarp", "lanes_per_row": 32, "vector_bytes": vb})
+    if vec:  # 4-16 lanes per row with 8 vectors each
+        for G in (4, 8, 16):
+            if 4 < -(-nvt // G) <= 8:
+                plans.append({"path": "subwarp", "lanes_per_row": G, "vector_bytes": vb})
     if slots >= 1:
         for T in (32, 64, 128, 256, 512):
             plans.append({"path": "cta", "threads": T, "vector_bytes": vb})

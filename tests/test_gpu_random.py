@@ -50,7 +50,7 @@ def _random_plan(rng, N, dtype, aligned, rs):
     if N > 0:
         if nvt <= 128:
             G = int(2 ** rng.integers(0, 6))
-            if -(-nvt // G) <= 4:
+            if -(-nvt // G) <= 4 or (vb == 16 and G >= 4 and -(-nvt // G) <= 8):
                 choices.append({"path": "subwarp", "lanes_per_row": G, "vector_bytes": vb})
         elif nvt <= 256:
             choices.append({"path": "subwarp", "lanes_per_row": 32, "vector_bytes": vb})

@@ -136,6 +136,30 @@ int pow2_ceil(int64_t v) {
     return p;
 }
 
+// Lanes per row of the automatic sub-warp plan for rows of nvt slots: the
+// fewest that keep <= kSubwarpMaxSlots slots per lane (four independent loads
+// per thread), at most a warp.  Vector rows of more than 16 slots take half
+// the lanes with 8 slots each, so a warp holds twice the rows: measured on
+// 256 MB of rows of 65-1024 elements (f32, bf16; aligned and peeled), faster
+// for every length, +1-11 % on full groups, up to +40 % where a row fills
+// half its slots.
+int subwarp_auto_lanes(int64_t nvt, bool vec) {
+    int G = pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
+    if (G > 32) G = 32;
+    if (vec && nvt > 4 * kSubwarpMaxSlots) {
+        G = pow2_ceil(ceil_div(nvt, kSubwarpWarpSlots));
+        if (G < 4) G = 4;
+    }
+    return G;
+}
+
+// Slots per row (lanes x slots per lane, padded to a power of two) of that plan.
+int64_t subwarp_auto_slots(int64_t nvt, bool vec) {
+    const int G = subwarp_auto_lanes(nvt, vec);
+    const int64_t V = ceil_div(nvt, G);
+    return G * (V <= 1 ? 1 : (V <= 2 ? 2 : (V <= 4 ? 4 : 8)));
+}
+
 // Fill in (or check) a plan.  `req` may be null (automatic).
 lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t row_stride,
                      const DeviceInfo& info, const lse_plan* req, bool with_logprob,
@@ -200,27 +224,56 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     // sub-warp mapping (with the head peel) on every such width but f32 rows
     // of 7, where the two are even.
     const bool rowtile_any_ok = !rowtile_ok && !with_logprob && !e16 && row_stride == N &&
-                                row_bytes <= 128 &&
+                                row_bytes <= rowtile_any_max_row_bytes() &&
                                 reinterpret_cast<uintptr_t>(x) % 16u == 0 &&
-                                (!req || req->vector_bytes != 16);
+                                (!req || req->vector_bytes == 0 ||
+                                 req->vector_bytes == (row_bytes <= 128 ? 1 : 16));
+    // Lanes per row of that ring: one thread per row up to 128 bytes, else a
+    // group of 4-32 lanes, the largest power of two giving each lane >= 8 of
+    // the row's 16-byte vectors (f32) or >= 16 (16-bit): the best group size
+    // measured for rows of 129 bytes to 4 KB.
+    int any_lanes = 1;
+    if (row_bytes > 128) {
+        const int64_t per_lane = eb == 4 ? 8 : 16;
+        any_lanes = 4;
+        while (any_lanes < 32 && ceil_div(row_bytes, 16) >= 2 * any_lanes * per_lane) any_lanes *= 2;
+    }
     if (path == LSE_PATH_AUTO) {
         const int64_t chunk_rows = rowtile_ok ? rowtile_rows_per_chunk(static_cast<int>(row_bytes / 16)) : 1;
         const int64_t any_rows =
             rowtile_any_ok ? rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)) : 1;
         if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
-        else if (rowtile_any_ok && B >= any_rows * info.sms * rowtile_ctas_per_sm())
+        else if (rowtile_any_ok && row_bytes <= 128 && B >= any_rows * info.sms * rowtile_ctas_per_sm())
+            path = LSE_PATH_ROWTILE;
+        // Back-to-back rows of more than 512 bytes take the grouped ring where
+        // the sub-warp mapping would leave more than a third of its slots empty
+        // (a row just past a power of two of slots) or cannot hold them:
+        // measured 1.1-1.5x there (f32 N = 129: 4.0 -> 6.0 TB/s, N = 520:
+        // 5.5 -> 6.1; bf16 N = 260: 3.5 -> 4.4, N = 1020: 3.5 -> 5.1, N = 2047:
+        // 3.5 -> 4.6), 0.85-0.95x where the sub-warp slots are full, and
+        // mixed below 512 bytes (f32 N = 65: 1.29x, N = 68: 0.91x; bf16
+        // N = 150: 0.94x).
+        else if (rowtile_any_ok && row_bytes > 512 && B >= any_rows * info.sms * rowtile_ctas_per_sm() &&
+                 (nvt > sub_capacity || 3 * nvt < 2 * subwarp_auto_slots(nvt, vec)))
             path = LSE_PATH_ROWTILE;
         else
             path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
     }
     if (path == LSE_PATH_ROWTILE && !rowtile_ok && rowtile_any_ok) {
+        if (req && req->lanes_per_row) {
+            const int L = req->lanes_per_row;
+            if (row_bytes <= 128 ? L != 1 : (L < 4 || L > 32 || (L & (L - 1)) != 0))
+                return LSE_ERR_INVALID_ARG;
+            any_lanes = L;
+        }
         const int64_t chunks = ceil_div(B, rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)));
         int64_t grid = static_cast<int64_t>(info.sms) * rowtile_ctas_per_sm();
         if (grid > chunks) grid = chunks;
         if (grid < 1) grid = 1;
         p.path = LSE_PATH_ROWTILE;
-        p.vector_bytes = 1;
+        p.vector_bytes = row_bytes <= 128 ? 1 : 16;
+        p.lanes_per_row = any_lanes;
         p.threads = 256;
         p.slots_per_lane = 0;  // any row width
         p.splits = 1;
@@ -247,23 +300,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
 
     if (path == LSE_PATH_SUBWARP) {
         if (nvt > sub_capacity) return LSE_ERR_INVALID_ARG;
-        // Fewest lanes per row that keep <= kSubwarpMaxSlots slots per lane:
-        // four independent 16-byte loads per thread (V * R = 4 in the kernel).
-        // Rows of more than 32 * 4 slots take a whole warp with up to 8 each.
-        int G = req && req->lanes_per_row ? req->lanes_per_row : 0;
-        if (G == 0) {
-            G = pow2_ceil(ceil_div(nvt, kSubwarpMaxSlots));
-            if (G > 32) G = 32;
-            // Vector rows of more than 16 slots: half the lanes, 8 slots each,
-            // so a warp holds twice the rows.  Measured on 256 MB of rows of
-            // 65-1024 elements (f32, bf16; aligned and peeled): faster for every
-            // length, +1-11 % on full groups, up to +40 % where a row fills
-            // half its slots.
-            if (vec && nvt > 4 * kSubwarpMaxSlots) {
-                G = pow2_ceil(ceil_div(nvt, kSubwarpWarpSlots));
-                if (G < 4) G = 4;
-            }
-        }
+        int G = req && req->lanes_per_row ? req->lanes_per_row : subwarp_auto_lanes(nvt, vec);
         if (G < 1 || G > 32 || (G & (G - 1)) != 0) return LSE_ERR_INVALID_ARG;
         int64_t V = ceil_div(nvt, G);
         const bool wide = G == 32 || (vec && G >= 4);  // groups that may hold 8 slots per lane
@@ -524,7 +561,7 @@ lse_status run_forward(const void* x, lse_dtype dtype, int64_t B, int64_t N, int
         e = launch_subwarp(dtype, a, p.vector_bytes == 16, p.lanes_per_row, p.slots_per_lane, p.grid);
         break;
     case LSE_PATH_ROWTILE:
-        e = launch_rowtile(dtype, p.slots_per_lane, a, static_cast<int>(p.grid));
+        e = launch_rowtile(dtype, p.slots_per_lane, p.lanes_per_row, a, static_cast<int>(p.grid));
         break;
     default:
         e = launch_segment(dtype, a, p.vector_bytes == 16, p.threads, p.splits, p.segment_slots,

@@ -158,10 +158,12 @@ int cols_warps_per_cta(int warps_per_tile);
 // Reads a.x, a.B, a.out, a.tl (token log-probability) and a.e16 (reduced-bit
 // exponentials; not together with a.tl).  nv = 1..8 vectors per row, or 0 for
 // rows of any width up to 128 bytes (a.N elements; row value only).
-cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid);
+// nv 0: rows of any width; lanes per row 1 (rows of <= 128 bytes) or 4..32.
+cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid);
 int rowtile_ctas_per_sm();
 int rowtile_rows_per_chunk(int nv);
-int rowtile_any_rows_per_chunk(int row_bytes);  // nv == 0: rows of any width <= 128 bytes
+int rowtile_any_rows_per_chunk(int row_bytes);  // nv == 0: rows of any width
+int rowtile_any_max_row_bytes();
 cudaError_t read_wait_timeouts(unsigned long long* count);
 
 // Sets the calling thread's error reported by lse_last_cuda_error.

@@ -15,6 +15,13 @@
 // lse[row]: each thread loads its rows' targets before the chunk lands and
 // reads the target element from the staged row in shared memory.
 //
+// Rows of other widths (not a multiple of 16 bytes, or longer than 128 bytes,
+// up to 4 KB) take the same ring with chunks that start and end on 16-byte
+// boundaries; each thread folds its rows with element reads from shared
+// memory (rows of <= 128 bytes), or a group of G lanes folds each row from
+// 16-byte reads of the staged chunk, masking the elements of the neighbouring
+// rows that share the row's first and last vectors.
+//
 // Waits are bounded: a stage that does not complete within kWaitPolls polls
 // counts a timeout in a device counter (read by lse_wait_timeouts), the whole
 // CTA stops, waits (also bounded) for its own copies still in flight, and
@@ -33,6 +40,7 @@ constexpr int kTileThreads = 256;
 constexpr int kChunkBytes = 32 * 1024;  // per stage
 constexpr int kStages = 2;
 constexpr uint32_t kWaitPolls = 1u << 26;
+constexpr int kAnyThreadRowBytes = 128;  // any-width rows up to this: one thread per row
 
 __device__ unsigned long long g_wait_timeouts;
 
@@ -204,24 +212,47 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
     }
 }
 
-// Back-to-back rows of any width RB = N * elem <= 128 bytes that is not a
-// multiple of 16 (row value only).  Chunks hold CR = 256 * floor(32 KB / (256
-// * RB)) rows, a multiple of 16, so every chunk starts and ends on a 16-byte
-// boundary as long as it has a multiple of k = 16 / gcd(RB, 16) rows: the
-// copies cover the first Bm = B - B % k rows, and the < k rows after them are
-// read from global memory by CTA 0 at the end.  A thread folds each of its
-// rows straight from shared memory (max, then the exp-sum) before the stage
-// is released for the next copy.
+// The words of one 16-byte vector staged at byte vb of a chunk, with every
+// element outside the row's bytes [rb0, rb1) replaced by -inf.
 template <int DT>
+__device__ __forceinline__ void mask_words(uint32_t (&w)[4], uint32_t vb, uint32_t rb0,
+                                           uint32_t rb1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = vb + 4u * i;
+        if constexpr (DT == kF32) {
+            if (b < rb0 || b >= rb1) w[i] = kNegInfF32;
+        } else {
+            const uint32_t ninf = neg_inf_word<DT>();  // -inf in both halves
+            const uint32_t lo = (b < rb0 || b >= rb1) ? (ninf & 0xffffu) : (w[i] & 0xffffu);
+            const uint32_t hi = (b + 2 < rb0 || b + 2 >= rb1) ? (ninf & 0xffff0000u) : (w[i] & 0xffff0000u);
+            w[i] = lo | hi;
+        }
+    }
+}
+
+// Back-to-back rows whose width RB = N * elem bytes is not a multiple of 16
+// or is above 128 bytes (up to kChunkBytes / 8; row value only).  A chunk of
+// CR rows starts and ends on a 16-byte boundary as long as CR is a multiple of
+// k = 16 / gcd(RB, 16): the copies cover the first Bm = B - B % k rows, and
+// the < k rows after them are read from global memory by CTA 0 at the end.
+// G == 1 (rows of <= 128 bytes): CR = 256 * floor(32 KB / (256 * RB)) and
+// each thread folds whole rows with element reads (max, then the exp-sum).
+// G > 1: CR = floor(32 KB / RB) rounded down to a multiple of k; the 256 / G
+// groups of G lanes take the chunk's rows in turn, a lane reading every G-th
+// 16-byte vector of its row from shared memory (conflict-free: a group reads
+// consecutive vectors), the two vectors the row shares with its neighbours
+// masked, folded online and merged over the group with shuffles.  A stage is
+// released for the next copy only after every thread is done with it.
+template <int DT, int G>
 __global__ void __launch_bounds__(kTileThreads)
 lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out) {
     constexpr int EB = DType<DT>::bytes;
+    constexpr int GROUPS = kTileThreads / G;
     extern __shared__ __align__(128) unsigned char stage[];
     __shared__ __align__(8) uint64_t full[kStages];
     const int tid = threadIdx.x;
-    const int RB = static_cast<int>(N) * EB;  // <= 128
-    const int RPT = kChunkBytes / (kTileThreads * RB);
-    const int64_t CR = static_cast<int64_t>(kTileThreads) * RPT;
+    const int RB = static_cast<int>(N) * EB;
     int g = RB;  // gcd(RB, 16)
     for (int t = 16; t != 0;) {
         const int r = g % t;
@@ -229,6 +260,8 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
         t = r;
     }
     const int64_t k = 16 / g;
+    const int64_t CR = G == 1 ? static_cast<int64_t>(kTileThreads) * (kChunkBytes / (kTileThreads * RB))
+                              : (kChunkBytes / RB) - (kChunkBytes / RB) % k;
     const int64_t Bm = B - B % k;
     const int64_t nchunks = (Bm + CR - 1) / CR;
     const char* xb = reinterpret_cast<const char*>(x);
@@ -254,7 +287,7 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
             if (c < nchunks) issue(c, s);
         }
 
-    auto fold = [&](auto elem) {  // elem(n) -> float; the row value
+    auto fold = [&](auto elem) {  // elem(n) -> float; the row value (G == 1)
         float m = __int_as_float(kNegInfF32);
         for (int n = 0; n < N; ++n) m = fmaxf(m, elem(n));
         const float mu = shift_of(m);
@@ -262,19 +295,53 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
         for (int n = 0; n < N; ++n) acc[n & 1] += ex2((elem(n) - mu) * kLog2e);
         return acc_finalize(Acc{m, acc[0] + acc[1]});
     };
+    const int sub = tid & (G - 1);
+    const int grp = tid / G;
 
     int64_t kc = 0;  // chunks consumed by this CTA
     bool timed_out = false;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++kc) {
         const int s = static_cast<int>(kc % kStages);
         const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((kc / kStages) & 1), kWaitPolls);
+        const unsigned char* st = stage + s * kChunkBytes;
         // Results are stored as soon as they are computed; the stage is only
         // read before the barrier below.
-        for (int q = 0; q < RPT; ++q) {
-            const int64_t row = c * CR + q * kTileThreads + tid;
-            if (ok && row < Bm) {
-                const unsigned char* rowp = stage + s * kChunkBytes + (q * kTileThreads + tid) * RB;
-                out[row] = fold([&](int n) { return staged_elem<DT>(rowp, n); });
+        if constexpr (G == 1) {
+            for (int64_t q = tid; q < CR; q += kTileThreads) {
+                const int64_t row = c * CR + q;
+                if (ok && row < Bm) out[row] = fold([&](int n) { return staged_elem<DT>(st + q * RB, n); });
+            }
+        } else {
+            const int64_t rows = Bm - c * CR < CR ? Bm - c * CR : CR;
+            // Every lane runs the same number of passes (the group merge is a
+            // warp-wide shuffle); rows past the chunk fold nothing.
+            for (int64_t q0 = 0; q0 < rows; q0 += GROUPS) {
+                const int64_t q = q0 + grp;
+                const bool live = ok && q < rows;
+                const uint32_t rb0 = live ? static_cast<uint32_t>(q * RB) : 0u;
+                const uint32_t rb1 = live ? rb0 + static_cast<uint32_t>(RB) : 0u;
+                Acc acc = acc_identity();
+                float mu = 0.0f;
+                const uint32_t v_end = (rb1 + 15u) >> 4;
+                for (uint32_t v = (rb0 >> 4) + sub; v < v_end; v += 2 * G) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t vh = v + h * G;
+                        uint32_t q4[4] = {neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                          neg_inf_word<DT>()};
+                        if (vh < v_end) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(st + vh * 16u);
+                            q4[0] = u.x; q4[1] = u.y; q4[2] = u.z; q4[3] = u.w;
+                            if (vh * 16u < rb0 || vh * 16u + 16u > rb1) mask_words<DT>(q4, vh * 16u, rb0, rb1);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w[4 * h + i] = q4[i];
+                    }
+                    acc_add_words<DT, 8>(acc, mu, w);
+                }
+                acc = warp_merge<G>(acc);
+                if (live && sub == 0) out[c * CR + q] = acc_finalize(acc);
             }
         }
         if (__syncthreads_or(!ok)) {
@@ -304,15 +371,27 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
     }
 }
 
-template <int DT>
-cudaError_t launch_rowtile_any_t(const LaunchArgs& a, int grid) {
+template <int DT, int G>
+cudaError_t launch_rowtile_any_g(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT>,
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_any_kernel<DT>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl_smem(lse_rowtile_any_kernel<DT, G>, dim3(static_cast<unsigned>(grid)),
                            dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B, a.N,
                            a.out);
+}
+
+template <int DT>
+cudaError_t launch_rowtile_any_t(const LaunchArgs& a, int lanes, int grid) {
+    switch (lanes) {
+    case 1: return launch_rowtile_any_g<DT, 1>(a, grid);
+    case 4: return launch_rowtile_any_g<DT, 4>(a, grid);
+    case 8: return launch_rowtile_any_g<DT, 8>(a, grid);
+    case 16: return launch_rowtile_any_g<DT, 16>(a, grid);
+    case 32: return launch_rowtile_any_g<DT, 32>(a, grid);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int DT, int NV, bool E16, bool TL>
@@ -352,13 +431,16 @@ cudaError_t launch_rowtile_e(int dt, int nv, const LaunchArgs& a, int grid) {
 
 }  // namespace
 
-cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid) {
+cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid) {
     if (nv == 0) {  // any row width: row value with f32 exponentials only
         if (a.tl.logprob || a.e16) return cudaErrorInvalidValue;
+        if ((lanes == 1) != (a.N * (dt == kF32 ? 4 : 2) <= kAnyThreadRowBytes) ||
+            a.N * (dt == kF32 ? 4 : 2) > kChunkBytes / 8)
+            return cudaErrorInvalidValue;
         switch (dt) {
-        case kF32: return launch_rowtile_any_t<kF32>(a, grid);
-        case kBF16: return launch_rowtile_any_t<kBF16>(a, grid);
-        default: return launch_rowtile_any_t<kF16>(a, grid);
+        case kF32: return launch_rowtile_any_t<kF32>(a, lanes, grid);
+        case kBF16: return launch_rowtile_any_t<kBF16>(a, lanes, grid);
+        default: return launch_rowtile_any_t<kF16>(a, lanes, grid);
         }
     }
     if (a.tl.logprob) return launch_rowtile_e<false, true>(dt, nv, a, grid);
@@ -369,8 +451,17 @@ cudaError_t launch_rowtile(int dt, int nv, const LaunchArgs& a, int grid) {
 int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
 int rowtile_rows_per_chunk(int nv) { return kTileThreads * (8 / nv); }
 int rowtile_any_rows_per_chunk(int row_bytes) {
-    return kTileThreads * (kChunkBytes / (kTileThreads * row_bytes));
+    if (row_bytes <= kAnyThreadRowBytes) return kTileThreads * (kChunkBytes / (kTileThreads * row_bytes));
+    int g = row_bytes;  // gcd(row_bytes, 16)
+    for (int t = 16; t != 0;) {
+        const int r = g % t;
+        g = t;
+        t = r;
+    }
+    const int rows = kChunkBytes / row_bytes;
+    return rows - rows % (16 / g);
 }
+int rowtile_any_max_row_bytes() { return kChunkBytes / 8; }
 
 cudaError_t read_wait_timeouts(unsigned long long* count) {
     return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));

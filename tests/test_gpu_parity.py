@@ -478,6 +478,45 @@ def test_short_row_mapping_rule():
             assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_rowtile_grouped_rows(dtype):
+    """The bulk-copy ring for back-to-back rows of 129 bytes to 4 KB (any
+    width): groups of 4-32 lanes fold each row from 16-byte reads of the
+    staged chunk, masking the neighbouring rows' elements in the row's first
+    and last vectors.  Partial last chunks, fewer rows than one alignment
+    period, special values, every group size."""
+    _need_gpu()
+    eb = 4 if dtype == "f32" else 2
+    for rb in (130, 144, 252, 516, 1000, 1026, 2048, 2050, 4094, 4096):
+        if rb % eb:
+            continue
+        N = rb // eb
+        for B in (1, 3, 9, 1001, 20003):
+            x = wl.random_rows(B, N, dtype, seed=B + rb, scale=6.0)
+            if B >= 9:
+                xi = x.view(np.uint16) if dtype != "f32" else x
+                ninf = {"f32": -np.inf, "bf16": 0xFF80, "f16": 0xFC00}[dtype]
+                pinf = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+                nan = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+                xi[1, 0] = nan
+                xi[2, N - 1] = pinf
+                xi[3, :] = ninf
+                xi[4, 0] = pinf
+                xi[4, N - 1] = nan
+            want = oracle.lse(x, dtype)
+            xd = torch_view(x, dtype).cuda()
+            for G in (None, 4, 8, 16, 32):
+                plan = {"path": "rowtile"} if G is None else {"path": "rowtile", "lanes_per_row": G}
+                got, p = run(xd, plan)
+                d = p.as_dict()
+                assert d["path"] == "rowtile" and d["slots_per_lane"] == 0, d
+                try:
+                    compare(got, want)
+                except AssertionError as e:
+                    raise AssertionError(f"rb={rb} B={B} plan={d}: {e}") from None
+    assert L.lse_wait_timeouts() == 0
+
+
 def test_any_width_ring_rule():
     """Back-to-back rows of other widths up to 128 bytes take the element-read
     ring when there are rows for every CTA (row value only); the 16-bit
@@ -492,6 +531,17 @@ def test_any_width_ring_rule():
             assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
             assert L.lse_plan_query(dtype=dtype, B=1 << 26, N=N, row_stride=N + 1)["path"] \
                 == "subwarp"
+    # Rows over 512 bytes: the grouped ring where the sub-warp slots would be
+    # a third empty or more, the sub-warp mapping where they are full.
+    for dtype, N, ring, lanes in (("f32", 129, True, 4), ("f32", 520, True, 16),
+                                  ("bf16", 1020, True, 8), ("bf16", 2047, True, 16),
+                                  ("f32", 128, False, 0), ("f32", 68, False, 0),
+                                  ("f32", 1001, False, 0), ("bf16", 800, False, 0)):
+        q = L.lse_plan_query(dtype=dtype, B=1 << 22, N=N, row_stride=N)
+        if ring:
+            assert q["path"] == "rowtile" and q["lanes_per_row"] == lanes, (dtype, N, q)
+        else:
+            assert q["path"] == "subwarp", (dtype, N, q)
     x = wl.random_rows(1 << 20, 5, "f32", seed=55, scale=4.0)  # >= 1536 rows per CTA
     xd = torch.from_numpy(x).cuda()
     want = oracle.lse(x, "f32")
@@ -502,6 +552,21 @@ def test_any_width_ring_rule():
     assert p16.as_dict()["path"] == "subwarp"
     compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
     t = np.arange(x.shape[0], dtype=np.int64) % 5
+    lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
+    assert pl.as_dict()["path"] == "subwarp"
+    want_lp, want_lse = oracle.token_logprob(x, t, "f32")
+    compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
+    # The same for rows of 516 bytes (the grouped ring for the row value).
+    x = wl.random_rows(1 << 16, 129, "f32", seed=56, scale=4.0)
+    xd = torch.from_numpy(x).cuda()
+    want = oracle.lse(x, "f32")
+    got, p = run(xd, None)
+    assert p.as_dict()["path"] == "rowtile" and p.as_dict()["lanes_per_row"] == 4
+    compare(got, want)
+    g16, p16 = L.lse_forward16(xd)
+    assert p16.as_dict()["path"] == "subwarp"
+    compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
+    t = np.arange(x.shape[0], dtype=np.int64) % 129
     lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
     assert pl.as_dict()["path"] == "subwarp"
     want_lp, want_lse = oracle.token_logprob(x, t, "f32")

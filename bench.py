@@ -101,6 +101,20 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
+def backward_kernel(N, eb):
+    """The kernel lse_backward launches for back-to-back rows of N elements
+    of eb bytes from a 16-byte aligned base into a dx of the same layout (the
+    library's choice for that layout)."""
+    epv = 16 // eb
+    if N * eb % 16 == 0:  # every row on a 16-byte boundary
+        return "lse_backward_small_kernel" if -(-N // epv) <= 8 else "lse_backward_kernel"
+    if N >= epv and N * eb <= 16384:
+        return "lse_backward_flat_kernel"
+    if N // epv >= 4:
+        return "lse_backward_kernel"  # head and tail peeled
+    return "lse_backward_small_kernel" if N <= 4 else "lse_backward_kernel"  # element slots
+
+
 def ncu_traffic(workload_key: str, plan: dict, op: str = "forward") -> float | None:
     """DRAM bytes per launch of the main kernel from the committed ncu record,
     or None when there is none for this workload, op and plan, or when the
@@ -424,7 +438,7 @@ def run_native(args) -> None:
         lses = [L.lse_forward(x) for x in xs]
         gs = [torch.ones(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
         dxs = [torch.empty_like(x) for x in xs]
-        plan = {"path": "backward", "launches": 1, "kernel": "lse_backward_kernel"}
+        plan = {"path": "backward", "launches": 1, "kernel": backward_kernel(w.N, 4 if dt == "f32" else 2)}
         bytes_per_step = 2 * in_bytes + 8 * w.B
 
         def step(i, evb=0, eve=0):
@@ -531,9 +545,11 @@ def run_native(args) -> None:
     main_kernel = {"subwarp": "lse_subwarp_kernel", "rowtile": "lse_rowtile_kernel",
                    "cta": "lse_segment_kernel",
                    "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
-                   "backward": "lse_backward_kernel", "columns_warp": "lse_cols_kernel",
+                   "backward": plan.get("kernel"), "columns_warp": "lse_cols_kernel",
                    "columns_cta": "lse_cols_kernel",
                    "columns_backward": "lse_backward_strided_kernel"}[plan["path"]]
+    if plan["path"] == "rowtile" and plan.get("slots_per_lane") == 0:
+        main_kernel = "lse_rowtile_any_kernel"  # rows of any width
     traffic = ncu_traffic(args.workload, plan, op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,

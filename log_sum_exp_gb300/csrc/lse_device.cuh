@@ -244,10 +244,12 @@ __device__ __forceinline__ float words_expsum(const uint32_t (&w)[W], float mu) 
 
 // Short rows with their shift mu known in advance: the same exp-sum with one
 // FFMA per element, t = x log2 e - c where c = fl(mu log2 e).  Every term then
-// carries the same factor 2^(mu log2 e - c); scaled_log corrects it exactly
-// with the rounding residual of c.  Valid while |mu| log2 e stays finite
-// (|mu| <= 2^126 is used as the bound).
-__device__ __forceinline__ bool ffma_shift_ok(float mu) { return fabsf(mu) <= 0x1.0p126f; }
+// carries the same factor 2^r, r = mu log2 e - c, which finalize_scaled takes
+// back out exactly.  r is the rounding residual of c, up to half its ulp, so
+// it grows with |mu| (r = 6e21 at mu = -1e30, overflowing every term): the
+// form is used while |mu| <= 2^24, where |r| <= 1 and the terms keep the
+// range of the two-step form.
+__device__ __forceinline__ bool ffma_shift_ok(float mu) { return fabsf(mu) <= 0x1.0p24f; }
 
 template <int DT, int W>
 __device__ __forceinline__ float words_expsum_scaled(const uint32_t (&w)[W], float c) {

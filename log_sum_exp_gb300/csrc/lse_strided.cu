@@ -33,10 +33,14 @@ namespace {
 // 32 warps per SM resident (<= 64 registers per thread); 16-bit tiles shared
 // by several warps hold 8 accumulators per lane and keep 24 (<= 85 registers;
 // capping them at 64 measured 15 % slower on long reductions).
+// How far a column's maximum may rise above the shift its terms are taken
+// against before the sum is rescaled: terms stay below e^8 (2^11.5).
+constexpr float kLazyShift = 8.0f;
+
 template <int WT> struct ColCta {
     static constexpr int warps = WT > 4 ? WT : 4;
     static constexpr int min_blocks(int elem_bytes) {
-        return (elem_bytes == 4 || WT == 1) ? 1024 / (32 * warps) : 896 / (32 * warps);
+        return elem_bytes == 4 ? 1024 / (32 * warps) : (WT == 1 ? 768 / (32 * warps) : 896 / (32 * warps));
     }
 };
 
@@ -89,12 +93,16 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             acc[e] = acc_identity();
             mu[e] = 0.0f;
         }
+        // VEC, 16-bit: acc[e].s is taken against the lazy shift mu[e]; bit e of `seen`
+        // records that column e has met a value above -inf (acc[e].m is set
+        // from mu and `seen` once the rows are done).
+        uint32_t seen = 0;
         // PIPE: the next batch's loads are issued before the current batch is
         // folded, so two batches per warp are in flight.  For one warp per
         // tile (short reductions, which otherwise wait a full memory round
-        // trip per batch) on 4-byte elements, where the second buffer still
-        // fits 4 CTAs per SM.
-        constexpr bool PIPE = VEC && WT == 1 && EB == 4;
+        // trip per batch); 16-bit tiles then run 6 CTAs per SM (+5 % on bf16
+        // [512, 64, 1024]).
+        constexpr bool PIPE = VEC && WT == 1;
         uint4 nxt[U];
         auto load_batch = [&](int64_t r, uint4 (&u)[U]) {
 #pragma unroll
@@ -109,7 +117,6 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             if (r_begin + phase < r_end) load_batch(r_begin + phase, nxt);
         }
         for (int64_t r = r_begin + phase; r < r_end; r += kStep) {
-            float v[U][EPV];
             if constexpr (VEC) {
                 uint4 cur[U];
                 if constexpr (PIPE) {
@@ -119,31 +126,99 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                 } else {
                     load_batch(r, cur);
                 }
+                if constexpr (EB == 4) {
+                    // f32: four columns per lane; the eager rescale measured
+                    // faster here than the lazy one below (5.8 vs 5.5 TB/s on
+                    // [512, 64, 1024]).
 #pragma unroll
-                for (int j = 0; j < U; ++j) {
-                    const uint32_t w4[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+                    for (int e = 0; e < EPV; ++e) {
+                        float v[U];
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) v[j][e] = word_elem<DT>(w4, e);
+                        for (int j = 0; j < U; ++j) v[j] = __uint_as_float(e == 0 ? cur[j].x : e == 1 ? cur[j].y
+                                                                           : e == 2 ? cur[j].z : cur[j].w);
+                        float cm = v[0];
+#pragma unroll
+                        for (int j = 1; j < U; ++j) cm = fmaxf(cm, v[j]);
+                        acc_raise(acc[e], mu[e], cm);
+                        float sum = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < U; ++j) sum += ex2((v[j] - mu[e]) * kLog2e);
+                        acc[e].s += sum;
+                    }
+                } else {
+                    uint32_t w[U][4];
+#pragma unroll
+                    for (int j = 0; j < U; ++j) {
+                        w[j][0] = cur[j].x; w[j][1] = cur[j].y; w[j][2] = cur[j].z; w[j][3] = cur[j].w;
+                    }
+                    // Column maxima of the batch, packed over the rows (NaN
+                    // lanes ignored, as fmaxf does), kept as 4 words.
+                    uint32_t cmw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t t = w[0][i];
+#pragma unroll
+                        for (int j = 1; j < U; ++j)
+                            t = DT == kBF16 ? hmax2_bf16(t, w[j][i]) : hmax2_f16(t, w[j][i]);
+                        cmw[i] = t;
+                    }
+                    auto cm = [&](int e) { return word_elem<DT>(cmw, e); };
+                    // Lazy shifts: a column's terms are taken relative to a shift
+                    // mu that only moves when the batch maximum exceeds it by more
+                    // than kLazyShift (or is the column's first value above -inf),
+                    // so terms stay below e^kLazyShift and most batches skip the
+                    // rescale; the warp branches over it uniformly.
+                    auto need = [&](int e) {
+                        return ((seen >> e) & 1u) ? cm(e) > mu[e] + kLazyShift
+                                                  : cm(e) > __int_as_float(kNegInfF32);
+                    };
+                    bool any = false;
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) any = any || need(e);
+                    if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) {
+                            if (need(e)) {
+                                const float mn = shift_of(cm(e));
+                                acc[e].s = ((seen >> e) & 1u) ? acc[e].s * ex2((mu[e] - mn) * kLog2e) : 0.0f;
+                                mu[e] = mn;
+                                seen |= 1u << e;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        float sum = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < U; ++j) sum += ex2((word_elem<DT>(w[j], e) - mu[e]) * kLog2e);
+                        acc[e].s += sum;
+                    }
                 }
             } else {
+                float v[U];
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
                     const int64_t rr = r + j * WT;
-                    v[j][0] = active && rr < r_end ? load_elem<DT>(base, rr * stride_r)
-                                                   : __int_as_float(kNegInfF32);
+                    v[j] = active && rr < r_end ? load_elem<DT>(base, rr * stride_r)
+                                                : __int_as_float(kNegInfF32);
                 }
-            }
+                float cm = v[0];
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                float cm = v[0][e];
-#pragma unroll
-                for (int j = 1; j < U; ++j) cm = fmaxf(cm, v[j][e]);
-                acc_raise(acc[e], mu[e], cm);
+                for (int j = 1; j < U; ++j) cm = fmaxf(cm, v[j]);
+                acc_raise(acc[0], mu[0], cm);
                 float sum = 0.0f;
 #pragma unroll
-                for (int j = 0; j < U; ++j) sum += ex2((v[j][e] - mu[e]) * kLog2e);
-                acc[e].s += sum;
+                for (int j = 0; j < U; ++j) sum += ex2((v[j] - mu[0]) * kLog2e);
+                acc[0].s += sum;
             }
+        }
+        if constexpr (VEC && EB == 2) {
+            // (shift, sum) as an accumulator: the shift stands in for the
+            // maximum (it is within kLazyShift below it, and the merge and
+            // the finalize only use m as a shift); -inf for a column of -inf.
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+                acc[e].m = ((seen >> e) & 1u) ? mu[e] : __int_as_float(kNegInfF32);
         }
         if constexpr (WT > 1) {
 #pragma unroll

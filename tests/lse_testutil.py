@@ -36,7 +36,7 @@ def compare(got: np.ndarray, want: np.ndarray, atol: float = ATOL, rtol: float =
     }
     if bad_nan.size or bad_inf.size or bad_fin.size:
         idx = np.concatenate([bad_nan, bad_inf, bad_fin])[:8]
-        detail = [(int(i), float(got[i]), float(want[i])) for i in idx]
+        detail = [(int(i), float(got.flat[i]), float(want.flat[i])) for i in idx]
         raise AssertionError(f"{bad_nan.size} NaN mismatches, {bad_inf.size} inf mismatches, "
                              f"{bad_fin.size} out of tolerance; first: {detail}; {summary}")
     return summary

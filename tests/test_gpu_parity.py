@@ -187,6 +187,45 @@ def test_extreme_magnitudes():
         compare(got, want)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_magnitudes_every_mapping(dtype):
+    """Rows of 32 elements whose maximum is far beyond 2^24 (the shift's
+    rounding residual in the one-FFMA term form would then be large: 6e21 at
+    -1e30) or near the top of the range, beside ordinary rows, on every
+    mapping that takes such rows: sub-warp groups, the bulk-copy ring,
+    CTA and split."""
+    _need_gpu()
+    N = 32
+    rng = np.random.default_rng(9)
+    base = rng.normal(0, 3, (16, N)).astype(np.float32)
+    centres = [-1e30, 1e30, 3e9, -3e9, 2.0 ** 24 + 1.0, -7e7, 3e38, -3e38, 1e20, 0.0,
+               5e4, -5e4, 2.0 ** 127, 1e36, -1e36, 1.5e19]
+    x = np.zeros_like(base)
+    for i, c in enumerate(centres):
+        spread = abs(c) * 1e-6 if c else 1.0
+        x[i] = np.float32(c) + (base[i] * spread).astype(np.float32)
+    x[6, 5] = np.float32(3.4e38)
+    if dtype == "bf16":
+        x = wl.f32_to_bf16_bits(x)
+    want = oracle.lse(x, dtype)
+    xd = torch_view(x, dtype).cuda()
+    eb = 4 if dtype == "f32" else 2
+    plans = [None, {"path": "subwarp", "lanes_per_row": 2}, {"path": "subwarp", "lanes_per_row": 8},
+             {"path": "subwarp", "lanes_per_row": 32}, {"path": "cta", "threads": 64},
+             {"path": "split", "splits": 2}]
+    if N * eb <= 128:
+        plans.append({"path": "rowtile"})
+    for plan in plans:
+        got, p = run(xd, plan)
+        try:
+            compare(got, want)
+        except AssertionError as e:
+            raise AssertionError(f"plan {p.as_dict()}: {e}") from None
+    lp = L.lse_token_logprob(xd, torch.zeros(16, dtype=torch.int64, device="cuda"))
+    want_lp, want_lse = oracle.token_logprob(x, np.zeros(16, dtype=np.int64), dtype)
+    compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
+
+
 def test_special_value_in_every_split_segment():
     """NaN / +inf / only -inf inside one segment of a split row."""
     _need_gpu()

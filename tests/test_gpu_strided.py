@@ -134,3 +134,36 @@ def test_logsumexp_autograd_last_dim(dtype):
         dec = lambda a: oracle.decode(a, dtype).reshape(a.shape)  # noqa: E731
         compare_backward(dec(raw), dec(x), dtype, lse64, w.astype(np.float64),
                          oracle.backward(x, lse64, w.astype(np.float64), dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_columns_extreme_magnitudes(dtype):
+    """Columns whose maximum is beyond 2^126 (the one-FFMA term form would
+    overflow its shift; the fold falls back to the two-step form for the
+    whole warp) beside ordinary columns, and the special values, on every
+    column plan."""
+    _need_gpu()
+    big = 3.0e38
+    cols = [[big, big], [-big, big], [big, -np.inf], [-big, -big], [1e-40, -1e-40],
+            [-1e30, -1e30 + 1e24], [88.7, 88.7, 88.7], [-103.0, -103.0], [np.inf, -np.inf],
+            [np.nan, -np.inf], [1.0, 2.0, 3.0], [2.0 ** 127, 2.0 ** 126]]
+    R = 40
+    rng = np.random.default_rng(7)
+    C = 256
+    base = rng.normal(0, 3, (2, R, C)).astype(np.float32)
+    for k, col in enumerate(cols):
+        c = (k * 37) % C
+        base[:, :, c] = -np.inf
+        base[:, :len(col), c] = col
+    if dtype == "f32":
+        x = base
+    else:
+        x = wl.f32_to_bf16_bits(np.where(np.isnan(base), np.float32(0.0), base))
+        x[np.isnan(base)] = 0x7FC0
+    for plan in (None, {"path": "columns_warp"}, {"path": "columns_cta", "lanes_per_row": 2},
+                 {"path": "columns_cta", "lanes_per_row": 8}, {"path": "columns_warp", "splits": 3}):
+        got, want = run_strided(x, dtype, plan=plan)
+        try:
+            compare(got, want)
+        except AssertionError as e:
+            raise AssertionError(f"plan {plan}: {e}") from None

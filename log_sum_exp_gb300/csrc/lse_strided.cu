@@ -168,9 +168,12 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                     // than kLazyShift (or is the column's first value above -inf),
                     // so terms stay below e^kLazyShift and most batches skip the
                     // rescale; the warp branches over it uniformly.
+                    // A column whose sum is already +inf (it met +inf) never
+                    // moves its shift again: the rescale factor could flush to 0.
                     auto need = [&](int e) {
-                        return ((seen >> e) & 1u) ? cm(e) > mu[e] + kLazyShift
-                                                  : cm(e) > __int_as_float(kNegInfF32);
+                        return ((seen >> e) & 1u)
+                                   ? cm(e) > mu[e] + kLazyShift && acc[e].s != __int_as_float(0x7f800000)
+                                   : cm(e) > __int_as_float(kNegInfF32);
                     };
                     bool any = false;
 #pragma unroll
@@ -215,10 +218,15 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
         if constexpr (VEC && EB == 2) {
             // (shift, sum) as an accumulator: the shift stands in for the
             // maximum (it is within kLazyShift below it, and the merge and
-            // the finalize only use m as a shift); -inf for a column of -inf.
+            // the finalize only use m as a shift); -inf for a column of -inf,
+            // +inf for a column holding +inf (its sum is +inf: the terms, at
+            // most e^kLazyShift each, cannot overflow it otherwise), so that
+            // merging it with other partials keeps +inf.
 #pragma unroll
             for (int e = 0; e < EPV; ++e)
-                acc[e].m = ((seen >> e) & 1u) ? mu[e] : __int_as_float(kNegInfF32);
+                acc[e].m = !((seen >> e) & 1u)                        ? __int_as_float(kNegInfF32)
+                           : acc[e].s == __int_as_float(0x7f800000) ? __int_as_float(0x7f800000)
+                                                                     : mu[e];
         }
         if constexpr (WT > 1) {
 #pragma unroll

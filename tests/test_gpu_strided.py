@@ -167,3 +167,44 @@ def test_columns_extreme_magnitudes(dtype):
             compare(got, want)
         except AssertionError as e:
             raise AssertionError(f"plan {plan}: {e}") from None
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_columns_inf_between_shifts(dtype, offset):
+    """Columns where +inf arrives between runs of values far apart (the
+    16-bit fold keeps a lazy shift per column: once a column has met +inf its
+    shift must not move again), +inf first or last, two +inf, NaN beside
+    +inf; aligned and realigned (offset) tiles, every column plan."""
+    _need_gpu()
+    R, C = 96, 40
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 2, (2, R, C)).astype(np.float32)
+    x[:, :, 0] = 100.0
+    x[:, 30, 0] = np.inf                                # finite, +inf, finite
+    x[:, :40, 1] = -100.0
+    x[:, 40, 1] = np.inf
+    x[:, 41:, 1] = 100.0                                # low, +inf, high
+    x[:, 0, 2] = np.inf                                 # +inf first
+    x[:, R - 1, 3] = np.inf                             # +inf last
+    x[:, 5, 4] = np.inf
+    x[:, 70, 4] = np.inf                                # twice
+    x[:, 10, 5] = np.nan
+    x[:, 60, 5] = np.inf                                # NaN and +inf
+    x[:, :, 6] = -np.inf
+    x[:, 50, 6] = np.inf                                # only -inf and +inf
+    if dtype == "f32":
+        xx = x
+    elif dtype == "f16":
+        xx = x.astype(np.float16)
+    else:
+        xx = wl.f32_to_bf16_bits(np.where(np.isnan(x), np.float32(0.0), x))
+        xx[np.isnan(x)] = 0x7FC0
+    for plan in (None, {"path": "columns_warp"}, {"path": "columns_cta", "lanes_per_row": 2},
+                 {"path": "columns_cta", "lanes_per_row": 4}, {"path": "columns_cta", "lanes_per_row": 8},
+                 {"path": "columns_warp", "splits": 3}):
+        got, want = run_strided(xx, dtype, offset=offset, plan=plan)
+        try:
+            compare(got, want)
+        except AssertionError as e:
+            raise AssertionError(f"plan {plan}: {e}") from None

@@ -295,16 +295,27 @@ def oracle_sample_rows(w: wl.Workload, target_s: float) -> int:
 # ---------------------------------------------------------------------------
 # The reference arm: the oracle as the comparison program.
 # ---------------------------------------------------------------------------
+REFERENCE_BUDGET_S = 60.0  # oracle seconds for a whole --impl reference run
+
+
 def run_reference(args) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = wl.WORKLOADS[args.workload]
-    rows = oracle_sample_rows(w, 4.0)
-    x = wl.generate(args.workload, B=rows)
+    # Each step is a bounded sample, sized so that the whole run (the steps
+    # plus the warm-up steps, an eighth of a step each) takes about a minute
+    # of oracle time whatever --steps is (at most 4 s per step).
+    per_step_s = min(4.0, REFERENCE_BUDGET_S / (args.steps + args.warmup / 8))
     import oracle
 
-    oracle.lse(x[:1], w.dtype)
+    probe = wl.generate(args.workload, B=min(w.B, max(1, oracle_sample_rows(w, 0.05))))
+    oracle.lse(probe[:1], w.dtype)
+    t0 = time.perf_counter()
+    oracle.lse(probe, w.dtype)
+    per_row = max((time.perf_counter() - t0) / len(probe), 1e-9)  # this host's oracle speed
+    rows = int(max(1, min(w.B, per_step_s / per_row)))
+    x = wl.generate(args.workload, B=rows)
     for _ in range(args.warmup):
         oracle.lse(x[: max(1, rows // 8)], w.dtype)
     times = []

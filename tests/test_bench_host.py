@@ -50,3 +50,22 @@ def test_single_process_helpers():
     peak, src = bench.measured_peaks()
     assert peak > 0 and isinstance(src, str)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_reference_arm_bounded_and_complete(capsys, monkeypatch):
+    """--impl reference times the oracle on the host: each step is a sample
+    sized from this host's measured oracle speed so the whole run stays near
+    the budget whatever --steps is; the line carries the contract's keys."""
+    import json
+    import time
+
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 2.0)
+    t0 = time.perf_counter()
+    bench.main(["--impl", "reference", "--steps", "400", "--warmup", "3"])
+    elapsed = time.perf_counter() - t0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert elapsed < 30, elapsed
+    assert line["impl"] == "reference" and line["steps"] == 400 and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["gpu_launches"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["rows_per_step"] >= 1

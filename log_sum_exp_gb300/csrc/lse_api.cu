@@ -219,11 +219,11 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     const bool rowtile_auto =
         row_vecs > 2 && !(eb == 2 && (row_vecs == 4 || row_vecs == 8));
     // Rows of other widths up to 128 bytes, still back to back from a 16-byte
-    // aligned base: the same ring with element reads (row value with f32
-    // exponentials only).  Chosen automatically: it measured 1.15-2.9x the
-    // sub-warp mapping (with the head peel) on every such width but f32 rows
-    // of 7, where the two are even.
-    const bool rowtile_any_ok = !rowtile_ok && !with_logprob && !e16 && row_stride == N &&
+    // aligned base: the same ring with element reads (row value or token
+    // log-probability, f32 exponentials).  Chosen automatically: it measured
+    // 1.15-2.9x the sub-warp mapping (with the head peel) on the row value
+    // for every such width but f32 rows of 7, where the two are even.
+    const bool rowtile_any_ok = !rowtile_ok && !e16 && row_stride == N &&
                                 row_bytes <= rowtile_any_max_row_bytes() &&
                                 reinterpret_cast<uintptr_t>(x) % 16u == 0 &&
                                 (!req || req->vector_bytes == 0 ||

@@ -243,10 +243,13 @@ __device__ __forceinline__ void mask_words(uint32_t (&w)[4], uint32_t vb, uint32
 // 16-byte vector of its row from shared memory (conflict-free: a group reads
 // consecutive vectors), the two vectors the row shares with its neighbours
 // masked, folded online and merged over the group with shuffles.  A stage is
-// released for the next copy only after every thread is done with it.
-template <int DT, int G>
+// released for the next copy only after every thread is done with it.  TL:
+// the token log-probability epilogue (out may then be null): each row's target
+// is loaded before its fold, and x[row, target] read from the staged row.
+template <int DT, int G, bool TL>
 __global__ void __launch_bounds__(kTileThreads)
-lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out) {
+lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out,
+                       const int64_t* __restrict__ target, float* __restrict__ logprob) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int GROUPS = kTileThreads / G;
     extern __shared__ __align__(128) unsigned char stage[];
@@ -309,7 +312,13 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
         if constexpr (G == 1) {
             for (int64_t q = tid; q < CR; q += kTileThreads) {
                 const int64_t row = c * CR + q;
-                if (ok && row < Bm) out[row] = fold([&](int n) { return staged_elem<DT>(st + q * RB, n); });
+                if (ok && row < Bm) {
+                    const int64_t t = TL ? __ldg(target + row) : -1;
+                    const float lse = fold([&](int n) { return staged_elem<DT>(st + q * RB, n); });
+                    const float xt = TL && t >= 0 && t < N ? staged_elem<DT>(st + q * RB, static_cast<int>(t))
+                                                           : __int_as_float(0x7fc00000);
+                    store_row(out, TL ? logprob : nullptr, row, lse, xt);
+                }
             }
         } else {
             const int64_t rows = Bm - c * CR < CR ? Bm - c * CR : CR;
@@ -320,6 +329,7 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                 const bool live = ok && q < rows;
                 const uint32_t rb0 = live ? static_cast<uint32_t>(q * RB) : 0u;
                 const uint32_t rb1 = live ? rb0 + static_cast<uint32_t>(RB) : 0u;
+                const int64_t t = TL && live && sub == 0 ? __ldg(target + c * CR + q) : -1;
                 Acc acc = acc_identity();
                 float mu = 0.0f;
                 const uint32_t v_end = (rb1 + 15u) >> 4;
@@ -341,7 +351,12 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                     acc_add_words<DT, 8>(acc, mu, w);
                 }
                 acc = warp_merge<G>(acc);
-                if (live && sub == 0) out[c * CR + q] = acc_finalize(acc);
+                if (live && sub == 0) {
+                    const float xt = TL && t >= 0 && t < N
+                                         ? staged_elem<DT>(st + rb0, static_cast<int>(t))
+                                         : __int_as_float(0x7fc00000);
+                    store_row(out, TL ? logprob : nullptr, c * CR + q, acc_finalize(acc), xt);
+                }
             }
         }
         if (__syncthreads_or(!ok)) {
@@ -367,30 +382,42 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
     if (blockIdx.x == 0 && Bm + tid < B) {  // the < k rows after the last copy
         const int64_t row = Bm + tid;
         const char* rowp = xb + row * RB;
-        out[row] = fold([&](int n) { return load_elem<DT>(rowp, n); });
+        const int64_t t = TL ? __ldg(target + row) : -1;
+        const float lse = fold([&](int n) { return load_elem<DT>(rowp, n); });
+        const float xt = TL && t >= 0 && t < N ? load_elem<DT>(rowp, t) : __int_as_float(0x7fc00000);
+        store_row(out, TL ? logprob : nullptr, row, lse, xt);
     }
 }
 
-template <int DT, int G>
+template <int DT, int G, bool TL>
 cudaError_t launch_rowtile_any_g(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT, G>,
+    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT, G, TL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_any_kernel<DT, G>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl_smem(lse_rowtile_any_kernel<DT, G, TL>, dim3(static_cast<unsigned>(grid)),
                            dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B, a.N,
-                           a.out);
+                           a.out, a.tl.target, a.tl.logprob);
 }
 
-template <int DT>
+template <int DT, bool TL>
 cudaError_t launch_rowtile_any_t(const LaunchArgs& a, int lanes, int grid) {
     switch (lanes) {
-    case 1: return launch_rowtile_any_g<DT, 1>(a, grid);
-    case 4: return launch_rowtile_any_g<DT, 4>(a, grid);
-    case 8: return launch_rowtile_any_g<DT, 8>(a, grid);
-    case 16: return launch_rowtile_any_g<DT, 16>(a, grid);
-    case 32: return launch_rowtile_any_g<DT, 32>(a, grid);
+    case 1: return launch_rowtile_any_g<DT, 1, TL>(a, grid);
+    case 4: return launch_rowtile_any_g<DT, 4, TL>(a, grid);
+    case 8: return launch_rowtile_any_g<DT, 8, TL>(a, grid);
+    case 16: return launch_rowtile_any_g<DT, 16, TL>(a, grid);
+    case 32: return launch_rowtile_any_g<DT, 32, TL>(a, grid);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool TL>
+cudaError_t launch_rowtile_any(int dt, int lanes, const LaunchArgs& a, int grid) {
+    switch (dt) {
+    case kF32: return launch_rowtile_any_t<kF32, TL>(a, lanes, grid);
+    case kBF16: return launch_rowtile_any_t<kBF16, TL>(a, lanes, grid);
+    default: return launch_rowtile_any_t<kF16, TL>(a, lanes, grid);
     }
 }
 
@@ -432,16 +459,13 @@ cudaError_t launch_rowtile_e(int dt, int nv, const LaunchArgs& a, int grid) {
 }  // namespace
 
 cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid) {
-    if (nv == 0) {  // any row width: row value with f32 exponentials only
-        if (a.tl.logprob || a.e16) return cudaErrorInvalidValue;
+    if (nv == 0) {  // any row width: row value or token log-probability, f32 exponentials
+        if (a.e16) return cudaErrorInvalidValue;
         if ((lanes == 1) != (a.N * (dt == kF32 ? 4 : 2) <= kAnyThreadRowBytes) ||
             a.N * (dt == kF32 ? 4 : 2) > kChunkBytes / 8)
             return cudaErrorInvalidValue;
-        switch (dt) {
-        case kF32: return launch_rowtile_any_t<kF32>(a, lanes, grid);
-        case kBF16: return launch_rowtile_any_t<kBF16>(a, lanes, grid);
-        default: return launch_rowtile_any_t<kF16>(a, lanes, grid);
-        }
+        return a.tl.logprob ? launch_rowtile_any<true>(dt, lanes, a, grid)
+                            : launch_rowtile_any<false>(dt, lanes, a, grid);
     }
     if (a.tl.logprob) return launch_rowtile_e<false, true>(dt, nv, a, grid);
     return a.e16 ? launch_rowtile_e<true, false>(dt, nv, a, grid)

@@ -162,3 +162,47 @@ def test_logprob_rejects_bad_pointers():
         L.lse_token_logprob_ptr(x.data_ptr(), "f32", 4, 8, 8, t.data_ptr() + 4, lp.data_ptr())
     with pytest.raises(L.LseError):
         L.lse_token_logprob_ptr(x.data_ptr(), "f32", 4, 8, 8, t.data_ptr(), lp.data_ptr() + 2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_logprob_any_width_ring(dtype):
+    """The bulk-copy ring for back-to-back rows of any width with the token
+    log-probability epilogue: a thread per row up to 128 bytes, 4-32 lanes per
+    row up to 4 KB; targets in and out of range, on special values, partial
+    last chunks and the rows after the last copy, with and without lse_out."""
+    _need_gpu()
+    eb = 4 if dtype == "f32" else 2
+    widths = (1, 3, 5, 7, 9, 31, 33, 129, 257, 1023) if dtype == "f32" else \
+        (1, 3, 7, 9, 63, 65, 257, 1025, 2047)
+    for N in widths:
+        for B in (1, 9, 1001, 20003):
+            x = wl.random_rows(B, N, dtype, seed=B + 3 * N, scale=6.0)
+            if B >= 9 and N >= 3:
+                xi = x.view(np.uint16) if dtype != "f32" else x
+                ninf = {"f32": -np.inf, "bf16": 0xFF80, "f16": 0xFC00}[dtype]
+                pinf = {"f32": np.inf, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+                nan = {"f32": np.nan, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+                xi[5, 1] = nan
+                xi[6, N - 1] = pinf
+                xi[7, :] = ninf
+                xi[8, 2] = ninf
+            t = _targets(B, N, seed=N * 7 + B)
+            if B >= 9:
+                t[8] = 2 if N > 2 else 0  # a -inf entry
+            want_lp, want_lse = oracle.token_logprob(x, t, dtype)
+            xd = torch_view(x, dtype).cuda()
+            plans = [{"path": "rowtile"}]
+            if N * eb > 128:
+                plans += [{"path": "rowtile", "lanes_per_row": G} for G in (4, 32)]
+            for plan in plans:
+                for with_lse in (True, False):
+                    lp, lse, p = run_logprob(xd, t, plan, with_lse)
+                    d = p.as_dict()
+                    assert d["path"] == "rowtile", d
+                    try:
+                        compare_logprob(lp, want_lp, want_lse)
+                        if with_lse:
+                            compare(lse, want_lse)
+                    except AssertionError as e:
+                        raise AssertionError(f"N={N} B={B} plan={d} lse={with_lse}: {e}") from None
+    assert L.lse_wait_timeouts() == 0

@@ -558,8 +558,8 @@ def test_rowtile_grouped_rows(dtype):
 
 def test_any_width_ring_rule():
     """Back-to-back rows of other widths up to 128 bytes take the element-read
-    ring when there are rows for every CTA (row value only); the 16-bit
-    exponential and token log-probability entry points keep the register
+    ring when there are rows for every CTA (row value and token
+    log-probability); the 16-bit exponential entry point keeps the register
     mappings for them."""
     _need_gpu()
     for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
@@ -592,10 +592,11 @@ def test_any_width_ring_rule():
     compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
     t = np.arange(x.shape[0], dtype=np.int64) % 5
     lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
-    assert pl.as_dict()["path"] == "subwarp"
+    assert pl.as_dict()["path"] == "rowtile"
     want_lp, want_lse = oracle.token_logprob(x, t, "f32")
     compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
-    # The same for rows of 516 bytes (the grouped ring for the row value).
+    # The same for rows of 516 bytes (the grouped ring for the row value and
+    # the token log-probability).
     x = wl.random_rows(1 << 16, 129, "f32", seed=56, scale=4.0)
     xd = torch.from_numpy(x).cuda()
     want = oracle.lse(x, "f32")
@@ -607,7 +608,7 @@ def test_any_width_ring_rule():
     compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
     t = np.arange(x.shape[0], dtype=np.int64) % 129
     lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
-    assert pl.as_dict()["path"] == "subwarp"
+    assert pl.as_dict()["path"] == "rowtile"
     want_lp, want_lse = oracle.token_logprob(x, t, "f32")
     compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
 

@@ -1,0 +1,142 @@
+// Host-side checks of the kernel-mapping rules (make_plan and its helpers)
+// on a stand-in device description: 152 SMs and segment-kernel occupancies
+// of 2048 / threads / 2 CTAs per SM.  Only host code runs; no device needed.
+// Each expectation restates a rule that the library's comments give with
+// the measurement behind it.
+#include <cstdio>
+
+#include "../../log_sum_exp_gb300/csrc/lse_api.cu"
+
+namespace {
+
+int g_fail = 0;
+
+void expect(bool ok, const char* what) {
+    if (!ok) {
+        std::printf("FAIL: %s\n", what);
+        ++g_fail;
+    }
+}
+
+lse::DeviceInfo fake_device() {
+    lse::DeviceInfo info;
+    info.ready = true;
+    info.sms = 152;
+    for (int dt = 0; dt < 3; ++dt)
+        for (int v = 0; v < 2; ++v)
+            for (int t = 0; t < 5; ++t) info.seg_occ[dt][v][t] = 2048 / (32 << t) / 2;
+    return info;
+}
+
+const void* const kAligned = reinterpret_cast<const void*>(static_cast<uintptr_t>(1) << 20);
+
+lse_plan plan(lse_dtype dt, int64_t B, int64_t N, int64_t rs, const void* x = kAligned,
+              const lse_plan* req = nullptr, bool logprob = false, bool e16 = false,
+              lse_status* st = nullptr) {
+    static const lse::DeviceInfo info = fake_device();
+    lse_plan p;
+    std::memset(&p, 0, sizeof p);
+    const lse_status s = lse::make_plan(x, dt, B, N, rs, info, req, logprob, &p, e16);
+    if (st) *st = s;
+    else expect(s == LSE_OK, "make_plan returned an error");
+    return p;
+}
+
+}  // namespace
+
+int main() {
+    // Back-to-back rows of 16..128 bytes: the vector ring where it measured
+    // faster (3, 5, 6, 7 vectors; f32 rows of 4 or 8), else the sub-warp kernel.
+    lse_plan p = plan(LSE_F32, 1 << 20, 32, 32);
+    expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8, "f32 rows of 128 bytes: ring, 8 vectors");
+    p = plan(LSE_BF16, 1 << 20, 64, 64);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 2 && p.slots_per_lane == 4,
+           "bf16 rows of 128 bytes: sub-warp, 2 lanes x 4 vectors");
+    p = plan(LSE_F32, 1 << 20, 32, 36);
+    expect(p.path == LSE_PATH_SUBWARP, "rows not back to back: no ring");
+    p = plan(LSE_F32, 1000, 32, 32);
+    expect(p.path == LSE_PATH_SUBWARP, "too few rows for every CTA: no ring");
+
+    // Other widths up to 128 bytes: the element-read ring (row value and token
+    // log-probability, not the 16-bit exponentials).
+    p = plan(LSE_F32, 1 << 22, 5, 5);
+    expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 0 && p.lanes_per_row == 1 &&
+               p.vector_bytes == 1,
+           "f32 rows of 20 bytes: any-width ring, a thread per row");
+    p = plan(LSE_F32, 1 << 22, 5, 5, kAligned, nullptr, true);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 1, "token log-probability: the same ring");
+    p = plan(LSE_F32, 1 << 22, 5, 5, kAligned, nullptr, false, true);
+    expect(p.path == LSE_PATH_SUBWARP, "16-bit exponentials: sub-warp kernel");
+    p = plan(LSE_F32, 1 << 22, 5, 6);
+    expect(p.path == LSE_PATH_SUBWARP, "strided rows: sub-warp kernel");
+
+    // Longer back-to-back rows: the grouped ring where a third or more of the
+    // sub-warp slots would be empty (rows just past a power of two of slots).
+    p = plan(LSE_F32, 1 << 20, 129, 129);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 4, "f32 N=129: grouped ring, 4 lanes");
+    p = plan(LSE_F32, 1 << 20, 520, 520);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16, "f32 N=520: grouped ring, 16 lanes");
+    p = plan(LSE_BF16, 1 << 18, 2047, 2047);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16, "bf16 N=2047: grouped ring, 16 lanes");
+    p = plan(LSE_F32, 1 << 20, 68, 68);
+    expect(p.path == LSE_PATH_SUBWARP, "rows of <= 512 bytes: no grouped ring");
+    p = plan(LSE_F32, 1 << 20, 129, 129, kAligned, nullptr, false, true);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 8 && p.slots_per_lane == 8,
+           "f32 N=129 with 16-bit exponentials: 8 lanes x 8 slots (32 vectors + 2 peel slots)");
+
+    // Sub-warp shapes: fewest lanes with <= 4 slots; vector rows of more than
+    // 16 slots take half the lanes with 8 slots each.
+    p = plan(LSE_F32, 1 << 20, 40, 44);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 4,
+           "f32 N=40: 4 lanes x 4 slots");
+    p = plan(LSE_F32, 1 << 20, 128, 128);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 8,
+           "f32 N=128: 4 lanes x 8 slots");
+    p = plan(LSE_F32, 1 << 17, 1001, 1001);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 32 && p.slots_per_lane == 8,
+           "f32 N=1001 (250 vectors + 2 peel slots): a warp x 8 slots");
+    expect(lse::subwarp_auto_slots(33, true) == 64 && lse::subwarp_auto_slots(32, true) == 32,
+           "sub-warp slot counts");
+
+    // Long rows: a CTA per row, split when the rows cannot fill the GPU.
+    p = plan(LSE_F32, 512, 128256, 128256);
+    expect(p.path == LSE_PATH_CTA && p.threads == 512 && p.splits == 1, "512 x 128256 f32: CTA 512");
+    p = plan(LSE_BF16, 8192, 32000, 32000);
+    expect(p.path == LSE_PATH_CTA && p.threads == 128 && p.splits == 1, "8192 x 32000 bf16: CTA 128");
+    p = plan(LSE_F32, 16, 16777216, 16777216);
+    expect(p.path == LSE_PATH_SPLIT && p.threads == 512 && p.splits == 128 && p.launches == 2 &&
+               p.scratch_bytes == 16 * 128 * 8,
+           "16 x 16.7M f32: 128 splits of 512 threads and a merge");
+
+    // Alignment: rows off a 16-byte boundary keep vectors (peeled); a base
+    // that is not element aligned gets element loads.
+    p = plan(LSE_F32, 64, 4096, 4096, reinterpret_cast<const void*>((1u << 20) + 4));
+    expect(p.vector_bytes == 16, "f32 rows 4 bytes off a boundary: vectors with a peel");
+    p = plan(LSE_F32, 64, 4096, 4096, reinterpret_cast<const void*>((1u << 20) + 2));
+    expect(p.vector_bytes == 1, "a base that is not element aligned: element loads");
+
+    // Requests.
+    lse_status st;
+    lse_plan req;
+    std::memset(&req, 0, sizeof req);
+    req.path = LSE_PATH_ROWTILE;
+    plan(LSE_F32, 1 << 20, 5, 6, kAligned, &req, false, false, &st);
+    expect(st == LSE_ERR_INVALID_ARG, "forced ring on strided rows: invalid");
+    req.path = LSE_PATH_SUBWARP;
+    req.lanes_per_row = 2;
+    plan(LSE_F32, 1 << 20, 80, 80, kAligned, &req, false, false, &st);
+    expect(st == LSE_ERR_INVALID_ARG, "2 lanes for 20 slots (10 each): invalid");
+    req.lanes_per_row = 4;
+    p = plan(LSE_F32, 1 << 20, 80, 80, kAligned, &req, false, false, &st);
+    expect(st == LSE_OK && p.slots_per_lane == 8, "4 lanes for 20 slots: 8 slots each");
+    req.path = LSE_PATH_SPLIT;
+    req.lanes_per_row = 0;
+    req.splits = 3;
+    p = plan(LSE_F32, 4, 4096, 4096, kAligned, &req, false, false, &st);
+    expect(st == LSE_OK && p.path == LSE_PATH_SPLIT && p.splits == 3, "forced 3 splits");
+    p = plan(LSE_F32, 7, 0, 0);
+    expect(p.path == LSE_PATH_EMPTY && p.launches == 1, "N = 0: the fill kernel");
+
+    std::printf(g_fail ? "planner: %d failures\n" : "planner: ok\n", g_fail);
+    return g_fail != 0;
+}

@@ -391,6 +391,75 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     return LSE_OK;
 }
 
+// The launch shape of lse_backward for x and dx rows (host logic only):
+// fills the mode and a's grid, block, seg_slots and small fields.
+lse_status plan_backward(const void* x, int eb, int64_t B, int64_t N, int64_t row_stride,
+                         const void* dx, int64_t dx_row_stride, const DeviceInfo& info,
+                         BackwardArgs* a, int* mode_out) {
+    // 16-byte vectors when every row of x and dx starts on a 16-byte boundary;
+    // vectors with a peeled head and tail when each x row and its dx row sit
+    // at the same offset from one (same base offset, strides equal mod 16
+    // bytes) and hold at least 4 vectors; elements otherwise.  Rows of fewer
+    // vectors measured faster as elements (f32 N = 5: 2.8 vs 1.4 TB/s; N = 13:
+    // 3.3 vs 3.1), longer ones faster peeled (N = 33: 3.2 vs 2.6; bf16 N = 50257:
+    // 6.5 vs 2.7).
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), da = reinterpret_cast<uintptr_t>(dx);
+    const bool aligned = xa % 16u == 0 && (row_stride * eb) % 16 == 0 && da % 16u == 0 &&
+                         (dx_row_stride * eb) % 16 == 0;
+    const bool coaligned = (xa - da) % 16u == 0 && ((row_stride - dx_row_stride) * eb) % 16 == 0;
+    int mode = aligned ? kBwdVector : (coaligned && N / (16 / eb) >= 4 ? kBwdPeel : kBwdScalar);
+    // Back-to-back rows of x and dx at the same offset from a boundary, not
+    // all on one, from one vector up to 16 KB long: one flat array of vectors
+    // (1.2-2.4x the peeled rows up to 4 K elements; longer rows peel faster).
+    const bool flat_ok = row_stride == N && dx_row_stride == N && coaligned && N >= 16 / eb &&
+                         N * eb <= 16384;
+    if (flat_ok && !aligned) mode = kBwdFlat;
+    const bool vec = mode != kBwdScalar;
+    const int64_t epv = vec ? 16 / eb : 1;
+    // Slots per row: the tail vector, and with the peel the head slot too.
+    const int64_t nvt = mode == kBwdPeel ? N / epv + 2 : ceil_div(N, epv);
+    const int U = backward_slots_per_thread();
+    const int threads = backward_threads();
+    // Threads across a row: just enough for U slots each (not rounded to a
+    // power of two: rows of 33-257 peeled slots measured 1.1-1.3x faster).
+    const int64_t tx = ceil_div(nvt, U);
+    const int TX = tx > threads ? threads : static_cast<int>(tx);
+    const int TY = threads / TX;
+    const int64_t seg = nvt <= static_cast<int64_t>(TX) * U * 4 ? nvt : static_cast<int64_t>(TX) * U * 4;
+    const int64_t P = ceil_div(nvt, seg);
+    if (P > INT_MAX) return LSE_ERR_INVALID_ARG;
+    int64_t gy = ceil_div(B, TY);
+    if (gy > 65535) gy = 65535;  // grid-stride over the remaining rows
+
+    a->seg_slots = seg;
+    a->grid = dim3(static_cast<unsigned>(P), static_cast<unsigned>(gy));
+    a->block = dim3(static_cast<unsigned>(TX), static_cast<unsigned>(TY));
+    // Short rows: flattened (row, slot) pairs, U per thread in flight, at most
+    // 4 waves of 256-thread CTAs striding over them.  Up to 2U slots for
+    // aligned vectors (f32 rows of 6 and 8 vectors: +1.8 %; 16 vectors: -7 %),
+    // up to U with the peel or with elements.
+    a->small = nvt <= (mode == kBwdVector ? 2 * U : U);
+    if (a->small) {
+        int64_t ctas = ceil_div(ceil_div(B * nvt, U), threads);
+        const int64_t cap = static_cast<int64_t>(info.sms) * 8 * 4;
+        if (ctas > cap) ctas = cap;
+        a->grid = dim3(static_cast<unsigned>(ctas));
+        a->block = dim3(static_cast<unsigned>(threads));
+    }
+    if (mode == kBwdFlat) {  // one wave of resident CTAs (4 per SM) striding over the vectors
+        int64_t ctas = ceil_div(ceil_div(B * N, 16 / eb),
+                                static_cast<int64_t>(threads) * backward_flat_vectors_per_thread());
+        const int64_t cap = static_cast<int64_t>(info.sms) * 4;
+        if (ctas > cap) ctas = cap;
+        if (ctas < 1) ctas = 1;
+        a->small = false;
+        a->grid = dim3(static_cast<unsigned>(ctas));
+        a->block = dim3(static_cast<unsigned>(threads));
+    }
+    *mode_out = mode;
+    return LSE_OK;
+}
+
 cudaError_t launch_subwarp(lse_dtype dt, const LaunchArgs& a, bool vec, int G, int V, int64_t grid) {
     const bool tl = a.tl.logprob != nullptr;
     if (a.e16) {
@@ -643,42 +712,10 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
     const DeviceInfo* info = nullptr;
     if ((st = device_info(&dev, &info)) != LSE_OK) return st;
 
-    // 16-byte vectors when every row of x and dx starts on a 16-byte boundary;
-    // vectors with a peeled head and tail when each x row and its dx row sit
-    // at the same offset from one (same base offset, strides equal mod 16
-    // bytes) and hold at least 4 vectors; elements otherwise.  Rows of fewer
-    // vectors measured faster as elements (f32 N = 5: 2.8 vs 1.4 TB/s; N = 13:
-    // 3.3 vs 3.1), longer ones faster peeled (N = 33: 3.2 vs 2.6; bf16 N = 50257:
-    // 6.5 vs 2.7).
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), da = reinterpret_cast<uintptr_t>(dx);
-    const bool aligned = xa % 16u == 0 && (row_stride * eb) % 16 == 0 && da % 16u == 0 &&
-                         (dx_row_stride * eb) % 16 == 0;
-    const bool coaligned = (xa - da) % 16u == 0 && ((row_stride - dx_row_stride) * eb) % 16 == 0;
-    int mode = aligned ? kBwdVector : (coaligned && N / (16 / eb) >= 4 ? kBwdPeel : kBwdScalar);
-    // Back-to-back rows of x and dx at the same offset from a boundary, not
-    // all on one, from one vector up to 16 KB long: one flat array of vectors
-    // (1.2-2.4x the peeled rows up to 4 K elements; longer rows peel faster).
-    const bool flat_ok = row_stride == N && dx_row_stride == N && coaligned && N >= 16 / eb &&
-                         N * eb <= 16384;
-    if (flat_ok && !aligned) mode = kBwdFlat;
-    const bool vec = mode != kBwdScalar;
-    const int64_t epv = vec ? 16 / eb : 1;
-    // Slots per row: the tail vector, and with the peel the head slot too.
-    const int64_t nvt = mode == kBwdPeel ? N / epv + 2 : ceil_div(N, epv);
-    const int U = backward_slots_per_thread();
-    const int threads = backward_threads();
-    // Threads across a row: just enough for U slots each (not rounded to a
-    // power of two: rows of 33-257 peeled slots measured 1.1-1.3x faster).
-    const int64_t tx = ceil_div(nvt, U);
-    const int TX = tx > threads ? threads : static_cast<int>(tx);
-    const int TY = threads / TX;
-    const int64_t seg = nvt <= static_cast<int64_t>(TX) * U * 4 ? nvt : static_cast<int64_t>(TX) * U * 4;
-    const int64_t P = ceil_div(nvt, seg);
-    if (P > INT_MAX) return LSE_ERR_INVALID_ARG;
-    int64_t gy = ceil_div(B, TY);
-    if (gy > 65535) gy = 65535;  // grid-stride over the remaining rows
-
     BackwardArgs a;
+    int mode = kBwdScalar;
+    if ((st = plan_backward(x, eb, B, N, row_stride, dx, dx_row_stride, *info, &a, &mode)) != LSE_OK)
+        return st;
     a.x = x;
     a.B = B;
     a.N = N;
@@ -687,31 +724,6 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
     a.grad = grad;
     a.dx = dx;
     a.dx_row_stride = dx_row_stride;
-    a.seg_slots = seg;
-    a.grid = dim3(static_cast<unsigned>(P), static_cast<unsigned>(gy));
-    a.block = dim3(static_cast<unsigned>(TX), static_cast<unsigned>(TY));
-    // Short rows: flattened (row, slot) pairs, U per thread in flight, at most
-    // 4 waves of 256-thread CTAs striding over them.  Up to 2U slots for
-    // aligned vectors (f32 rows of 6 and 8 vectors: +1.8 %; 16 vectors: -7 %),
-    // up to U with the peel or with elements.
-    a.small = nvt <= (mode == kBwdVector ? 2 * U : U);
-    if (a.small) {
-        int64_t ctas = ceil_div(ceil_div(B * nvt, U), threads);
-        const int64_t cap = static_cast<int64_t>(info->sms) * 8 * 4;
-        if (ctas > cap) ctas = cap;
-        a.grid = dim3(static_cast<unsigned>(ctas));
-        a.block = dim3(static_cast<unsigned>(threads));
-    }
-    if (mode == kBwdFlat) {  // one wave of resident CTAs (4 per SM) striding over the vectors
-        int64_t ctas = ceil_div(ceil_div(B * N, 16 / eb),
-                                static_cast<int64_t>(threads) * backward_flat_vectors_per_thread());
-        const int64_t cap = static_cast<int64_t>(info->sms) * 4;
-        if (ctas > cap) ctas = cap;
-        if (ctas < 1) ctas = 1;
-        a.small = false;
-        a.grid = dim3(static_cast<unsigned>(ctas));
-        a.block = dim3(static_cast<unsigned>(threads));
-    }
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = launch_backward(dtype, mode, a);
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);

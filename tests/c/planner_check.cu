@@ -137,6 +137,49 @@ int main() {
     p = plan(LSE_F32, 7, 0, 0);
     expect(p.path == LSE_PATH_EMPTY && p.launches == 1, "N = 0: the fill kernel");
 
+    // Row backward: vectors, peeled vectors, the flat array or elements;
+    // flattened short rows; threads across a row = ceil(slots / 4).
+    {
+        const lse::DeviceInfo info = fake_device();
+        const char* base = static_cast<const char*>(kAligned);
+        auto bwd = [&](int eb, int64_t B, int64_t N, int64_t rs, const void* x, const void* dx,
+                       int64_t drs, lse::BackwardArgs* a) {
+            int mode = -1;
+            expect(lse::plan_backward(x, eb, B, N, rs, dx, drs, info, a, &mode) == LSE_OK,
+                   "plan_backward returned an error");
+            return mode;
+        };
+        lse::BackwardArgs a;
+        const void* dx = base + (64 << 20);
+        int m = bwd(4, 1 << 20, 32, 32, base, dx, 32, &a);
+        expect(m == lse::kBwdVector && a.small && a.block.x == 256,
+               "f32 rows of 8 vectors: flattened short rows");
+        m = bwd(4, 512, 128256, 128256, base, dx, 128256, &a);
+        expect(m == lse::kBwdVector && !a.small && a.block.x == 256 && a.block.y == 1 &&
+                   a.seg_slots == 4096 && a.grid.x == 8 && a.grid.y == 512,
+               "512 x 128256 f32: 256 threads per row, 8 segments of 4096 vectors");
+        m = bwd(4, 1 << 20, 129, 129, base, dx, 129, &a);
+        expect(m == lse::kBwdFlat && a.grid.x == 152 * 4 && a.block.x == 256,
+               "f32 N=129 back to back: the flat array, one wave");
+        m = bwd(4, 1335, 50257, 50257, base, dx, 50257, &a);
+        expect(m == lse::kBwdPeel && a.block.x == 256, "f32 N=50257 (rows over 16 KB): peeled rows");
+        m = bwd(4, 1335, 1001, 1001, base, base + (64 << 20) + 4, 1001, &a);
+        expect(m == lse::kBwdScalar, "dx at another offset from a boundary than x: elements");
+        m = bwd(4, 4096, 13, 14, base, dx, 14, &a);
+        expect(m == lse::kBwdScalar, "f32 N=13 (3 vectors), not back to back: elements");
+        m = bwd(2, 4096, 9, 9, base, dx, 9, &a);
+        expect(m == lse::kBwdFlat, "bf16 N=9 back to back: the flat array");
+        m = bwd(2, 4096, 5, 5, base, dx, 5, &a);
+        expect(m == lse::kBwdScalar && !a.small && a.block.x == 2 && a.block.y == 128,
+               "bf16 N=5: elements, 2 threads across a row");
+        m = bwd(4, 1 << 16, 132, 133, base, dx, 133, &a);
+        expect(m == lse::kBwdPeel && a.block.x == 9 && a.block.y == 28,
+               "f32 N=132 peeled (33 vectors + 2 slots): 9 threads across a row");
+        m = bwd(4, 1 << 16, 132, 136, base, dx, 136, &a);
+        expect(m == lse::kBwdVector && a.block.x == 9 && !a.small,
+               "f32 N=132 on boundaries (33 vectors): 9 threads across a row");
+    }
+
     std::printf(g_fail ? "planner: %d failures\n" : "planner: ok\n", g_fail);
     return g_fail != 0;
 }

@@ -227,6 +227,11 @@ LSE_API lse_status lse_token_logprob_plan(const void *x, lse_dtype dtype, int64_
  *   dx       device pointer, same element type as x, row b at b * dx_row_stride
  *            (elements, >= N); computed in f32, rounded to nearest-even on store.
  *            dx may be x itself (same row_stride); other overlaps are undefined.
+ *            dx must be aligned to its element size (LSE_ERR_INVALID_ARG).
+ * Loads and stores are 16-byte vectors when each x row and its dx row sit at
+ * the same offset from a 16-byte boundary (rows off a boundary move their head
+ * and tail element by element, or, back to back, as one flat array of
+ * vectors); element by element otherwise.
  * Special values follow IEEE arithmetic on that formula (an all -inf row, whose
  * lse is -inf, gives NaN).  Asynchronous on `stream`; allocates nothing.
  */

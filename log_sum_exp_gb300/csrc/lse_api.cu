@@ -731,6 +731,92 @@ lse_status lse_backward(const void* x, lse_dtype dtype, int64_t B, int64_t N, in
 
 namespace {
 
+// The plan of lse_forward_strided for R > 0 (host logic only): load width,
+// warps per column tile, row splits and grid.  occ(dtype, vec, warps per
+// tile) gives the resident CTAs per SM of a column-kernel variant.
+lse_status plan_columns(const void* x, lse_dtype dtype, int64_t A, int64_t R, int64_t C,
+                        int64_t stride_a, int64_t stride_r, int sms, int (*occ)(int, bool, int),
+                        const lse_plan* req, lse_plan* plan) {
+    const int eb = elem_bytes(dtype);
+    const int64_t outputs = A * C;
+    const int rpath = req ? req->path : LSE_PATH_AUTO;
+    lse_plan p;
+    std::memset(&p, 0, sizeof p);
+    const int64_t epv16 = 16 / eb;
+    const bool aligned = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (stride_r * eb) % 16 == 0 &&
+                         (stride_a * eb) % 16 == 0 && C % epv16 == 0;
+    bool vec = aligned;
+    if (req && req->vector_bytes) {
+        if (req->vector_bytes == 16) {
+            if (!aligned) return LSE_ERR_INVALID_ARG;
+        } else if (req->vector_bytes != 1) {
+            return LSE_ERR_INVALID_ARG;
+        }
+        vec = req->vector_bytes == 16;
+    }
+    const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
+    int64_t units = 0;  // (a, tile) pairs
+    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
+    // Resident warps of the single-warp-tile variant (used to pick WT).
+    const int64_t resident_warps = static_cast<int64_t>(sms) * cols_warps_per_cta(1) *
+                                   occ(dtype, vec, 1);
+    const int64_t batch = cols_rows_per_batch(vec);
+    // Warps per tile (measured on 256 MB of [A, R, C] for R = 2..4096, C =
+    // 128..16384): one warp walks each tile up to R = 64, or whenever the
+    // units alone give every resident warp two; 2 warps up to R = 128 and 4
+    // beyond share a tile (a shared-memory merge is cheaper than a split);
+    // row splits below fill the GPU only where that is still not enough.
+    int WT = req && req->lanes_per_row ? req->lanes_per_row : 0;
+    int path = rpath;
+    if (path == LSE_PATH_COLUMNS_WARP) {
+        if (WT > 1) return LSE_ERR_INVALID_ARG;
+        WT = 1;
+    }
+    if (WT == 0) {
+        if (path == LSE_PATH_COLUMNS_CTA)
+            WT = 8;
+        else
+            WT = (R <= 64 || units >= 2 * resident_warps) ? 1 : (R <= 128 ? 2 : 4);
+    }
+    if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
+    path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
+    const int W = cols_warps_per_cta(WT);
+    int64_t gx = ceil_div(units, W / WT);  // CTAs if each took one group of units
+    const int64_t rows_per_warp_batch = WT * batch;
+    const int64_t resident_ctas = static_cast<int64_t>(sms) * occ(dtype, vec, WT);
+    int64_t P = req ? req->splits : 0;
+    if (P == 0) {
+        // No split while the CTAs already fill half the resident slots (a
+        // split costs a merge kernel); otherwise as many splits as fit in ONE
+        // wave of resident CTAs -- a partial second wave of these long-lived
+        // CTAs would nearly double the time -- keeping >= 4 batches per warp.
+        const int64_t base = gx;
+        P = 2 * base >= resident_ctas ? 1 : resident_ctas / base;
+        const int64_t max_p = R / (4 * rows_per_warp_batch);
+        if (P > max_p) P = max_p;
+        if (P < 1) P = 1;
+    }
+    if (P > R) return LSE_ERR_INVALID_ARG;
+    const int64_t rows_per_split = ceil_div(R, P);
+    P = ceil_div(R, rows_per_split);
+    if (P > 65535) return LSE_ERR_INVALID_ARG;
+    // Beyond a few waves CTAs loop over the units instead of being launched
+    // one per group (tiny groups made the launch itself the bottleneck).
+    if (gx > 4 * resident_ctas) gx = 4 * resident_ctas;
+    if (P > 1 && outputs > INT64_MAX / (8 * P)) return LSE_ERR_INVALID_ARG;
+    p.path = path;
+    p.vector_bytes = vec ? 16 : 1;
+    p.threads = 32 * W;
+    p.lanes_per_row = WT;
+    p.splits = P;
+    p.segment_slots = rows_per_split;
+    p.grid = gx * P;
+    p.scratch_bytes = P > 1 ? outputs * P * static_cast<int64_t>(sizeof(float2)) : 0;
+    p.launches = P > 1 ? 2 : 1;
+    *plan = p;
+    return LSE_OK;
+}
+
 // Elements spanned by an [A, R, C] layout with the given strides (0 when
 // empty), or -1 when its byte extent overflows.
 int64_t strided_extent(int64_t A, int64_t R, int64_t C, int64_t sa, int64_t sr, int eb) {
@@ -861,78 +947,15 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
         return e == cudaSuccess ? LSE_OK : cuda_fail(e);
     }
     if (rpath == LSE_PATH_EMPTY) return LSE_ERR_INVALID_ARG;
-    const int64_t epv16 = 16 / eb;
-    const bool aligned = reinterpret_cast<uintptr_t>(x) % 16u == 0 && (stride_r * eb) % 16 == 0 &&
-                         (stride_a * eb) % 16 == 0 && C % epv16 == 0;
-    bool vec = aligned;
-    if (req && req->vector_bytes) {
-        if (req->vector_bytes == 16) {
-            if (!aligned) return LSE_ERR_INVALID_ARG;
-        } else if (req->vector_bytes != 1) {
-            return LSE_ERR_INVALID_ARG;
-        }
-        vec = req->vector_bytes == 16;
-    }
-    const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
-    int64_t units = 0;  // (a, tile) pairs
-    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
-    // Resident warps of the single-warp-tile variant (used to pick WT).
-    const int64_t resident_warps = static_cast<int64_t>(info->sms) * cols_warps_per_cta(1) *
-                                   cols_occupancy(dtype, vec, 1);
-    const int64_t batch = cols_rows_per_batch(vec);
-    // Warps per tile (measured on 256 MB of [A, R, C] for R = 2..4096, C =
-    // 128..16384): one warp walks each tile up to R = 64, or whenever the
-    // units alone give every resident warp two; 2 warps up to R = 128 and 4
-    // beyond share a tile (a shared-memory merge is cheaper than a split);
-    // row splits below fill the GPU only where that is still not enough.
-    int WT = req && req->lanes_per_row ? req->lanes_per_row : 0;
-    int path = rpath;
-    if (path == LSE_PATH_COLUMNS_WARP) {
-        if (WT > 1) return LSE_ERR_INVALID_ARG;
-        WT = 1;
-    }
-    if (WT == 0) {
-        if (path == LSE_PATH_COLUMNS_CTA)
-            WT = 8;
-        else
-            WT = (R <= 64 || units >= 2 * resident_warps) ? 1 : (R <= 128 ? 2 : 4);
-    }
-    if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
-    path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
-    const int W = cols_warps_per_cta(WT);
-    int64_t gx = ceil_div(units, W / WT);  // CTAs if each took one group of units
-    const int64_t rows_per_warp_batch = WT * batch;
-    const int64_t resident_ctas = static_cast<int64_t>(info->sms) * cols_occupancy(dtype, vec, WT);
-    int64_t P = req ? req->splits : 0;
-    if (P == 0) {
-        // No split while the CTAs already fill half the resident slots (a
-        // split costs a merge kernel); otherwise as many splits as fit in ONE
-        // wave of resident CTAs -- a partial second wave of these long-lived
-        // CTAs would nearly double the time -- keeping >= 4 batches per warp.
-        const int64_t base = gx;
-        P = 2 * base >= resident_ctas ? 1 : resident_ctas / base;
-        const int64_t max_p = R / (4 * rows_per_warp_batch);
-        if (P > max_p) P = max_p;
-        if (P < 1) P = 1;
-    }
-    if (P > R) return LSE_ERR_INVALID_ARG;
-    const int64_t rows_per_split = ceil_div(R, P);
-    P = ceil_div(R, rows_per_split);
-    if (P > 65535) return LSE_ERR_INVALID_ARG;
-    // Beyond a few waves CTAs loop over the units instead of being launched
-    // one per group (tiny groups made the launch itself the bottleneck).
-    if (gx > 4 * resident_ctas) gx = 4 * resident_ctas;
-    if (P > 1 && outputs > INT64_MAX / (8 * P)) return LSE_ERR_INVALID_ARG;
-    p.path = path;
-    p.vector_bytes = vec ? 16 : 1;
-    p.threads = 32 * W;
-    p.lanes_per_row = WT;
-    p.splits = P;
-    p.segment_slots = rows_per_split;
-    p.grid = gx * P;
-    p.scratch_bytes = P > 1 ? outputs * P * static_cast<int64_t>(sizeof(float2)) : 0;
-    p.launches = P > 1 ? 2 : 1;
+    if ((st = plan_columns(x, dtype, A, R, C, stride_a, stride_r, info->sms, cols_occupancy, req,
+                           &p)) != LSE_OK)
+        return st;
     if (plan) *plan = p;
+    const bool vec = p.vector_bytes == 16;
+    const int WT = p.lanes_per_row;
+    const int64_t P = p.splits;
+    const int64_t rows_per_split = p.segment_slots;
+    const int64_t gx = p.grid / P;
 
     float2* scratch = nullptr;
     cudaError_t e = cudaSuccess;

@@ -180,6 +180,51 @@ int main() {
                "f32 N=132 on boundaries (33 vectors): 9 threads across a row");
     }
 
+    // Value over a non-last dimension: one warp per column tile up to R = 64,
+    // 2 or 4 warps sharing a tile beyond, row splits filling one wave.
+    {
+        // Column-kernel CTAs per SM: 8 (f32; 4 warps per CTA), 4 with 8-warp
+        // tiles; 16-bit: 6 one-warp tiles, 7 shared, 3 with 8 warps.
+        auto occ = [](int dt, bool, int wt) -> int {
+            if (dt == LSE_F32) return wt == 8 ? 4 : 8;
+            return wt == 1 ? 6 : (wt == 8 ? 3 : 7);
+        };
+        auto cols = [&](lse_dtype dt, int64_t A, int64_t R, int64_t C, const void* x,
+                        const lse_plan* req, lse_status* st) {
+            lse_plan q;
+            std::memset(&q, 0, sizeof q);
+            *st = plan_columns(x, dt, A, R, C, R * C, C, 152, occ, req, &q);
+            return q;
+        };
+        lse_status cst;
+        lse_plan q = cols(LSE_F32, 512, 64, 1024, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.splits == 1 && q.grid == 1024 &&
+                   q.threads == 128 && q.vector_bytes == 16,
+               "[512, 64, 1024] f32: a warp per tile, no split, 1024 CTAs");
+        q = cols(LSE_F32, 1, 8192, 16384, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_CTA && q.lanes_per_row == 4 &&
+                   q.splits == 9 && q.segment_slots == 911 && q.grid == 1152 && q.launches == 2,
+               "[1, 8192, 16384] f32: 4 warps per tile, 9 splits of 911 rows");
+        q = cols(LSE_F32, 64, 100, 1000, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.lanes_per_row == 2, "R = 100: 2 warps per tile");
+        q = cols(LSE_F32, 512, 64, 1023, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.vector_bytes == 1, "C = 1023: one element per lane");
+        lse_plan r;
+        std::memset(&r, 0, sizeof r);
+        r.vector_bytes = 16;
+        cols(LSE_F32, 512, 64, 1023, kAligned, &r, &cst);
+        expect(cst == LSE_ERR_INVALID_ARG, "vectors forced on C = 1023: invalid");
+        std::memset(&r, 0, sizeof r);
+        r.path = LSE_PATH_COLUMNS_WARP;
+        r.lanes_per_row = 2;
+        cols(LSE_F32, 512, 64, 1024, kAligned, &r, &cst);
+        expect(cst == LSE_ERR_INVALID_ARG, "one-warp path with 2 warps per tile: invalid");
+        std::memset(&r, 0, sizeof r);
+        r.path = LSE_PATH_COLUMNS_CTA;
+        q = cols(LSE_BF16, 4, 512, 4096, kAligned, &r, &cst);
+        expect(cst == LSE_OK && q.lanes_per_row == 8 && q.threads == 256, "forced CTA path: 8 warps per tile");
+    }
+
     std::printf(g_fail ? "planner: %d failures\n" : "planner: ok\n", g_fail);
     return g_fail != 0;
 }

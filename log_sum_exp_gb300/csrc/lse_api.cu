@@ -108,28 +108,6 @@ cudaError_t scratch_alloc(const DeviceInfo& info, void** p, size_t bytes, cudaSt
 
 bool valid_dtype(int dt) { return dt == LSE_F32 || dt == LSE_BF16 || dt == LSE_F16; }
 
-lse_status check_args(const void* x, int dt, int64_t B, int64_t N, int64_t row_stride,
-                      const void* out) {
-    if (!valid_dtype(dt)) return LSE_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || N < 0 || row_stride < N) return LSE_ERR_INVALID_ARG;
-    if (B > 0 && out == nullptr) return LSE_ERR_INVALID_ARG;
-    if (B > 0 && N > 0 && x == nullptr) return LSE_ERR_INVALID_ARG;
-    // Every load is at least one whole element: x must be element aligned.
-    if (B > 0 && N > 0 &&
-        reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(elem_bytes(static_cast<lse_dtype>(dt))) != 0)
-        return LSE_ERR_INVALID_ARG;
-    if (out != nullptr && (reinterpret_cast<uintptr_t>(out) & 3u) != 0) return LSE_ERR_INVALID_ARG;
-    // Byte extent of x and of out must fit in int64.
-    int64_t extent = 0;
-    if (B > 0 && __builtin_mul_overflow(B - 1, row_stride, &extent)) return LSE_ERR_INVALID_ARG;
-    if (__builtin_add_overflow(extent, N, &extent)) return LSE_ERR_INVALID_ARG;
-    if (__builtin_mul_overflow(extent, static_cast<int64_t>(elem_bytes(static_cast<lse_dtype>(dt))),
-                               &extent))
-        return LSE_ERR_INVALID_ARG;
-    if (B > INT64_MAX / 4) return LSE_ERR_INVALID_ARG;
-    return LSE_OK;
-}
-
 int pow2_ceil(int64_t v) {
     int p = 1;
     while (p < v) p <<= 1;
@@ -532,6 +510,29 @@ merge_kernel(const float2* __restrict__ partial, const float* __restrict__ xt_bu
 }
 
 }  // namespace
+
+// Argument checks shared by every row entry point (lse_internal.h).
+lse_status check_args(const void* x, int dt, int64_t B, int64_t N, int64_t row_stride,
+                      const void* out) {
+    if (!valid_dtype(dt)) return LSE_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || N < 0 || row_stride < N) return LSE_ERR_INVALID_ARG;
+    if (B > 0 && out == nullptr) return LSE_ERR_INVALID_ARG;
+    if (B > 0 && N > 0 && x == nullptr) return LSE_ERR_INVALID_ARG;
+    // Every load is at least one whole element: x must be element aligned.
+    if (B > 0 && N > 0 &&
+        reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(elem_bytes(static_cast<lse_dtype>(dt))) != 0)
+        return LSE_ERR_INVALID_ARG;
+    if (out != nullptr && (reinterpret_cast<uintptr_t>(out) & 3u) != 0) return LSE_ERR_INVALID_ARG;
+    // Byte extent of x and of out must fit in int64.
+    int64_t extent = 0;
+    if (B > 0 && __builtin_mul_overflow(B - 1, row_stride, &extent)) return LSE_ERR_INVALID_ARG;
+    if (__builtin_add_overflow(extent, N, &extent)) return LSE_ERR_INVALID_ARG;
+    if (__builtin_mul_overflow(extent, static_cast<int64_t>(elem_bytes(static_cast<lse_dtype>(dt))),
+                               &extent))
+        return LSE_ERR_INVALID_ARG;
+    if (B > INT64_MAX / 4) return LSE_ERR_INVALID_ARG;
+    return LSE_OK;
+}
 
 void record_cuda_error(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "../../include/lse.h"
+
 namespace lse {
 
 constexpr int kSubwarpThreads = 256;
@@ -168,5 +170,10 @@ cudaError_t read_wait_timeouts(unsigned long long* count);
 
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);
+
+// The argument checks of the row entry points (lse_api.cu): dtype, B, N,
+// row_stride, NULL and alignment of x and out, int64 byte extent.
+lse_status check_args(const void* x, int dt, int64_t B, int64_t N, int64_t row_stride,
+                      const void* out);
 
 }  // namespace lse

@@ -98,19 +98,11 @@ using namespace lse;
 extern "C" lse_status lse_forward_split_static(const void* x, lse_dtype dtype, int64_t B,
                                                int64_t N, int64_t row_stride, float* out,
                                                lse_stream_t stream_) {
-    if (dtype != LSE_F32 && dtype != LSE_BF16 && dtype != LSE_F16) return LSE_ERR_UNSUPPORTED_DTYPE;
-    if (B < 0 || N < 0 || row_stride < N) return LSE_ERR_INVALID_ARG;
+    lse_status st = check_args(x, dtype, B, N, row_stride, out);
+    if (st != LSE_OK) return st;
     if (B == 0) return LSE_OK;
-    if (x == nullptr || out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
-        return LSE_ERR_INVALID_ARG;
-    const int eb = dtype == LSE_F32 ? 4 : 2;
-    if (reinterpret_cast<uintptr_t>(x) % static_cast<uintptr_t>(eb) != 0) return LSE_ERR_INVALID_ARG;
     if (B > kScratchPartials / 2) return LSE_ERR_INVALID_ARG;  // needs >= 2 partials per row
-    int64_t extent = 0;
-    if (__builtin_mul_overflow(B - 1, row_stride, &extent) ||
-        __builtin_add_overflow(extent, N, &extent) ||
-        __builtin_mul_overflow(extent, static_cast<int64_t>(eb), &extent))
-        return LSE_ERR_INVALID_ARG;
+    const int eb = dtype == LSE_F32 ? 4 : 2;
     // 16-byte vectors; rows off a 16-byte boundary peel their head and tail
     // into element loads, unless they hold fewer than two vectors.
     const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16u == 0) && ((row_stride * eb) % 16 == 0);
@@ -119,7 +111,7 @@ extern "C" lse_status lse_forward_split_static(const void* x, lse_dtype dtype, i
     if (slots < 2) return LSE_ERR_INVALID_ARG;     // too short to split
 
     const StaticScratch* s = nullptr;
-    lse_status st = setup(&s);
+    st = setup(&s);
     if (st != LSE_OK) return st;
 
     // Splits per row: cover the GPU ~4 times over, >= 1 batch per segment,

@@ -142,11 +142,13 @@ def ncu_traffic(workload_key: str, plan: dict, op: str = "forward") -> float | N
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms, each sample
+    with its timestamp so a summary can keep the samples of one window."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
@@ -174,25 +176,37 @@ class ClockSampler:
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
         return False
 
-    def summary(self) -> dict:
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, flag in zip(names, parts[5:9]):
-                if flag.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+    @staticmethod
+    def parse(line: str):
+        """(unix time, sm MHz, max sm MHz, active throttle reasons) of one
+        sample line, or None."""
+        import datetime
+
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            return None
+        try:
+            t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, smax = float(parts[2]), float(parts[3])
+        except ValueError:
+            return None
+        reasons = [n for n, f in zip(ClockSampler.REASONS, parts[6:10])
+                   if f.lower().startswith("active")]
+        return t, sm, smax, reasons
+
+    def summary(self, t_from: float | None = None, t_to: float | None = None) -> dict:
+        """Median SM clock, max clock and throttle reasons over the samples
+        taken in [t_from, t_to] (every sample when none falls in it)."""
+        samples = [s for s in map(self.parse, self.lines) if s is not None]
+        inside = [s for s in samples if (t_from is None or s[0] >= t_from) and
+                  (t_to is None or s[0] <= t_to)]
+        chosen = inside or samples
+        if not chosen:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(s[1] for s in chosen),
+                "sm_max_mhz": max(s[2] for s in chosen),
+                "reasons": sorted({r for s in chosen for r in s[3]}), "samples": len(chosen),
+                "samples_in_window": len(inside)}
 
 
 # ---------------------------------------------------------------------------
@@ -344,6 +358,95 @@ def run_reference(args) -> None:
 
 
 # ---------------------------------------------------------------------------
+# Host logic of the timing (also exercised by the CPU tests).
+# ---------------------------------------------------------------------------
+ROTATION_BYTES_MAX = 4 << 30  # device bytes the rotating input copies may take
+CONFIG_STEPS_MIN = 200        # timed calls per config in per_config (>= 200 calls)
+CONFIG_ORACLE_S = 2.0         # oracle seconds per config in per_config
+CONFIG_BLOCKS = 4             # event blocks per config region (3 events inside 200+ calls)
+REPEATS = 5                   # clean K-step regions repeated after the headline region
+CLOCK_PROBE_S = 0.4           # the same step, untimed, after the region: clocks under load
+SWEEP_BYTES = 512 << 20       # input bytes per step of the throughput-vs-N sweep
+SWEEP_N = [16, 31, 32, 33, 64, 100, 128, 129, 256, 257, 300, 512, 520, 1000, 1024, 1025,
+           2048, 4096, 4097, 8192, 16383, 16384, 32000, 32768, 50257, 65536, 128256, 262144,
+           1048576, 4194304, 16777216]
+
+
+def rotation_copies(in_bytes: int, l2_bytes: int = L2_BYTES,
+                    max_bytes: int = ROTATION_BYTES_MAX) -> int:
+    """Input copies to rotate over so that each step reads rows that at least
+    3x the L2 capacity of other copies' traffic has passed since (inputs
+    larger than L2), within max_bytes of device memory."""
+    if in_bytes <= 0:
+        return 1
+    want = -(-3 * l2_bytes // in_bytes)
+    return int(max(1, min(want, max_bytes // in_bytes)))
+
+
+def block_bounds(K: int, blocks: int) -> list[int]:
+    """Step indices 0 = b_0 < b_1 < ... < b_n = K cutting K steps into
+    min(blocks, K) nearly equal blocks."""
+    n = max(1, min(blocks, K))
+    return [round(i * K / n) for i in range(n + 1)]
+
+
+def block_stats(bounds: list[int], block_ms: list[float]) -> dict:
+    """µs per step of each block of back-to-back steps, their median, and the
+    means over the first and the second half of the blocks (by steps)."""
+    if not block_ms:
+        return {}
+    steps = [b - a for a, b in zip(bounds, bounds[1:])]
+    per = [1e3 * t / n for t, n in zip(block_ms, steps)]
+    h = len(per) // 2
+
+    def mean(lo, hi):
+        n = sum(steps[lo:hi])
+        return 1e3 * sum(block_ms[lo:hi]) / n
+
+    first, second = (mean(0, h), mean(h, len(per))) if h else (per[0], per[0])
+    return {"us_per_step_blocks": per, "us_median": statistics.median(per),
+            "us_mean": 1e3 * sum(block_ms) / sum(steps),
+            "us_mean_first_half": first, "us_mean_second_half": second,
+            "steps": sum(steps), "blocks": len(per)}
+
+
+def main_kernel_name(plan: dict) -> str:
+    """The kernel that moves the bytes in a plan (the roofline's kernel)."""
+    path = plan["path"]
+    if path == "rowtile" and plan.get("slots_per_lane") == 0:
+        return "lse_rowtile_any_kernel"  # rows of any width
+    return {"subwarp": "lse_subwarp_kernel", "rowtile": "lse_rowtile_kernel",
+            "cta": "lse_segment_kernel", "split": "lse_segment_kernel",
+            "empty": "fill_neg_inf_kernel", "backward": plan.get("kernel"),
+            "columns_warp": "lse_cols_kernel", "columns_cta": "lse_cols_kernel",
+            "columns_backward": "lse_backward_strided_kernel"}[path]
+
+
+def sweep_shape(N: int, eb: int, total: int = SWEEP_BYTES) -> tuple[int, int]:
+    """(B, N) of one sweep point: rows of N elements filling ~total bytes."""
+    return max(1, total // (N * eb)), N
+
+
+def sweep_table(points: list[dict]) -> str:
+    """Markdown table of sweep points."""
+    lines = ["| dtype | N | B | plan | µs / call (median) | GB/s | frac of measured |",
+             "|---|---|---|---|---|---|---|"]
+    for q in points:
+        p = q["plan"]
+        desc = p["path"]
+        if p["path"] in ("cta", "split"):
+            desc += f" T={p['threads']}" + (f" P={p['splits']}" if p["splits"] > 1 else "")
+        elif p["path"] == "subwarp":
+            desc += f" G={p['lanes_per_row']} V={p['slots_per_lane']}"
+        elif p["path"] == "rowtile":
+            desc += f" {'any-width' if p['slots_per_lane'] == 0 else str(p['slots_per_lane']) + ' vec'}" \
+                    + (f" G={p['lanes_per_row']}" if p["slots_per_lane"] == 0 else "")
+        lines.append(f"| {q['dtype']} | {q['N']} | {q['B']} | {desc} | {q['us_median']:.2f} | "
+                     f"{q['gbs']:.0f} | {q['frac']:.3f} |")
+    return "\n".join(lines)
+
+
+# ---------------------------------------------------------------------------
 # The native arm.
 # ---------------------------------------------------------------------------
 def to_torch(x: np.ndarray, dtype: str):
@@ -355,6 +458,158 @@ def to_torch(x: np.ndarray, dtype: str):
     return torch.from_numpy(x.view(np.int16)).view(tdt)
 
 
+def timed_steps(step, K: int, stream, blocks: int = 1, event_every: dict | None = None,
+                first: int = 0):
+    """Run step(first .. first+K-1) back to back, with CUDA events only at the
+    block bounds (block_bounds(K, blocks)): an event between two launches
+    removes their programmatic overlap (measured: +4.5 µs on a 40 µs step), so
+    a one-block region has none inside it.  Returns (bounds, total ms, ms per
+    block).  event_every maps a step index to (begin, end) events handed to
+    the step (its main kernel)."""
+    import torch
+
+    bounds = block_bounds(K, blocks)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in bounds]
+    evs[0].record(stream)
+    b = 1
+    for i in range(K):
+        if event_every and i in event_every:
+            step(first + i, event_every[i][0].cuda_event, event_every[i][1].cuda_event)
+        else:
+            step(first + i)
+        if i + 1 == bounds[b]:
+            evs[b].record(stream)
+            b += 1
+    torch.cuda.synchronize()
+    per = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(bounds) - 1)]
+    return bounds, evs[0].elapsed_time(evs[-1]), per
+
+
+def graph_us_per_call(L, xs, outs, plan_req, stream, dev, reps: int = 100) -> float:
+    """lse_forward replayed from a CUDA graph of `reps` calls over the rotating
+    copies: µs per call with the launch overhead removed."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream(dev)
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        L.lse_forward_plan(xs[0], plan=plan_req, out=outs[0])
+    stream.wait_stream(s2)
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            L.lse_forward_plan(xs[i % len(xs)], plan=plan_req, out=outs[i % len(xs)])
+    g.replay()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(10):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    return 1e3 * t0.elapsed_time(t1) / (10 * reps)
+
+
+def measure_config(L, key: str, rank: int, dev, stream, steps: int, peak: float,
+                   graph: bool = True) -> tuple[dict, np.ndarray]:
+    """One row workload through lse_forward: µs per call (per-step CUDA events,
+    inputs rotated past L2), GB/s and fraction of the measured peak, and the
+    CUDA-graph µs per call.  Returns (entry, a host sample for the oracle)."""
+    import torch
+
+    w = wl.WORKLOADS[key]
+    x_host = wl.generate(key, seed=rank_seed(w, rank))
+    in_bytes = w.B * w.N * w.elem_bytes
+    copies = rotation_copies(in_bytes)
+    xt = to_torch(x_host, w.dtype)
+    xs = [xt.to(dev) for _ in range(copies)]
+    outs = [torch.empty(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
+    ptrs = [(t.data_ptr(), o.data_ptr()) for t, o in zip(xs, outs)]
+    sh = stream.cuda_stream
+    plan = L.lse_plan_query(xs[0])
+
+    def step(i, evb=0, eve=0):
+        xp, op = ptrs[i % copies]
+        L.lse_forward_plan_ptr(xp, w.dtype, w.B, w.N, w.N, op, sh, None, evb, eve)
+
+    for i in range(10):
+        step(i)
+    torch.cuda.synchronize(dev)
+    K = max(steps, CONFIG_STEPS_MIN)
+    bounds, total_ms, per = timed_steps(step, K, stream, blocks=CONFIG_BLOCKS)
+    stats = block_stats(bounds, per)
+    bytes_per_call = in_bytes + w.write_bytes
+    us_mean = 1e3 * total_ms / K
+    entry = {"workload": key, "B": w.B, "N": w.N, "input_dtype": w.dtype,
+             "plan": {k: plan[k] for k in ("path", "threads", "splits", "grid", "lanes_per_row",
+                                           "slots_per_lane", "launches")},
+             "kernel": main_kernel_name(plan), "bytes_per_call": bytes_per_call,
+             "us_per_call": us_mean, "us_median_of_blocks": stats["us_median"],
+             "us_mean_first_half": stats["us_mean_first_half"],
+             "us_mean_second_half": stats["us_mean_second_half"], "calls": K,
+             "timing": f"CUDA events at {CONFIG_BLOCKS + 1} points of {K} back-to-back calls "
+                       f"(inputs in HBM); us_per_call = total / {K}",
+             "gbs": bytes_per_call / (us_mean * 1e-6) / 1e9,
+             "frac": bytes_per_call / (us_mean * 1e-6) / 1e9 / peak,
+             "traffic": ncu_traffic(key, plan, "forward"),
+             "l2": f"{copies} rotating copies of {in_bytes / 1e6:.1f} MB (L2 {L2_BYTES / 1e6:.0f} MB)"}
+    entry["us_per_call_graph"] = graph_us_per_call(L, xs, outs, None, stream, dev) if graph else None
+    del xs, outs
+    torch.cuda.empty_cache()
+    rows = max(1, min(w.B, oracle_sample_rows(w, CONFIG_ORACLE_S / 4)))
+    return entry, x_host[:rows].copy()
+
+
+def run_sweep(args) -> None:
+    """Throughput of lse_forward against the row length N at ~512 MB of input
+    per call, f32 and bf16, automatic plan: one JSON line per point, then a
+    markdown table."""
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from log_sum_exp_gb300 import build as lse_build
+    lse_build.build()
+    import log_sum_exp_gb300 as L
+
+    peak, _ = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    points = []
+    for dtype in ("f32", "bf16"):
+        eb = 4 if dtype == "f32" else 2
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        for N in SWEEP_N:
+            B, N = sweep_shape(N, eb)
+            gen.manual_seed(wl.SEED_BASE + 100 + N)
+            # Two copies of ~512 MB each: every call reads rows absent from L2.
+            xs = [(3.0 * torch.randn(B, N, device=dev, generator=gen)).to(tdt) for _ in range(2)]
+            outs = [torch.empty(B, dtype=torch.float32, device=dev) for _ in range(2)]
+            plan = L.lse_plan_query(xs[0])
+
+            def step(i, evb=0, eve=0):
+                L.lse_forward_plan_ptr(xs[i % 2].data_ptr(), dtype, B, N, N, outs[i % 2].data_ptr(),
+                                       sh, None)
+
+            for i in range(5):
+                step(i)
+            torch.cuda.synchronize(dev)
+            bounds, _, per = timed_steps(step, args.sweep_steps, stream, blocks=3)
+            st = block_stats(bounds, per)
+            nbytes = B * N * eb + 4 * B
+            q = {"dtype": dtype, "N": N, "B": B, "plan": plan, "us_median": st["us_median"],
+                 "gbs": nbytes / (st["us_median"] * 1e-6) / 1e9}
+            q["frac"] = q["gbs"] / peak
+            points.append(q)
+            print(json.dumps(q), flush=True)
+            del xs, outs
+            torch.cuda.empty_cache()
+    print(sweep_table(points), flush=True)
+
+
 def run_native(args) -> None:
     import torch
     import torch.distributed as dist
@@ -364,10 +619,25 @@ def run_native(args) -> None:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    clocks = ClockSampler(local_rank)
+    clocks.__enter__()
 
     from log_sum_exp_gb300 import build as lse_build
     lse_build.build()
     import log_sum_exp_gb300 as L
+
+    peak, peak_src = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # The five row workloads, each through lse_forward (one GPU, rank 0).
+    per_config, config_samples = None, {}
+    if args.op == "forward" and args.per_config and world == 1:
+        per_config = {}
+        for key in wl.ORDER:
+            entry, sample = measure_config(L, key, rank, dev, stream, args.steps, peak, args.graph)
+            per_config[key] = entry
+            config_samples[key] = sample
 
     if args.op in COLUMN_OPS:
         cw = wl.COLUMN_WORKLOADS[args.workload]
@@ -380,13 +650,9 @@ def run_native(args) -> None:
         x_host = wl.generate(args.workload, seed=rank_seed(w, rank))
     xt_host = to_torch(x_host, w.dtype)
     in_bytes = w.B * w.N * w.elem_bytes
-    # Rotate over enough copies that consecutive steps never find their rows in L2.
-    copies = max(1, -(-3 * L2_BYTES // max(in_bytes, 1)))
-    copies = min(copies, 64)
+    copies = rotation_copies(in_bytes)
     xs = [xt_host.to(dev) for _ in range(copies)]
     outs = [torch.empty(w.B, dtype=torch.float32, device=dev) for _ in range(copies)]
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
     dt = w.dtype
     ptrs = [(t.data_ptr(), o.data_ptr()) for t, o in zip(xs, outs)]
     op_name = args.op
@@ -457,67 +723,50 @@ def run_native(args) -> None:
             L.lse_backward_ptr(ptrs[c][0], dt, w.B, w.N, w.N, lses[c].data_ptr(), gs[c].data_ptr(),
                                dxs[c].data_ptr(), w.N, sh)
 
+    # W untimed warm-up steps right before the timed region (no idle gap).
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-
     K = args.steps
-    # Every EVENT_EVERY-th timed step brackets its main kernel with events (the
-    # roofline's launch duration); the other steps run back to back untouched.
-    # A one-kernel plan needs no per-step events: its launches are the whole
-    # timed region.  Multi-kernel plans sample the main kernel's duration.
+    # One clean region: events only before the first step and after the last
+    # (an event between two launches would cost them their programmatic
+    # overlap).  For a two-kernel row-value plan, every EVENT_EVERY-th step
+    # also brackets its main kernel (the roofline's launch duration).
     sampled = list(range(0, K, EVENT_EVERY)) \
         if plan["launches"] > 1 and op_name == "forward" else []
-    kb = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
-    ke = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
-    for e in list(kb.values()) + list(ke.values()):
-        e.record(stream)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
+    kev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for i in sampled}
     barrier(dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clocks:
-        time.sleep(0.25)  # a clock sample before the timed region
-        start.record(stream)
-        for i in range(K):
-            if i in kb:
-                step(i, kb[i].cuda_event, ke[i].cuda_event)
-            else:
-                step(i)
-        end.record(stream)
-        torch.cuda.synchronize(dev)
-        time.sleep(0.25)
+    t_region = time.time()
+    _, ms_total, _ = timed_steps(step, K, stream, 1, kev)
+    t_region_end = time.time()
     barrier(dev)
-    ms_total = start.elapsed_time(end)
-    kernel_ms = [kb[i].elapsed_time(ke[i]) for i in sampled]
+    # The same K-step region repeated (clean): start-up against steady state.
+    repeats = [timed_steps(step, K, stream, 1, None, (r + 1) * K)[1] for r in range(REPEATS)]
+    # Clocks under the same load: the same step, untimed, for CLOCK_PROBE_S after the region.
+    t0 = time.perf_counter()
+    i = (REPEATS + 1) * K
+    while time.perf_counter() - t0 < CLOCK_PROBE_S:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    t_probe_end = time.time()
+    kernel_ms = [kev[i][0].elapsed_time(kev[i][1]) for i in sampled]
     ms_total = reduce_max(ms_total, dev)
     ms_per_step = ms_total / K
     value = world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    region_us = [1e3 * ms_per_step] + [1e3 * t / K for t in repeats]
+    steps_summary = {"region_means_us": region_us, "median_of_regions_us": statistics.median(region_us),
+                     "about": f"the timed region, then the same {K} steps {REPEATS} more times, "
+                              f"each region clean (events at its ends only)"}
 
     # Graph-replayed µs/call (launch overhead removed), same step.
     graph_us = None
     if args.graph and op_name == "forward":
-        g = torch.cuda.CUDAGraph()
-        s2 = torch.cuda.Stream(dev)
-        s2.wait_stream(stream)
-        with torch.cuda.stream(s2):
-            L.lse_forward_plan(xs[0], plan=args.plan, out=outs[0])
-        stream.wait_stream(s2)
-        reps = 100
-        with torch.cuda.graph(g):
-            for i in range(reps):
-                L.lse_forward_plan(xs[i % copies], plan=args.plan, out=outs[i % copies])
-        g.replay()
-        torch.cuda.synchronize(dev)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(10):
-            g.replay()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-        graph_us = 1e3 * t0.elapsed_time(t1) / (10 * reps)
+        graph_us = graph_us_per_call(L, xs, outs, args.plan, stream, dev)
 
     # End to end through the host entry point: H2D of x, compute, D2H of out.
     e2e = None
@@ -537,30 +786,26 @@ def run_native(args) -> None:
                "steps": e2e_steps,
                "call": "lse_forward_host on page-locked host x and out: the kernel "
                        "streams x over NVLink-C2C in place (zero copy), writes out in place"}
+    clocks.__exit__(None, None, None)
 
     if rank != 0:
         return
-    peak, peak_src = measured_peaks()
     if kernel_ms:
         kmean_ms = sum(kernel_ms) / len(kernel_ms)
         kmed_ms = statistics.median(kernel_ms)
         timing = (f"CUDA events around the main kernel on every {EVENT_EVERY}th timed step "
                   f"({len(kernel_ms)} launches); includes the launch latency they bracket")
     else:
-        kmean_ms = kmed_ms = ms_per_step
+        kmean_ms = ms_per_step
+        kmed_ms = steps_summary["median_of_regions_us"] * 1e-3
         timing = (f"one-kernel plan: CUDA events around the {K} back-to-back launches of the "
-                  f"timed region, divided by {K}") if plan["launches"] == 1 else \
+                  f"timed region, divided by {K}; median over that region and {REPEATS} "
+                  f"repeats of it") if plan["launches"] == 1 else \
                  (f"{plan['launches']} kernels per step: CUDA events around the {K} steps of the "
-                  f"timed region, divided by {K} (main kernel and merge together)")
+                  f"timed region, divided by {K} (main kernel and merge together); median over "
+                  f"that region and {REPEATS} repeats of it")
     achieved = bytes_per_step / (kmean_ms * 1e-3) / 1e9
-    main_kernel = {"subwarp": "lse_subwarp_kernel", "rowtile": "lse_rowtile_kernel",
-                   "cta": "lse_segment_kernel",
-                   "split": "lse_segment_kernel", "empty": "fill_neg_inf_kernel",
-                   "backward": plan.get("kernel"), "columns_warp": "lse_cols_kernel",
-                   "columns_cta": "lse_cols_kernel",
-                   "columns_backward": "lse_backward_strided_kernel"}[plan["path"]]
-    if plan["path"] == "rowtile" and plan.get("slots_per_lane") == 0:
-        main_kernel = "lse_rowtile_any_kernel"  # rows of any width
+    main_kernel = main_kernel_name(plan)
     traffic = ncu_traffic(args.workload, plan, op_name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": main_kernel,
@@ -576,6 +821,10 @@ def run_native(args) -> None:
         else:
             rows = oracle_sample_rows(w, args.cpu_seconds / 4)
             cpu = time_oracle(x_host[:rows], w, args.cpu_seconds, op_name)
+        if per_config is not None:
+            for key, entry in per_config.items():
+                entry["cpu_baseline"] = time_oracle(config_samples[key], wl.WORKLOADS[key],
+                                                    CONFIG_ORACLE_S)
     metric = METRIC if op_name == "forward" else f"{METRIC} [{OP_NAMES[op_name]}]"
     line = {
         "metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -597,12 +846,17 @@ def run_native(args) -> None:
         "read_gbs": world * in_bytes / (ms_per_step * 1e-3) / 1e9,
         "pct_of_spec_8tbs": 100.0 * value / SPEC_HBM_GBS,
         "us_per_call_graph": graph_us,
+        "step_times": steps_summary,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * plan["launches"],
-        "clocks": clocks.summary(),
+        "clocks": {**clocks.summary(t_region - 0.05, t_probe_end + 0.05),
+                   "window": f"the {1e3 * (t_region_end - t_region):.1f} ms timed region and "
+                             f"{CLOCK_PROBE_S} s of the same step right after it"},
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
 
 
@@ -625,6 +879,13 @@ def main(argv=None) -> None:
     ap.add_argument("--plan", type=json.loads, default=None,
                     help='forced plan as JSON (fields of lse_plan, path by name), e.g. '
                          '{"path": "subwarp"} or, for --op columns, {"path": "columns_cta"}')
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the per_config block (every row workload timed through "
+                         "lse_forward before the headline step)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="throughput against N at ~512 MB per call (f32, bf16): JSON lines "
+                         "and a markdown table instead of the bench line")
+    ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -640,6 +901,8 @@ def main(argv=None) -> None:
                  "the row workloads")
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_native(args)
 

@@ -307,9 +307,27 @@ LSE_API lse_status lse_trim_memory(void);
  * the library was loaded, on the current device (synchronous read).  Kernels
  * that wait for their own asynchronous copies (LSE_PATH_ROWTILE) stop and
  * count here instead of waiting forever; a non-zero count means results of
- * such a launch are incomplete.  Zero in correct operation.
+ * such a launch are incomplete.  Zero in correct operation.  A launch whose
+ * wait gave up has still returned LSE_OK from its entry point (the wait runs
+ * on the device after the call returned): this counter is the only report.
  */
 LSE_API lse_status lse_wait_timeouts(unsigned long long *count);
+
+/* Poll limit of the LSE_PATH_ROWTILE stage waits unless changed below. */
+#define LSE_DEFAULT_WAIT_POLLS (1u << 26)
+
+/*
+ * lse_set_wait_limit -- testing aid: the number of mbarrier polls after which
+ * a LSE_PATH_ROWTILE stage wait gives up, for every launch that follows in
+ * this process (all devices).  LSE_DEFAULT_WAIT_POLLS restores the default;
+ * 0 makes every stage wait give up at once.  A wait that gives up stops its
+ * warp (or CTA): the rows it had not finished are left unwritten, the warp
+ * first waits, with the default limit, for the bulk copies it already issued
+ * so that none is in flight when it exits, lse_wait_timeouts counts one, and
+ * the entry point that launched it has returned LSE_OK.  Not for production
+ * use: it exists so that tests can run the give-up path without a hang.
+ */
+LSE_API lse_status lse_set_wait_limit(uint32_t polls);
 
 /* Short English description of a status code (static storage). */
 LSE_API const char *lse_status_string(lse_status status);

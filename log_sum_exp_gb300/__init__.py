@@ -7,6 +7,7 @@ Wall, Integer Arithmetic at the Compute Wall" (Sec. 3.1, FuseLSE).
 """
 from ._binding import (  # noqa: F401
     ABI_FUNCTIONS,
+    DEFAULT_WAIT_POLLS,
     DTYPES,
     PATHS,
     LseError,
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     lse_forward_strided_ptr,
     lse_plan_query,
     lse_plan_query_ptr,
+    lse_set_wait_limit,
     lse_token_logprob,
     lse_token_logprob_ptr,
     lse_trim_memory,

@@ -24,7 +24,7 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 ABI_FUNCTIONS = ["lse_forward", "lse_plan_query", "lse_forward_plan", "lse_forward16",
                  "lse_forward_host", "lse_token_logprob", "lse_token_logprob_plan",
                  "lse_backward", "lse_forward_strided", "lse_backward_strided",
-                 "lse_trim_memory", "lse_wait_timeouts", "lse_status_string",
+                 "lse_trim_memory", "lse_wait_timeouts", "lse_set_wait_limit", "lse_status_string",
                  "lse_last_cuda_error", "lse_forward_split_static"]
 
 
@@ -107,6 +107,8 @@ def load() -> ctypes.CDLL:
         lib.lse_backward_strided.restype = i32
         lib.lse_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
         lib.lse_wait_timeouts.restype = i32
+        lib.lse_set_wait_limit.argtypes = [ctypes.c_uint32]
+        lib.lse_set_wait_limit.restype = i32
         lib.lse_trim_memory.argtypes = []
         lib.lse_trim_memory.restype = i32
         lib.lse_status_string.argtypes = [i32]
@@ -134,6 +136,15 @@ def lse_wait_timeouts() -> int:
     v = ctypes.c_ulonglong(0)
     _check(load().lse_wait_timeouts(ctypes.byref(v)), "lse_wait_timeouts")
     return v.value
+
+
+DEFAULT_WAIT_POLLS = 1 << 26
+
+
+def lse_set_wait_limit(polls: int) -> None:
+    """Testing aid: poll limit of the bulk-copy ring's stage waits for later
+    launches (DEFAULT_WAIT_POLLS restores it; 0 gives up at once)."""
+    _check(load().lse_set_wait_limit(polls), "lse_set_wait_limit")
 
 
 def status_string(status: int) -> str:

@@ -222,7 +222,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
             rowtile_any_ok ? rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)) : 1;
         if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
-        else if (rowtile_any_ok && row_bytes <= 128 && B >= any_rows * info.sms * rowtile_ctas_per_sm())
+        else if (rowtile_any_ok && row_bytes <= 128 && B >= any_rows * info.sms * rowtile_any_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
         // Back-to-back rows of more than 512 bytes take the grouped ring where
         // the sub-warp mapping would leave more than a third of its slots empty
@@ -232,7 +232,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         // 3.5 -> 4.6), 0.85-0.95x where the sub-warp slots are full, and
         // mixed below 512 bytes (f32 N = 65: 1.29x, N = 68: 0.91x; bf16
         // N = 150: 0.94x).
-        else if (rowtile_any_ok && row_bytes > 512 && B >= any_rows * info.sms * rowtile_ctas_per_sm() &&
+        else if (rowtile_any_ok && row_bytes > 512 && B >= any_rows * info.sms * rowtile_any_ctas_per_sm() &&
                  (nvt > sub_capacity || 3 * nvt < 2 * subwarp_auto_slots(nvt, vec)))
             path = LSE_PATH_ROWTILE;
         else
@@ -246,7 +246,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
             any_lanes = L;
         }
         const int64_t chunks = ceil_div(B, rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)));
-        int64_t grid = static_cast<int64_t>(info.sms) * rowtile_ctas_per_sm();
+        int64_t grid = static_cast<int64_t>(info.sms) * rowtile_any_ctas_per_sm();
         if (grid > chunks) grid = chunks;
         if (grid < 1) grid = 1;
         p.path = LSE_PATH_ROWTILE;
@@ -1059,6 +1059,11 @@ lse_status lse_forward_host(const void* x_host, lse_dtype dtype, int64_t B, int6
     if (st != LSE_OK) return st;
     if (e != cudaSuccess) return cuda_fail(e);
     if (es != cudaSuccess) return cuda_fail(es);
+    return LSE_OK;
+}
+
+lse_status lse_set_wait_limit(uint32_t polls) {
+    set_stage_wait_polls(polls);
     return LSE_OK;
 }
 

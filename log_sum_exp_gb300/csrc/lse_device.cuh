@@ -158,6 +158,26 @@ __device__ __forceinline__ void store_row(float* out, float* logprob, int64_t ro
     if (logprob) logprob[row] = xt - lse;
 }
 
+// The words of one 16-byte vector that starts at byte vb of a row's
+// surroundings, with every element outside the row's bytes [rb0, rb1)
+// replaced by -inf (f32 words whole, 16-bit elements by halves).
+template <int DT>
+__device__ __forceinline__ void mask_words(uint32_t (&w)[4], uint32_t vb, uint32_t rb0,
+                                           uint32_t rb1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = vb + 4u * i;
+        if constexpr (DT == kF32) {
+            if (b < rb0 || b >= rb1) w[i] = kNegInfF32;
+        } else {
+            const uint32_t ninf = neg_inf_word<DT>();  // -inf in both halves
+            const uint32_t lo = (b < rb0 || b >= rb1) ? (ninf & 0xffffu) : (w[i] & 0xffffu);
+            const uint32_t hi = (b + 2 < rb0 || b + 2 >= rb1) ? (ninf & 0xffff0000u) : (w[i] & 0xffff0000u);
+            w[i] = lo | hi;
+        }
+    }
+}
+
 // Element i (0 .. elements-per-vector - 1) of a 16-byte vector held as 4 words.
 template <int DT>
 __device__ __forceinline__ float word_elem(const uint32_t* w4, int i) {

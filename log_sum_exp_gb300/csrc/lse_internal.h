@@ -163,10 +163,15 @@ int cols_warps_per_cta(int warps_per_tile);
 // nv 0: rows of any width; lanes per row 1 (rows of <= 128 bytes) or 4..32.
 cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid);
 int rowtile_ctas_per_sm();
-int rowtile_rows_per_chunk(int nv);
+int rowtile_rows_per_chunk(int nv);  // rows a CTA takes per round (one chunk per warp)
+int rowtile_any_ctas_per_sm();
 int rowtile_any_rows_per_chunk(int row_bytes);  // nv == 0: rows of any width
 int rowtile_any_max_row_bytes();
 cudaError_t read_wait_timeouts(unsigned long long* count);
+// Poll limit of the rings' stage waits (the drain after a timeout keeps the
+// default limit).
+void set_stage_wait_polls(uint32_t polls);
+uint32_t default_stage_wait_polls();
 
 // Sets the calling thread's error reported by lse_last_cuda_error.
 void record_cuda_error(cudaError_t e);

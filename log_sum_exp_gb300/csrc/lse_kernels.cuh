@@ -25,47 +25,12 @@
 
 namespace lse {
 
-// Raw 32-bit words of up to 4 tail elements (fewer than one vector) starting at
-// element `start`, padded with -inf; 16-bit elements are packed in pairs.
-template <int DT>
-__device__ __forceinline__ void load_tail_words(const void* row, int64_t start, int count,
-                                                uint32_t (&w)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = neg_inf_word<DT>();
-    if constexpr (DT == kF32) {
-        const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + start;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < count) w[i] = __ldg(p + i);
-    } else {
-        const unsigned short* p = reinterpret_cast<const unsigned short*>(row) + start;
-        const uint32_t ninf_half = neg_inf_word<DT>() & 0xffffu;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t h = i < count ? static_cast<uint32_t>(__ldg(p + i)) : ninf_half;
-            if (i & 1)
-                w[i >> 1] = (w[i >> 1] & 0xffffu) | (h << 16);
-            else
-                w[i >> 1] = (w[i >> 1] & 0xffff0000u) | h;
-        }
-    }
-}
-
-// Elements of a row before its first 16-byte boundary (the scalar head peel
-// of a row that does not start on one); the vectors start right after.
-template <int DT>
-__device__ __forceinline__ int head_elems(const void* row, int64_t N) {
-    const int h = static_cast<int>((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row)) & 15u)) & 15u) /
-                  DType<DT>::bytes;
-    return N < h ? static_cast<int>(N) : h;
-}
-
 // ---------------------------------------------------------------------------
 // subwarp: G lanes per row, V slots per lane, R row-groups per warp iteration.
-// VEC: a slot is one 16-byte vector of the row's aligned part; a row that does
-// not start on a 16-byte boundary peels its head (< EPV elements) and tail
-// (< EPV elements) into two more slots: slot nv holds the tail, the slot after
-// it the head (nv = full vectors of that row).  !VEC: a slot is one element.
+// VEC: a slot is one 16-byte vector of the aligned span covering the row; a
+// row that does not start or end on a 16-byte boundary takes one or two more
+// slots than its full vectors, whose outside elements are masked.  !VEC: a
+// slot is one element.
 // V = 8 (a whole warp per row of up to 256 slots, or 4-16 lanes per row of
 // vectors: twice the rows in flight of V = 4 with half the lanes) keeps 32
 // words per lane and runs at 4 CTAs per SM.
@@ -82,7 +47,6 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                    float* __restrict__ out, const int64_t* __restrict__ target,
                    float* __restrict__ logprob) {
     constexpr int EB = DType<DT>::bytes;
-    constexpr int EPV = VEC ? 16 / EB : 1;  // elements per slot
     constexpr int RPW = 32 / G;             // rows per warp per row-group
     constexpr int R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
     const int lane = threadIdx.x & 31;
@@ -106,39 +70,35 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
             t[r] = (tt >= 0 && tt < N) ? static_cast<int>(tt) : -1;
         }
         if constexpr (VEC) {
+            // Slot k of a row is the k-th 16-byte vector of the aligned span
+            // covering the row, [rp - off, rp + N * EB) rounded out to 16
+            // bytes: the first and the last vectors may hold bytes of the
+            // neighbouring rows or of padding, masked to -inf.  A 16-byte block
+            // holding a byte of the row lies in the row's memory page, so the
+            // wider read cannot fault.
             uint32_t w[R][4 * V];
-            int head[R], tail[R], nv[R];  // per row: peeled head, tail, full vectors
+            uint32_t off[R];  // byte offset of each row from the 16-byte boundary below it
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int64_t row = row0 + r * RPW + grp;
                 const char* rp = xb + (row < B ? row : 0) * row_stride * EB;
-                head[r] = head_elems<DT>(rp, N);
-                const char* rv = rp + head[r] * EB;  // 16-byte aligned
-                nv[r] = static_cast<int>((N - head[r]) / EPV);
-                tail[r] = static_cast<int>(N - head[r] - static_cast<int64_t>(nv[r]) * EPV);
+                off[r] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(rp) & 15u);
+                const char* a0 = rp - off[r];  // 16-byte aligned
+                const uint32_t rb1 = off[r] + static_cast<uint32_t>(N) * EB;  // row end in the span
+                const int nvc = static_cast<int>((rb1 + 15u) >> 4);           // vectors in the span
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
                     const int k = sub + j * G;
-                    uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
-                                         neg_inf_word<DT>());
-                    if (row < B && k < nv[r]) u = ldg_stream16(rv + k * 16);
-                    w[r][4 * j] = u.x; w[r][4 * j + 1] = u.y; w[r][4 * j + 2] = u.z; w[r][4 * j + 3] = u.w;
-                }
-                if (row < B && (tail[r] > 0 || head[r] > 0)) {
-#pragma unroll
-                    for (int j = 0; j < V; ++j) {
-                        const int k = sub + j * G;
-                        uint32_t q[4];
-                        if (tail[r] > 0 && k == nv[r]) {
-                            load_tail_words<DT>(rv, static_cast<int64_t>(nv[r]) * EPV, tail[r], q);
-                        } else if (head[r] > 0 && k == nv[r] + (tail[r] > 0 ? 1 : 0)) {
-                            load_tail_words<DT>(rp, 0, head[r], q);
-                        } else {
-                            continue;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                    uint32_t q[4] = {neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                     neg_inf_word<DT>()};
+                    if (row < B && k < nvc) {
+                        const uint4 u = ldg_stream16(a0 + k * 16);
+                        q[0] = u.x; q[1] = u.y; q[2] = u.z; q[3] = u.w;
+                        if ((k == 0 && off[r] != 0) || (k == nvc - 1 && (rb1 & 15u) != 0))
+                            mask_words<DT>(q, static_cast<uint32_t>(k) * 16u, off[r], rb1);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
                 }
             }
 #pragma unroll
@@ -166,16 +126,10 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                 if constexpr (TL) {
                     const bool valid = t[r] >= 0;
                     if (valid) {
-                        // slot and position of x[row, t]: head slot, a vector, or the tail slot
-                        int slot, pos;
-                        if (t[r] < head[r]) {
-                            slot = nv[r] + (tail[r] > 0 ? 1 : 0);
-                            pos = t[r];
-                        } else {
-                            const int t2 = t[r] - head[r];
-                            slot = t2 / EPV < nv[r] ? t2 / EPV : nv[r];
-                            pos = t2 - slot * EPV;
-                        }
+                        // slot and position of x[row, t] in the covering span
+                        const int tb = static_cast<int>(off[r]) + t[r] * EB;
+                        const int slot = tb >> 4;
+                        const int pos = (tb & 15) / EB;
 #pragma unroll
                         for (int j = 0; j < V; ++j)
                             if (sub + j * G == slot) xt = word_elem<DT>(&w[r][4 * j], pos);
@@ -246,10 +200,12 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 }
 
 // ---------------------------------------------------------------------------
-// segment: blockIdx.x = row * P + seg.  Segment seg covers slots
-// [seg * seg_slots, min(nv, (seg + 1) * seg_slots)) of its row; the last
-// segment also takes the < EPV tail elements and the first segment the < EPV
-// head elements before the row's first 16-byte boundary (VEC only).
+// segment: blockIdx.x = row * P + seg.  VEC: the row's slots are the 16-byte
+// vectors of the aligned span covering it (as in subwarp: the first and the
+// last may be partly outside the row and are masked by the one thread that
+// loads each).  Segment seg covers slots [seg * seg_slots, (seg + 1) *
+// seg_slots); the last segment runs to the row's last slot.  !VEC: slots are
+// elements.
 // ---------------------------------------------------------------------------
 template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
 
@@ -260,7 +216,6 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
                    const int64_t* __restrict__ target, float* __restrict__ logprob,
                    float* __restrict__ xt_buf) {
     constexpr int EB = DType<DT>::bytes;
-    constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 8 : 16;  // slots per thread per batch
     constexpr int NW = T / 32;
 
@@ -271,11 +226,27 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
     const int64_t row = unit / P;
     const int64_t seg = unit - row * P;
     const char* rp = reinterpret_cast<const char*>(x) + row * row_stride * EB;
-    const int head = VEC ? head_elems<DT>(rp, N) : 0;
-    const char* rv = rp + head * EB;  // VEC: 16-byte aligned vectors from here
-    const int64_t nv = (N - head) / EPV;
+    // VEC: the span [rp - off, rp + N * EB) rounded up to 16 bytes.
+    const uint32_t off = VEC ? static_cast<uint32_t>(reinterpret_cast<uintptr_t>(rp) & 15u) : 0u;
+    const char* a0 = rp - off;
+    const int64_t rb1 = off + N * EB;                      // row end in the span, bytes
+    const int64_t nslots = VEC ? (rb1 + 15) >> 4 : N;      // slots of the row
     const int64_t s_begin = seg * seg_slots;
-    const int64_t s_end = s_begin + seg_slots < nv ? s_begin + seg_slots : nv;
+    const int64_t s_end = seg == P - 1 || s_begin + seg_slots > nslots ? nslots : s_begin + seg_slots;
+    // The threads that load the row's first or last vector when it is partly
+    // outside the row.
+    const bool edge = VEC && ((off != 0 && seg == 0 && threadIdx.x == 0) ||
+                              ((rb1 & 15) != 0 && s_end == nslots &&
+                               (nslots - 1 - s_begin) % T == threadIdx.x));
+    auto mask_edge = [&](uint32_t* w4, int64_t kk) {
+        if (kk == 0 || kk == nslots - 1) {
+            uint32_t q[4] = {w4[0], w4[1], w4[2], w4[3]};
+            mask_words<DT>(q, 0u, kk == 0 ? off : 0u,
+                           kk == nslots - 1 ? static_cast<uint32_t>(rb1 - kk * 16) : 16u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w4[i] = q[i];
+        }
+    };
 
     Acc acc = acc_identity();
     float mu = 0.0f;
@@ -293,8 +264,12 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             uint32_t w[4 * U];
 #pragma unroll
             for (int j = 0; j < U; ++j) {
-                const uint4 u = ldg_stream16(rv + (k + j * T) * 16);
+                const uint4 u = ldg_stream16(a0 + (k + j * T) * 16);
                 w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+            }
+            if (edge) {
+#pragma unroll
+                for (int j = 0; j < U; ++j) mask_edge(&w[4 * j], k + j * T);
             }
             if (xt_pending) {
                 if (t >= 0 && t < N) xt = load_elem<DT>(rp, t);
@@ -308,25 +283,15 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             for (int j = 0; j < U; ++j) {
                 const int64_t kk = k + j * T;
                 if (kk < s_end) {
-                    const uint4 u = ldg_stream16(rv + kk * 16);
+                    const uint4 u = ldg_stream16(a0 + kk * 16);
                     w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+                    if (edge) mask_edge(&w[4 * j], kk);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
                 }
             }
             acc_add_words<DT, 4 * U, E16>(acc, mu, w);
-        }
-        const int tail = static_cast<int>(N - head - nv * EPV);
-        if (tail > 0 && seg == P - 1 && threadIdx.x == 0) {
-            uint32_t w[4];
-            load_tail_words<DT>(rv, nv * EPV, tail, w);
-            acc_add_words<DT, 4, E16>(acc, mu, w);
-        }
-        if (head > 0 && seg == 0 && threadIdx.x == 0) {
-            uint32_t w[4];
-            load_tail_words<DT>(rp, 0, head, w);
-            acc_add_words<DT, 4, E16>(acc, mu, w);
         }
     } else {
         for (; k + (U - 1) * T < s_end; k += U * T) {

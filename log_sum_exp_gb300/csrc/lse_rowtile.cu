@@ -26,6 +26,7 @@
 // counts a timeout in a device counter (read by lse_wait_timeouts), the whole
 // CTA stops, waits (also bounded) for its own copies still in flight, and
 // returns.  Such a timeout does not happen in correct operation.
+#include <atomic>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -36,11 +37,16 @@
 namespace lse {
 namespace {
 
-constexpr int kTileThreads = 256;
-constexpr int kChunkBytes = 32 * 1024;  // per stage
-constexpr int kStages = 2;
+constexpr int kTileThreads = 256;      // any-width ring: threads per CTA
+constexpr int kChunkBytes = 32 * 1024;  // any-width ring: bytes per stage
+constexpr int kStages = 2;              // any-width ring: stages per CTA
+constexpr int kWarpChunkBytes = 4096;   // vector ring: bytes per warp stage
+constexpr int kRingWarps = 24;          // vector ring: warps per CTA
+constexpr int kRingStages = 1;          // vector ring: stages per warp
+constexpr int kRingCtasPerSm = 1;       // 96 KB of stages per SM
 constexpr uint32_t kWaitPolls = 1u << 26;
 constexpr int kAnyThreadRowBytes = 128;  // any-width rows up to this: one thread per row
+constexpr int kAnyThreadRowVectors = 9;  // 16-byte vectors such a row can touch
 
 __device__ unsigned long long g_wait_timeouts;
 
@@ -99,91 +105,116 @@ __device__ __forceinline__ float staged_elem(const unsigned char* row, int i) {
     }
 }
 
-// NV (1..8) 16-byte vectors per row; RPT = floor(8 / NV) rows per thread per
-// chunk, so a chunk is 256 * RPT rows of at most 32 KB (exactly 32 KB when NV
-// divides 8).  Chunks are dealt round-robin to the CTAs.
+// Lanes per repeat of the 16-byte bank group at which consecutive rows of NV
+// vectors start: 8 / gcd(NV, 8).
+template <int NV>
+constexpr int kRotationPeriod = 8 / (NV % 8 == 0 ? 8 : (NV % 4 == 0 ? 4 : (NV % 2 == 0 ? 2 : 1)));
+
+// NV (1..8) 16-byte vectors per row.  Every warp runs a ring of its own:
+// S stages of one warp chunk each, a warp chunk being 32 * RPL rows
+// (RPL = floor(8 / NV) rows per lane, at most 4 KB).  Lane 0 issues the bulk
+// copy of each chunk into a free stage of its warp and every lane waits on
+// that stage's mbarrier; once the 32 lanes have read the stage into registers
+// (a __syncwarp), lane 0 refills it with the warp's next chunk, so a warp
+// never waits for another one.  Warp chunks are dealt round-robin to the
+// warps of the grid.  `polls` bounds every stage wait (kWaitPolls unless a
+// caller lowered it through lse_set_wait_limit).
 // E16: reduced-bit exponentials; TL: token log-probability epilogue (out may
 // then be null).
-template <int DT, int NV, bool E16, bool TL>
-__global__ void __launch_bounds__(kTileThreads)
+template <int DT, int NV, bool E16, bool TL, int W, int S>
+__global__ void __launch_bounds__(W * 32)
 lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ out,
-                   const int64_t* __restrict__ target, float* __restrict__ logprob) {
+                   const int64_t* __restrict__ target, float* __restrict__ logprob,
+                   uint32_t polls) {
     constexpr int RB = NV * 16;                // bytes per row
-    constexpr int RPT = 8 / NV;                // rows per thread per chunk
-    constexpr int CR = kTileThreads * RPT;     // rows per chunk
+    constexpr int RPL = 8 / NV;                // rows per lane per chunk
+    constexpr int CR = 32 * RPL;               // rows per warp chunk
     constexpr int NE = RB / DType<DT>::bytes;  // elements per row
-    static_assert(NV >= 1 && NV <= 8 && CR * RB <= kChunkBytes, "a chunk must fit one stage");
-    extern __shared__ __align__(128) unsigned char stage[];
-    __shared__ __align__(8) uint64_t full[kStages];
-    const int tid = threadIdx.x;
+    static_assert(NV >= 1 && NV <= 8 && CR * RB <= kWarpChunkBytes, "a chunk must fit one stage");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full_bars[W * S];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    unsigned char* ring = smem + wid * (S * kWarpChunkBytes);
+    uint64_t* full = full_bars + wid * S;
     const int64_t nchunks = (B + CR - 1) / CR;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * W;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + wid;
     const char* xb = reinterpret_cast<const char*>(x);
 
-    pdl_trigger();
-    pdl_wait();
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    // The barriers live in this CTA's shared memory: set them up before
+    // waiting for the previous kernel in the stream.
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncthreads();
+    __syncwarp();
+    pdl_trigger();
+    pdl_wait();
 
-    auto issue = [&](int64_t chunk, int s) {  // thread 0 only
+    auto issue = [&](int64_t chunk, int s) {  // lane 0 only
         const int64_t r0 = chunk * CR;
         const int64_t rows = B - r0 < CR ? B - r0 : CR;
         const uint32_t bytes = static_cast<uint32_t>(rows * RB);
         mbar_expect_tx(&full[s], bytes);
-        bulk_load(stage + s * kChunkBytes, xb + r0 * RB, bytes, &full[s]);
+        bulk_load(ring + s * kWarpChunkBytes, xb + r0 * RB, bytes, &full[s]);
     };
-    if (tid == 0)
-        for (int s = 0; s < kStages; ++s) {
-            const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = gw + static_cast<int64_t>(s) * nwarps;
             if (c < nchunks) issue(c, s);
         }
 
-    int64_t k = 0;  // chunks consumed by this CTA
+    int64_t k = 0;  // chunks consumed by this warp
+    int64_t c = gw;
     bool timed_out = false;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
-        const int s = static_cast<int>(k % kStages);
-        // Targets of this thread's rows (coalesced), loaded while the chunk lands.
-        int tq[TL ? RPT : 1];
+    for (; c < nchunks; c += nwarps, ++k) {
+        const int s = static_cast<int>(k % S);
+        // Targets of this lane's rows (coalesced), loaded while the chunk lands.
+        int tq[TL ? RPL : 1];
         if constexpr (TL) {
 #pragma unroll
-            for (int q = 0; q < RPT; ++q) {
-                const int64_t row = c * CR + q * kTileThreads + tid;
+            for (int q = 0; q < RPL; ++q) {
+                const int64_t row = c * CR + q * 32 + lane;
                 const int64_t t = row < B ? __ldg(target + row) : -1;
                 tq[q] = (t >= 0 && t < NE) ? static_cast<int>(t) : -1;
             }
         }
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((k / kStages) & 1), kWaitPolls);
-        uint32_t w[RPT][4 * NV];
-        float xt[TL ? RPT : 1];
-#pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-            const unsigned char* rowp = stage + s * kChunkBytes + (q * kTileThreads + tid) * RB;
-            const uint4* rp = reinterpret_cast<const uint4*>(rowp);
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                // Rotated reads: consecutive threads start at different 16-byte
-                // bank groups.  Max and sum do not depend on the order.
-                const uint4 u = ok ? rp[(j + tid) % NV] : make_uint4(0, 0, 0, 0);
-                w[q][4 * j] = u.x; w[q][4 * j + 1] = u.y; w[q][4 * j + 2] = u.z; w[q][4 * j + 3] = u.w;
-            }
-            if constexpr (TL)
-                xt[q] = ok && tq[q] >= 0 ? staged_elem<DT>(rowp, tq[q]) : __int_as_float(0x7fc00000);
-        }
-        // Every thread has read stage s: it may be refilled.  A timed-out wait
-        // in any thread stops the whole CTA.
-        if (__syncthreads_or(!ok)) {
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), polls));
+        if (!ok) {  // every lane stops; lane 0 drains the copies below
             timed_out = true;
             break;
         }
-        if (tid == 0) {
-            const int64_t cn = c + static_cast<int64_t>(kStages) * gridDim.x;
+        uint32_t w[RPL][4 * NV];
+        float xt[TL ? RPL : 1];
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            const unsigned char* rowp = ring + s * kWarpChunkBytes + (q * 32 + lane) * RB;
+            const uint4* rp = reinterpret_cast<const uint4*>(rowp);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                // A 16-byte read by a warp is served a quarter-warp (8 lanes)
+                // at a time: conflict free when the 8 lanes hit the 8
+                // different 16-byte bank groups of a 128-byte line.  Lane l's
+                // row starts at group NV * l (mod 8), a pattern of period
+                // P = 8 / gcd(NV, 8) lanes, so lanes P apart start at the same
+                // group; rotating the vector order by (l mod 8) / P moves them
+                // apart.  Max and sum do not depend on the order.
+                const uint4 u = rp[(j + (lane & 7) / kRotationPeriod<NV>) % NV];
+                w[q][4 * j] = u.x; w[q][4 * j + 1] = u.y; w[q][4 * j + 2] = u.z; w[q][4 * j + 3] = u.w;
+            }
+            if constexpr (TL)
+                xt[q] = tq[q] >= 0 ? staged_elem<DT>(rowp, tq[q]) : __int_as_float(0x7fc00000);
+        }
+        __syncwarp();  // every lane has read stage s: it may be refilled
+        if (lane == 0) {
+            const int64_t cn = c + static_cast<int64_t>(S) * nwarps;
             if (cn < nchunks) issue(cn, s);
         }
 #pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-            const int64_t row = c * CR + q * kTileThreads + tid;
+        for (int q = 0; q < RPL; ++q) {
+            const int64_t row = c * CR + q * 32 + lane;
             if (row < B) {
                 const float m = words_max<DT, 4 * NV>(w[q]);
                 const float mu = shift_of(m);
@@ -198,37 +229,17 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
             }
         }
     }
-    if (timed_out) {
-        if (tid == 0) {
-            atomicAdd(&g_wait_timeouts, 1ull);
-            // Let every copy this CTA may still have in flight land (bounded)
-            // before the shared memory is released.
-            for (int s = 0; s < kStages; ++s) {
-                mbar_wait(&full[s], 0, kWaitPolls);
-                mbar_wait(&full[s], 1, kWaitPolls);
-            }
-        }
-        __syncthreads();
-    }
-}
-
-// The words of one 16-byte vector staged at byte vb of a chunk, with every
-// element outside the row's bytes [rb0, rb1) replaced by -inf.
-template <int DT>
-__device__ __forceinline__ void mask_words(uint32_t (&w)[4], uint32_t vb, uint32_t rb0,
-                                           uint32_t rb1) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t b = vb + 4u * i;
-        if constexpr (DT == kF32) {
-            if (b < rb0 || b >= rb1) w[i] = kNegInfF32;
-        } else {
-            const uint32_t ninf = neg_inf_word<DT>();  // -inf in both halves
-            const uint32_t lo = (b < rb0 || b >= rb1) ? (ninf & 0xffffu) : (w[i] & 0xffffu);
-            const uint32_t hi = (b + 2 < rb0 || b + 2 >= rb1) ? (ninf & 0xffff0000u) : (w[i] & 0xffff0000u);
-            w[i] = lo | hi;
+    if (timed_out && lane == 0) {
+        atomicAdd(&g_wait_timeouts, 1ull);
+        // Chunks c, c + nwarps, ..., c + (S-1) nwarps were issued and not yet
+        // consumed: let each land (bounded) before the shared memory is released.
+        for (int j = 0; j < S; ++j) {
+            const int64_t kk = k + j;
+            if (c + j * nwarps < nchunks)
+                mbar_wait(&full[kk % S], static_cast<uint32_t>((kk / S) & 1), kWaitPolls);
         }
     }
+    __syncwarp();
 }
 
 // Back-to-back rows whose width RB = N * elem bytes is not a multiple of 16
@@ -249,7 +260,8 @@ __device__ __forceinline__ void mask_words(uint32_t (&w)[4], uint32_t vb, uint32
 template <int DT, int G, bool TL>
 __global__ void __launch_bounds__(kTileThreads)
 lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out,
-                       const int64_t* __restrict__ target, float* __restrict__ logprob) {
+                       const int64_t* __restrict__ target, float* __restrict__ logprob,
+                       uint32_t polls) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int GROUPS = kTileThreads / G;
     extern __shared__ __align__(128) unsigned char stage[];
@@ -302,10 +314,11 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
     const int grp = tid / G;
 
     int64_t kc = 0;  // chunks consumed by this CTA
+    int64_t c = blockIdx.x;
     bool timed_out = false;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++kc) {
+    for (; c < nchunks; c += gridDim.x, ++kc) {
         const int s = static_cast<int>(kc % kStages);
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((kc / kStages) & 1), kWaitPolls);
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((kc / kStages) & 1), polls);
         const unsigned char* st = stage + s * kChunkBytes;
         // Results are stored as soon as they are computed; the stage is only
         // read before the barrier below.
@@ -314,7 +327,29 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                 const int64_t row = c * CR + q;
                 if (ok && row < Bm) {
                     const int64_t t = TL ? __ldg(target + row) : -1;
-                    const float lse = fold([&](int n) { return staged_elem<DT>(st + q * RB, n); });
+                    // The <= 9 aligned 16-byte vectors holding the row's <= 128
+                    // bytes, the neighbours' elements in the first and the last
+                    // masked to -inf, folded from registers (max, then exp-sum).
+                    const uint32_t rb0 = static_cast<uint32_t>(q * RB);
+                    const uint32_t rb1 = rb0 + static_cast<uint32_t>(RB);
+                    const uint32_t v0 = rb0 >> 4, v1 = (rb1 + 15u) >> 4;
+                    uint32_t w[4 * kAnyThreadRowVectors];
+#pragma unroll
+                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                        uint32_t q4[4] = {neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                          neg_inf_word<DT>()};
+                        const uint32_t v = v0 + j;
+                        if (v < v1) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(st + v * 16u);
+                            q4[0] = u.x; q4[1] = u.y; q4[2] = u.z; q4[3] = u.w;
+                            if (v * 16u < rb0 || v * 16u + 16u > rb1) mask_words<DT>(q4, v * 16u, rb0, rb1);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w[4 * j + i] = q4[i];
+                    }
+                    const float m = words_max<DT, 4 * kAnyThreadRowVectors>(w);
+                    const float lse =
+                        acc_finalize(Acc{m, words_expsum<DT, 4 * kAnyThreadRowVectors>(w, shift_of(m))});
                     const float xt = TL && t >= 0 && t < N ? staged_elem<DT>(st + q * RB, static_cast<int>(t))
                                                            : __int_as_float(0x7fc00000);
                     store_row(out, TL ? logprob : nullptr, row, lse, xt);
@@ -371,9 +406,13 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
     if (timed_out) {
         if (tid == 0) {
             atomicAdd(&g_wait_timeouts, 1ull);
-            for (int s = 0; s < kStages; ++s) {
-                mbar_wait(&full[s], 0, kWaitPolls);
-                mbar_wait(&full[s], 1, kWaitPolls);
+            // Chunks c, c + grid, ..., c + (kStages-1) grid were issued and not
+            // yet consumed: let each land (bounded) before the shared memory
+            // is released.
+            for (int j = 0; j < kStages; ++j) {
+                const int64_t kk = kc + j;
+                if (c + j * static_cast<int64_t>(gridDim.x) < nchunks)
+                    mbar_wait(&full[kk % kStages], static_cast<uint32_t>((kk / kStages) & 1), kWaitPolls);
             }
         }
         __syncthreads();
@@ -389,15 +428,32 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
     }
 }
 
+// The poll limit of the stage waits (lse_set_wait_limit; kWaitPolls by default).
+std::atomic<uint32_t> g_stage_polls{kWaitPolls};
+
+// Raise kernel K's dynamic shared-memory limit once per device (the
+// attribute belongs to the function in the current device's context).
+template <auto K>
+cudaError_t allow_smem(int bytes) {
+    static std::atomic<uint64_t> done{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 template <int DT, int G, bool TL>
 cudaError_t launch_rowtile_any_g(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_any_kernel<DT, G, TL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = allow_smem<lse_rowtile_any_kernel<DT, G, TL>>(smem);
     if (e != cudaSuccess) return e;
     return launch_pdl_smem(lse_rowtile_any_kernel<DT, G, TL>, dim3(static_cast<unsigned>(grid)),
                            dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B, a.N,
-                           a.out, a.tl.target, a.tl.logprob);
+                           a.out, a.tl.target, a.tl.logprob, g_stage_polls.load(std::memory_order_relaxed));
 }
 
 template <int DT, bool TL>
@@ -423,13 +479,13 @@ cudaError_t launch_rowtile_any(int dt, int lanes, const LaunchArgs& a, int grid)
 
 template <int DT, int NV, bool E16, bool TL>
 cudaError_t launch_rowtile_t(const LaunchArgs& a, int grid) {
-    const int smem = kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(lse_rowtile_kernel<DT, NV, E16, TL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int W = kRingWarps, S = kRingStages;
+    const int smem = W * S * kWarpChunkBytes;
+    cudaError_t e = allow_smem<lse_rowtile_kernel<DT, NV, E16, TL, W, S>>(smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_kernel<DT, NV, E16, TL>, dim3(static_cast<unsigned>(grid)),
-                           dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B,
-                           a.out, a.tl.target, a.tl.logprob);
+    return launch_pdl_smem(lse_rowtile_kernel<DT, NV, E16, TL, W, S>, dim3(static_cast<unsigned>(grid)),
+                           dim3(W * 32), static_cast<size_t>(smem), a.stream, a.x, a.B,
+                           a.out, a.tl.target, a.tl.logprob, g_stage_polls.load(std::memory_order_relaxed));
 }
 
 template <int DT, bool E16, bool TL>
@@ -472,8 +528,9 @@ cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int g
                  : launch_rowtile_e<false, false>(dt, nv, a, grid);
 }
 
-int rowtile_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
-int rowtile_rows_per_chunk(int nv) { return kTileThreads * (8 / nv); }
+int rowtile_ctas_per_sm() { return kRingCtasPerSm; }
+int rowtile_rows_per_chunk(int nv) { return kRingWarps * 32 * (8 / nv); }  // one chunk per warp
+int rowtile_any_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
 int rowtile_any_rows_per_chunk(int row_bytes) {
     if (row_bytes <= kAnyThreadRowBytes) return kTileThreads * (kChunkBytes / (kTileThreads * row_bytes));
     int g = row_bytes;  // gcd(row_bytes, 16)
@@ -490,5 +547,8 @@ int rowtile_any_max_row_bytes() { return kChunkBytes / 8; }
 cudaError_t read_wait_timeouts(unsigned long long* count) {
     return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));
 }
+
+void set_stage_wait_polls(uint32_t polls) { g_stage_polls.store(polls, std::memory_order_relaxed); }
+uint32_t default_stage_wait_polls() { return kWaitPolls; }
 
 }  // namespace lse

@@ -736,6 +736,9 @@ def run_native(args) -> None:
         if plan["launches"] > 1 and op_name == "forward" else []
     kev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for i in sampled}
+    for pair in kev.values():  # create the events (torch does so lazily, on a first record)
+        for e in pair:
+            e.record(stream)
     barrier(dev)
     torch.cuda.synchronize(dev)
     t_region = time.time()

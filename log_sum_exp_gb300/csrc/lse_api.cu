@@ -114,6 +114,16 @@ int pow2_ceil(int64_t v) {
     return p;
 }
 
+// Slots per lane the sub-warp kernel is built for that hold v: 1, 2, 3, 4, and
+// 6 or 8 in groups that may hold more than 4 (a whole warp, or 4-16 lanes of
+// 16-byte vectors).  Rows just above a power of two of slots (an unaligned row
+// adds up to two) waste less on -inf padding with 3 or 6 than with 4 or 8: on
+// those the kernel is bound by instruction issue, not memory.
+int64_t subwarp_slot_count(int64_t v, bool wide) {
+    if (v <= 4) return v;
+    return wide && v <= 6 ? 6 : 8;
+}
+
 // Lanes per row of the automatic sub-warp plan for rows of nvt slots: the
 // fewest that keep <= kSubwarpMaxSlots slots per lane (four independent loads
 // per thread), at most a warp.  Vector rows of more than 16 slots take half
@@ -134,8 +144,7 @@ int subwarp_auto_lanes(int64_t nvt, bool vec) {
 // Slots per row (lanes x slots per lane, padded to a power of two) of that plan.
 int64_t subwarp_auto_slots(int64_t nvt, bool vec) {
     const int G = subwarp_auto_lanes(nvt, vec);
-    const int64_t V = ceil_div(nvt, G);
-    return G * (V <= 1 ? 1 : (V <= 2 ? 2 : (V <= 4 ? 4 : 8)));
+    return G * subwarp_slot_count(ceil_div(nvt, G), G == 32 || (vec && G >= 4));
 }
 
 // Fill in (or check) a plan.  `req` may be null (automatic).
@@ -185,22 +194,20 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     const int64_t sub_capacity = 32 * kSubwarpWarpSlots;  // slots per row
     // Bulk-copy ring for short back-to-back rows: contiguous 16-byte aligned
     // rows of 16..128 bytes, enough rows for every CTA.  Chosen automatically
-    // where it measured faster than the sub-warp mapping (256 MB of rows):
-    // rows of 3, 5, 6 or 7 vectors (the sub-warp mapping pads those to 4 or 8
-    // slots) and f32 rows of 4 or 8; the sub-warp mapping keeps rows of 1 or 2
-    // vectors and 16-bit rows of 4 or 8, where one thread per row would fold
-    // 32 or 64 elements alone.
+    // where it measured faster than the sub-warp mapping (256 MB of rows per
+    // width): every width but f32 rows of 2 vectors (sub-warp 6.94 TB/s, ring
+    // 6.67); e.g. bf16 rows of 8 vectors 6.58 against 5.99.
     const int64_t row_bytes = N * eb;
     const bool rowtile_ok = vec && aligned && row_stride == N && row_bytes % 16 == 0 &&
                             row_bytes >= 16 && row_bytes <= 128;
     const int64_t row_vecs = row_bytes / 16;
-    const bool rowtile_auto =
-        row_vecs > 2 && !(eb == 2 && (row_vecs == 4 || row_vecs == 8));
+    const bool rowtile_auto = !(eb == 4 && row_vecs == 2);
     // Rows of other widths up to 128 bytes, still back to back from a 16-byte
-    // aligned base: the same ring with element reads (row value or token
-    // log-probability, f32 exponentials).  Chosen automatically: it measured
-    // 1.15-2.9x the sub-warp mapping (with the head peel) on the row value
-    // for every such width but f32 rows of 7, where the two are even.
+    // aligned base: the same ring, one thread per row (row value or token
+    // log-probability, f32 exponentials).  Chosen automatically for rows of at
+    // least 32 bytes (f32 N = 13: 5.06 against 3.93 TB/s, bf16 N = 31: 3.28
+    // against 2.63); shorter rows measured faster on the sub-warp mapping
+    // (f32 N = 7: 4.56 against 3.02).
     const bool rowtile_any_ok = !rowtile_ok && !e16 && row_stride == N &&
                                 row_bytes <= rowtile_any_max_row_bytes() &&
                                 reinterpret_cast<uintptr_t>(x) % 16u == 0 &&
@@ -222,18 +229,20 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
             rowtile_any_ok ? rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)) : 1;
         if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
-        else if (rowtile_any_ok && row_bytes <= 128 && B >= any_rows * info.sms * rowtile_any_ctas_per_sm())
+        else if (rowtile_any_ok && row_bytes >= 32 && row_bytes <= 128 &&
+                 B >= any_rows * info.sms * rowtile_any_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
         // Back-to-back rows of more than 512 bytes take the grouped ring where
-        // the sub-warp mapping would leave more than a third of its slots empty
-        // (a row just past a power of two of slots) or cannot hold them:
-        // measured 1.1-1.5x there (f32 N = 129: 4.0 -> 6.0 TB/s, N = 520:
-        // 5.5 -> 6.1; bf16 N = 260: 3.5 -> 4.4, N = 1020: 3.5 -> 5.1, N = 2047:
-        // 3.5 -> 4.6), 0.85-0.95x where the sub-warp slots are full, and
-        // mixed below 512 bytes (f32 N = 65: 1.29x, N = 68: 0.91x; bf16
-        // N = 150: 0.94x).
+        // the sub-warp mapping cannot hold them, or would leave a quarter or
+        // more of its slots empty (a row just past a power of two of slots)
+        // and the row is f32 or at most 1.5 KB: measured f32 N = 129 6.14
+        // against 5.51 TB/s, N = 257 5.74 / 5.46, N = 520 6.29 / 5.89, bf16
+        // N = 520 5.09 / 4.93; with fuller slots the sub-warp mapping wins
+        // (f32 N = 300 6.44 / 6.37, bf16 N = 300 4.47 / 4.29), and so it does
+        // on longer 16-bit rows (bf16 N = 1025 4.06 / 3.02).
         else if (rowtile_any_ok && row_bytes > 512 && B >= any_rows * info.sms * rowtile_any_ctas_per_sm() &&
-                 (nvt > sub_capacity || 3 * nvt < 2 * subwarp_auto_slots(nvt, vec)))
+                 (nvt > sub_capacity ||
+                  (4 * nvt < 3 * subwarp_auto_slots(nvt, vec) && (eb == 4 || row_bytes <= 1536))))
             path = LSE_PATH_ROWTILE;
         else
             path = nvt <= sub_capacity ? LSE_PATH_SUBWARP : LSE_PATH_CTA;
@@ -283,8 +292,8 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         int64_t V = ceil_div(nvt, G);
         const bool wide = G == 32 || (vec && G >= 4);  // groups that may hold 8 slots per lane
         if (V > (wide ? kSubwarpWarpSlots : kSubwarpMaxSlots)) return LSE_ERR_INVALID_ARG;
-        V = V <= 1 ? 1 : (V <= 2 ? 2 : (V <= 4 ? 4 : 8));
-        const int64_t R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
+        V = subwarp_slot_count(V, wide);
+        const int64_t R = V >= 3 ? 1 : (V == 2 ? 2 : 4);
         const int64_t rows_per_warp_iter = (32 / G) * R;
         const int64_t warps = ceil_div(B, rows_per_warp_iter);
         int64_t grid = ceil_div(warps, kSubwarpThreads / 32);
@@ -357,7 +366,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     p.path = P > 1 ? LSE_PATH_SPLIT : LSE_PATH_CTA;
     p.threads = T;
     p.splits = P;
-    p.grid = B * P;
+    p.grid = T == 32 ? ceil_div(B * P, kSegmentWarpUnitsPerCta) : B * P;  // CTAs
     // Split scratch: B*P (m, s) partials, then (token log-probability) the
     // gathered x[b, target[b]] per row.
     p.scratch_bytes = P > 1 ? B * P * static_cast<int64_t>(sizeof(float2)) +

@@ -15,6 +15,8 @@ constexpr int kSubwarpThreads = 256;
 // Five resident CTAs per SM (<= 48 registers, no spills): one-shot CTAs whose
 // 16-byte loads are all in flight at once; occupancy sets the bytes in flight.
 constexpr int kSubwarpMinBlocks = 5;
+// Segment plans of 32 threads per unit run this many units (one per warp) in a CTA.
+constexpr int kSegmentWarpUnitsPerCta = 8;
 
 // Optional fused consumer of the row value, the token log-probability
 // logprob[b] = x[b, target[b]] - lse[b] (NaN when target[b] is not in [0, N)).

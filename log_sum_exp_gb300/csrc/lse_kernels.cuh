@@ -38,7 +38,7 @@ namespace lse {
 // The token log-probability epilogue keeps the targets and the peel state of
 // every row group live: one CTA per SM less, so it does not spill.
 template <int V, bool TL> struct SubwarpOccupancy {
-    static constexpr int min_blocks = (V >= 8 ? 4 : kSubwarpMinBlocks) - (TL ? 1 : 0);
+    static constexpr int min_blocks = (V >= 6 ? 4 : kSubwarpMinBlocks) - (TL ? 1 : 0);
 };
 
 template <int DT, int G, int V, bool VEC, bool TL, bool E16>
@@ -48,7 +48,7 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                    float* __restrict__ logprob) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int RPW = 32 / G;             // rows per warp per row-group
-    constexpr int R = V >= 4 ? 1 : (V == 2 ? 2 : 4);
+    constexpr int R = V >= 3 ? 1 : (V == 2 ? 2 : 4);
     const int lane = threadIdx.x & 31;
     const int sub = lane & (G - 1);
     const int grp = lane / G;
@@ -87,18 +87,24 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                 const uint32_t rb1 = off[r] + static_cast<uint32_t>(N) * EB;  // row end in the span
                 const int nvc = static_cast<int>((rb1 + 15u) >> 4);           // vectors in the span
 #pragma unroll
-                for (int j = 0; j < V; ++j) {
+                for (int j = 0; j < V; ++j) {  // every load issued before any mask
                     const int k = sub + j * G;
-                    uint32_t q[4] = {neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
-                                     neg_inf_word<DT>()};
-                    if (row < B && k < nvc) {
-                        const uint4 u = ldg_stream16(a0 + k * 16);
-                        q[0] = u.x; q[1] = u.y; q[2] = u.z; q[3] = u.w;
-                        if ((k == 0 && off[r] != 0) || (k == nvc - 1 && (rb1 & 15u) != 0))
-                            mask_words<DT>(q, static_cast<uint32_t>(k) * 16u, off[r], rb1);
-                    }
+                    uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                         neg_inf_word<DT>());
+                    if (row < B && k < nvc) u = ldg_stream16(a0 + k * 16);
+                    w[r][4 * j] = u.x; w[r][4 * j + 1] = u.y; w[r][4 * j + 2] = u.z; w[r][4 * j + 3] = u.w;
+                }
+                if (off[r] != 0 || (rb1 & 15u) != 0) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                    for (int j = 0; j < V; ++j) {
+                        const int k = sub + j * G;
+                        if (k == 0 || k == nvc - 1) {
+                            uint32_t q[4] = {w[r][4 * j], w[r][4 * j + 1], w[r][4 * j + 2], w[r][4 * j + 3]};
+                            mask_words<DT>(q, static_cast<uint32_t>(k) * 16u, off[r], rb1);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
+                        }
+                    }
                 }
             }
 #pragma unroll
@@ -113,7 +119,7 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                 // two vectors); same decision for the whole group.  Not with E16:
                 // there the maximum's own argument must be exactly 0 (its bf16
                 // term exactly 1), not the rounding residual of mu log2 e.
-                const bool scaled = !E16 && V >= 4 && ffma_shift_ok(mu);
+                const bool scaled = !E16 && V >= 3 && ffma_shift_ok(mu);
                 const float c = mu * kLog2e;
                 float s = scaled ? words_expsum_scaled<DT, 4 * V>(w[r], c)
                                  : expsum_words<DT, 4 * V, E16>(w[r], mu);
@@ -207,22 +213,31 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
 // seg_slots); the last segment runs to the row's last slot.  !VEC: slots are
 // elements.
 // ---------------------------------------------------------------------------
-template <int T> struct SegmentOccupancy { static constexpr int min_blocks = 2048 / T / 2; };
+// A 32-thread plan runs 8 units per CTA, one per warp (single-warp CTAs are
+// launched too slowly to keep up with 4 KB rows); wider plans one unit per CTA.
+template <int T> struct SegmentOccupancy {
+    static constexpr int cta_threads = T == 32 ? 32 * kSegmentWarpUnitsPerCta : T;
+    static constexpr int units_per_cta = cta_threads / T;
+    static constexpr int min_blocks = 2048 / cta_threads / 2;
+};
 
 template <int DT, int T, bool VEC, bool TL, bool E16>
-__global__ void __launch_bounds__(T, SegmentOccupancy<T>::min_blocks)
-lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, int64_t P,
+__global__ void __launch_bounds__(SegmentOccupancy<T>::cta_threads, SegmentOccupancy<T>::min_blocks)
+lse_segment_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row_stride, int64_t P,
                    int64_t seg_slots, float* __restrict__ out, float2* __restrict__ partial,
                    const int64_t* __restrict__ target, float* __restrict__ logprob,
                    float* __restrict__ xt_buf) {
     constexpr int EB = DType<DT>::bytes;
     constexpr int U = VEC ? 8 : 16;  // slots per thread per batch
     constexpr int NW = T / 32;
+    constexpr int UPC = SegmentOccupancy<T>::units_per_cta;
 
     pdl_trigger();
     pdl_wait();
 
-    const int64_t unit = blockIdx.x;
+    const int tid = UPC > 1 ? static_cast<int>(threadIdx.x & (T - 1)) : static_cast<int>(threadIdx.x);
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * UPC + (UPC > 1 ? threadIdx.x / T : 0);
+    if (UPC > 1 && unit >= B * P) return;  // uniform per warp; no CTA-wide barrier follows
     const int64_t row = unit / P;
     const int64_t seg = unit - row * P;
     const char* rp = reinterpret_cast<const char*>(x) + row * row_stride * EB;
@@ -235,9 +250,9 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
     const int64_t s_end = seg == P - 1 || s_begin + seg_slots > nslots ? nslots : s_begin + seg_slots;
     // The threads that load the row's first or last vector when it is partly
     // outside the row.
-    const bool edge = VEC && ((off != 0 && seg == 0 && threadIdx.x == 0) ||
+    const bool edge = VEC && ((off != 0 && seg == 0 && tid == 0) ||
                               ((rb1 & 15) != 0 && s_end == nslots &&
-                               (nslots - 1 - s_begin) % T == threadIdx.x));
+                               (nslots - 1 - s_begin) % T == tid));
     auto mask_edge = [&](uint32_t* w4, int64_t kk) {
         if (kk == 0 || kk == nslots - 1) {
             uint32_t q[4] = {w4[0], w4[1], w4[2], w4[3]};
@@ -250,11 +265,11 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
 
     Acc acc = acc_identity();
     float mu = 0.0f;
-    int64_t k = s_begin + threadIdx.x;
+    int64_t k = s_begin + tid;
 
     // Token log-probability: thread 0 of the row's first segment gathers
     // x[row, target[row]] once, issued behind its first batch of loads.
-    const bool gather = TL && seg == 0 && threadIdx.x == 0;
+    const bool gather = TL && seg == 0 && tid == 0;
     const int64_t t = gather ? __ldg(target + row) : -1;
     bool xt_pending = gather;
     float xt = __int_as_float(0x7fc00000);
@@ -285,11 +300,15 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
                 if (kk < s_end) {
                     const uint4 u = ldg_stream16(a0 + kk * 16);
                     w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
-                    if (edge) mask_edge(&w[4 * j], kk);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
                 }
+            }
+            if (edge) {  // after every load is issued
+#pragma unroll
+                for (int j = 0; j < U; ++j)
+                    if (k + j * T < s_end) mask_edge(&w[4 * j], k + j * T);
             }
             acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
@@ -325,7 +344,7 @@ lse_segment_kernel(const void* __restrict__ x, int64_t N, int64_t row_stride, in
             acc = warp_merge<NW>(acc);
         }
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         if (P == 1) {
             store_row(out, TL ? logprob : nullptr, row, acc_finalize(acc), xt);
         } else {
@@ -350,8 +369,12 @@ cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     switch (V) {
     case 1: return launch_subwarp_gv<DT, G, 1, VEC, TL, E16>(a, grid);
     case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL, E16>(a, grid);
+    case 3: return launch_subwarp_gv<DT, G, 3, VEC, TL, E16>(a, grid);
     case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL, E16>(a, grid);
-    case 8:  // a whole warp per row, or 4-16 lanes per row of 16-byte vectors
+    case 6:  // 6 or 8 slots per lane: a whole warp per row, or 4-16 lanes per row of vectors
+        if constexpr (G == 32 || (VEC && G >= 4)) return launch_subwarp_gv<DT, G, 6, VEC, TL, E16>(a, grid);
+        else return cudaErrorInvalidValue;
+    case 8:
         if constexpr (G == 32 || (VEC && G >= 4)) return launch_subwarp_gv<DT, G, 8, VEC, TL, E16>(a, grid);
         else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
@@ -374,20 +397,22 @@ cudaError_t launch_subwarp_dt(const LaunchArgs& a, int G, int V, int64_t grid) {
 template <int DT, int T, bool VEC, bool TL, bool E16>
 cudaError_t launch_segment_t(const LaunchArgs& a, int64_t P, int64_t seg_slots, float2* partial,
                              float* xt_buf) {
-    const int64_t grid = a.B * P;
-    return launch_pdl(lse_segment_kernel<DT, T, VEC, TL, E16>, dim3(static_cast<unsigned>(grid)), dim3(T),
-                      a.stream, a.x, a.N, a.row_stride, P, seg_slots, a.out, partial,
-                      a.tl.target, a.tl.logprob, xt_buf);
+    using Occ = SegmentOccupancy<T>;
+    const int64_t grid = (a.B * P + Occ::units_per_cta - 1) / Occ::units_per_cta;
+    return launch_pdl(lse_segment_kernel<DT, T, VEC, TL, E16>, dim3(static_cast<unsigned>(grid)),
+                      dim3(Occ::cta_threads), a.stream, a.x, a.B, a.N, a.row_stride, P, seg_slots,
+                      a.out, partial, a.tl.target, a.tl.logprob, xt_buf);
 }
 
 template <int DT, int T, bool VEC, bool TL, bool E16>
 int segment_occupancy_t() {
+    // Resident units of T threads per SM.
+    using Occ = SegmentOccupancy<T>;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC, TL, E16>, T,
-                                                      0) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_segment_kernel<DT, T, VEC, TL, E16>,
+                                                      Occ::cta_threads, 0) != cudaSuccess)
         return 0;
-    return blocks;
+    return blocks * Occ::units_per_cta;
 }
 
 }  // namespace lse

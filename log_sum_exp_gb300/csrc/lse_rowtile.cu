@@ -327,29 +327,42 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                 const int64_t row = c * CR + q;
                 if (ok && row < Bm) {
                     const int64_t t = TL ? __ldg(target + row) : -1;
-                    // The <= 9 aligned 16-byte vectors holding the row's <= 128
-                    // bytes, the neighbours' elements in the first and the last
-                    // masked to -inf, folded from registers (max, then exp-sum).
+                    // The aligned 16-byte vectors holding the row's <= 128 bytes
+                    // (at most 9; only those are read and folded), the
+                    // neighbours' elements in the first and the last masked to
+                    // -inf, folded from registers (max, then exp-sum).
                     const uint32_t rb0 = static_cast<uint32_t>(q * RB);
                     const uint32_t rb1 = rb0 + static_cast<uint32_t>(RB);
-                    const uint32_t v0 = rb0 >> 4, v1 = (rb1 + 15u) >> 4;
+                    const uint32_t v0 = rb0 >> 4;
+                    const int nvec = static_cast<int>(((rb1 + 15u) >> 4) - v0);
                     uint32_t w[4 * kAnyThreadRowVectors];
 #pragma unroll
                     for (int j = 0; j < kAnyThreadRowVectors; ++j) {
-                        uint32_t q4[4] = {neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
-                                          neg_inf_word<DT>()};
-                        const uint32_t v = v0 + j;
-                        if (v < v1) {
-                            const uint4 u = *reinterpret_cast<const uint4*>(st + v * 16u);
-                            q4[0] = u.x; q4[1] = u.y; q4[2] = u.z; q4[3] = u.w;
-                            if (v * 16u < rb0 || v * 16u + 16u > rb1) mask_words<DT>(q4, v * 16u, rb0, rb1);
-                        }
+                        uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                             neg_inf_word<DT>());
+                        if (j < nvec) u = *reinterpret_cast<const uint4*>(st + (v0 + j) * 16u);
+                        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+                    }
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) w[4 * j + i] = q4[i];
+                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                        if (j == 0 || j == nvec - 1) {
+                            uint32_t q4[4] = {w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]};
+                            mask_words<DT>(q4, (v0 + j) * 16u, rb0, rb1);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) w[4 * j + i] = q4[i];
+                        }
                     }
                     const float m = words_max<DT, 4 * kAnyThreadRowVectors>(w);
-                    const float lse =
-                        acc_finalize(Acc{m, words_expsum<DT, 4 * kAnyThreadRowVectors>(w, shift_of(m))});
+                    const float mu = shift_of(m);
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                        if (j < nvec) {
+                            const uint32_t q4[4] = {w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]};
+                            sum += words_expsum<DT, 4>(q4, mu);
+                        }
+                    }
+                    const float lse = acc_finalize(Acc{m, sum});
                     const float xt = TL && t >= 0 && t < N ? staged_elem<DT>(st + q * RB, static_cast<int>(t))
                                                            : __int_as_float(0x7fc00000);
                     store_row(out, TL ? logprob : nullptr, row, lse, xt);

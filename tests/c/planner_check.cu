@@ -46,56 +46,69 @@ lse_plan plan(lse_dtype dt, int64_t B, int64_t N, int64_t rs, const void* x = kA
 
 int main() {
     // Back-to-back rows of 16..128 bytes: the vector ring where it measured
-    // faster (3, 5, 6, 7 vectors; f32 rows of 4 or 8), else the sub-warp kernel.
+    // faster (every width but f32 rows of 2 vectors), else the sub-warp kernel.
     lse_plan p = plan(LSE_F32, 1 << 20, 32, 32);
     expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8, "f32 rows of 128 bytes: ring, 8 vectors");
     p = plan(LSE_BF16, 1 << 20, 64, 64);
-    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 2 && p.slots_per_lane == 4,
-           "bf16 rows of 128 bytes: sub-warp, 2 lanes x 4 vectors");
+    expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8, "bf16 rows of 128 bytes: ring, 8 vectors");
+    p = plan(LSE_F32, 1 << 22, 8, 8);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 1 && p.slots_per_lane == 2,
+           "f32 rows of 32 bytes: sub-warp, 1 lane x 2 vectors");
     p = plan(LSE_F32, 1 << 20, 32, 36);
     expect(p.path == LSE_PATH_SUBWARP, "rows not back to back: no ring");
     p = plan(LSE_F32, 1000, 32, 32);
     expect(p.path == LSE_PATH_SUBWARP, "too few rows for every CTA: no ring");
 
-    // Other widths up to 128 bytes: the element-read ring (row value and token
-    // log-probability, not the 16-bit exponentials).
-    p = plan(LSE_F32, 1 << 22, 5, 5);
+    // Other widths of 32..128 bytes: the any-width ring, a thread per row (row
+    // value and token log-probability, not the 16-bit exponentials); shorter
+    // rows stay on the sub-warp kernel.
+    p = plan(LSE_F32, 1 << 22, 13, 13);
     expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 0 && p.lanes_per_row == 1 &&
                p.vector_bytes == 1,
-           "f32 rows of 20 bytes: any-width ring, a thread per row");
-    p = plan(LSE_F32, 1 << 22, 5, 5, kAligned, nullptr, true);
+           "f32 rows of 52 bytes: any-width ring, a thread per row");
+    p = plan(LSE_F32, 1 << 22, 13, 13, kAligned, nullptr, true);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 1, "token log-probability: the same ring");
-    p = plan(LSE_F32, 1 << 22, 5, 5, kAligned, nullptr, false, true);
+    p = plan(LSE_F32, 1 << 22, 13, 13, kAligned, nullptr, false, true);
     expect(p.path == LSE_PATH_SUBWARP, "16-bit exponentials: sub-warp kernel");
-    p = plan(LSE_F32, 1 << 22, 5, 6);
+    p = plan(LSE_F32, 1 << 22, 13, 14);
     expect(p.path == LSE_PATH_SUBWARP, "strided rows: sub-warp kernel");
+    p = plan(LSE_F32, 1 << 22, 7, 7);
+    expect(p.path == LSE_PATH_SUBWARP, "f32 rows of 28 bytes: sub-warp kernel");
 
-    // Longer back-to-back rows: the grouped ring where a third or more of the
-    // sub-warp slots would be empty (rows just past a power of two of slots).
+    // Longer back-to-back rows: the grouped ring where a quarter or more of the
+    // sub-warp slots would be empty (rows just past a power of two of slots),
+    // for f32 rows and 16-bit rows of at most 1.5 KB, or where the sub-warp
+    // kernel cannot hold the row.
     p = plan(LSE_F32, 1 << 20, 129, 129);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 4, "f32 N=129: grouped ring, 4 lanes");
     p = plan(LSE_F32, 1 << 20, 520, 520);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16, "f32 N=520: grouped ring, 16 lanes");
+    p = plan(LSE_F32, 1 << 20, 300, 300);
+    expect(p.path == LSE_PATH_SUBWARP, "f32 N=300 (80 % of the slots full): sub-warp kernel");
+    p = plan(LSE_BF16, 1 << 20, 1025, 1025);
+    expect(p.path == LSE_PATH_SUBWARP, "bf16 N=1025 (2 KB rows): sub-warp kernel");
     p = plan(LSE_BF16, 1 << 18, 2047, 2047);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16, "bf16 N=2047: grouped ring, 16 lanes");
     p = plan(LSE_F32, 1 << 20, 68, 68);
     expect(p.path == LSE_PATH_SUBWARP, "rows of <= 512 bytes: no grouped ring");
     p = plan(LSE_F32, 1 << 20, 129, 129, kAligned, nullptr, false, true);
-    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 8 && p.slots_per_lane == 8,
-           "f32 N=129 with 16-bit exponentials: 8 lanes x 8 slots (32 vectors + 2 peel slots)");
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 8 && p.slots_per_lane == 6,
+           "f32 N=129 with 16-bit exponentials: 8 lanes x 6 slots (32 vectors + 2 edge slots)");
 
     // Sub-warp shapes: fewest lanes with <= 4 slots; vector rows of more than
-    // 16 slots take half the lanes with 8 slots each.
+    // 16 slots take half the lanes with up to 8 slots each; slots per lane are
+    // 1, 2, 3, 4, 6 or 8.
     p = plan(LSE_F32, 1 << 20, 40, 44);
-    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 4,
-           "f32 N=40: 4 lanes x 4 slots");
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 3,
+           "f32 N=40: 4 lanes x 3 slots");
     p = plan(LSE_F32, 1 << 20, 128, 128);
     expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 8,
            "f32 N=128: 4 lanes x 8 slots");
     p = plan(LSE_F32, 1 << 17, 1001, 1001);
     expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 32 && p.slots_per_lane == 8,
            "f32 N=1001 (250 vectors + 2 peel slots): a warp x 8 slots");
-    expect(lse::subwarp_auto_slots(33, true) == 64 && lse::subwarp_auto_slots(32, true) == 32,
+    expect(lse::subwarp_auto_slots(33, true) == 48 && lse::subwarp_auto_slots(32, true) == 32 &&
+               lse::subwarp_auto_slots(18, true) == 24 && lse::subwarp_auto_slots(10, true) == 12,
            "sub-warp slot counts");
 
     // Long rows: a CTA per row, split when the rows cannot fill the GPU.
@@ -128,7 +141,7 @@ int main() {
     expect(st == LSE_ERR_INVALID_ARG, "2 lanes for 20 slots (10 each): invalid");
     req.lanes_per_row = 4;
     p = plan(LSE_F32, 1 << 20, 80, 80, kAligned, &req, false, false, &st);
-    expect(st == LSE_OK && p.slots_per_lane == 8, "4 lanes for 20 slots: 8 slots each");
+    expect(st == LSE_OK && p.slots_per_lane == 6, "4 lanes for 20 slots: 6 slots each");
     req.path = LSE_PATH_SPLIT;
     req.lanes_per_row = 0;
     req.splits = 3;

@@ -502,14 +502,14 @@ def test_rowtile_any_width_ragged():
 
 def test_short_row_mapping_rule():
     """Automatic choice between the bulk-copy ring and the sub-warp mapping for
-    back-to-back rows of 16..128 bytes (the measured rule): the ring for rows
-    of 3, 5, 6 or 7 vectors and f32 rows of 4 or 8, sub-warp otherwise."""
+    back-to-back rows of 16..128 bytes (the measured rule): the ring for every
+    width but f32 rows of 2 vectors."""
     _need_gpu()
     for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
         for nv in range(1, 9):
             N = nv * 16 // eb
             q = L.lse_plan_query(dtype=dtype, B=1 << 20, N=N, row_stride=N)
-            ring = nv > 2 and not (eb == 2 and nv in (4, 8))
+            ring = not (eb == 4 and nv == 2)
             assert q["path"] == ("rowtile" if ring else "subwarp"), (dtype, nv, q)
             # not back to back, or too few rows: never the ring
             assert L.lse_plan_query(dtype=dtype, B=1 << 20, N=N, row_stride=N + 16 // eb)["path"] \
@@ -557,23 +557,28 @@ def test_rowtile_grouped_rows(dtype):
 
 
 def test_any_width_ring_rule():
-    """Back-to-back rows of other widths up to 128 bytes take the element-read
-    ring when there are rows for every CTA (row value and token
-    log-probability); the 16-bit exponential entry point keeps the register
-    mappings for them."""
+    """Back-to-back rows of other widths of 32 to 128 bytes take the any-width
+    ring, a thread per row, when there are rows for every CTA (row value and
+    token log-probability); shorter rows and the 16-bit exponential entry
+    point keep the register mappings."""
     _need_gpu()
     for dtype, eb in (("f32", 4), ("bf16", 2), ("f16", 2)):
         for N in (1, 3, 5, 7, 9, 17, 128 // eb - 1):
             # (a query only: 2^26 rows fill every CTA's chunk for any width)
             q = L.lse_plan_query(dtype=dtype, B=1 << 26, N=N, row_stride=N)
+            if N * eb < 32:
+                assert q["path"] == "subwarp", (dtype, N, q)
+                continue
             assert q["path"] == "rowtile" and q["slots_per_lane"] == 0, (dtype, N, q)
             assert L.lse_plan_query(dtype=dtype, B=1000, N=N, row_stride=N)["path"] == "subwarp"
             assert L.lse_plan_query(dtype=dtype, B=1 << 26, N=N, row_stride=N + 1)["path"] \
                 == "subwarp"
     # Rows over 512 bytes: the grouped ring where the sub-warp slots would be
-    # a third empty or more, the sub-warp mapping where they are full.
+    # a quarter empty or more (f32, or 16-bit rows up to 1.5 KB) or cannot hold
+    # the row, the sub-warp mapping otherwise.
     for dtype, N, ring, lanes in (("f32", 129, True, 4), ("f32", 520, True, 16),
-                                  ("bf16", 1020, True, 8), ("bf16", 2047, True, 16),
+                                  ("bf16", 1020, False, 0), ("bf16", 2047, True, 16),
+                                  ("bf16", 520, True, 4), ("f32", 300, False, 0),
                                   ("f32", 128, False, 0), ("f32", 68, False, 0),
                                   ("f32", 1001, False, 0), ("bf16", 800, False, 0)):
         q = L.lse_plan_query(dtype=dtype, B=1 << 22, N=N, row_stride=N)
@@ -581,7 +586,7 @@ def test_any_width_ring_rule():
             assert q["path"] == "rowtile" and q["lanes_per_row"] == lanes, (dtype, N, q)
         else:
             assert q["path"] == "subwarp", (dtype, N, q)
-    x = wl.random_rows(1 << 20, 5, "f32", seed=55, scale=4.0)  # >= 1536 rows per CTA
+    x = wl.random_rows(1 << 20, 13, "f32", seed=55, scale=4.0)  # >= 768 rows per CTA
     xd = torch.from_numpy(x).cuda()
     want = oracle.lse(x, "f32")
     got, p = run(xd, None)
@@ -590,7 +595,7 @@ def test_any_width_ring_rule():
     g16, p16 = L.lse_forward16(xd)
     assert p16.as_dict()["path"] == "subwarp"
     compare_e16(g16.cpu().numpy(), want, e16_bound(x, "f32", want))
-    t = np.arange(x.shape[0], dtype=np.int64) % 5
+    t = np.arange(x.shape[0], dtype=np.int64) % 13
     lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), return_plan=True)
     assert pl.as_dict()["path"] == "rowtile"
     want_lp, want_lse = oracle.token_logprob(x, t, "f32")

@@ -18,8 +18,9 @@
  *               2 for bf16 and f16).
  *   row_stride  distance between row starts, in ELEMENTS, >= N; any value.
  *               Rows are read as 16-byte vectors; a row that does not start
- *               on a 16-byte boundary reads its head and tail (< 16 bytes
- *               each) element by element.
+ *               or end on a 16-byte boundary reads the aligned 16-byte
+ *               vectors that cover it and ignores the bytes outside the row
+ *               (such a vector never leaves the row's memory page).
  *   out         device pointer (host pointer for lse_forward_host) to B
  *               floats, 4-byte aligned.  Written once per row; not retained.
  *   stream      CUDA stream for all work (0 = legacy default stream).  The
@@ -83,15 +84,18 @@ typedef enum {
     LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
     LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: 2, 4 or 8 warps share the
                                   rows of one column tile                       */
-    LSE_PATH_ROWTILE = 7       /* short back-to-back rows (<= 128 bytes) from a
-                                  16-byte aligned base: 32 KB chunks of rows
-                                  streamed into shared memory by bulk copies
-                                  (TMA), one thread per row.  Rows of 16..128
-                                  bytes in multiples of 16 (slots_per_lane =
-                                  vectors per row): row value and token
-                                  log-probability; rows of other widths
-                                  (slots_per_lane = 0, vector_bytes = 1): row
-                                  value with f32 exponentials only            */
+    LSE_PATH_ROWTILE = 7       /* back-to-back rows (<= 4 KB) from a 16-byte
+                                  aligned base, streamed into shared memory by
+                                  bulk copies (TMA).  Rows of 16..128 bytes in
+                                  multiples of 16 (slots_per_lane = vectors per
+                                  row): each warp streams 4 KB chunks of 32
+                                  rows, a lane per row; row value, token
+                                  log-probability and 16-bit exponentials.
+                                  Rows of other widths (slots_per_lane = 0):
+                                  32 KB chunks per CTA, a thread per row up to
+                                  128 bytes (vector_bytes = 1), else a group
+                                  of 4..32 lanes (lanes_per_row); row value and
+                                  token log-probability with f32 exponentials */
 } lse_path;
 
 /*
@@ -102,12 +106,13 @@ typedef enum {
 typedef struct {
     int32_t path;           /* lse_path                                              */
     int32_t vector_bytes;   /* 16: 128-bit loads (a row that does not start on a
-                               16-byte boundary peels its head and tail into
-                               element loads); 1: element loads only;
+                               16-byte boundary reads the vectors covering it and
+                               masks the bytes outside it); 1: element loads only;
                                0 in a request: let the library choose              */
     int32_t lanes_per_row;  /* SUBWARP: lanes per row, a power of two 1..32;
                                column paths: warps sharing one column tile, 1/2/4/8 */
-    int32_t slots_per_lane; /* SUBWARP: vectors (or elements) per lane (output)      */
+    int32_t slots_per_lane; /* SUBWARP: vectors (or elements) per lane, 1/2/3/4/6/8
+                               (output)                                            */
     int32_t threads;        /* CTA / SPLIT: threads per CTA, 32/64/128/256/512      */
     int32_t launches;       /* kernels launched per call (output)                    */
     int64_t splits;         /* SPLIT: CTAs per row (>= 2); 1 otherwise               */

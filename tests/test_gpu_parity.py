@@ -650,3 +650,50 @@ def test_no_wait_timed_out():
     _need_gpu()
     torch.cuda.synchronize()
     assert L.lse_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_subwarp_three_and_six_slots(dtype):
+    """The 3- and 6-slot sub-warp variants (rows just past a power of two of
+    slots): the row value, the token log-probability and the 16-bit
+    exponentials, on rows that start on a 16-byte boundary and on rows that
+    do not (their covering vectors take one or two more slots), with special
+    values at the first and the last element."""
+    _need_gpu()
+    eb = 4 if dtype == "f32" else 2
+    epv = 16 // eb
+    seen = set()
+    for nvec, lanes in ((3, 1), (5, 2), (9, 4), (11, 4), (18, 4), (21, 4), (40, 8), (90, 16),
+                        (170, 32)):
+        for extra, offset in ((0, 0), (1, 0), (0, 1), (epv - 1, 1)):
+            N = nvec * epv + extra
+            B = 37
+            x = wl.random_rows(B, N, dtype, seed=N + offset, scale=6.0, shift=-1.0)
+            xi = x.view(np.uint16) if dtype != "f32" else x
+            nan, pinf, ninf = {"f32": (np.nan, np.inf, -np.inf), "bf16": (0x7FC0, 0x7F80, 0xFF80),
+                               "f16": (0x7E00, 0x7C00, 0xFC00)}[dtype]
+            xi[1, 0], xi[2, N - 1], xi[3, :] = nan, pinf, ninf
+            xi[4, :] = ninf
+            xi[4, N - 1] = 0
+            want = oracle.lse(x, dtype)
+            _, xv = device_rows(x, dtype, row_stride=N + 5, offset=offset)
+            plan = {"path": "subwarp", "lanes_per_row": lanes, "vector_bytes": 16}
+            try:
+                got, p = run(xv, plan)
+            except L.LseError:
+                continue  # more slots than this group can hold
+            V = p.as_dict()["slots_per_lane"]
+            seen.add(V)
+            try:
+                compare(got, want)
+                t = np.arange(B, dtype=np.int64) * 7 % (N + 2) - 1  # includes -1 and N
+                want_lp, want_lse = oracle.token_logprob(x, t, dtype)
+                lp, pl = L.lse_token_logprob(xv, torch.from_numpy(t).cuda(), plan=plan, return_plan=True)
+                assert pl.as_dict()["slots_per_lane"] == V
+                compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
+                g16, p16 = L.lse_forward16(xv, plan=plan)
+                assert p16.as_dict()["slots_per_lane"] == V
+                compare_e16(g16.cpu().numpy(), want, e16_bound(x, dtype, want))
+            except AssertionError as e:
+                raise AssertionError(f"N={N} offset={offset} plan={p.as_dict()}: {e}") from None
+    assert {3, 6} <= seen, seen

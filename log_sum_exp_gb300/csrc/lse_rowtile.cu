@@ -1,30 +1,31 @@
-// lse_rowtile.cu -- short contiguous rows fed by 1-D bulk copies (sm_103a).
+// lse_rowtile.cu -- back-to-back rows fed by 1-D bulk copies (sm_103a).
 //
-// For rows of 16..128 bytes (a multiple of 16) stored back to back
-// (row_stride == N, 16-byte aligned), a persistent CTA streams 32 KB chunks of whole rows from
-// HBM into a ring of shared-memory stages with cp.async.bulk (the Tensor
-// Memory Accelerator's 1-D copy; one instruction per chunk, completion tracked
-// by an mbarrier transaction count), and each of its 256 threads reduces whole
-// rows out of shared memory: max, then one FFMA + ex2 per element (or, with
-// E16, one packed bf16 ex2 per two elements), then the finalize of
-// lse_device.cuh.  Memory traffic never waits for the arithmetic:
-// while one stage is consumed the others are in flight.  ("Speeding up
+// Rows of 16..128 bytes (a multiple of 16) stored back to back (row_stride ==
+// N, 16-byte aligned): one persistent CTA per SM of kRingWarps warps, and every
+// warp runs a ring of its own.  Lane 0 streams the warp's 4 KB chunks of whole
+// rows from HBM into shared memory with cp.async.bulk (the Tensor Memory
+// Accelerator's 1-D copy; completion tracked by an mbarrier transaction
+// count); each lane reduces its rows out of shared memory: max, then one FFMA +
+// ex2 per element (or, with E16, one packed bf16 ex2 per two elements), then
+// the finalize of lse_device.cuh.  A stage is refilled as soon as its own 32
+// lanes have read it, so no warp waits for another.  ("Speeding up
 // Log-Sum-Exp ...", Sec. 3.1: one pass, a register accumulator per row.)
 //
 // With TL the same pass writes the token log-probability x[row, target[row]] -
-// lse[row]: each thread loads its rows' targets before the chunk lands and
-// reads the target element from the staged row in shared memory.
+// lse[row]: each lane loads its rows' targets before the chunk lands and reads
+// the target element from the staged row in shared memory.
 //
 // Rows of other widths (not a multiple of 16 bytes, or longer than 128 bytes,
-// up to 4 KB) take the same ring with chunks that start and end on 16-byte
-// boundaries; each thread folds its rows with element reads from shared
-// memory (rows of <= 128 bytes), or a group of G lanes folds each row from
-// 16-byte reads of the staged chunk, masking the elements of the neighbouring
-// rows that share the row's first and last vectors.
+// up to 4 KB) take 32 KB chunks per CTA that start and end on 16-byte
+// boundaries; each thread folds its row (rows of <= 128 bytes), or a group of
+// G lanes folds each row, from 16-byte reads of the staged chunk, masking the
+// elements of the neighbouring rows that share the row's first and last
+// vectors.
 //
-// Waits are bounded: a stage that does not complete within kWaitPolls polls
-// counts a timeout in a device counter (read by lse_wait_timeouts), the whole
-// CTA stops, waits (also bounded) for its own copies still in flight, and
+// Waits are bounded: a stage that does not complete within the poll limit
+// (kWaitPolls, or lower through lse_set_wait_limit) counts a timeout in a
+// device counter (read by lse_wait_timeouts); the warp (or CTA) stops, waits
+// with the default limit for the copies it issued and nobody consumed, and
 // returns.  Such a timeout does not happen in correct operation.
 #include <atomic>
 #include <cstdint>

@@ -155,6 +155,9 @@ cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t
                                  cudaStream_t stream);
 int cols_occupancy(int dt, bool vec, int warps_per_tile);  // CTAs per SM
 int cols_columns_per_warp(bool vec, int dt);
+// Lanes per column tile: 32, or 16 for one-warp tiles of narrow C (a warp then
+// folds two tiles).
+int cols_lanes_per_tile(int dt, bool vec, int64_t C, int warps_per_tile);
 int cols_rows_per_batch(bool vec);  // per warp per iteration
 int cols_warps_per_cta(int warps_per_tile);
 

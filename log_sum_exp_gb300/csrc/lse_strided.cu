@@ -47,17 +47,22 @@ template <int WT> struct ColCta {
 // WT warps share one column tile and interleave its rows (merged in shared
 // memory); the CTA's warps cover warps / WT tiles.  WT = 1: each warp walks
 // all rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
-// works on one tile (long reductions with few tiles).
-template <int DT, bool VEC, int WT>
+// works on one tile (long reductions with few tiles).  LPT lanes make a tile:
+// 32, or 16 with one-warp tiles when 32-lane tiles would leave a quarter or
+// more of the lanes without a column (narrow C); a warp then folds two tiles,
+// one per half.
+template <int DT, bool VEC, int WT, int LPT>
 __global__ void __launch_bounds__(32 * ColCta<WT>::warps, ColCta<WT>::min_blocks(DType<DT>::bytes))
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
+    static_assert(LPT == 32 || (LPT == 16 && WT == 1), "half-warp tiles are one-warp tiles");
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
     constexpr int NW = ColCta<WT>::warps;
-    constexpr int TPC = NW / WT;  // tiles per CTA
+    constexpr int UPW = 32 / LPT;         // tiles per warp
+    constexpr int TPC = NW / WT * UPW;    // tiles per CTA
     __shared__ float2 part[WT > 1 ? NW : 1][32][EPV];
 
     pdl_trigger();
@@ -73,17 +78,17 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
     // Work units are (a, tile) pairs in a-major order; a CTA's TPC tile slots
     // take consecutive units (several a when C is narrow), and CTAs stride
     // over the units (the loop bound is the same for every warp of the CTA).
-    const int64_t wtiles = (C + 32 * EPV - 1) / (32 * EPV);
+    const int64_t wtiles = (C + LPT * EPV - 1) / (LPT * EPV);
     const int64_t units = A * wtiles;
 
     constexpr int64_t kStep = static_cast<int64_t>(WT) * U;  // rows per batch of one warp
 #pragma unroll 1
     for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * TPC; u0 < units;
          u0 += static_cast<int64_t>(gridDim.x) * TPC) {
-        const int64_t unit = u0 + wid / WT;
+        const int64_t unit = u0 + (wid / WT) * UPW + (UPW > 1 ? lane / LPT : 0);
         const int64_t a = unit < units ? unit / wtiles : 0;
         const int64_t tile = unit - a * wtiles;
-        const int64_t c0 = (tile * 32 + lane) * EPV;
+        const int64_t c0 = (tile * LPT + (lane & (LPT - 1))) * EPV;
         const bool active = unit < units && c0 < C;  // VEC: whole vectors only (C % EPV == 0)
         const char* base = xb + (a * stride_a + (active ? c0 : 0)) * EB;
         Acc acc[EPV];
@@ -278,24 +283,28 @@ merge_columns_kernel(const float2* __restrict__ partial, int64_t outputs, int64_
 
 template <int DT, bool VEC>
 cudaError_t launch_cols_t(const StridedArgs& a) {
-#define LSE_COLS_LAUNCH(WT)                                                                     \
-    return launch_pdl(lse_cols_kernel<DT, VEC, WT>, a.grid, dim3(32 * ColCta<WT>::warps), a.stream, \
-                      a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out,          \
+#define LSE_COLS_LAUNCH_L(WT, LPT)                                                                       \
+    return launch_pdl(lse_cols_kernel<DT, VEC, WT, LPT>, a.grid, dim3(32 * ColCta<WT>::warps), a.stream, \
+                      a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out,               \
                       a.partial, a.P)
+#define LSE_COLS_LAUNCH(WT) LSE_COLS_LAUNCH_L(WT, 32)
     switch (a.warps_per_tile) {
-    case 1: LSE_COLS_LAUNCH(1);
+    case 1:
+        if (cols_lanes_per_tile(DT, VEC, a.C, 1) == 16) LSE_COLS_LAUNCH_L(1, 16);
+        LSE_COLS_LAUNCH(1);
     case 2: LSE_COLS_LAUNCH(2);
     case 4: LSE_COLS_LAUNCH(4);
     case 8: LSE_COLS_LAUNCH(8);
     default: return cudaErrorInvalidValue;
     }
 #undef LSE_COLS_LAUNCH
+#undef LSE_COLS_LAUNCH_L
 }
 
 template <int DT, bool VEC, int WT>
 int cols_occupancy_w() {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, WT>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_cols_kernel<DT, VEC, WT, 32>,
                                                       32 * ColCta<WT>::warps, 0) != cudaSuccess)
         return 1;
     return blocks > 0 ? blocks : 1;
@@ -338,6 +347,13 @@ cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t
 }
 
 int cols_columns_per_warp(bool vec, int dt) { return 32 * (vec ? 16 / (dt == kF32 ? 4 : 2) : 1); }
+int cols_lanes_per_tile(int dt, bool vec, int64_t C, int warps_per_tile) {
+    // Half-warp tiles for one-warp tiles when 32-lane tiles would leave a
+    // quarter or more of their lanes without a column.
+    const int64_t w = cols_columns_per_warp(vec, dt);
+    const int64_t padded = (C + w - 1) / w * w;
+    return warps_per_tile == 1 && 4 * C <= 3 * padded ? 16 : 32;
+}
 int cols_rows_per_batch(bool vec) { return vec ? 4 : 8; }
 int cols_warps_per_cta(int wt) { return wt > 4 ? wt : 4; }
 

@@ -222,6 +222,18 @@ int main() {
         expect(cst == LSE_OK && q.lanes_per_row == 2, "R = 100: 2 warps per tile");
         q = cols(LSE_F32, 512, 64, 1023, kAligned, nullptr, &cst);
         expect(cst == LSE_OK && q.vector_bytes == 1, "C = 1023: one element per lane");
+        // Narrow C: one-warp tiles of 16 lanes, two per warp, at any R.
+        q = cols(LSE_BF16, 8192, 128, 128, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.lanes_per_row == 1,
+               "[8192, 128, 128] bf16 (half the lanes of a 32-lane tile idle): a warp per two tiles");
+        expect(lse::cols_lanes_per_tile(LSE_BF16, true, 128, 1) == 16 &&
+                   lse::cols_lanes_per_tile(LSE_BF16, true, 256, 1) == 32 &&
+                   lse::cols_lanes_per_tile(LSE_F32, true, 128, 1) == 32 &&
+                   lse::cols_lanes_per_tile(LSE_F32, true, 64, 1) == 16 &&
+                   lse::cols_lanes_per_tile(LSE_BF16, true, 128, 2) == 32,
+               "lanes per column tile");
+        q = cols(LSE_F32, 4096, 128, 128, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.lanes_per_row == 2, "[4096, 128, 128] f32 (full 32-lane tiles): 2 warps per tile");
         lse_plan r;
         std::memset(&r, 0, sizeof r);
         r.vector_bytes = 16;

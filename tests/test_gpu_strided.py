@@ -208,3 +208,33 @@ def test_columns_inf_between_shifts(dtype, offset):
             compare(got, want)
         except AssertionError as e:
             raise AssertionError(f"plan {plan}: {e}") from None
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_columns_half_warp_tiles(dtype):
+    """Narrow C: one-warp tiles of 16 lanes, two per warp (the second half of
+    a warp folds the next (a, tile) unit, possibly of the next a).  Special
+    values in columns of both halves; aligned and element layouts; the warp
+    path forced and automatic; a row split."""
+    _need_gpu()
+    for A, R, C in ((37, 64, 64), (100, 9, 128), (20, 33, 40), (7, 70, 200), (3, 5, 384), (1, 3, 16),
+                    (513, 2, 8)):
+        x = wl.random_rows(A * R, C, dtype, seed=A + R + C, scale=5.0).reshape(A, R, C)
+        xi = x.view(np.uint16) if dtype != "f32" else x
+        nan, pinf, ninf = {"f32": (np.nan, np.inf, -np.inf), "bf16": (0x7FC0, 0x7F80, 0xFF80),
+                           "f16": (0x7E00, 0x7C00, 0xFC00)}[dtype]
+        if C >= 4:
+            xi[A - 1, :, C - 1] = ninf
+            xi[A - 1, R // 2, C - 2] = nan
+            xi[0, R - 1, C // 2] = pinf
+            xi[0, :, 0] = ninf
+            xi[0, 0, 0] = 0
+        for lay in (dict(), dict(pad_c=3), dict(offset=1)):
+            for plan in (None, {"path": "columns_warp"}, {"path": "columns_warp", "splits": 2}):
+                if plan and plan.get("splits", 0) > R:
+                    continue
+                got, want = run_strided(x, dtype, plan=plan, **lay)
+                try:
+                    compare(got, want)
+                except AssertionError as e:
+                    raise AssertionError(f"shape {(A, R, C)} layout {lay} plan {plan}: {e}") from None

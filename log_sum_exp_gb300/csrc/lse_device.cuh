@@ -46,6 +46,11 @@ template <int DT> __device__ __forceinline__ constexpr uint32_t neg_inf_word() {
     return DT == kF32 ? kNegInfF32 : (DT == kBF16 ? kNegInfBF16x2 : kNegInfF16x2);
 }
 
+// A compile-time int carried by value (template arguments of generic lambdas).
+template <int V> struct IntConst {
+    static constexpr int value = V;
+};
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -56,6 +61,46 @@ __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed FP32 (add/sub/mul/fma .f32x2, PTX ISA 8.6 on sm_100 and later): two
+// f32 operations in one instruction, each rounded as its scalar form rounds
+// it (round to nearest, no flush), so pairing two independent sums halves the
+// issue slots of their FP32 work without changing a bit of the result.  A
+// pair is one 64-bit register, the low word the first element.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t p, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// 2^t for both elements of a pair (two SFU operations; the SFU has no f32 pair form).
+__device__ __forceinline__ uint64_t f2_ex2(uint64_t t) {
+    float lo, hi;
+    f2_unpack(t, lo, hi);
+    return f2_pack(ex2(lo), ex2(hi));
 }
 
 // Three-input maximum (sm_100+ PTX); a NaN operand is ignored like in max.f32.
@@ -294,19 +339,31 @@ __device__ __forceinline__ float words_max(const uint32_t (&w)[W]) {
 
 // sum of 2^((x - mu) log2 e) over W raw words, into four interleaved
 // accumulators (few live registers, short dependent add chains).
+// Accumulator k takes words i with i % 4 == k (f32), or the low and high
+// halves of word i as accumulators 2i % 4 and 2i % 4 + 1 (16-bit); the work is
+// done on pairs (accumulators 0-1 and 2-3, elements two at a time) with the
+// packed FP32 operations.
 template <int DT, int W>
 __device__ __forceinline__ float words_expsum(const uint32_t (&w)[W], float mu) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    static_assert(W % 2 == 0, "whole word pairs");
+    const uint64_t mu2 = f2_pack(mu, mu);
+    const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
+    uint64_t acc[2] = {0ull, 0ull};  // (+0, +0)
 #pragma unroll
     for (int i = 0; i < W; ++i) {
         if constexpr (DT == kF32) {
-            acc[i & 3] += ex2((__uint_as_float(w[i]) - mu) * kLog2e);
+            if (i & 1) continue;
+            const uint64_t x = f2_pack(__uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+            acc[(i >> 1) & 1] = f2_add(acc[(i >> 1) & 1], f2_ex2(f2_mul(f2_sub(x, mu2), log2e2)));
         } else {
-            acc[(2 * i) & 3] += ex2((word_lo<DT>(w[i]) - mu) * kLog2e);
-            acc[(2 * i + 1) & 3] += ex2((word_hi<DT>(w[i]) - mu) * kLog2e);
+            const uint64_t x = f2_pack(word_lo<DT>(w[i]), word_hi<DT>(w[i]));
+            acc[i & 1] = f2_add(acc[i & 1], f2_ex2(f2_mul(f2_sub(x, mu2), log2e2)));
         }
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    float a0, a1, a2, a3;
+    f2_unpack(acc[0], a0, a1);
+    f2_unpack(acc[1], a2, a3);
+    return (a0 + a1) + (a2 + a3);
 }
 
 // Short rows with their shift mu known in advance: the same exp-sum with one
@@ -320,17 +377,25 @@ __device__ __forceinline__ bool ffma_shift_ok(float mu) { return fabsf(mu) <= 0x
 
 template <int DT, int W>
 __device__ __forceinline__ float words_expsum_scaled(const uint32_t (&w)[W], float c) {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    static_assert(W % 2 == 0, "whole word pairs");
+    const uint64_t nc2 = f2_pack(-c, -c);
+    const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
+    uint64_t acc[2] = {0ull, 0ull};  // accumulators as in words_expsum
 #pragma unroll
     for (int i = 0; i < W; ++i) {
         if constexpr (DT == kF32) {
-            acc[i & 3] += ex2(fmaf(__uint_as_float(w[i]), kLog2e, -c));
+            if (i & 1) continue;
+            const uint64_t x = f2_pack(__uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+            acc[(i >> 1) & 1] = f2_add(acc[(i >> 1) & 1], f2_ex2(f2_fma(x, log2e2, nc2)));
         } else {
-            acc[(2 * i) & 3] += ex2(fmaf(word_lo<DT>(w[i]), kLog2e, -c));
-            acc[(2 * i + 1) & 3] += ex2(fmaf(word_hi<DT>(w[i]), kLog2e, -c));
+            const uint64_t x = f2_pack(word_lo<DT>(w[i]), word_hi<DT>(w[i]));
+            acc[i & 1] = f2_add(acc[i & 1], f2_ex2(f2_fma(x, log2e2, nc2)));
         }
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    float a0, a1, a2, a3;
+    f2_unpack(acc[0], a0, a1);
+    f2_unpack(acc[1], a2, a3);
+    return (a0 + a1) + (a2 + a3);
 }
 
 // log(sum exp) from a maximum m and a sum s of 2^(x log2 e - c), c = fl(mu log2 e):

@@ -293,24 +293,40 @@ lse_segment_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
             acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
         if (k < s_end) {
-            uint32_t w[4 * U];
+            // One-warp units take the last, partial batch with 1, 2, 4 or U
+            // slots per thread, as few as cover what is left of the segment,
+            // so a row just past a whole batch does not pay a full batch of
+            // arithmetic on -inf.
+            auto partial_batch = [&](auto n) {
+                constexpr int UU = decltype(n)::value;
+                uint32_t w[4 * UU];
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const int64_t kk = k + j * T;
-                if (kk < s_end) {
-                    const uint4 u = ldg_stream16(a0 + kk * 16);
-                    w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
-                } else {
+                for (int j = 0; j < UU; ++j) {
+                    const int64_t kk = k + j * T;
+                    if (kk < s_end) {
+                        const uint4 u = ldg_stream16(a0 + kk * 16);
+                        w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
+                        for (int i = 0; i < 4; ++i) w[4 * j + i] = neg_inf_word<DT>();
+                    }
                 }
-            }
-            if (edge) {  // after every load is issued
+                if (edge) {  // after every load is issued
 #pragma unroll
-                for (int j = 0; j < U; ++j)
-                    if (k + j * T < s_end) mask_edge(&w[4 * j], k + j * T);
+                    for (int j = 0; j < UU; ++j)
+                        if (k + j * T < s_end) mask_edge(&w[4 * j], k + j * T);
+                }
+                acc_add_words<DT, 4 * UU, E16>(acc, mu, w);
+            };
+            const int64_t left = s_end - (k - tid);  // slots from this batch's first on
+            if constexpr (T == 32) {  // short segments, where the last batch is much of the work
+                if (left <= T) partial_batch(IntConst<1>{});
+                else if (left <= 2 * T) partial_batch(IntConst<2>{});
+                else if (left <= 4 * T) partial_batch(IntConst<4>{});
+                else partial_batch(IntConst<U>{});
+            } else {  // (wider CTAs: one more variant would spill at their 64 registers)
+                partial_batch(IntConst<U>{});
             }
-            acc_add_words<DT, 4 * U, E16>(acc, mu, w);
         }
     } else {
         for (; k + (U - 1) * T < s_end; k += U * T) {

@@ -783,10 +783,10 @@ lse_status plan_columns(const void* x, lse_dtype dtype, int64_t A, int64_t R, in
         WT = 1;
     }
     // Narrow C (32-lane tiles would leave a quarter or more of their lanes
-    // without a column) takes one-warp tiles of 16 lanes at any R: measured
-    // bf16 [8192, 128, 128] 4.55 against 2.14 TB/s with two warps per 32-lane
-    // tile, [2048, 512, 128] 4.35 against 2.11.
-    const bool narrow = cols_lanes_per_tile(dtype, vec, C, 1) == 16;
+    // without a column) takes one-warp tiles of 16 or 8 lanes at any R:
+    // measured bf16 [8192, 128, 128] 4.55 against 2.14 TB/s with two warps per
+    // 32-lane tile, [2048, 512, 128] 4.35 against 2.11.
+    const bool narrow = cols_lanes_per_tile(dtype, vec, C, 1) != 32;
     if (WT == 0) {
         if (path == LSE_PATH_COLUMNS_CTA)
             WT = 8;
@@ -796,7 +796,7 @@ lse_status plan_columns(const void* x, lse_dtype dtype, int64_t A, int64_t R, in
     if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
     path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
     const int W = cols_warps_per_cta(WT);
-    // One-warp tiles of narrow C: half-warp tiles, two per warp.
+    // One-warp tiles of narrow C: 16- or 8-lane tiles, 2 or 4 per warp.
     const int lpt = cols_lanes_per_tile(dtype, vec, C, WT);
     if (lpt != 32) units = A * ceil_div(C, cols_columns_per_warp(vec, dtype) * lpt / 32);
     int64_t gx = ceil_div(units, W / WT * (32 / lpt));  // CTAs if each took one group of units
@@ -880,17 +880,20 @@ lse_status lse_backward_strided(const void* x, lse_dtype dtype, int64_t A, int64
     const bool vec = al16(x) && al16(dx) && C % epv16 == 0 && (stride_a * eb) % 16 == 0 &&
                      (stride_r * eb) % 16 == 0 && (dx_stride_a * eb) % 16 == 0 &&
                      (dx_stride_r * eb) % 16 == 0;
-    const int64_t wtiles = ceil_div(C, 32 * (vec ? epv16 : 1));  // 32-lane column tiles
-    int64_t units = 0;  // (a, tile) pairs
-    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
     // Warps per unit: a warp takes a whole unit when rows are few (one batch
-    // of rows per warp would leave a shared unit's warps idle), else the CTA's
+    // of rows per warp would leave a shared unit's warps idle) or C is narrow
+    // (16- or 8-lane tiles, as the column kernel takes them), else the CTA's
     // warps share it.  Row splits only while the units cannot cover the GPU
     // 4x, keeping >= 2 batches per warp; beyond 4 waves CTAs loop over units.
     const int64_t W = backward_strided_warps();
     const int64_t U = backward_slots_per_thread();
-    const int wpu = R <= 2 * W * U ? 1 : static_cast<int>(W);
-    const int64_t upc = W / wpu;  // units per CTA
+    const int narrow_lanes = cols_lanes_per_tile(dtype, vec, C, 1);
+    const int wpu = R <= 2 * W * U || narrow_lanes != 32 ? 1 : static_cast<int>(W);
+    const int lpt = wpu == 1 ? narrow_lanes : 32;
+    const int64_t wtiles = ceil_div(C, lpt * (vec ? epv16 : 1));  // column tiles of lpt lanes
+    int64_t units = 0;  // (a, tile) pairs
+    if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
+    const int64_t upc = W / wpu * (32 / lpt);  // units per CTA
     const int64_t resident_ctas = static_cast<int64_t>(info->sms) * (64 / W);
     int64_t gx = ceil_div(units, upc);
     int64_t P = ceil_div(4 * resident_ctas, gx);
@@ -916,6 +919,7 @@ lse_status lse_backward_strided(const void* x, lse_dtype dtype, int64_t A, int64
     a.dx_stride_r = dx_stride_r;
     a.rows_per_split = rows_per_split;
     a.warps_per_unit = wpu;
+    a.lanes_per_tile = lpt;
     a.grid = dim3(static_cast<unsigned>(gx), 1, static_cast<unsigned>(P));
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = launch_backward_strided(dtype, vec, a);

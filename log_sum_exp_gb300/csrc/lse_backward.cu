@@ -61,23 +61,44 @@ __device__ __forceinline__ float grad_term(float x, float lse, float g) {
     return g * ex2((x - lse) * kLog2e);
 }
 
-// One 16-byte vector: 4 f32 or 8 16-bit elements.
+// grad_term on two elements at once (packed FP32, the same rounding), each
+// with its own lse and gradient.
+__device__ __forceinline__ void grad_term2(float x0, float x1, uint64_t l2, uint64_t g2, float& d0,
+                                           float& d1) {
+    const uint64_t t = f2_mul(f2_sub(f2_pack(x0, x1), l2), f2_pack(kLog2e, kLog2e));
+    f2_unpack(f2_mul(g2, f2_ex2(t)), d0, d1);
+}
+
+// One 16-byte vector, l2[i] and g2[i] the lse and gradient pairs of its
+// elements 2i and 2i + 1 (f32: i < 2; 16-bit: the halves of word i).  The row
+// gradient passes one pair throughout, the column gradient its columns'.
 template <int DT>
-__device__ __forceinline__ uint4 grad_vector(uint4 u, float lse, float g) {
+__device__ __forceinline__ uint4 grad_vector_pairs(uint4 u, const uint64_t (&l2)[4],
+                                                   const uint64_t (&g2)[4]) {
+    float d[8];
     if constexpr (DT == kF32) {
-        return make_uint4(__float_as_uint(grad_term(__uint_as_float(u.x), lse, g)),
-                          __float_as_uint(grad_term(__uint_as_float(u.y), lse, g)),
-                          __float_as_uint(grad_term(__uint_as_float(u.z), lse, g)),
-                          __float_as_uint(grad_term(__uint_as_float(u.w), lse, g)));
+        grad_term2(__uint_as_float(u.x), __uint_as_float(u.y), l2[0], g2[0], d[0], d[1]);
+        grad_term2(__uint_as_float(u.z), __uint_as_float(u.w), l2[1], g2[1], d[2], d[3]);
+        return make_uint4(__float_as_uint(d[0]), __float_as_uint(d[1]), __float_as_uint(d[2]),
+                          __float_as_uint(d[3]));
     } else {
         const uint32_t in[4] = {u.x, u.y, u.z, u.w};
         uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = pack2<DT>(grad_term(word_lo<DT>(in[i]), lse, g),
-                             grad_term(word_hi<DT>(in[i]), lse, g));
+        for (int i = 0; i < 4; ++i) {
+            grad_term2(word_lo<DT>(in[i]), word_hi<DT>(in[i]), l2[i], g2[i], d[2 * i], d[2 * i + 1]);
+            o[i] = pack2<DT>(d[2 * i], d[2 * i + 1]);
+        }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
+}
+
+// One 16-byte vector of a row: 4 f32 or 8 16-bit elements, one lse and gradient.
+template <int DT>
+__device__ __forceinline__ uint4 grad_vector(uint4 u, float lse, float g) {
+    const uint64_t l2 = f2_pack(lse, lse), g2 = f2_pack(g, g);
+    const uint64_t lp[4] = {l2, l2, l2, l2}, gp[4] = {g2, g2, g2, g2};
+    return grad_vector_pairs<DT>(u, lp, gp);
 }
 
 // Elements of row `rp` before its first 16-byte boundary, at most N.
@@ -181,42 +202,48 @@ template <int DT, int EPV>
 __device__ __forceinline__ uint4 grad_vector_cols(uint4 u, const float (&l)[EPV],
                                                   const float (&g)[EPV]) {
     if constexpr (DT == kF32) {
+        // f32 columns stay scalar: the pairs cost the one-warp tiles 16
+        // registers and two CTAs per SM (pcsum [512, 64, 1024] 41.3 -> 45.5 us).
         return make_uint4(__float_as_uint(grad_term(__uint_as_float(u.x), l[0], g[0])),
                           __float_as_uint(grad_term(__uint_as_float(u.y), l[1], g[1])),
                           __float_as_uint(grad_term(__uint_as_float(u.z), l[2], g[2])),
                           __float_as_uint(grad_term(__uint_as_float(u.w), l[3], g[3])));
-    } else {
-        const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = pack2<DT>(grad_term(word_lo<DT>(in[i]), l[2 * i], g[2 * i]),
-                             grad_term(word_hi<DT>(in[i]), l[2 * i + 1], g[2 * i + 1]));
-        return make_uint4(o[0], o[1], o[2], o[3]);
     }
+    uint64_t lp[4], gp[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = 2 * i < EPV ? 2 * i : 0;  // f32: pairs 0 and 1 only
+        lp[i] = f2_pack(l[e], l[e + 1 < EPV ? e + 1 : 0]);
+        gp[i] = f2_pack(g[e], g[e + 1 < EPV ? e + 1 : 0]);
+    }
+    return grad_vector_pairs<DT>(u, lp, gp);
 }
 
 // Gradient of the value over a non-last dimension:
 //     dx[a, r, c] = grad[a, c] * exp(x[a, r, c] - lse[a, c]),
 // lse and grad dense [A, C].  A unit is one (a, column tile) pair, the tile
-// 32 lanes x EPV columns (a 16-byte vector per lane, or one element when the
+// LPT lanes x EPV columns (a 16-byte vector per lane, or one element when the
 // layout is not 16-byte aligned); a lane loads its columns' lse and gradient
-// once per unit.  WT warps (1 or kStrWarps) share a unit and interleave the
-// rows of blockIdx.z's split, each with kBwdU rows in flight (all loads before
-// any store, so dx may be x).  A CTA's warps take consecutive units (several
-// a when C is narrow) and CTAs stride over the units; nothing is merged, so
-// every warp loops on its own.
+// once per unit.  LPT is 32, or 16 or 8 for one-warp units of narrow C (the
+// column kernel's rule), a warp then taking 32 / LPT units side by side.  WT
+// warps (1 or kStrWarps) share a unit and interleave the rows of blockIdx.z's
+// split, each with kBwdU rows in flight (all loads before any store, so dx
+// may be x).  A CTA's warps take consecutive units (several a when C is
+// narrow) and CTAs stride over the units; nothing is merged, so every warp
+// loops on its own.
 constexpr int kStrWarps = 4;
 
-template <int DT, bool VEC, int WT>
+template <int DT, bool VEC, int WT, int LPT>
 __global__ void __launch_bounds__(32 * kStrWarps)
 lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C,
                             int64_t stride_a, int64_t stride_r, const float* __restrict__ lse,
                             const float* __restrict__ grad, void* __restrict__ dx,
                             int64_t dx_stride_a, int64_t dx_stride_r, int64_t rows_per_split) {
+    static_assert(LPT == 32 || ((LPT == 16 || LPT == 8) && WT == 1), "narrow tiles are one-warp units");
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
-    constexpr int UPC = kStrWarps / WT;  // units per CTA
+    constexpr int UPW = 32 / LPT;             // units per warp
+    constexpr int UPC = kStrWarps / WT * UPW;  // units per CTA
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -224,13 +251,15 @@ lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, in
     const int phase = wid % WT;
     const int64_t r_begin = static_cast<int64_t>(blockIdx.z) * rows_per_split;
     const int64_t r_end = r_begin + rows_per_split < R ? r_begin + rows_per_split : R;
-    const int64_t wtiles = (C + 32 * EPV - 1) / (32 * EPV);
+    const int64_t wtiles = (C + LPT * EPV - 1) / (LPT * EPV);
     const int64_t units = A * wtiles;
-    for (int64_t unit = static_cast<int64_t>(blockIdx.x) * UPC + wid / WT; unit < units;
-         unit += static_cast<int64_t>(gridDim.x) * UPC) {
-        const int64_t a = unit / wtiles;
-        const int64_t c0 = ((unit - a * wtiles) * 32 + lane) * EPV;
-        const bool active = c0 < C;  // VEC: C is a multiple of EPV, whole vectors only
+    for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * UPC + (wid / WT) * UPW; u0 < units;
+         u0 += static_cast<int64_t>(gridDim.x) * UPC) {
+        const int64_t unit = u0 + (UPW > 1 ? lane / LPT : 0);
+        const int64_t a = unit < units ? unit / wtiles : 0;
+        const int64_t c0 = ((unit - a * wtiles) * LPT + (lane & (LPT - 1))) * EPV;
+        // VEC: C is a multiple of EPV, whole vectors only
+        const bool active = unit < units && c0 < C;
         float l[EPV], g[EPV];
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
@@ -274,13 +303,18 @@ lse_backward_strided_kernel(const void* __restrict__ x, int64_t A, int64_t R, in
 
 template <int DT, bool VEC>
 cudaError_t launch_backward_strided_t(const BackwardStridedArgs& a) {
-    if (a.warps_per_unit == 1)
-        return launch_pdl(lse_backward_strided_kernel<DT, VEC, 1>, a.grid, dim3(32 * kStrWarps),
-                          a.stream, a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad,
-                          a.dx, a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
-    return launch_pdl(lse_backward_strided_kernel<DT, VEC, kStrWarps>, a.grid, dim3(32 * kStrWarps),
-                      a.stream, a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad, a.dx,
-                      a.dx_stride_a, a.dx_stride_r, a.rows_per_split);
+#define LSE_SBWD_LAUNCH(WT, LPT)                                                                     \
+    return launch_pdl(lse_backward_strided_kernel<DT, VEC, WT, LPT>, a.grid, dim3(32 * kStrWarps), \
+                      a.stream, a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.lse, a.grad, a.dx,    \
+                      a.dx_stride_a, a.dx_stride_r, a.rows_per_split)
+    if (a.warps_per_unit != 1) LSE_SBWD_LAUNCH(kStrWarps, 32);
+    switch (a.lanes_per_tile) {
+    case 8: LSE_SBWD_LAUNCH(1, 8);
+    case 16: LSE_SBWD_LAUNCH(1, 16);
+    case 32: LSE_SBWD_LAUNCH(1, 32);
+    default: return cudaErrorInvalidValue;
+    }
+#undef LSE_SBWD_LAUNCH
 }
 
 // Rows of at most kBwdU slots: the (row, slot) pairs are flattened and each

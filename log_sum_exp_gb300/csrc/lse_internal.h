@@ -125,6 +125,7 @@ struct BackwardStridedArgs {
     int64_t dx_stride_r;
     int64_t rows_per_split;
     int warps_per_unit;  // 1, or backward_strided_warps(): warps sharing one (a, tile) unit
+    int lanes_per_tile;  // 32; 16 or 8 for one-warp units of narrow C (cols_lanes_per_tile)
     dim3 grid;           // (CTAs striding over the (a, tile) units, 1, row splits)
     cudaStream_t stream;
 };

@@ -9,7 +9,8 @@
 // pairwise merge and finalize as the row kernels (lse_device.cuh).
 //
 // Mapping: a column tile is 32 lanes x EPV columns (EPV = elements per
-// 16-byte vector, or 1 when the layout is not 16-byte aligned) of one index a;
+// 16-byte vector, or 1 when the layout is not 16-byte aligned) of one index a,
+// or 16 or 8 lanes when C is narrow;
 // every load instruction of a warp covers one contiguous stretch of a row, and
 // a thread folds U rows per batch into EPV accumulators with one rescale per
 // batch.  WT = 1, 2, 4 or 8 warps share a tile, interleaving its rows and
@@ -48,15 +49,15 @@ template <int WT> struct ColCta {
 // memory); the CTA's warps cover warps / WT tiles.  WT = 1: each warp walks
 // all rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
 // works on one tile (long reductions with few tiles).  LPT lanes make a tile:
-// 32, or 16 with one-warp tiles when 32-lane tiles would leave a quarter or
-// more of the lanes without a column (narrow C); a warp then folds two tiles,
-// one per half.
+// 32, or 16 or 8 with one-warp tiles when the wider tile would leave a
+// quarter or more of its lanes without a column (narrow C); a warp then folds
+// 32 / LPT tiles, one per group of LPT lanes.
 template <int DT, bool VEC, int WT, int LPT>
 __global__ void __launch_bounds__(32 * ColCta<WT>::warps, ColCta<WT>::min_blocks(DType<DT>::bytes))
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
-    static_assert(LPT == 32 || (LPT == 16 && WT == 1), "half-warp tiles are one-warp tiles");
+    static_assert(LPT == 32 || ((LPT == 16 || LPT == 8) && WT == 1), "narrow tiles are one-warp tiles");
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
@@ -194,6 +195,9 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                             }
                         }
                     }
+                    // Scalar sums: packed pairs (add/sub/mul .f32x2) measured
+                    // 5-6 % slower on the short 16-bit reductions ([131072, 8,
+                    // 128] bf16) and no faster for f32.
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
                         float sum = 0.0f;
@@ -290,8 +294,11 @@ cudaError_t launch_cols_t(const StridedArgs& a) {
 #define LSE_COLS_LAUNCH(WT) LSE_COLS_LAUNCH_L(WT, 32)
     switch (a.warps_per_tile) {
     case 1:
-        if (cols_lanes_per_tile(DT, VEC, a.C, 1) == 16) LSE_COLS_LAUNCH_L(1, 16);
-        LSE_COLS_LAUNCH(1);
+        switch (cols_lanes_per_tile(DT, VEC, a.C, 1)) {
+        case 8: LSE_COLS_LAUNCH_L(1, 8);
+        case 16: LSE_COLS_LAUNCH_L(1, 16);
+        default: LSE_COLS_LAUNCH(1);
+        }
     case 2: LSE_COLS_LAUNCH(2);
     case 4: LSE_COLS_LAUNCH(4);
     case 8: LSE_COLS_LAUNCH(8);
@@ -348,11 +355,16 @@ cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t
 
 int cols_columns_per_warp(bool vec, int dt) { return 32 * (vec ? 16 / (dt == kF32 ? 4 : 2) : 1); }
 int cols_lanes_per_tile(int dt, bool vec, int64_t C, int warps_per_tile) {
-    // Half-warp tiles for one-warp tiles when 32-lane tiles would leave a
-    // quarter or more of their lanes without a column.
-    const int64_t w = cols_columns_per_warp(vec, dt);
-    const int64_t padded = (C + w - 1) / w * w;
-    return warps_per_tile == 1 && 4 * C <= 3 * padded ? 16 : 32;
+    // One-warp tiles narrow to 16 or 8 lanes while the wider tile would leave
+    // a quarter or more of its lanes without a column: the widest tile that
+    // keeps more than three quarters of them busy, else 8 lanes.
+    if (warps_per_tile != 1) return 32;
+    for (int lanes = 32; lanes > 8; lanes /= 2) {
+        const int64_t w = cols_columns_per_warp(vec, dt) * lanes / 32;
+        const int64_t padded = (C + w - 1) / w * w;
+        if (4 * C > 3 * padded) return lanes;
+    }
+    return 8;
 }
 int cols_rows_per_batch(bool vec) { return vec ? 4 : 8; }
 int cols_warps_per_cta(int wt) { return wt > 4 ? wt : 4; }

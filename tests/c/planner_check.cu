@@ -232,6 +232,18 @@ int main() {
                    lse::cols_lanes_per_tile(LSE_F32, true, 64, 1) == 16 &&
                    lse::cols_lanes_per_tile(LSE_BF16, true, 128, 2) == 32,
                "lanes per column tile");
+        // 8-lane tiles where a 16-lane tile would leave a quarter idle too.
+        expect(lse::cols_lanes_per_tile(LSE_BF16, true, 64, 1) == 8 &&
+                   lse::cols_lanes_per_tile(LSE_BF16, true, 192, 1) == 8 &&
+                   lse::cols_lanes_per_tile(LSE_BF16, true, 384, 1) == 16 &&
+                   lse::cols_lanes_per_tile(LSE_F32, true, 32, 1) == 8 &&
+                   lse::cols_lanes_per_tile(LSE_F32, false, 8, 1) == 8 &&
+                   lse::cols_lanes_per_tile(LSE_BF16, true, 64, 4) == 32,
+               "8-lane column tiles");
+        q = cols(LSE_BF16, 16384, 64, 64, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.lanes_per_row == 1 && q.splits == 1 &&
+                   q.grid == 16384 / 16,
+               "[16384, 64, 64] bf16: 8-lane tiles, four per warp, 16 per CTA");
         q = cols(LSE_F32, 4096, 128, 128, kAligned, nullptr, &cst);
         expect(cst == LSE_OK && q.lanes_per_row == 2, "[4096, 128, 128] f32 (full 32-lane tiles): 2 warps per tile");
         lse_plan r;

@@ -211,14 +211,14 @@ def test_columns_inf_between_shifts(dtype, offset):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
-def test_columns_half_warp_tiles(dtype):
-    """Narrow C: one-warp tiles of 16 lanes, two per warp (the second half of
-    a warp folds the next (a, tile) unit, possibly of the next a).  Special
-    values in columns of both halves; aligned and element layouts; the warp
-    path forced and automatic; a row split."""
+def test_columns_narrow_tiles(dtype):
+    """Narrow C: one-warp tiles of 16 or 8 lanes, two or four per warp (the
+    later groups of lanes fold the next (a, tile) units, possibly of the next
+    a).  Special values in columns of several groups; aligned and element
+    layouts; the warp path forced and automatic; a row split."""
     _need_gpu()
     for A, R, C in ((37, 64, 64), (100, 9, 128), (20, 33, 40), (7, 70, 200), (3, 5, 384), (1, 3, 16),
-                    (513, 2, 8)):
+                    (513, 2, 8), (65, 4, 32), (9, 17, 192)):
         x = wl.random_rows(A * R, C, dtype, seed=A + R + C, scale=5.0).reshape(A, R, C)
         xi = x.view(np.uint16) if dtype != "f32" else x
         nan, pinf, ninf = {"f32": (np.nan, np.inf, -np.inf), "bf16": (0x7FC0, 0x7F80, 0xFF80),

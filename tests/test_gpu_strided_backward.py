@@ -97,6 +97,21 @@ def test_shapes_and_layouts(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_narrow_column_tiles(dtype):
+    """Narrow C: one-warp units of 16- or 8-lane tiles, two or four side by
+    side in a warp (the later groups of lanes take the next units, possibly of
+    the next a); aligned, padded and element layouts, and in place."""
+    _need_gpu()
+    eb = 4 if dtype == "f32" else 2
+    for A, R, C in ((37, 64, 64), (100, 9, 128), (20, 33, 40), (7, 70, 200), (3, 5, 384),
+                    (1, 3, 16), (513, 2, 8), (65, 4, 32)):
+        x3 = wl.random_rows(A * R, C, dtype, seed=A + R + C, scale=4.0).reshape(A, R, C)
+        for pad_r, pad_a, offset in ((0, 0, 0), (16 // eb, 8, 0), (3, 5, 0), (0, 0, 1)):
+            run(x3, dtype, pad_r, pad_a, offset, seed=A + pad_r + offset)
+        run(x3, dtype, inplace=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_special_values(dtype):
     _need_gpu()
     A, R, C = 2, 33, 64

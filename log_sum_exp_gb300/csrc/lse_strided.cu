@@ -30,10 +30,11 @@ namespace lse {
 namespace {
 
 // Warps per CTA for WT warps per tile: 4 (small CTAs balance better across
-// SMs) unless the tile itself takes 8.  f32 variants and one-warp tiles keep
-// 32 warps per SM resident (<= 64 registers per thread); 16-bit tiles shared
-// by several warps hold 8 accumulators per lane and keep 24 (<= 85 registers;
-// capping them at 64 measured 15 % slower on long reductions).
+// SMs) unless the tile itself takes 8.  f32 variants keep 32 warps per SM
+// resident (<= 64 registers per thread); 16-bit tiles hold 8 accumulators per
+// lane and keep 28 (<= 73 registers; capping them at 64 measured 15 % slower
+// on long reductions, 6 CTAs of one-warp tiles instead of 7 5-10 % slower on
+// short ones).
 // How far a column's maximum may rise above the shift its terms are taken
 // against before the sum is rescaled: terms stay below e^8 (2^11.5).
 constexpr float kLazyShift = 8.0f;
@@ -41,7 +42,7 @@ constexpr float kLazyShift = 8.0f;
 template <int WT> struct ColCta {
     static constexpr int warps = WT > 4 ? WT : 4;
     static constexpr int min_blocks(int elem_bytes) {
-        return elem_bytes == 4 ? 1024 / (32 * warps) : (WT == 1 ? 768 / (32 * warps) : 896 / (32 * warps));
+        return elem_bytes == 4 ? 1024 / (32 * warps) : 896 / (32 * warps);
     }
 };
 
@@ -81,13 +82,20 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
     // over the units (the loop bound is the same for every warp of the CTA).
     const int64_t wtiles = (C + LPT * EPV - 1) / (LPT * EPV);
     const int64_t units = A * wtiles;
+    const bool small = units <= 0xffffffffll;  // unit indices divide in 32 bits
+    // 16-byte output stores: out on a 16-byte boundary (C % EPV == 0 and
+    // c0 % EPV == 0 keep every lane's EPV outputs on one).
+    const bool out_vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
 
     constexpr int64_t kStep = static_cast<int64_t>(WT) * U;  // rows per batch of one warp
 #pragma unroll 1
     for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * TPC; u0 < units;
          u0 += static_cast<int64_t>(gridDim.x) * TPC) {
         const int64_t unit = u0 + (wid / WT) * UPW + (UPW > 1 ? lane / LPT : 0);
-        const int64_t a = unit < units ? unit / wtiles : 0;
+        // (past the last unit: the last a, whose rows the neighbouring units read)
+        const int64_t a = unit >= units ? A - 1
+                          : small ? static_cast<int64_t>(static_cast<uint32_t>(unit) / static_cast<uint32_t>(wtiles))
+                                  : unit / wtiles;
         const int64_t tile = unit - a * wtiles;
         const int64_t c0 = (tile * LPT + (lane & (LPT - 1))) * EPV;
         const bool active = unit < units && c0 < C;  // VEC: whole vectors only (C % EPV == 0)
@@ -106,107 +114,131 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
         // PIPE: the next batch's loads are issued before the current batch is
         // folded, so two batches per warp are in flight.  For one warp per
         // tile (short reductions, which otherwise wait a full memory round
-        // trip per batch); 16-bit tiles then run 6 CTAs per SM (+5 % on bf16
-        // [512, 64, 1024]).
+        // trip per batch; +5 % on bf16 [512, 64, 1024]).
         constexpr bool PIPE = VEC && WT == 1;
-        uint4 nxt[U];
-        auto load_batch = [&](int64_t r, uint4 (&u)[U]) {
+        const int64_t srb = stride_r * EB;  // bytes from one row to the next
+        // A batch of U rows r0 + j * WT.  When all of them are in range (every
+        // batch but a split's last, uniform per warp) the loads go without a
+        // per-row test or -inf defaults; lanes without a column read the
+        // column-0 rows of their a (in bounds, never stored).
+        auto load_batch = [&](int64_t r0, const char* q, uint4 (&u)[U]) {
+            if (r0 + (U - 1) * WT < r_end) {
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const int64_t rr = r + j * WT;
-                u[j] = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
-                                  neg_inf_word<DT>());
-                if (active && rr < r_end) u[j] = ldg_stream16(base + rr * stride_r * EB);
+                for (int j = 0; j < U; ++j) u[j] = ldg_stream16(q + j * WT * srb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    u[j] = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
+                                      neg_inf_word<DT>());
+                    if (r0 + j * WT < r_end) u[j] = ldg_stream16(q + j * WT * srb);
+                }
             }
         };
-        if constexpr (PIPE) {
-            if (r_begin + phase < r_end) load_batch(r_begin + phase, nxt);
-        }
-        for (int64_t r = r_begin + phase; r < r_end; r += kStep) {
-            if constexpr (VEC) {
-                uint4 cur[U];
-                if constexpr (PIPE) {
+        auto fold = [&](const uint4 (&cur)[U]) {
+            if constexpr (EB == 4) {
+                // f32: four columns per lane; the eager rescale measured
+                // faster here than the lazy one below (5.8 vs 5.5 TB/s on
+                // [512, 64, 1024]).
 #pragma unroll
-                    for (int j = 0; j < U; ++j) cur[j] = nxt[j];
-                    if (r + kStep < r_end) load_batch(r + kStep, nxt);  // uniform per warp
-                } else {
-                    load_batch(r, cur);
-                }
-                if constexpr (EB == 4) {
-                    // f32: four columns per lane; the eager rescale measured
-                    // faster here than the lazy one below (5.8 vs 5.5 TB/s on
-                    // [512, 64, 1024]).
+                for (int e = 0; e < EPV; ++e) {
+                    float v[U];
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        float v[U];
+                    for (int j = 0; j < U; ++j) v[j] = __uint_as_float(e == 0 ? cur[j].x : e == 1 ? cur[j].y
+                                                                       : e == 2 ? cur[j].z : cur[j].w);
+                    float cm = v[0];
 #pragma unroll
-                        for (int j = 0; j < U; ++j) v[j] = __uint_as_float(e == 0 ? cur[j].x : e == 1 ? cur[j].y
-                                                                           : e == 2 ? cur[j].z : cur[j].w);
-                        float cm = v[0];
+                    for (int j = 1; j < U; ++j) cm = fmaxf(cm, v[j]);
+                    acc_raise(acc[e], mu[e], cm);
+                    float sum = 0.0f;
 #pragma unroll
-                        for (int j = 1; j < U; ++j) cm = fmaxf(cm, v[j]);
-                        acc_raise(acc[e], mu[e], cm);
-                        float sum = 0.0f;
-#pragma unroll
-                        for (int j = 0; j < U; ++j) sum += ex2((v[j] - mu[e]) * kLog2e);
-                        acc[e].s += sum;
-                    }
-                } else {
-                    uint32_t w[U][4];
-#pragma unroll
-                    for (int j = 0; j < U; ++j) {
-                        w[j][0] = cur[j].x; w[j][1] = cur[j].y; w[j][2] = cur[j].z; w[j][3] = cur[j].w;
-                    }
-                    // Column maxima of the batch, packed over the rows (NaN
-                    // lanes ignored, as fmaxf does), kept as 4 words.
-                    uint32_t cmw[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t t = w[0][i];
-#pragma unroll
-                        for (int j = 1; j < U; ++j)
-                            t = DT == kBF16 ? hmax2_bf16(t, w[j][i]) : hmax2_f16(t, w[j][i]);
-                        cmw[i] = t;
-                    }
-                    auto cm = [&](int e) { return word_elem<DT>(cmw, e); };
-                    // Lazy shifts: a column's terms are taken relative to a shift
-                    // mu that only moves when the batch maximum exceeds it by more
-                    // than kLazyShift (or is the column's first value above -inf),
-                    // so terms stay below e^kLazyShift and most batches skip the
-                    // rescale; the warp branches over it uniformly.
-                    // A column whose sum is already +inf (it met +inf) never
-                    // moves its shift again: the rescale factor could flush to 0.
-                    auto need = [&](int e) {
-                        return ((seen >> e) & 1u)
-                                   ? cm(e) > mu[e] + kLazyShift && acc[e].s != __int_as_float(0x7f800000)
-                                   : cm(e) > __int_as_float(kNegInfF32);
-                    };
-                    bool any = false;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) any = any || need(e);
-                    if (__any_sync(0xffffffffu, any)) {
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) {
-                            if (need(e)) {
-                                const float mn = shift_of(cm(e));
-                                acc[e].s = ((seen >> e) & 1u) ? acc[e].s * ex2((mu[e] - mn) * kLog2e) : 0.0f;
-                                mu[e] = mn;
-                                seen |= 1u << e;
-                            }
-                        }
-                    }
-                    // Scalar sums: packed pairs (add/sub/mul .f32x2) measured
-                    // 5-6 % slower on the short 16-bit reductions ([131072, 8,
-                    // 128] bf16) and no faster for f32.
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        float sum = 0.0f;
-#pragma unroll
-                        for (int j = 0; j < U; ++j) sum += ex2((word_elem<DT>(w[j], e) - mu[e]) * kLog2e);
-                        acc[e].s += sum;
-                    }
+                    for (int j = 0; j < U; ++j) sum += ex2((v[j] - mu[e]) * kLog2e);
+                    acc[e].s += sum;
                 }
             } else {
+                uint32_t w[U][4];
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    w[j][0] = cur[j].x; w[j][1] = cur[j].y; w[j][2] = cur[j].z; w[j][3] = cur[j].w;
+                }
+                // Column maxima of the batch, packed over the rows (NaN
+                // lanes ignored, as fmaxf does), kept as 4 words.
+                uint32_t cmw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t t = w[0][i];
+#pragma unroll
+                    for (int j = 1; j < U; ++j)
+                        t = DT == kBF16 ? hmax2_bf16(t, w[j][i]) : hmax2_f16(t, w[j][i]);
+                    cmw[i] = t;
+                }
+                auto cm = [&](int e) { return word_elem<DT>(cmw, e); };
+                // Lazy shifts: a column's terms are taken relative to a shift
+                // mu that only moves when the batch maximum exceeds it by more
+                // than kLazyShift (or is the column's first value above -inf),
+                // so terms stay below e^kLazyShift and most batches skip the
+                // rescale; the warp branches over it uniformly.
+                // A column whose sum is already +inf (it met +inf) never
+                // moves its shift again: the rescale factor could flush to 0.
+                auto need = [&](int e) {
+                    return ((seen >> e) & 1u)
+                               ? cm(e) > mu[e] + kLazyShift && acc[e].s != __int_as_float(0x7f800000)
+                               : cm(e) > __int_as_float(kNegInfF32);
+                };
+                bool any = false;
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) any = any || need(e);
+                if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        if (need(e)) {
+                            const float mn = shift_of(cm(e));
+                            acc[e].s = ((seen >> e) & 1u) ? acc[e].s * ex2((mu[e] - mn) * kLog2e) : 0.0f;
+                            mu[e] = mn;
+                            seen |= 1u << e;
+                        }
+                    }
+                }
+                // Scalar sums: packed pairs (add/sub/mul .f32x2) measured
+                // 5-6 % slower on the short 16-bit reductions ([131072, 8,
+                // 128] bf16) and no faster for f32.
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < U; ++j) sum += ex2((word_elem<DT>(w[j], e) - mu[e]) * kLog2e);
+                    acc[e].s += sum;
+                }
+            }
+        };
+        if constexpr (VEC) {
+            const char* q = base + (r_begin + phase) * srb;
+            const int64_t qstep = kStep * srb;
+            int64_t r = r_begin + phase;
+            if constexpr (PIPE) {
+                // Two batches in flight, in two buffers used in turn (no copy
+                // from the prefetched batch to the folded one).
+                uint4 b0[U], b1[U];
+                if (r < r_end) load_batch(r, q, b0);
+                while (r < r_end) {
+                    if (r + kStep < r_end) load_batch(r + kStep, q + qstep, b1);
+                    fold(b0);
+                    r += kStep;
+                    q += qstep;
+                    if (r >= r_end) break;
+                    if (r + kStep < r_end) load_batch(r + kStep, q + qstep, b0);
+                    fold(b1);
+                    r += kStep;
+                    q += qstep;
+                }
+            } else {
+                for (; r < r_end; r += kStep, q += qstep) {
+                    uint4 cur[U];
+                    load_batch(r, q, cur);
+                    fold(cur);
+                }
+            }
+        } else {
+            for (int64_t r = r_begin + phase; r < r_end; r += kStep) {
                 float v[U];
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
@@ -254,15 +286,33 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             __syncthreads();  // part[] is reused by the next a
         }
         if (phase == 0 && active) {
+            if constexpr (VEC) {
+                // EPV consecutive outputs (C % EPV == 0, so all in range): 16-byte
+                // stores where the destination allows (the scratch always does).
+                if (P == 1) {
+                    float* o = out + a * C + c0;
+                    float r[EPV];
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                const int64_t c = c0 + e;
-                if (c < C) {
-                    if (P == 1)
-                        out[a * C + c] = acc_finalize(acc[e]);
-                    else  // split-major: coalesced here and in merge_columns_kernel
-                        partial[split * (A * C) + a * C + c] = make_float2(acc[e].m, acc[e].s);
+                    for (int e = 0; e < EPV; ++e) r[e] = acc_finalize(acc[e]);
+                    if (out_vec) {
+#pragma unroll
+                        for (int e = 0; e < EPV; e += 4)
+                            *reinterpret_cast<float4*>(o + e) = make_float4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) o[e] = r[e];
+                    }
+                } else {  // split-major: coalesced here and in merge_columns_kernel
+                    float2* o = partial + split * (A * C) + a * C + c0;
+#pragma unroll
+                    for (int e = 0; e < EPV; e += 2)
+                        *reinterpret_cast<float4*>(o + e) = make_float4(acc[e].m, acc[e].s, acc[e + 1].m, acc[e + 1].s);
                 }
+            } else {
+                if (P == 1)
+                    out[a * C + c0] = acc_finalize(acc[0]);
+                else
+                    partial[split * (A * C) + a * C + c0] = make_float2(acc[0].m, acc[0].s);
             }
         }
     }

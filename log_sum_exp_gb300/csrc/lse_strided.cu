@@ -107,10 +107,13 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             acc[e] = acc_identity();
             mu[e] = 0.0f;
         }
-        // VEC, 16-bit: acc[e].s is taken against the lazy shift mu[e]; bit e of `seen`
-        // records that column e has met a value above -inf (acc[e].m is set
-        // from mu and `seen` once the rows are done).
-        uint32_t seen = 0;
+        // VEC, 16-bit: acc[e].s is taken against the lazy shift mu[e], which
+        // moves when a batch maximum exceeds thr[e]: -inf until column e has
+        // met a value above -inf, then mu[e] + kLazyShift (acc[e].m is set
+        // from mu and thr once the rows are done).
+        float thr[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) thr[e] = __int_as_float(kNegInfF32);
         // PIPE: the next batch's loads are issued before the current batch is
         // folded, so two batches per warp are in flight.  For one warp per
         // tile (short reductions, which otherwise wait a full memory round
@@ -176,25 +179,24 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                 // mu that only moves when the batch maximum exceeds it by more
                 // than kLazyShift (or is the column's first value above -inf),
                 // so terms stay below e^kLazyShift and most batches skip the
-                // rescale; the warp branches over it uniformly.
-                // A column whose sum is already +inf (it met +inf) never
-                // moves its shift again: the rescale factor could flush to 0.
-                auto need = [&](int e) {
-                    return ((seen >> e) & 1u)
-                               ? cm(e) > mu[e] + kLazyShift && acc[e].s != __int_as_float(0x7f800000)
-                               : cm(e) > __int_as_float(kNegInfF32);
-                };
+                // rescale; the warp branches over it uniformly.  The rescale
+                // exponent is clamped to [-126, 0]: a sum that is already
+                // +inf (the column met +inf) stays +inf instead of meeting a
+                // factor flushed to 0, the first move scales the empty sum 0
+                // by at most 1, and an older sum cut to 2^-126 of itself
+                // instead of 0 is below any term that can follow (>= 1 for
+                // the new maximum; the older sum holds < R e^8).
                 bool any = false;
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) any = any || need(e);
+                for (int e = 0; e < EPV; ++e) any = any || cm(e) > thr[e];
                 if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
-                        if (need(e)) {
+                        if (cm(e) > thr[e]) {
                             const float mn = shift_of(cm(e));
-                            acc[e].s = ((seen >> e) & 1u) ? acc[e].s * ex2((mu[e] - mn) * kLog2e) : 0.0f;
+                            acc[e].s *= ex2(fminf(fmaxf((mu[e] - mn) * kLog2e, -126.0f), 0.0f));
                             mu[e] = mn;
-                            seen |= 1u << e;
+                            thr[e] = mn + kLazyShift;
                         }
                     }
                 }
@@ -265,7 +267,7 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
             // merging it with other partials keeps +inf.
 #pragma unroll
             for (int e = 0; e < EPV; ++e)
-                acc[e].m = !((seen >> e) & 1u)                        ? __int_as_float(kNegInfF32)
+                acc[e].m = thr[e] == __int_as_float(kNegInfF32)      ? __int_as_float(kNegInfF32)
                            : acc[e].s == __int_as_float(0x7f800000) ? __int_as_float(0x7f800000)
                                                                      : mu[e];
         }

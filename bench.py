@@ -370,6 +370,9 @@ SWEEP_BYTES = 512 << 20       # input bytes per step of the throughput-vs-N swee
 SWEEP_N = [16, 31, 32, 33, 64, 100, 128, 129, 256, 257, 300, 512, 520, 1000, 1024, 1025,
            2048, 4096, 4097, 8192, 16383, 16384, 32000, 32768, 50257, 65536, 128256, 262144,
            1048576, 4194304, 16777216]
+COLS_SWEEP_BYTES = 256 << 20  # input bytes per call of the column sweep
+COLS_SWEEP_R = [2, 8, 64, 512, 4096]
+COLS_SWEEP_C = [64, 128, 192, 1000, 1024, 16384]
 
 
 def rotation_copies(in_bytes: int, l2_bytes: int = L2_BYTES,
@@ -425,6 +428,26 @@ def main_kernel_name(plan: dict) -> str:
 def sweep_shape(N: int, eb: int, total: int = SWEEP_BYTES) -> tuple[int, int]:
     """(B, N) of one sweep point: rows of N elements filling ~total bytes."""
     return max(1, total // (N * eb)), N
+
+
+def columns_sweep_shape(R: int, C: int, eb: int, total: int = COLS_SWEEP_BYTES) -> int:
+    """A of one column-sweep point: [A, R, C] filling ~total bytes (0: does not fit once)."""
+    return total // (R * C * eb)
+
+
+def columns_sweep_table(points: list[dict]) -> str:
+    """Markdown table of column-sweep points (forward and backward)."""
+    lines = ["| dtype | R | C | A | forward plan | forward µs | forward GB/s | frac | "
+             "backward µs | backward GB/s | frac |",
+             "|---|---|---|---|---|---|---|---|---|---|---|"]
+    for q in points:
+        p = q["plan"]
+        desc = ("warp" if p["path"] == "columns_warp" else f"cta WT={p['lanes_per_row']}") + \
+               (" elem" if p["vector_bytes"] == 1 else "") + (f" P={p['splits']}" if p["splits"] > 1 else "")
+        lines.append(f"| {q['dtype']} | {q['R']} | {q['C']} | {q['A']} | {desc} | {q['fwd_us']:.2f} | "
+                     f"{q['fwd_gbs']:.0f} | {q['fwd_frac']:.3f} | {q['bwd_us']:.2f} | "
+                     f"{q['bwd_gbs']:.0f} | {q['bwd_frac']:.3f} |")
+    return "\n".join(lines)
 
 
 def sweep_table(points: list[dict]) -> str:
@@ -608,6 +631,68 @@ def run_sweep(args) -> None:
             del xs, outs
             torch.cuda.empty_cache()
     print(sweep_table(points), flush=True)
+
+
+def run_sweep_columns(args) -> None:
+    """Throughput of lse_forward_strided and lse_backward_strided over R (the
+    reduced dimension) and C at ~256 MB of input per call, f32 and bf16,
+    automatic plan: one JSON line per point, then a markdown table."""
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from log_sum_exp_gb300 import build as lse_build
+    lse_build.build()
+    import log_sum_exp_gb300 as L
+
+    peak, _ = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    points = []
+    for dtype in ("f32", "bf16"):
+        eb = 4 if dtype == "f32" else 2
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        for R in COLS_SWEEP_R:
+            for C in COLS_SWEEP_C:
+                A = columns_sweep_shape(R, C, eb)
+                if A < 1:
+                    continue
+                gen.manual_seed(wl.SEED_BASE + 200 + R + C)
+                # Two copies: every call reads rows absent from L2.
+                xs = [(3.0 * torch.randn(A, R, C, device=dev, generator=gen)).to(tdt) for _ in range(2)]
+                outs = [torch.empty(A, C, dtype=torch.float32, device=dev) for _ in range(2)]
+                grad = torch.ones(A, C, dtype=torch.float32, device=dev)
+                dx = torch.empty_like(xs[0])
+                plan = L.lse_forward_strided_ptr(xs[0].data_ptr(), dtype, A, R, C, R * C, C,
+                                                 outs[0].data_ptr(), sh).as_dict()
+
+                def fwd(i, evb=0, eve=0):
+                    L.lse_forward_strided_ptr(xs[i % 2].data_ptr(), dtype, A, R, C, R * C, C,
+                                              outs[i % 2].data_ptr(), sh)
+
+                def bwd(i, evb=0, eve=0):
+                    L.lse_backward_strided_ptr(xs[i % 2].data_ptr(), dtype, A, R, C, R * C, C,
+                                               outs[i % 2].data_ptr(), grad.data_ptr(),
+                                               dx.data_ptr(), R * C, C, sh)
+
+                q = {"dtype": dtype, "R": R, "C": C, "A": A, "plan": plan}
+                for name, step, nbytes in (("fwd", fwd, A * R * C * eb + 4 * A * C),
+                                           ("bwd", bwd, 2 * A * R * C * eb + 8 * A * C)):
+                    for i in range(5):
+                        step(i)
+                    torch.cuda.synchronize(dev)
+                    bounds, _, per = timed_steps(step, args.sweep_steps, stream, blocks=3)
+                    us = block_stats(bounds, per)["us_median"]
+                    q[name + "_us"] = us
+                    q[name + "_gbs"] = nbytes / (us * 1e-6) / 1e9
+                    q[name + "_frac"] = q[name + "_gbs"] / peak
+                points.append(q)
+                print(json.dumps(q), flush=True)
+                del xs, outs, grad, dx
+                torch.cuda.empty_cache()
+    print(columns_sweep_table(points), flush=True)
 
 
 def run_native(args) -> None:
@@ -888,6 +973,10 @@ def main(argv=None) -> None:
     ap.add_argument("--sweep", action="store_true",
                     help="throughput against N at ~512 MB per call (f32, bf16): JSON lines "
                          "and a markdown table instead of the bench line")
+    ap.add_argument("--sweep-columns", action="store_true",
+                    help="throughput of the value over a non-last dimension and its backward "
+                         "against R and C at ~256 MB per call (f32, bf16): JSON lines and a "
+                         "markdown table instead of the bench line")
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -906,6 +995,8 @@ def main(argv=None) -> None:
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.sweep_columns:
+        run_sweep_columns(args)
     else:
         run_native(args)
 

@@ -126,3 +126,16 @@ def test_clock_samples_kept_by_window():
     everything = c.summary(t0 + 100, t0 + 200)  # nothing inside: every sample
     assert everything["samples_in_window"] == 0 and everything["samples"] == 4
     assert bench.ClockSampler.parse("garbage") is None
+
+
+def test_columns_sweep_helpers():
+    assert bench.columns_sweep_shape(64, 1024, 4) == (256 << 20) // (64 * 1024 * 4)
+    assert bench.columns_sweep_shape(4096, 16384, 4) == 1
+    assert bench.columns_sweep_shape(1 << 20, 1 << 20, 4) == 0
+    plan = {"path": "columns_warp", "lanes_per_row": 1, "vector_bytes": 16, "splits": 1}
+    q = {"dtype": "bf16", "R": 8, "C": 64, "A": 262144, "plan": plan, "fwd_us": 50.0,
+         "fwd_gbs": 5400.0, "fwd_frac": 0.812, "bwd_us": 80.0, "bwd_gbs": 6800.0, "bwd_frac": 1.02}
+    t = bench.columns_sweep_table([q, dict(q, plan=dict(plan, path="columns_cta", lanes_per_row=4,
+                                                           splits=9, vector_bytes=1))])
+    assert "| bf16 | 8 | 64 | 262144 | warp | 50.00 | 5400 | 0.812 | 80.00 | 6800 | 1.020 |" in t
+    assert "| cta WT=4 elem P=9 |" in t

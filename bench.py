@@ -422,6 +422,7 @@ def main_kernel_name(plan: dict) -> str:
             "cta": "lse_segment_kernel", "split": "lse_segment_kernel",
             "empty": "fill_neg_inf_kernel", "backward": plan.get("kernel"),
             "columns_warp": "lse_cols_kernel", "columns_cta": "lse_cols_kernel",
+            "columns_short": "lse_cols_short_kernel",
             "columns_backward": "lse_backward_strided_kernel"}[path]
 
 
@@ -442,7 +443,7 @@ def columns_sweep_table(points: list[dict]) -> str:
              "|---|---|---|---|---|---|---|---|---|---|---|"]
     for q in points:
         p = q["plan"]
-        desc = ("warp" if p["path"] == "columns_warp" else f"cta WT={p['lanes_per_row']}") + \
+        desc = {"columns_warp": "warp", "columns_short": "short"}.get(p["path"], f"cta WT={p['lanes_per_row']}") + \
                (" elem" if p["vector_bytes"] == 1 else "") + (f" P={p['splits']}" if p["splits"] > 1 else "")
         lines.append(f"| {q['dtype']} | {q['R']} | {q['C']} | {q['A']} | {desc} | {q['fwd_us']:.2f} | "
                      f"{q['fwd_gbs']:.0f} | {q['fwd_frac']:.3f} | {q['bwd_us']:.2f} | "

@@ -84,7 +84,7 @@ typedef enum {
     LSE_PATH_COLUMNS_WARP = 5, /* lse_forward_strided: one warp per column tile */
     LSE_PATH_COLUMNS_CTA = 6,  /* lse_forward_strided: 2, 4 or 8 warps share the
                                   rows of one column tile                       */
-    LSE_PATH_ROWTILE = 7       /* back-to-back rows (<= 4 KB) from a 16-byte
+    LSE_PATH_ROWTILE = 7,      /* back-to-back rows (<= 4 KB) from a 16-byte
                                   aligned base, streamed into shared memory by
                                   bulk copies (TMA).  Rows of 16..128 bytes in
                                   multiples of 16 (slots_per_lane = vectors per
@@ -96,6 +96,10 @@ typedef enum {
                                   128 bytes (vector_bytes = 1), else a group
                                   of 4..32 lanes (lanes_per_row); row value and
                                   token log-probability with f32 exponentials */
+    LSE_PATH_COLUMNS_SHORT = 8 /* lse_forward_strided, R <= 8 rows of 16-byte
+                                  column vectors: one thread per vector loads
+                                  all R rows at once and folds them (max,
+                                  then exp-sum); no split                     */
 } lse_path;
 
 /*
@@ -255,9 +259,11 @@ LSE_API lse_status lse_backward(const void *x, lse_dtype dtype, int64_t B, int64
  *   out      device pointer to A * C floats (row-major [A, C]); must not
  *            overlap x.
  *   plan     NULL (automatic) or an lse_plan: path 0, LSE_PATH_COLUMNS_WARP
- *            (one warp per 32-lane column tile walks all its rows) or
+ *            (one warp per 32-lane column tile walks all its rows),
  *            LSE_PATH_COLUMNS_CTA (lanes_per_row = 2, 4 or 8 warps interleave
- *            the rows of one tile, merged in shared memory; 0 = 8);
+ *            the rows of one tile, merged in shared memory; 0 = 8) or
+ *            LSE_PATH_COLUMNS_SHORT (R <= 8 and a 16-byte vector layout, no
+ *            split; the automatic choice there);
  *            splits 0 (automatic) or k >= 1 (<= R, <= 65535) row splits
  *            across CTAs -- with k > 1 the call takes A * C * k * 8 bytes of
  *            stream-ordered scratch and a merge kernel; vector_bytes as for

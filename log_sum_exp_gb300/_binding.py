@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "LSE_OK", 1: "LSE_ERR_INVALID_ARG", 2: "LSE_ERR_UNSUPPORTED_D
                 3: "LSE_ERR_ALLOC", 4: "LSE_ERR_CUDA"}
 DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
 PATHS = {"auto": 0, "empty": 1, "subwarp": 2, "cta": 3, "split": 4, "columns_warp": 5,
-         "columns_cta": 6, "rowtile": 7}
+         "columns_cta": 6, "rowtile": 7, "columns_short": 8}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 # Exported names, in header order.

@@ -764,6 +764,29 @@ lse_status plan_columns(const void* x, lse_dtype dtype, int64_t A, int64_t R, in
         }
         vec = req->vector_bytes == 16;
     }
+    // Short reductions of the vector layout: a thread per 16-byte column
+    // vector folds all R rows from registers (automatic for R <= 8 unless a
+    // split or warps per tile are asked for).
+    const bool short_ok = vec && R <= kColsShortMaxRows;
+    if (rpath == LSE_PATH_COLUMNS_SHORT ||
+        (rpath == LSE_PATH_AUTO && short_ok && (!req || (req->splits <= 1 && req->lanes_per_row == 0)))) {
+        if (!short_ok || (req && (req->splits > 1 || req->lanes_per_row != 0))) return LSE_ERR_INVALID_ARG;
+        const int64_t nvec = outputs / epv16;
+        int64_t grid = ceil_div(nvec, kColsShortThreads);
+        const int64_t cap = static_cast<int64_t>(sms) * 32;  // 4 waves of 8 CTAs per SM
+        if (grid > cap) grid = cap;
+        p.path = LSE_PATH_COLUMNS_SHORT;
+        p.vector_bytes = 16;
+        p.threads = kColsShortThreads;
+        p.lanes_per_row = 0;
+        p.splits = 1;
+        p.segment_slots = R;
+        p.grid = grid;
+        p.scratch_bytes = 0;
+        p.launches = 1;
+        *plan = p;
+        return LSE_OK;
+    }
     const int64_t wtiles = ceil_div(C, cols_columns_per_warp(vec, dtype));  // 32-lane column tiles
     int64_t units = 0;  // (a, tile) pairs
     if (__builtin_mul_overflow(A, wtiles, &units)) return LSE_ERR_INVALID_ARG;
@@ -944,7 +967,7 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
     const lse_plan* req = plan;
     const int rpath = req ? req->path : LSE_PATH_AUTO;
     if (rpath != LSE_PATH_AUTO && rpath != LSE_PATH_COLUMNS_WARP && rpath != LSE_PATH_COLUMNS_CTA &&
-        rpath != LSE_PATH_EMPTY)
+        rpath != LSE_PATH_COLUMNS_SHORT && rpath != LSE_PATH_EMPTY)
         return LSE_ERR_INVALID_ARG;
     if (req && req->splits < 0) return LSE_ERR_INVALID_ARG;
     if (outputs == 0) return LSE_OK;
@@ -973,6 +996,22 @@ lse_status lse_forward_strided(const void* x, lse_dtype dtype, int64_t A, int64_
                            &p)) != LSE_OK)
         return st;
     if (plan) *plan = p;
+    if (p.path == LSE_PATH_COLUMNS_SHORT) {
+        StridedArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.x = x;
+        a.A = A;
+        a.R = R;
+        a.C = C;
+        a.stride_a = stride_a;
+        a.stride_r = stride_r;
+        a.out = out;
+        a.P = 1;
+        a.grid = dim3(static_cast<unsigned>(p.grid));
+        a.stream = stream;
+        const cudaError_t e = launch_cols_short(dtype, a);
+        return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+    }
     const bool vec = p.vector_bytes == 16;
     const int WT = p.lanes_per_row;
     const int64_t P = p.splits;

@@ -152,6 +152,11 @@ struct StridedArgs {
     cudaStream_t stream;
 };
 cudaError_t launch_cols(int dt, bool vec, const StridedArgs& a);
+// R <= kColsShortMaxRows rows of 16-byte column vectors, a thread per vector
+// (lse_cols_short_kernel); a.grid is the 1-D grid, a.R the rows.
+constexpr int kColsShortThreads = 256;
+constexpr int kColsShortMaxRows = 8;
+cudaError_t launch_cols_short(int dt, const StridedArgs& a);
 cudaError_t launch_merge_columns(const float2* partial, int64_t outputs, int64_t P, float* out,
                                  cudaStream_t stream);
 int cols_occupancy(int dt, bool vec, int warps_per_tile);  // CTAs per SM

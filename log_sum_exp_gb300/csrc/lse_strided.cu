@@ -337,6 +337,93 @@ merge_columns_kernel(const float2* __restrict__ partial, int64_t outputs, int64_
     }
 }
 
+// Short reductions (R = RR <= 8 rows, the 16-byte vector layout): one thread
+// per 16-byte vector of EPV columns of one a loads all RR rows at once, takes
+// each column's maximum and then its exp-sum against it (two passes over
+// registers, no online state, no rescale), and stores its EPV values, with
+// 16-byte stores where out allows.  Threads stride over the A * C / EPV
+// vectors in a-major order, so a warp's loads cover consecutive vectors of
+// one row.
+template <int DT, int RR>
+__global__ void __launch_bounds__(kColsShortThreads)
+lse_cols_short_kernel(const void* __restrict__ x, int64_t A, int64_t C, int64_t stride_a,
+                      int64_t stride_r, float* __restrict__ out) {
+    constexpr int EB = DType<DT>::bytes;
+    constexpr int EPV = 16 / EB;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t cv = C / EPV;  // vectors per row (C % EPV == 0)
+    const int64_t nvec = A * cv;
+    const bool small = nvec <= 0xffffffffll;  // indices divide in 32 bits
+    const bool out_vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    const int64_t srb = stride_r * EB;
+    const char* xb = reinterpret_cast<const char*>(x);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < nvec;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t a = small ? static_cast<int64_t>(static_cast<uint32_t>(t) / static_cast<uint32_t>(cv))
+                                : t / cv;
+        const int64_t c0 = (t - a * cv) * EPV;
+        const char* p = xb + (a * stride_a + c0) * EB;
+        uint32_t w[RR][4];
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            const uint4 u = ldg_stream16(p + r * srb);
+            w[r][0] = u.x; w[r][1] = u.y; w[r][2] = u.z; w[r][3] = u.w;
+        }
+        // Column maxima (NaN ignored, as fmaxf does), as 4 words: f32 one
+        // column per word, 16-bit two.
+        uint32_t cmw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t t4 = w[0][i];
+#pragma unroll
+            for (int r = 1; r < RR; ++r) {
+                if constexpr (DT == kF32) t4 = __float_as_uint(fmaxf(__uint_as_float(t4), __uint_as_float(w[r][i])));
+                else t4 = DT == kBF16 ? hmax2_bf16(t4, w[r][i]) : hmax2_f16(t4, w[r][i]);
+            }
+            cmw[i] = t4;
+        }
+        float res[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const float m = word_elem<DT>(cmw, e);
+            const float mu = shift_of(m);
+            float sum = 0.0f;
+#pragma unroll
+            for (int r = 0; r < RR; ++r) sum += ex2((word_elem<DT>(w[r], e) - mu) * kLog2e);
+            res[e] = acc_finalize(Acc{m, sum});
+        }
+        float* o = out + a * C + c0;
+        if (out_vec) {
+#pragma unroll
+            for (int e = 0; e < EPV; e += 4)
+                *reinterpret_cast<float4*>(o + e) = make_float4(res[e], res[e + 1], res[e + 2], res[e + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) o[e] = res[e];
+        }
+    }
+}
+
+template <int DT>
+cudaError_t launch_cols_short_t(const StridedArgs& a) {
+#define LSE_COLS_SHORT(RR)                                                                          \
+    return launch_pdl(lse_cols_short_kernel<DT, RR>, a.grid, dim3(kColsShortThreads), a.stream, a.x, \
+                      a.A, a.C, a.stride_a, a.stride_r, a.out)
+    switch (a.R) {
+    case 1: LSE_COLS_SHORT(1);
+    case 2: LSE_COLS_SHORT(2);
+    case 3: LSE_COLS_SHORT(3);
+    case 4: LSE_COLS_SHORT(4);
+    case 5: LSE_COLS_SHORT(5);
+    case 6: LSE_COLS_SHORT(6);
+    case 7: LSE_COLS_SHORT(7);
+    case 8: LSE_COLS_SHORT(8);
+    default: return cudaErrorInvalidValue;
+    }
+#undef LSE_COLS_SHORT
+}
+
 template <int DT, bool VEC>
 cudaError_t launch_cols_t(const StridedArgs& a) {
 #define LSE_COLS_LAUNCH_L(WT, LPT)                                                                       \
@@ -394,6 +481,14 @@ int cols_occupancy(int dt, bool vec, int wt) {
     case kF32: return vec ? cols_occupancy_t<kF32, true>(wt) : cols_occupancy_t<kF32, false>(wt);
     case kBF16: return vec ? cols_occupancy_t<kBF16, true>(wt) : cols_occupancy_t<kBF16, false>(wt);
     default: return vec ? cols_occupancy_t<kF16, true>(wt) : cols_occupancy_t<kF16, false>(wt);
+    }
+}
+
+cudaError_t launch_cols_short(int dt, const StridedArgs& a) {
+    switch (dt) {
+    case kF32: return launch_cols_short_t<kF32>(a);
+    case kBF16: return launch_cols_short_t<kBF16>(a);
+    default: return launch_cols_short_t<kF16>(a);
     }
 }
 

@@ -244,6 +244,38 @@ int main() {
         expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.lanes_per_row == 1 && q.splits == 1 &&
                    q.grid == 16384 / 16,
                "[16384, 64, 64] bf16: 8-lane tiles, four per warp, 16 per CTA");
+        // Short reductions: a thread per 16-byte column vector, R <= 8.
+        q = cols(LSE_F32, 1024, 2, 1024, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_SHORT && q.splits == 1 && q.threads == 256 &&
+                   q.segment_slots == 2 && q.grid == 1024 && q.launches == 1,
+               "[1024, 2, 1024] f32: short reduction, 1024 CTAs");
+        q = cols(LSE_BF16, 1 << 20, 8, 64, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_SHORT && q.grid == 152 * 32,
+               "[1M, 8, 64] bf16: short reduction, 4 waves of 8 CTAs per SM");
+        q = cols(LSE_F32, 1024, 9, 1024, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP, "R = 9: column tiles");
+        q = cols(LSE_F32, 512, 4, 1023, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.vector_bytes == 1,
+               "C = 1023 (element layout): column tiles");
+        {
+            lse_plan r2;
+            std::memset(&r2, 0, sizeof r2);
+            r2.splits = 2;
+            q = cols(LSE_F32, 1024, 4, 1024, kAligned, &r2, &cst);
+            expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.splits == 2,
+                   "R = 4 with 2 splits asked: column tiles");
+            std::memset(&r2, 0, sizeof r2);
+            r2.path = LSE_PATH_COLUMNS_SHORT;
+            q = cols(LSE_F32, 1024, 4, 1024, kAligned, &r2, &cst);
+            expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_SHORT, "short path forced");
+            q = cols(LSE_F32, 1024, 9, 1024, kAligned, &r2, &cst);
+            expect(cst == LSE_ERR_INVALID_ARG, "short path forced on R = 9: invalid");
+            q = cols(LSE_F32, 512, 4, 1023, kAligned, &r2, &cst);
+            expect(cst == LSE_ERR_INVALID_ARG, "short path forced on an element layout: invalid");
+            r2.splits = 2;
+            q = cols(LSE_F32, 1024, 4, 1024, kAligned, &r2, &cst);
+            expect(cst == LSE_ERR_INVALID_ARG, "short path forced with splits: invalid");
+        }
         q = cols(LSE_F32, 4096, 128, 128, kAligned, nullptr, &cst);
         expect(cst == LSE_OK && q.lanes_per_row == 2, "[4096, 128, 128] f32 (full 32-lane tiles): 2 warps per tile");
         lse_plan r;

@@ -139,3 +139,6 @@ def test_columns_sweep_helpers():
                                                            splits=9, vector_bytes=1))])
     assert "| bf16 | 8 | 64 | 262144 | warp | 50.00 | 5400 | 0.812 | 80.00 | 6800 | 1.020 |" in t
     assert "| cta WT=4 elem P=9 |" in t
+    assert "| short |" in bench.columns_sweep_table([dict(q, plan=dict(plan, path="columns_short",
+                                                                        lanes_per_row=0))])
+    assert bench.main_kernel_name({"path": "columns_short"}) == "lse_cols_short_kernel"

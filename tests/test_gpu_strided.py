@@ -238,3 +238,57 @@ def test_columns_narrow_tiles(dtype):
                     compare(got, want)
                 except AssertionError as e:
                     raise AssertionError(f"shape {(A, R, C)} layout {lay} plan {plan}: {e}") from None
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_columns_short_reductions(dtype):
+    """R <= 8 rows of 16-byte column vectors: a thread per vector folds all R
+    rows (automatic there, and forced).  Every R, special values (an all -inf
+    column, NaN, +inf, -inf among finite values), padded strides that keep
+    the vector layout, and an output off a 16-byte boundary (scalar stores)."""
+    _need_gpu()
+    eb = 4 if dtype == "f32" else 2
+    epv = 16 // eb
+    for R in range(1, 9):
+        for A, C in ((3, 8 * epv), (37, 2 * epv), (1, 64 * epv)):
+            x = wl.random_rows(A * R, C, dtype, seed=R * 100 + A + C, scale=5.0).reshape(A, R, C)
+            xi = x.view(np.uint16) if dtype != "f32" else x
+            ninf, pinf, nan = {"f32": (-np.inf, np.inf, np.nan), "bf16": (0xFF80, 0x7F80, 0x7FC0),
+                               "f16": (0xFC00, 0x7C00, 0x7E00)}[dtype]
+            xi[0, :, 1] = ninf                   # all -inf
+            xi[A - 1, R - 1, C - 1] = nan
+            xi[A // 2, 0, C // 2] = pinf
+            if R > 1:
+                xi[0, R // 2, 3] = ninf          # -inf among finite values
+            for lay in (dict(), dict(pad_c=epv), dict(pad_a=2 * epv, pad_r=1)):
+                for plan in (None, {"path": "columns_short"}):
+                    got, want = run_strided(x, dtype, plan=plan, **lay)
+                    try:
+                        compare(got, want)
+                    except AssertionError as e:
+                        raise AssertionError(f"R={R} A={A} C={C} layout {lay} plan {plan}: {e}") from None
+            # out off a 16-byte boundary
+            xd = torch_view(np.ascontiguousarray(x).reshape(-1) if dtype == "f32"
+                            else np.ascontiguousarray(xi).reshape(-1), dtype).cuda()
+            out = torch.full((A * C + 8,), float("nan"), device="cuda")
+            p = L.lse_forward_strided_ptr(xd.data_ptr(), dtype, A, R, C, R * C, C, out.data_ptr() + 4,
+                                          torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            assert p.as_dict()["path"] == "columns_short"
+            o = out.cpu().numpy()
+            assert np.isnan(o[0]) and np.all(np.isnan(o[A * C + 1:])), "write outside out"
+            want = oracle.lse_strided(np.ascontiguousarray(x).reshape(-1), dtype, A, R, C, R * C, C)
+            compare(o[1:A * C + 1].reshape(A, C), want)
+
+
+def test_columns_short_rejects_other_layouts():
+    _need_gpu()
+    x = torch.zeros(4, 9, 64, device="cuda")
+    with pytest.raises(L.LseError):
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 4, 9, 64, 9 * 64, 64,
+                                  torch.empty(256, device="cuda").data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream, {"path": "columns_short"})
+    with pytest.raises(L.LseError):  # C = 63: element layout
+        L.lse_forward_strided_ptr(x.data_ptr(), "f32", 4, 4, 63, 4 * 63, 63,
+                                  torch.empty(256, device="cuda").data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream, {"path": "columns_short"})

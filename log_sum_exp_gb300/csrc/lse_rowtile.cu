@@ -216,7 +216,7 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
 // released for the next copy only after every thread is done with it.  TL:
 // the token log-probability epilogue (out may then be null): each row's target
 // is loaded before its fold, and x[row, target] read from the staged row.
-template <int DT, int G, bool TL>
+template <int DT, int G, bool TL, int NVT = kAnyThreadRowVectors>
 __global__ void __launch_bounds__(kTileThreads)
 lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* __restrict__ out,
                        const int64_t* __restrict__ target, float* __restrict__ logprob,
@@ -287,23 +287,24 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                 if (ok && row < Bm) {
                     const int64_t t = TL ? __ldg(target + row) : -1;
                     // The aligned 16-byte vectors holding the row's <= 128 bytes
-                    // (at most 9; only those are read and folded), the
+                    // (at most NVT: 9, or 5 for rows of <= 64 + elem bytes; only
+                    // those are read and folded), the
                     // neighbours' elements in the first and the last masked to
                     // -inf, folded from registers (max, then exp-sum).
                     const uint32_t rb0 = static_cast<uint32_t>(q * RB);
                     const uint32_t rb1 = rb0 + static_cast<uint32_t>(RB);
                     const uint32_t v0 = rb0 >> 4;
                     const int nvec = static_cast<int>(((rb1 + 15u) >> 4) - v0);
-                    uint32_t w[4 * kAnyThreadRowVectors];
+                    uint32_t w[4 * NVT];
 #pragma unroll
-                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                    for (int j = 0; j < NVT; ++j) {
                         uint4 u = make_uint4(neg_inf_word<DT>(), neg_inf_word<DT>(), neg_inf_word<DT>(),
                                              neg_inf_word<DT>());
                         if (j < nvec) u = *reinterpret_cast<const uint4*>(st + (v0 + j) * 16u);
                         w[4 * j] = u.x; w[4 * j + 1] = u.y; w[4 * j + 2] = u.z; w[4 * j + 3] = u.w;
                     }
 #pragma unroll
-                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                    for (int j = 0; j < NVT; ++j) {
                         if (j == 0 || j == nvec - 1) {
                             uint32_t q4[4] = {w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]};
                             mask_words<DT>(q4, (v0 + j) * 16u, rb0, rb1);
@@ -311,11 +312,11 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
                             for (int i = 0; i < 4; ++i) w[4 * j + i] = q4[i];
                         }
                     }
-                    const float m = words_max<DT, 4 * kAnyThreadRowVectors>(w);
+                    const float m = words_max<DT, 4 * NVT>(w);
                     const float mu = shift_of(m);
                     float sum = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < kAnyThreadRowVectors; ++j) {
+                    for (int j = 0; j < NVT; ++j) {
                         if (j < nvec) {
                             const uint32_t q4[4] = {w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]};
                             sum += words_expsum<DT, 4>(q4, mu);
@@ -418,12 +419,12 @@ cudaError_t allow_smem(int bytes) {
     return e;
 }
 
-template <int DT, int G, bool TL>
+template <int DT, int G, bool TL, int NVT = kAnyThreadRowVectors>
 cudaError_t launch_rowtile_any_g(const LaunchArgs& a, int grid) {
     const int smem = kStages * kChunkBytes;
-    cudaError_t e = allow_smem<lse_rowtile_any_kernel<DT, G, TL>>(smem);
+    cudaError_t e = allow_smem<lse_rowtile_any_kernel<DT, G, TL, NVT>>(smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(lse_rowtile_any_kernel<DT, G, TL>, dim3(static_cast<unsigned>(grid)),
+    return launch_pdl_smem(lse_rowtile_any_kernel<DT, G, TL, NVT>, dim3(static_cast<unsigned>(grid)),
                            dim3(kTileThreads), static_cast<size_t>(smem), a.stream, a.x, a.B, a.N,
                            a.out, a.tl.target, a.tl.logprob, g_stage_polls.load(std::memory_order_relaxed));
 }
@@ -431,7 +432,9 @@ cudaError_t launch_rowtile_any_g(const LaunchArgs& a, int grid) {
 template <int DT, bool TL>
 cudaError_t launch_rowtile_any_t(const LaunchArgs& a, int lanes, int grid) {
     switch (lanes) {
-    case 1: return launch_rowtile_any_g<DT, 1, TL>(a, grid);
+    case 1:  // a thread per row: 5 vector slots cover rows of <= 64 + elem bytes
+        if (a.N * DType<DT>::bytes <= 64 + DType<DT>::bytes) return launch_rowtile_any_g<DT, 1, TL, 5>(a, grid);
+        return launch_rowtile_any_g<DT, 1, TL>(a, grid);
     case 4: return launch_rowtile_any_g<DT, 4, TL>(a, grid);
     case 8: return launch_rowtile_any_g<DT, 8, TL>(a, grid);
     case 16: return launch_rowtile_any_g<DT, 16, TL>(a, grid);

@@ -200,15 +200,23 @@ lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int
                         }
                     }
                 }
-                // Scalar sums: packed pairs (add/sub/mul .f32x2) measured
-                // 5-6 % slower on the short 16-bit reductions ([131072, 8,
-                // 128] bf16) and no faster for f32.
+                // Columns 2i and 2i + 1 (the halves of word i) as packed pairs
+                // (sub/mul/add .f32x2); each column's terms still summed in
+                // row order.  +1-5 % on bf16 reductions of 64-4096 rows; the
+                // f32 tiles above keep scalar sums (no gain there).
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    float sum = 0.0f;
+                for (int i = 0; i < 4; ++i) {
+                    const uint64_t mu2 = f2_pack(mu[2 * i], mu[2 * i + 1]);
+                    uint64_t sum2 = 0ull;
 #pragma unroll
-                    for (int j = 0; j < U; ++j) sum += ex2((word_elem<DT>(w[j], e) - mu[e]) * kLog2e);
-                    acc[e].s += sum;
+                    for (int j = 0; j < U; ++j) {
+                        const uint64_t x2 = f2_pack(word_lo<DT>(w[j][i]), word_hi<DT>(w[j][i]));
+                        sum2 = f2_add(sum2, f2_ex2(f2_mul(f2_sub(x2, mu2), f2_pack(kLog2e, kLog2e))));
+                    }
+                    float s0, s1;
+                    f2_unpack(sum2, s0, s1);
+                    acc[2 * i].s += s0;
+                    acc[2 * i + 1].s += s1;
                 }
             }
         };

@@ -119,8 +119,8 @@ int pow2_ceil(int64_t v) {
 // 16-byte vectors).  Rows just above a power of two of slots (an unaligned row
 // adds up to two) waste less on -inf padding with 3 or 6 than with 4 or 8: on
 // those the kernel is bound by instruction issue, not memory.
-int64_t subwarp_slot_count(int64_t v, bool wide) {
-    if (v <= 4) return v;
+int64_t subwarp_slot_count(int64_t v, bool wide, bool warp) {
+    if (v <= 4 || warp) return v;  // a whole warp per row: 5 and 7 slots too
     return wide && v <= 6 ? 6 : 8;
 }
 
@@ -141,10 +141,14 @@ int subwarp_auto_lanes(int64_t nvt, bool vec) {
     return G;
 }
 
-// Slots per row (lanes x slots per lane, padded to a power of two) of that plan.
+// Slots per row of that plan (lanes x slots per lane) as the grouped-ring rule
+// below was measured: slots per lane padded to 6 or 8 even for a whole warp
+// (whose plans now take 5 and 7 too: f32 N = 520, 132 slots in 160, still
+// measured faster on the ring, 1.018 against 0.971 of the copy peak; N = 600,
+// 152 in 160, faster on the warp, 1.037 against 1.015).
 int64_t subwarp_auto_slots(int64_t nvt, bool vec) {
     const int G = subwarp_auto_lanes(nvt, vec);
-    return G * subwarp_slot_count(ceil_div(nvt, G), G == 32 || (vec && G >= 4));
+    return G * subwarp_slot_count(ceil_div(nvt, G), G == 32 || (vec && G >= 4), false);
 }
 
 // Fill in (or check) a plan.  `req` may be null (automatic).
@@ -292,7 +296,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         int64_t V = ceil_div(nvt, G);
         const bool wide = G == 32 || (vec && G >= 4);  // groups that may hold 8 slots per lane
         if (V > (wide ? kSubwarpWarpSlots : kSubwarpMaxSlots)) return LSE_ERR_INVALID_ARG;
-        V = subwarp_slot_count(V, wide);
+        V = subwarp_slot_count(V, wide, G == 32);
         const int64_t R = V >= 3 ? 1 : (V == 2 ? 2 : 4);
         const int64_t rows_per_warp_iter = (32 / G) * R;
         const int64_t warps = ceil_div(B, rows_per_warp_iter);

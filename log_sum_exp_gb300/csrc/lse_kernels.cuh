@@ -33,12 +33,13 @@ namespace lse {
 // slot is one element.
 // V = 8 (a whole warp per row of up to 256 slots, or 4-16 lanes per row of
 // vectors: twice the rows in flight of V = 4 with half the lanes) keeps 32
-// words per lane and runs at 4 CTAs per SM.
+// words per lane and runs at 4 CTAs per SM; a whole warp per row also takes
+// V = 5 or 7, so a row of 129-256 slots pads to the next multiple of 32.
 // ---------------------------------------------------------------------------
 // The token log-probability epilogue keeps the targets and the peel state of
 // every row group live: one CTA per SM less, so it does not spill.
 template <int V, bool TL> struct SubwarpOccupancy {
-    static constexpr int min_blocks = (V >= 6 ? 4 : kSubwarpMinBlocks) - (TL ? 1 : 0);
+    static constexpr int min_blocks = (V >= 5 ? 4 : kSubwarpMinBlocks) - (TL ? 1 : 0);
 };
 
 template <int DT, int G, int V, bool VEC, bool TL, bool E16>
@@ -387,6 +388,12 @@ cudaError_t launch_subwarp_g(const LaunchArgs& a, int V, int64_t grid) {
     case 2: return launch_subwarp_gv<DT, G, 2, VEC, TL, E16>(a, grid);
     case 3: return launch_subwarp_gv<DT, G, 3, VEC, TL, E16>(a, grid);
     case 4: return launch_subwarp_gv<DT, G, 4, VEC, TL, E16>(a, grid);
+    case 5:  // 5 or 7 slots per lane: a whole warp per row
+        if constexpr (G == 32) return launch_subwarp_gv<DT, G, 5, VEC, TL, E16>(a, grid);
+        else return cudaErrorInvalidValue;
+    case 7:
+        if constexpr (G == 32) return launch_subwarp_gv<DT, G, 7, VEC, TL, E16>(a, grid);
+        else return cudaErrorInvalidValue;
     case 6:  // 6 or 8 slots per lane: a whole warp per row, or 4-16 lanes per row of vectors
         if constexpr (G == 32 || (VEC && G >= 4)) return launch_subwarp_gv<DT, G, 6, VEC, TL, E16>(a, grid);
         else return cudaErrorInvalidValue;

@@ -97,7 +97,7 @@ int main() {
 
     // Sub-warp shapes: fewest lanes with <= 4 slots; vector rows of more than
     // 16 slots take half the lanes with up to 8 slots each; slots per lane are
-    // 1, 2, 3, 4, 6 or 8.
+    // 1, 2, 3, 4, 6 or 8 (5 and 7 too for a whole warp).
     p = plan(LSE_F32, 1 << 20, 40, 44);
     expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 4 && p.slots_per_lane == 3,
            "f32 N=40: 4 lanes x 3 slots");
@@ -107,6 +107,17 @@ int main() {
     p = plan(LSE_F32, 1 << 17, 1001, 1001);
     expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 32 && p.slots_per_lane == 8,
            "f32 N=1001 (250 vectors + 2 peel slots): a warp x 8 slots");
+    // A whole warp per row takes 5 and 7 slots per lane too (row stride 1040
+    // elements keeps the rows strided, off the bulk-copy rings).
+    p = plan(LSE_BF16, 1 << 16, 1025, 1040);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 32 && p.slots_per_lane == 5,
+           "bf16 N=1025 (128 vectors + 2 slots): a warp x 5 slots");
+    p = plan(LSE_BF16, 1 << 16, 1700, 1704);
+    expect(p.path == LSE_PATH_SUBWARP && p.lanes_per_row == 32 && p.slots_per_lane == 7,
+           "bf16 N=1700 (212 vectors + 2 slots): a warp x 7 slots");
+    p = plan(LSE_F32, 1 << 16, 520, 520);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16,
+           "f32 N=520 back to back (132 slots): the grouped ring, as measured against 6 slots");
     expect(lse::subwarp_auto_slots(33, true) == 48 && lse::subwarp_auto_slots(32, true) == 32 &&
                lse::subwarp_auto_slots(18, true) == 24 && lse::subwarp_auto_slots(10, true) == 12,
            "sub-warp slot counts");

@@ -655,16 +655,17 @@ def test_no_wait_timed_out():
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_subwarp_three_and_six_slots(dtype):
     """The 3- and 6-slot sub-warp variants (rows just past a power of two of
-    slots): the row value, the token log-probability and the 16-bit
-    exponentials, on rows that start on a 16-byte boundary and on rows that
-    do not (their covering vectors take one or two more slots), with special
-    values at the first and the last element."""
+    slots), and the 5- and 7-slot ones of a whole warp per row: the row value,
+    the token log-probability and the 16-bit exponentials, on rows that start
+    on a 16-byte boundary and on rows that do not (their covering vectors take
+    one or two more slots), with special values at the first and the last
+    element."""
     _need_gpu()
     eb = 4 if dtype == "f32" else 2
     epv = 16 // eb
     seen = set()
     for nvec, lanes in ((3, 1), (5, 2), (9, 4), (11, 4), (18, 4), (21, 4), (40, 8), (90, 16),
-                        (170, 32)):
+                        (170, 32), (140, 32), (200, 32)):
         for extra, offset in ((0, 0), (1, 0), (0, 1), (epv - 1, 1)):
             N = nvec * epv + extra
             B = 37
@@ -696,4 +697,4 @@ def test_subwarp_three_and_six_slots(dtype):
                 compare_e16(g16.cpu().numpy(), want, e16_bound(x, dtype, want))
             except AssertionError as e:
                 raise AssertionError(f"N={N} offset={offset} plan={p.as_dict()}: {e}") from None
-    assert {3, 6} <= seen, seen
+    assert {3, 5, 6, 7} <= seen, seen

@@ -280,7 +280,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         int64_t grid = static_cast<int64_t>(info.sms) * rowtile_ctas_per_sm();
         if (grid > chunks) grid = chunks;
         p.path = LSE_PATH_ROWTILE;
-        p.threads = 256;
+        p.threads = rowtile_threads();
         p.slots_per_lane = nvec;
         p.splits = 1;
         p.grid = grid;

@@ -174,6 +174,7 @@ int cols_warps_per_cta(int warps_per_tile);
 // nv 0: rows of any width; lanes per row 1 (rows of <= 128 bytes) or 4..32.
 cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid);
 int rowtile_ctas_per_sm();
+int rowtile_threads();  // threads per CTA of the vector ring (one ring per warp)
 int rowtile_rows_per_chunk(int nv);  // rows a CTA takes per round (one chunk per warp)
 int rowtile_any_ctas_per_sm();
 int rowtile_any_rows_per_chunk(int row_bytes);  // nv == 0: rows of any width

@@ -504,6 +504,7 @@ cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int g
 }
 
 int rowtile_ctas_per_sm() { return kRingCtasPerSm; }
+int rowtile_threads() { return kRingWarps * 32; }
 int rowtile_rows_per_chunk(int nv) { return kRingWarps * 32 * (8 / nv); }  // one chunk per warp
 int rowtile_any_ctas_per_sm() { return 3; }  // 3 x 64 KB of stages per SM
 int rowtile_any_rows_per_chunk(int row_bytes) {

@@ -48,7 +48,8 @@ int main() {
     // Back-to-back rows of 16..128 bytes: the vector ring where it measured
     // faster (every width but f32 rows of 2 vectors), else the sub-warp kernel.
     lse_plan p = plan(LSE_F32, 1 << 20, 32, 32);
-    expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8, "f32 rows of 128 bytes: ring, 8 vectors");
+    expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8 && p.threads == 768 && p.grid == 152,
+           "f32 rows of 128 bytes: ring, 8 vectors, one CTA of 24 warps per SM");
     p = plan(LSE_BF16, 1 << 20, 64, 64);
     expect(p.path == LSE_PATH_ROWTILE && p.slots_per_lane == 8, "bf16 rows of 128 bytes: ring, 8 vectors");
     p = plan(LSE_F32, 1 << 22, 8, 8);

@@ -133,6 +133,14 @@ int main() {
                p.scratch_bytes == 16 * 128 * 8,
            "16 x 16.7M f32: 128 splits of 512 threads and a merge");
 
+    // Fewer rows than SMs: 128 threads where one full batch each covers the
+    // row, else at least 256.
+    p = plan(LSE_F32, 64, 4096, 4096);
+    expect(p.path == LSE_PATH_CTA && p.threads == 128 && p.splits == 1 && p.grid == 64,
+           "64 x 4096 f32: a CTA of 128 per row, one batch per thread");
+    p = plan(LSE_F32, 64, 8192, 8192);
+    expect(p.path == LSE_PATH_CTA && p.threads == 256, "64 x 8192 f32: a CTA of 256 per row");
+
     // Alignment: rows off a 16-byte boundary keep vectors (peeled); a base
     // that is not element aligned gets element loads.
     p = plan(LSE_F32, 64, 4096, 4096, reinterpret_cast<const void*>((1u << 20) + 4));

@@ -812,21 +812,26 @@ lse_status plan_columns(const void* x, lse_dtype dtype, int64_t A, int64_t R, in
         WT = 1;
     }
     // Narrow C (32-lane tiles would leave a quarter or more of their lanes
-    // without a column) takes one-warp tiles of 16 or 8 lanes at any R:
-    // measured bf16 [8192, 128, 128] 4.55 against 2.14 TB/s with two warps per
-    // 32-lane tile, [2048, 512, 128] 4.35 against 2.11.
-    const bool narrow = cols_lanes_per_tile(dtype, vec, C, 1) != 32;
+    // without a column) takes tiles of 16 or 8 lanes.  16-bit ones keep one
+    // warp per tile at any R (with row splits): bf16 [8192, 128, 128] 4.55
+    // against 2.14 TB/s with two warps per 32-lane tile, and one warp still
+    // beats 2 or 4 per narrow tile at R = 128-4096 (C = 64, 192: 0.87-0.95
+    // against 0.77-0.85 of the copy peak).  f32 narrow tiles take warps per
+    // tile by the rule for wide ones: [A, R, 64] f32 at R = 256 / 512 / 4096
+    // 0.978 / 0.956 / 0.933 with 4 warps against 0.856 / 0.862 / 0.859 with
+    // one warp and splits; C = 192 0.92-0.97 against 0.87-0.93.
+    const bool narrow16 = eb != 4 && cols_lanes_per_tile(dtype, vec, C, 1) != 32;
     if (WT == 0) {
         if (path == LSE_PATH_COLUMNS_CTA)
             WT = 8;
         else
-            WT = (R <= 64 || units >= 2 * resident_warps || narrow) ? 1 : (R <= 128 ? 2 : 4);
+            WT = (R <= 64 || units >= 2 * resident_warps || narrow16) ? 1 : (R <= 128 ? 2 : 4);
     }
     if (WT != 1 && WT != 2 && WT != 4 && WT != 8) return LSE_ERR_INVALID_ARG;
     path = WT == 1 ? LSE_PATH_COLUMNS_WARP : LSE_PATH_COLUMNS_CTA;
     const int W = cols_warps_per_cta(WT);
-    // One-warp tiles of narrow C: 16- or 8-lane tiles, 2 or 4 per warp.
-    const int lpt = cols_lanes_per_tile(dtype, vec, C, WT);
+    // Narrow C: 16- or 8-lane tiles, 2 or 4 per warp (any warps per tile).
+    const int lpt = cols_lanes_per_tile(dtype, vec, C, 1);
     if (lpt != 32) units = A * ceil_div(C, cols_columns_per_warp(vec, dtype) * lpt / 32);
     int64_t gx = ceil_div(units, W / WT * (32 / lpt));  // CTAs if each took one group of units
     const int64_t rows_per_warp_batch = WT * batch;

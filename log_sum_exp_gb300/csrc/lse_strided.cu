@@ -50,15 +50,16 @@ template <int WT> struct ColCta {
 // memory); the CTA's warps cover warps / WT tiles.  WT = 1: each warp walks
 // all rows of its own tile (short reductions, no merge); WT = 8: the whole CTA
 // works on one tile (long reductions with few tiles).  LPT lanes make a tile:
-// 32, or 16 or 8 with one-warp tiles when the wider tile would leave a
-// quarter or more of its lanes without a column (narrow C); a warp then folds
-// 32 / LPT tiles, one per group of LPT lanes.
+// 32, or 16 or 8 when the wider tile would leave a quarter or more of its
+// lanes without a column (narrow C); a warp then folds 32 / LPT tiles, one per
+// group of LPT lanes, and WT warps share that group of tiles (each lane
+// merges with the same lane of the group's other warps).
 template <int DT, bool VEC, int WT, int LPT>
 __global__ void __launch_bounds__(32 * ColCta<WT>::warps, ColCta<WT>::min_blocks(DType<DT>::bytes))
 lse_cols_kernel(const void* __restrict__ x, int64_t A, int64_t R, int64_t C, int64_t stride_a,
                 int64_t stride_r, int64_t rows_per_split, float* __restrict__ out,
                 float2* __restrict__ partial, int64_t P) {
-    static_assert(LPT == 32 || ((LPT == 16 || LPT == 8) && WT == 1), "narrow tiles are one-warp tiles");
+    static_assert(LPT == 32 || LPT == 16 || LPT == 8, "tiles of 32, 16 or 8 lanes");
     constexpr int EB = DType<DT>::bytes;
     constexpr int EPV = VEC ? 16 / EB : 1;
     constexpr int U = VEC ? 4 : 8;  // rows per batch per thread
@@ -439,18 +440,20 @@ cudaError_t launch_cols_t(const StridedArgs& a) {
                       a.x, a.A, a.R, a.C, a.stride_a, a.stride_r, a.rows_per_split, a.out,               \
                       a.partial, a.P)
 #define LSE_COLS_LAUNCH(WT) LSE_COLS_LAUNCH_L(WT, 32)
+#define LSE_COLS_LAUNCH_W(WT)                                     \
+    switch (cols_lanes_per_tile(DT, VEC, a.C, 1)) {               \
+    case 8: LSE_COLS_LAUNCH_L(WT, 8);                             \
+    case 16: LSE_COLS_LAUNCH_L(WT, 16);                           \
+    default: LSE_COLS_LAUNCH(WT);                                 \
+    }
     switch (a.warps_per_tile) {
-    case 1:
-        switch (cols_lanes_per_tile(DT, VEC, a.C, 1)) {
-        case 8: LSE_COLS_LAUNCH_L(1, 8);
-        case 16: LSE_COLS_LAUNCH_L(1, 16);
-        default: LSE_COLS_LAUNCH(1);
-        }
-    case 2: LSE_COLS_LAUNCH(2);
-    case 4: LSE_COLS_LAUNCH(4);
-    case 8: LSE_COLS_LAUNCH(8);
+    case 1: LSE_COLS_LAUNCH_W(1);
+    case 2: LSE_COLS_LAUNCH_W(2);
+    case 4: LSE_COLS_LAUNCH_W(4);
+    case 8: LSE_COLS_LAUNCH_W(8);
     default: return cudaErrorInvalidValue;
     }
+#undef LSE_COLS_LAUNCH_W
 #undef LSE_COLS_LAUNCH
 #undef LSE_COLS_LAUNCH_L
 }

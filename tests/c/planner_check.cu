@@ -260,6 +260,14 @@ int main() {
                    lse::cols_lanes_per_tile(LSE_F32, false, 8, 1) == 8 &&
                    lse::cols_lanes_per_tile(LSE_BF16, true, 64, 4) == 32,
                "8-lane column tiles");
+        // Narrow C over long reductions: f32 shares a narrow tile among 4 warps,
+        // 16-bit keeps one warp per tile.
+        q = cols(LSE_F32, 4096, 256, 64, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_CTA && q.lanes_per_row == 4 && q.splits == 1,
+               "[4096, 256, 64] f32: 4 warps per 16-lane tile");
+        q = cols(LSE_BF16, 8192, 256, 64, kAligned, nullptr, &cst);
+        expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.lanes_per_row == 1,
+               "[8192, 256, 64] bf16: one warp per 8-lane tile");
         q = cols(LSE_BF16, 16384, 64, 64, kAligned, nullptr, &cst);
         expect(cst == LSE_OK && q.path == LSE_PATH_COLUMNS_WARP && q.lanes_per_row == 1 && q.splits == 1 &&
                    q.grid == 16384 / 16,

@@ -212,10 +212,11 @@ def test_columns_inf_between_shifts(dtype, offset):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_columns_narrow_tiles(dtype):
-    """Narrow C: one-warp tiles of 16 or 8 lanes, two or four per warp (the
-    later groups of lanes fold the next (a, tile) units, possibly of the next
-    a).  Special values in columns of several groups; aligned and element
-    layouts; the warp path forced and automatic; a row split."""
+    """Narrow C: tiles of 16 or 8 lanes, two or four per warp (the later
+    groups of lanes fold the next (a, tile) units, possibly of the next a),
+    walked by one warp or shared by 2 or 4 (merged lane by lane).  Special
+    values in columns of several groups; aligned and element layouts; the
+    warp and CTA paths forced and automatic; row splits."""
     _need_gpu()
     for A, R, C in ((37, 64, 64), (100, 9, 128), (20, 33, 40), (7, 70, 200), (3, 5, 384), (1, 3, 16),
                     (513, 2, 8), (65, 4, 32), (9, 17, 192)):
@@ -230,7 +231,9 @@ def test_columns_narrow_tiles(dtype):
             xi[0, :, 0] = ninf
             xi[0, 0, 0] = 0
         for lay in (dict(), dict(pad_c=3), dict(offset=1)):
-            for plan in (None, {"path": "columns_warp"}, {"path": "columns_warp", "splits": 2}):
+            for plan in (None, {"path": "columns_warp"}, {"path": "columns_warp", "splits": 2},
+                         {"path": "columns_cta", "lanes_per_row": 2},
+                         {"path": "columns_cta", "lanes_per_row": 4, "splits": 2}):
                 if plan and plan.get("splits", 0) > R:
                     continue
                 got, want = run_strided(x, dtype, plan=plan, **lay)

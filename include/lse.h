@@ -93,7 +93,8 @@ typedef enum {
                                   log-probability and 16-bit exponentials.
                                   Rows of other widths (slots_per_lane = 0):
                                   32 KB chunks per CTA, a thread per row up to
-                                  128 bytes (vector_bytes = 1), else a group
+                                  128 bytes plus one element (vector_bytes =
+                                  1), else a group
                                   of 4..32 lanes (lanes_per_row); row value and
                                   token log-probability with f32 exponentials */
     LSE_PATH_COLUMNS_SHORT = 8 /* lse_forward_strided, R <= 8 rows of 16-byte

@@ -206,23 +206,24 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
                             row_bytes >= 16 && row_bytes <= 128;
     const int64_t row_vecs = row_bytes / 16;
     const bool rowtile_auto = !(eb == 4 && row_vecs == 2);
-    // Rows of other widths up to 128 bytes, still back to back from a 16-byte
-    // aligned base: the same ring, one thread per row (row value or token
-    // log-probability, f32 exponentials).  Chosen automatically for rows of at
-    // least 32 bytes (f32 N = 13: 5.06 against 3.93 TB/s, bf16 N = 31: 3.28
-    // against 2.63); shorter rows measured faster on the sub-warp mapping
-    // (f32 N = 7: 4.56 against 3.02).
+    // Rows of other widths up to 128 bytes plus one element, still back to
+    // back from a 16-byte aligned base: the same ring, one thread per row (row
+    // value or token log-probability, f32 exponentials).  Chosen automatically
+    // for rows of at least 32 bytes (f32 N = 13: 5.06 against 3.93 TB/s, bf16
+    // N = 31: 3.28 against 2.63); shorter rows measured faster on the sub-warp
+    // mapping (f32 N = 7: 4.56 against 3.02).
+    const int64_t thread_row_max = rowtile_any_thread_row_max_bytes(eb);
     const bool rowtile_any_ok = !rowtile_ok && !e16 && row_stride == N &&
                                 row_bytes <= rowtile_any_max_row_bytes() &&
                                 reinterpret_cast<uintptr_t>(x) % 16u == 0 &&
                                 (!req || req->vector_bytes == 0 ||
-                                 req->vector_bytes == (row_bytes <= 128 ? 1 : 16));
-    // Lanes per row of that ring: one thread per row up to 128 bytes, else a
+                                 req->vector_bytes == (row_bytes <= thread_row_max ? 1 : 16));
+    // Lanes per row of that ring: one thread per row up to thread_row_max, else a
     // group of 4-32 lanes, the largest power of two giving each lane >= 8 of
     // the row's 16-byte vectors (f32) or >= 16 (16-bit): the best group size
     // measured for rows of 129 bytes to 4 KB.
     int any_lanes = 1;
-    if (row_bytes > 128) {
+    if (row_bytes > thread_row_max) {
         const int64_t per_lane = eb == 4 ? 8 : 16;
         any_lanes = 4;
         while (any_lanes < 32 && ceil_div(row_bytes, 16) >= 2 * any_lanes * per_lane) any_lanes *= 2;
@@ -233,7 +234,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
             rowtile_any_ok ? rowtile_any_rows_per_chunk(static_cast<int>(row_bytes)) : 1;
         if (rowtile_ok && rowtile_auto && B >= chunk_rows * info.sms * rowtile_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
-        else if (rowtile_any_ok && row_bytes >= 32 && row_bytes <= 128 &&
+        else if (rowtile_any_ok && row_bytes >= 32 && row_bytes <= thread_row_max &&
                  B >= any_rows * info.sms * rowtile_any_ctas_per_sm())
             path = LSE_PATH_ROWTILE;
         // Back-to-back rows of more than 512 bytes take the grouped ring where
@@ -254,7 +255,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
     if (path == LSE_PATH_ROWTILE && !rowtile_ok && rowtile_any_ok) {
         if (req && req->lanes_per_row) {
             const int L = req->lanes_per_row;
-            if (row_bytes <= 128 ? L != 1 : (L < 4 || L > 32 || (L & (L - 1)) != 0))
+            if (row_bytes <= thread_row_max ? L != 1 : (L < 4 || L > 32 || (L & (L - 1)) != 0))
                 return LSE_ERR_INVALID_ARG;
             any_lanes = L;
         }
@@ -263,7 +264,7 @@ lse_status make_plan(const void* x, lse_dtype dt, int64_t B, int64_t N, int64_t 
         if (grid > chunks) grid = chunks;
         if (grid < 1) grid = 1;
         p.path = LSE_PATH_ROWTILE;
-        p.vector_bytes = row_bytes <= 128 ? 1 : 16;
+        p.vector_bytes = row_bytes <= thread_row_max ? 1 : 16;
         p.lanes_per_row = any_lanes;
         p.threads = 256;
         p.slots_per_lane = 0;  // any row width

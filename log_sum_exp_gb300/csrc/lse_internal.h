@@ -175,6 +175,10 @@ int cols_warps_per_cta(int warps_per_tile);
 cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid);
 int rowtile_ctas_per_sm();
 int rowtile_threads();  // threads per CTA of the vector ring (one ring per warp)
+// Widest back-to-back row the any-width ring folds with one thread: 128 bytes
+// plus one element (such a row, from any element offset, touches at most
+// nine 16-byte vectors).
+inline int rowtile_any_thread_row_max_bytes(int elem_bytes) { return 128 + elem_bytes; }
 int rowtile_rows_per_chunk(int nv);  // rows a CTA takes per round (one chunk per warp)
 int rowtile_any_ctas_per_sm();
 int rowtile_any_rows_per_chunk(int row_bytes);  // nv == 0: rows of any width

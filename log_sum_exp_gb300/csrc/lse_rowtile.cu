@@ -46,7 +46,7 @@ constexpr int kRingWarps = 24;          // vector ring: warps per CTA
 constexpr int kRingStages = 1;          // vector ring: stages per warp
 constexpr int kRingCtasPerSm = 1;       // 96 KB of stages per SM
 constexpr uint32_t kWaitPolls = 1u << 26;
-constexpr int kAnyThreadRowBytes = 128;  // any-width rows up to this: one thread per row
+constexpr int kAnyThreadRowBytes = 128;  // rows up to this: 256 per chunk, one per thread
 constexpr int kAnyThreadRowVectors = 9;  // 16-byte vectors such a row can touch
 
 __device__ unsigned long long g_wait_timeouts;
@@ -206,8 +206,9 @@ lse_rowtile_kernel(const void* __restrict__ x, int64_t B, float* __restrict__ ou
 // CR rows starts and ends on a 16-byte boundary as long as CR is a multiple of
 // k = 16 / gcd(RB, 16): the copies cover the first Bm = B - B % k rows, and
 // the < k rows after them are read from global memory by CTA 0 at the end.
-// G == 1 (rows of <= 128 bytes): CR = 256 * floor(32 KB / (256 * RB)) and
-// each thread folds whole rows with element reads (max, then the exp-sum).
+// G == 1 (rows of <= 128 bytes plus one element): CR = 256 * floor(32 KB /
+// (256 * RB)) up to 128 bytes, else as for G > 1, and each thread folds whole
+// rows from vector reads (max, then the exp-sum).
 // G > 1: CR = floor(32 KB / RB) rounded down to a multiple of k; the 256 / G
 // groups of G lanes take the chunk's rows in turn, a lane reading every G-th
 // 16-byte vector of its row from shared memory (conflict-free: a group reads
@@ -234,8 +235,9 @@ lse_rowtile_any_kernel(const void* __restrict__ x, int64_t B, int64_t N, float* 
         t = r;
     }
     const int64_t k = 16 / g;
-    const int64_t CR = G == 1 ? static_cast<int64_t>(kTileThreads) * (kChunkBytes / (kTileThreads * RB))
-                              : (kChunkBytes / RB) - (kChunkBytes / RB) % k;
+    const int64_t CR = RB <= kAnyThreadRowBytes
+                           ? static_cast<int64_t>(kTileThreads) * (kChunkBytes / (kTileThreads * RB))
+                           : (kChunkBytes / RB) - (kChunkBytes / RB) % k;
     const int64_t Bm = B - B % k;
     const int64_t nchunks = (Bm + CR - 1) / CR;
     const char* xb = reinterpret_cast<const char*>(x);
@@ -492,7 +494,7 @@ cudaError_t launch_rowtile_e(int dt, int nv, const LaunchArgs& a, int grid) {
 cudaError_t launch_rowtile(int dt, int nv, int lanes, const LaunchArgs& a, int grid) {
     if (nv == 0) {  // any row width: row value or token log-probability, f32 exponentials
         if (a.e16) return cudaErrorInvalidValue;
-        if ((lanes == 1) != (a.N * (dt == kF32 ? 4 : 2) <= kAnyThreadRowBytes) ||
+        if ((lanes == 1) != (a.N * (dt == kF32 ? 4 : 2) <= rowtile_any_thread_row_max_bytes(dt == kF32 ? 4 : 2)) ||
             a.N * (dt == kF32 ? 4 : 2) > kChunkBytes / 8)
             return cudaErrorInvalidValue;
         return a.tl.logprob ? launch_rowtile_any<true>(dt, lanes, a, grid)

@@ -82,6 +82,15 @@ int main() {
     // kernel cannot hold the row.
     p = plan(LSE_F32, 1 << 20, 129, 129);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 4, "f32 N=129: grouped ring, 4 lanes");
+    // One thread per row up to 128 bytes plus one element: f32 N = 33
+    // (132 bytes, at most 9 vectors from any 4-byte offset), bf16 N = 65.
+    p = plan(LSE_F32, 1 << 20, 33, 33);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 1 && p.vector_bytes == 1,
+           "f32 N=33: the ring, a thread per row");
+    p = plan(LSE_BF16, 1 << 20, 65, 65);
+    expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 1, "bf16 N=65: the ring, a thread per row");
+    p = plan(LSE_BF16, 1 << 20, 66, 66);
+    expect(!(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 1), "bf16 N=66: not a thread per row");
     p = plan(LSE_F32, 1 << 20, 520, 520);
     expect(p.path == LSE_PATH_ROWTILE && p.lanes_per_row == 16, "f32 N=520: grouped ring, 16 lanes");
     p = plan(LSE_F32, 1 << 20, 300, 300);

@@ -167,8 +167,8 @@ def test_logprob_rejects_bad_pointers():
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_logprob_any_width_ring(dtype):
     """The bulk-copy ring for back-to-back rows of any width with the token
-    log-probability epilogue: a thread per row up to 128 bytes, 4-32 lanes per
-    row up to 4 KB; targets in and out of range, on special values, partial
+    log-probability epilogue: a thread per row up to 128 bytes plus one
+    element, 4-32 lanes per row up to 4 KB; targets in and out of range, on special values, partial
     last chunks and the rows after the last copy, with and without lse_out."""
     _need_gpu()
     eb = 4 if dtype == "f32" else 2
@@ -192,7 +192,7 @@ def test_logprob_any_width_ring(dtype):
             want_lp, want_lse = oracle.token_logprob(x, t, dtype)
             xd = torch_view(x, dtype).cuda()
             plans = [{"path": "rowtile"}]
-            if N * eb > 128:
+            if N * eb > 128 + eb:  # past a thread per row
                 plans += [{"path": "rowtile", "lanes_per_row": G} for G in (4, 32)]
             for plan in plans:
                 for with_lse in (True, False):

@@ -487,16 +487,46 @@ def test_rowtile_any_width_ragged():
     16 bytes (element reads from shared memory; the last < 16/gcd(width, 16)
     rows come from global memory), every dtype, odd widths and row counts."""
     _need_gpu()
-    for dtype, eb, Ns in (("f32", 4, (1, 2, 3, 5, 6, 7, 9, 13, 17, 31)),
-                          ("bf16", 2, (1, 2, 3, 5, 7, 9, 12, 17, 33, 63)),
-                          ("f16", 2, (3, 5, 12, 31))):
+    for dtype, eb, Ns in (("f32", 4, (1, 2, 3, 5, 6, 7, 9, 13, 17, 31, 33)),
+                          ("bf16", 2, (1, 2, 3, 5, 7, 9, 12, 17, 33, 63, 65)),
+                          ("f16", 2, (3, 5, 12, 31, 65))):
         for N in Ns:
             for B in (1, 7, 255, 2049, 100003):
                 x = wl.random_rows(B, N, dtype, seed=B + 7 * N, scale=8.0)
                 got, p = run(torch_view(x, dtype).cuda(), {"path": "rowtile"})
                 d = p.as_dict()
                 assert d["path"] == "rowtile" and d["slots_per_lane"] == 0, d
+                assert d["lanes_per_row"] == 1, d  # a thread per row up to 128 bytes + one element
                 compare(got, oracle.lse(x, dtype))
+    assert L.lse_wait_timeouts() == 0
+
+
+def test_thread_rows_past_128_bytes():
+    """Rows of 128 bytes plus one element (f32 N = 33, 16-bit N = 65) on the
+    thread-per-row ring, whose chunks then hold fewer rows than threads: the
+    row value and the token log-probability, special values, ragged row counts,
+    forced and (with enough rows) chosen automatically."""
+    _need_gpu()
+    for dtype, N in (("f32", 33), ("bf16", 65), ("f16", 65)):
+        for B in (7, 249, 400003):
+            plan = None if B == 400003 else {"path": "rowtile"}  # enough rows to choose it alone
+            x = wl.random_rows(B, N, dtype, seed=B + N, scale=6.0, shift=-1.0)
+            xi = x.view(np.uint16) if dtype != "f32" else x
+            nan, pinf, ninf = {"f32": (np.nan, np.inf, -np.inf), "bf16": (0x7FC0, 0x7F80, 0xFF80),
+                               "f16": (0x7E00, 0x7C00, 0xFC00)}[dtype]
+            xi[B - 1, N - 1] = nan
+            xi[B // 2, 0] = pinf
+            xi[B // 3, :] = ninf
+            xd = torch_view(x, dtype).cuda()
+            got, p = run(xd, plan)
+            d = p.as_dict()
+            assert d["path"] == "rowtile" and d["lanes_per_row"] == 1 and d["slots_per_lane"] == 0, d
+            compare(got, oracle.lse(x, dtype))
+            t = np.arange(B, dtype=np.int64) * 5 % (N + 2) - 1
+            want_lp, want_lse = oracle.token_logprob(x, t, dtype)
+            lp, pl = L.lse_token_logprob(xd, torch.from_numpy(t).cuda(), plan=plan, return_plan=True)
+            assert pl.as_dict()["path"] == "rowtile" and pl.as_dict()["lanes_per_row"] == 1
+            compare_logprob(lp.cpu().numpy(), want_lp, want_lse)
     assert L.lse_wait_timeouts() == 0
 
 
@@ -526,8 +556,8 @@ def test_rowtile_grouped_rows(dtype):
     period, special values, every group size."""
     _need_gpu()
     eb = 4 if dtype == "f32" else 2
-    for rb in (130, 144, 252, 516, 1000, 1026, 2048, 2050, 4094, 4096):
-        if rb % eb:
+    for rb in (130, 134, 144, 252, 516, 1000, 1026, 2048, 2050, 4094, 4096):
+        if rb % eb or rb <= 128 + eb:  # up to 128 bytes + one element: a thread per row
             continue
         N = rb // eb
         for B in (1, 3, 9, 1001, 20003):

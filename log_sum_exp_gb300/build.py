@@ -16,7 +16,7 @@ SOURCES = ["lse_api.cu", "lse_kernels_f32.cu", "lse_kernels_bf16.cu", "lse_kerne
            "lse_logprob_f32.cu", "lse_logprob_bf16.cu", "lse_logprob_f16.cu", "lse_backward.cu",
            "lse_strided.cu", "lse_rowtile.cu", "lse_noalloc.cu", "lse_ex16_f32.cu",
            "lse_ex16_bf16.cu", "lse_ex16_f16.cu"]
-HEADERS = ["lse_device.cuh", "lse_kernels.cuh", "lse_internal.h"]
+HEADERS = ["lse_device.cuh", "lse_edges.cuh", "lse_kernels.cuh", "lse_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

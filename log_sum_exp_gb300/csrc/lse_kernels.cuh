@@ -21,6 +21,7 @@
 #pragma once
 
 #include "lse_device.cuh"
+#include "lse_edges.cuh"
 #include "lse_internal.h"
 
 namespace lse {
@@ -101,7 +102,8 @@ lse_subwarp_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
                         const int k = sub + j * G;
                         if (k == 0 || k == nvc - 1) {
                             uint32_t q[4] = {w[r][4 * j], w[r][4 * j + 1], w[r][4 * j + 2], w[r][4 * j + 3]};
-                            mask_words<DT>(q, static_cast<uint32_t>(k) * 16u, off[r], rb1);
+                            if (k == 0) mask_prefix<DT>(q, static_cast<int>(off[r]));
+                            if (k == nvc - 1) mask_suffix<DT>(q, static_cast<int>(rb1) - 16 * k);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) w[r][4 * j + i] = q[i];
                         }
@@ -257,8 +259,8 @@ lse_segment_kernel(const void* __restrict__ x, int64_t B, int64_t N, int64_t row
     auto mask_edge = [&](uint32_t* w4, int64_t kk) {
         if (kk == 0 || kk == nslots - 1) {
             uint32_t q[4] = {w4[0], w4[1], w4[2], w4[3]};
-            mask_words<DT>(q, 0u, kk == 0 ? off : 0u,
-                           kk == nslots - 1 ? static_cast<uint32_t>(rb1 - kk * 16) : 16u);
+            if (kk == 0) mask_prefix<DT>(q, static_cast<int>(off));
+            if (kk == nslots - 1) mask_suffix<DT>(q, static_cast<int>(rb1 - kk * 16));
 #pragma unroll
             for (int i = 0; i < 4; ++i) w4[i] = q[i];
         }
